@@ -1,0 +1,305 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+* brute-force pairwise neighbour search and a dense index-grid lookup (kernel map);
+* a dense zero-padded Conv3d (torch CPU, float64, padding 1) on small grids, masked
+  to the active sites -- equal to the submanifold convolution because inactive
+  sites hold zeros;
+* a hand-worked example (tests/golden/hand_worked.json);
+* invariants: isolated voxel, single asymmetric tap, translation and permutation
+  equivariance, linearity, batch independence, grid-boundary voxels, errors;
+* the C++ oracle against all of the above and against the Python oracle.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import cpu, ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def random_set(rng, res, batch, n):
+    """n distinct random lattice points per batch item (b, z, y, x) int32."""
+    rows = []
+    for b in range(batch):
+        flat = rng.choice(res ** 3, size=n, replace=False)
+        z, rem = np.divmod(flat, res * res)
+        y, x = np.divmod(rem, res)
+        rows.append(np.stack([np.full(n, b), z, y, x], axis=1))
+    c = np.concatenate(rows).astype(np.int32)
+    return c[rng.permutation(c.shape[0])]
+
+
+def dense_masked_conv3d(coords, feats, weight, bias, res):
+    """Dense zero-padded Conv3d (padding 1) on the densified grid, read at the active sites."""
+    coords = np.asarray(coords)
+    B = int(coords[:, 0].max()) + 1
+    I = feats.shape[1]
+    grid = torch.zeros(B, I, res, res, res, dtype=torch.float64)
+    b, z, y, x = (torch.from_numpy(coords[:, k].astype(np.int64)) for k in range(4))
+    grid[b, :, z, y, x] = torch.from_numpy(np.asarray(feats, np.float64))
+    w = torch.from_numpy(np.asarray(weight, np.float64)).permute(0, 4, 1, 2, 3).contiguous()
+    bt = None if bias is None else torch.from_numpy(np.asarray(bias, np.float64))
+    out = F.conv3d(grid, w, bt, stride=1, padding=1)
+    return out[b, :, z, y, x].numpy()
+
+
+def brute_force_nbr(coords):
+    """O(N^2): nbr[i, k] = j whenever coords[j] - coords[i] is offset k in the same batch item."""
+    c = np.asarray(coords, np.int64)
+    N = c.shape[0]
+    nbr = np.full((N, 27), -1, np.int32)
+    for i in range(N):
+        d = c[:, 1:] - c[i, 1:]
+        same = (c[:, 0] == c[i, 0]) & (np.abs(d).max(axis=1) <= 1)
+        for j in np.nonzero(same)[0]:
+            dz, dy, dx = d[j]
+            nbr[i, 9 * (dz + 1) + 3 * (dy + 1) + (dx + 1)] = j
+    return nbr
+
+
+def dense_lookup_nbr(coords, res):
+    """Index grid filled with -1, padded by one cell, read at the 27 shifted positions."""
+    c = np.asarray(coords, np.int64)
+    B = int(c[:, 0].max()) + 1
+    grid = np.full((B, res + 2, res + 2, res + 2), -1, np.int64)
+    grid[c[:, 0], c[:, 1] + 1, c[:, 2] + 1, c[:, 3] + 1] = np.arange(c.shape[0])
+    cols = []
+    for dz in (-1, 0, 1):
+        for dy in (-1, 0, 1):
+            for dx in (-1, 0, 1):
+                cols.append(grid[c[:, 0], c[:, 1] + 1 + dz, c[:, 2] + 1 + dy, c[:, 3] + 1 + dx])
+    return np.stack(cols, axis=1).astype(np.int32)
+
+
+def rand_values(rng, N, I, O, with_bias=True):
+    f = rng.standard_normal((N, I))
+    w = rng.standard_normal((O, 3, 3, 3, I))
+    b = rng.standard_normal(O) if with_bias else None
+    return f, w, b
+
+
+# ----------------------------------------------------------------------------- kernel map
+
+@pytest.mark.parametrize("seed,res,batch,n", [(0, 4, 1, 20), (1, 5, 2, 40), (2, 6, 1, 120),
+                                               (3, 3, 2, 27), (4, 7, 3, 60)])
+def test_kernel_map_brute_force_and_dense_lookup(seed, res, batch, n):
+    rng = np.random.default_rng(seed)
+    c = random_set(rng, res, batch, n)
+    want = brute_force_nbr(c)
+    np.testing.assert_array_equal(ref.kernel_map(c, res), want)
+    np.testing.assert_array_equal(dense_lookup_nbr(c, res), want)
+    np.testing.assert_array_equal(cpu.kernel_map(c, res), want)
+
+
+def test_kernel_map_full_block_and_symmetry():
+    # a full 3x3x3 block: the centre sees all 27 neighbours, tap k holding the voxel at offset k
+    c = np.array([[0, z, y, x] for z in range(3) for y in range(3) for x in range(3)], np.int32)
+    nbr = ref.kernel_map(c, 3)
+    np.testing.assert_array_equal(nbr[13], np.arange(27))
+    # neighbour relation is symmetric: nbr[i, k] = j  <=>  nbr[j, 26 - k] = i
+    rng = np.random.default_rng(7)
+    c = random_set(rng, 6, 2, 90)
+    nbr = ref.kernel_map(c, 6)
+    for i, k in zip(*np.nonzero(nbr >= 0)):
+        assert nbr[nbr[i, k], 26 - k] == i
+    assert (nbr[:, 13] == np.arange(c.shape[0])).all()
+
+
+def test_kernel_map_grid_boundary_and_batches():
+    res = 5
+    c = np.array([[0, 0, 0, 0], [0, 4, 4, 4], [1, 0, 0, 0], [1, 4, 4, 4], [0, 1, 1, 1]], np.int32)
+    nbr = ref.kernel_map(c, res)
+    # the corner voxels see nothing outside the grid, only their in-grid neighbours
+    assert nbr[0, 26] == 4 and (np.delete(nbr[0], [13, 26]) == -1).all()
+    assert (np.delete(nbr[1], 13) == -1).all()
+    # identical (z, y, x) in another batch item is not a neighbour
+    assert (np.delete(nbr[2], 13) == -1).all()
+    np.testing.assert_array_equal(cpu.kernel_map(c, res), nbr)
+
+
+@pytest.mark.parametrize("mod", [ref, cpu])
+def test_errors(mod):
+    with pytest.raises(ref.OracleError):
+        mod.kernel_map(np.array([[0, 0, 0, 4]], np.int32), 4)
+    with pytest.raises(ref.OracleError):
+        mod.kernel_map(np.array([[0, -1, 0, 0]], np.int32), 4)
+    with pytest.raises(ref.OracleError):
+        mod.kernel_map(np.array([[-1, 0, 0, 0]], np.int32), 4)
+    with pytest.raises(ref.OracleError):
+        mod.kernel_map(np.array([[0, 1, 2, 3], [0, 0, 0, 0], [0, 1, 2, 3]], np.int32), 4)
+
+
+# ----------------------------------------------------------------------------- forward
+
+@pytest.mark.parametrize("seed,res,batch,n,I,O", [(0, 4, 1, 30, 3, 5), (1, 6, 2, 70, 4, 2),
+                                                   (2, 8, 1, 200, 2, 3), (3, 5, 3, 50, 5, 4),
+                                                   (4, 3, 1, 27, 2, 2)])
+def test_forward_matches_dense_conv3d(seed, res, batch, n, I, O):
+    rng = np.random.default_rng(seed)
+    c = random_set(rng, res, batch, n)
+    f, w, b = rand_values(rng, c.shape[0], I, O, with_bias=seed % 2 == 0)
+    want = dense_masked_conv3d(c, f, w, b, res)
+    got = ref.subm_conv3d(c, f, w, b, res)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
+    got_cpp = cpu.forward_rows(c, f.astype(np.float32), w.astype(np.float32),
+                               None if b is None else b.astype(np.float32), res)
+    want32 = dense_masked_conv3d(c, f.astype(np.float32), w.astype(np.float32),
+                                 None if b is None else b.astype(np.float32), res)
+    np.testing.assert_allclose(got_cpp, want32, rtol=0, atol=1e-12 * max(1.0, np.abs(want32).max()))
+
+
+def test_forward_on_shell_matches_dense_conv3d():
+    from synth import ellipsoid_shell, union_coords, uniform_rotation
+    rng = np.random.default_rng(11)
+    pts = ellipsoid_shell(20, (9.6, 10.2, 9.1), (6.5, 4.2, 7.7), uniform_rotation(rng))
+    c = union_coords([(0, pts), (1, pts[::2])], 20)
+    f, w, b = rand_values(rng, c.shape[0], 6, 7)
+    want = dense_masked_conv3d(c, f, w, b, 20)
+    np.testing.assert_allclose(ref.subm_conv3d(c, f, w, b, 20), want, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(
+        cpu.forward_rows(c, f.astype(np.float32), w.astype(np.float32), b.astype(np.float32), 20),
+        dense_masked_conv3d(c, f.astype(np.float32), w.astype(np.float32), b.astype(np.float32), 20),
+        rtol=0, atol=1e-11)
+
+
+def test_hand_worked_golden():
+    spec = json.load(open(GOLDEN))
+    for cs in spec["cases"]:
+        c = np.array(cs["coords"], np.int32)
+        N = c.shape[0]
+        w = np.zeros((1, 3, 3, 3, 1))
+        for kz in range(3):
+            for ky in range(3):
+                for kx in range(3):
+                    w[0, kz, ky, kx, 0] = 1 + 9 * kz + 3 * ky + kx
+        f = np.array(cs["feats"], np.float64).reshape(N, 1)
+        b = np.array([cs["bias"]])
+        want_nbr = np.full((N, 27), -1)
+        for i, pairs in enumerate(cs["nbr_nonabsent"]):
+            for k, j in pairs:
+                want_nbr[i, k] = j
+        for mod in (ref, cpu):
+            np.testing.assert_array_equal(mod.kernel_map(c, cs["res"]), want_nbr, err_msg=cs["name"])
+        np.testing.assert_array_equal(ref.subm_conv3d(c, f, w, b, cs["res"])[:, 0], cs["out"])
+        np.testing.assert_array_equal(
+            cpu.forward_rows(c, f.astype(np.float32), w.astype(np.float32),
+                             b.astype(np.float32), cs["res"])[:, 0], cs["out"])
+
+
+def test_isolated_voxel_sees_only_centre_tap():
+    rng = np.random.default_rng(3)
+    c = np.array([[0, 2, 2, 2], [0, 6, 6, 6], [1, 2, 2, 2]], np.int32)
+    f, w, b = rand_values(rng, 3, 4, 5)
+    out = ref.subm_conv3d(c, f, w, b, 9)
+    for i in range(3):
+        np.testing.assert_allclose(out[i], w[:, 1, 1, 1, :] @ f[i] + b, rtol=1e-14)
+
+
+@pytest.mark.parametrize("tap", [(2, 1, 0), (0, 2, 1), (1, 0, 2), (0, 0, 0), (2, 2, 2)])
+def test_single_asymmetric_tap_orientation(tap):
+    """Only tap (kz, ky, kx) is non-zero: out at p reads the input at p + (tap - 1)."""
+    rng = np.random.default_rng(5)
+    c = random_set(rng, 5, 1, 60)
+    f, _, _ = rand_values(rng, c.shape[0], 3, 2)
+    w = np.zeros((2, 3, 3, 3, 3))
+    w[:, tap[0], tap[1], tap[2], :] = rng.standard_normal((2, 3))
+    out = ref.subm_conv3d(c, f, w, None, 5)
+    index = {tuple(r): i for i, r in enumerate(c.tolist())}
+    d = np.array(tap) - 1
+    for i, (b, z, y, x) in enumerate(c.tolist()):
+        j = index.get((b, z + d[0], y + d[1], x + d[2]))
+        want = np.zeros(2) if j is None else w[:, tap[0], tap[1], tap[2], :] @ f[j]
+        np.testing.assert_allclose(out[i], want, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(cpu.forward_rows(c, f.astype(np.float32), w.astype(np.float32),
+                                                None, 5),
+                               ref.subm_conv3d(c, f.astype(np.float32), w.astype(np.float32),
+                                               None, 5), rtol=1e-13, atol=1e-13)
+
+
+def test_translation_and_permutation_equivariance():
+    rng = np.random.default_rng(9)
+    c = random_set(rng, 6, 2, 80)
+    f, w, b = rand_values(rng, c.shape[0], 3, 4)
+    out = ref.subm_conv3d(c, f, w, b, 12)
+    t = np.array([0, 3, 5, 2], np.int32)
+    np.testing.assert_allclose(ref.subm_conv3d(c + t, f, w, b, 12), out, rtol=0, atol=1e-12)
+    p = rng.permutation(c.shape[0])
+    np.testing.assert_allclose(ref.subm_conv3d(c[p], f[p], w, b, 12), out[p], rtol=0, atol=1e-12)
+    f32, w32, b32 = f.astype(np.float32), w.astype(np.float32), b.astype(np.float32)
+    np.testing.assert_allclose(cpu.forward_rows(c[p], f32[p], w32, b32, 12),
+                               cpu.forward_rows(c, f32, w32, b32, 12)[p], rtol=0, atol=1e-12)
+
+
+def test_linearity_in_feats_and_weight():
+    rng = np.random.default_rng(13)
+    c = random_set(rng, 5, 1, 50)
+    f1, w1, _ = rand_values(rng, c.shape[0], 3, 4)
+    f2, w2, _ = rand_values(rng, c.shape[0], 3, 4)
+    a, s = 0.7, -1.9
+    conv = lambda f, w: ref.subm_conv3d(c, f, w, None, 5)
+    np.testing.assert_allclose(conv(a * f1 + s * f2, w1), a * conv(f1, w1) + s * conv(f2, w1),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(conv(f1, a * w1 + s * w2), a * conv(f1, w1) + s * conv(f1, w2),
+                               rtol=0, atol=1e-12)
+
+
+def test_batch_items_are_independent():
+    rng = np.random.default_rng(17)
+    c0 = random_set(rng, 5, 1, 40)
+    c1 = c0.copy()
+    c1[:, 0] = 1
+    f, w, b = rand_values(rng, 40, 3, 4)
+    both = ref.subm_conv3d(np.concatenate([c0, c1]), np.concatenate([f, f]), w, b, 5)
+    np.testing.assert_array_equal(both[:40], both[40:])
+    np.testing.assert_array_equal(both[:40], ref.subm_conv3d(c0, f, w, b, 5))
+
+
+def test_rows_subset_matches_full():
+    rng = np.random.default_rng(19)
+    c = random_set(rng, 7, 2, 100)
+    f, w, b = (v.astype(np.float32) for v in rand_values(rng, c.shape[0], 4, 3))
+    full = ref.subm_conv3d(c, f, w, b, 7)
+    rows = [0, 5, 199, 17, 17]
+    np.testing.assert_array_equal(ref.subm_conv3d_rows(c, f, w, b, 7, rows), full[rows])
+    np.testing.assert_allclose(cpu.forward_rows(c, f, w, b, 7, rows=rows), full[rows],
+                               rtol=0, atol=1e-12)
+
+
+def _golden_inputs(cs):
+    c = np.array(cs["coords"], np.int32)
+    w = np.zeros((1, 3, 3, 3, 1))
+    w.reshape(-1)[:] = np.arange(1, 28)
+    f = np.array(cs["feats"]).reshape(-1, 1)
+    return c, f, w, np.array([cs["bias"]])
+
+
+def test_planted_convolution_flip_is_caught(monkeypatch):
+    """Planting a flipped tap (true convolution instead of correlation) in the oracle
+    must break the hand-worked example."""
+    monkeypatch.setattr(ref, "tap", lambda dz, dy, dx: (1 - dz, 1 - dy, 1 - dx))
+    for cs in json.load(open(GOLDEN))["cases"][:2]:
+        c, f, w, b = _golden_inputs(cs)
+        got = ref.subm_conv3d(c, f, w, b, cs["res"])[:, 0]
+        assert not np.array_equal(got, cs["out"]), cs["name"]
+
+
+def test_planted_axis_swap_is_caught(monkeypatch):
+    """Planting a z/x swap of the tap axes in the oracle must break the example."""
+    monkeypatch.setattr(ref, "tap", lambda dz, dy, dx: (dx + 1, dy + 1, dz + 1))
+    for cs in json.load(open(GOLDEN))["cases"][:2]:
+        c, f, w, b = _golden_inputs(cs)
+        got = ref.subm_conv3d(c, f, w, b, cs["res"])[:, 0]
+        assert not np.array_equal(got, cs["out"]), cs["name"]
+
+
+def test_planted_offset_enumeration_mistake_is_caught(monkeypatch):
+    """Planting a reversed offset enumeration in the oracle must break the kernel map pin."""
+    monkeypatch.setattr(ref, "OFFSETS", ref.OFFSETS[::-1])
+    rng = np.random.default_rng(0)
+    c = random_set(rng, 4, 1, 20)
+    assert not np.array_equal(ref.kernel_map(c, 4), brute_force_nbr(c))

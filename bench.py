@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the submanifold convolution hot path on one B300 (or N replicas).
+
+One step = the whole path over one synthetic voxel set: subm3d_build_kmap
+(validate/pack, Morton radix sort, hash insert, 27-offset probe) followed by
+subm3d_forward (tcgen05 gather-GEMM with fused bias). Default workload: the
+1024^3 grid with 16 ellipsoid/torus shells (~2.9 M voxels), I = O = 64, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py --impl reference ...      # the CPU oracle, as the reference arm
+
+Prints one JSON line (rank 0). `value` = effective TFLOP/s of the whole step,
+2 * pairs * I * O / step time, summed over ranks (replicas: every rank runs the
+full workload). Inputs are resident in HBM before timing; they are larger than L2,
+so L2 is not flushed between steps. `e2e` repeats the measurement through the
+Python API with pinned-host inputs copied in and the output copied back every step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SubMConv3d bf16 TFLOP/s & Mvoxels/s (fraction of roofline); kmap build ms"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+CPU_SAMPLE_VOXELS = 1_000_000      # oracle CPU baseline: first 1 M voxels (raster order)
+REF_STEP_VOXELS = 20_000           # reference arm: voxels per step
+PROFILE = os.path.join(ROOT, "profiles", "fwd_tc_shells16_1024.md")
+KERNEL_SRC = os.path.join(ROOT, "submanifold_sparse_convolution_04_b300", "csrc", "forward_tc.cu")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--order", default="raster", choices=["raster", "shuffled"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(case, P):
+    cfg = case
+    return {"workload": f"{cfg['name']}: res {cfg['res']}^3, N={cfg['coords'].shape[0]}, "
+                        f"I={cfg['I']}, O={cfg['O']}, {cfg['dtype']}",
+            "name": cfg["name"], "res": cfg["res"], "N": int(cfg["coords"].shape[0]),
+            "pairs": None if P is None else int(P), "I": cfg["I"], "O": cfg["O"],
+            "order": cfg["info"]["order"]}
+
+
+# ------------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (x itself for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------- roofline
+
+def recorded_traffic():
+    """dram bytes per forward launch from the committed ncu summary, if it was taken on
+    the current kernel source (sha256 of forward_tc.cu recorded beside the number)."""
+    if not os.path.exists(PROFILE):
+        return None, "no ncu summary"
+    text = open(PROFILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"forward_tc_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None, "ncu summary has no traffic line"
+    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    if h.group(1) != cur:
+        return None, "kernel changed since the ncu capture"
+    return float(m.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum"
+
+
+def roofline(N, P, I, O, fwd_s, peaks, peak_kind):
+    e = 2
+    gathered = P * I * e + N * O * e + 108 * N + 27 * I * O * e
+    compulsory = N * I * e + N * O * e + 108 * N + 27 * I * O * e
+    flops = 2.0 * P * I * O
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks["bf16_tflops"])
+    achieved = gathered / fwd_s / 1e9
+    t_roof = max(flops / (tc * 1e12), gathered / (hbm * 1e9))
+    traffic, traffic_src = recorded_traffic()
+    return {
+        "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "frac": achieved / hbm, "traffic": traffic, "peak_source": f"hbm_gbs, {peak_kind}",
+        "algorithmic_bytes": gathered, "traffic_source": traffic_src,
+        "compulsory_bytes": compulsory, "compulsory_frac": compulsory / fwd_s / 1e9 / hbm,
+        "tensor_tflops": flops / fwd_s / 1e12, "tensor_frac": flops / fwd_s / 1e12 / tc,
+        "roofline_time_us": t_roof * 1e6, "roofline_frac": t_roof / fwd_s,
+    }
+
+
+# ------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(case, start, count):
+    """A bounded sample: the voxels [start, start+count) in raster order (a slab of the
+    grid) as a problem of its own, and its pair count from the oracle's kernel map."""
+    from oracle import cpu
+    N = case["coords"].shape[0]
+    a, b = start % N, min(start % N + count, N)
+    sub = case["coords"][a:b]
+    P = int((cpu.kernel_map(sub, case["res"]) >= 0).sum())
+    return sub, case["feats"][a:b], P
+
+
+def time_oracle(case, sub, feats, P):
+    from oracle import cpu
+    t0 = time.perf_counter()
+    cpu.forward_rows(sub, feats, case["weight"], case["bias"], case["res"])
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * P * case["I"] * case["O"]
+
+
+def cpu_baseline(case):
+    from oracle import cpu
+    sub, feats, P = oracle_sample(case, 0, CPU_SAMPLE_VOXELS)
+    dt, flops = time_oracle(case, sub, feats, P)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu.threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"C++ oracle (std::unordered_map + fp64 triple loop, OpenMP) on the first "
+                      f"{sub.shape[0]} voxels in raster order as a voxel set of their own "
+                      f"({P} pairs): map build + every output row"}
+
+
+# ------------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from oracle import cpu
+    from synth import make_case
+    case = make_case(args.workload, args.order)
+    steps = []
+    for s in range(args.warmup + args.steps):
+        steps.append(oracle_sample(case, s * REF_STEP_VOXELS, REF_STEP_VOXELS))
+    times, flops = [], []
+    for s, (sub, feats, P) in enumerate(steps):
+        dt, fl = time_oracle(case, sub, feats, P)
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    total = sum(times)
+    value = sum(flops) / total / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": dict(workload_desc(case, None), parallelism="1 process, host cores"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu.threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: the C++ oracle on {REF_STEP_VOXELS} consecutive "
+                                   "voxels (raster order) as a voxel set of their own"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from submanifold_sparse_convolution_04_b300 import (subm3d_build_kmap, subm3d_forward,
+                                                        subm3d_forward_status,
+                                                        subm3d_kernel_launches,
+                                                        subm3d_kmap_workspace_bytes)
+    from synth import make_case
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = make_case(args.workload, args.order)
+    N, I, O, res = case["coords"].shape[0], case["I"], case["O"], case["res"]
+    bf16 = case["dtype"] == "bf16"
+
+    def host(name):
+        if bf16:
+            return torch.from_numpy(case[name + "_bits"].view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(case[name])
+
+    coords_h = torch.from_numpy(case["coords"]).pin_memory()
+    feats_h, weight_h, bias_h = (host(k).pin_memory() for k in ("feats", "weight", "bias"))
+    c = coords_h.to(dev)
+    f = feats_h.to(dev)
+    w = weight_h.to(dev)
+    b = bias_h.to(dev)
+    ws = torch.empty(subm3d_kmap_workspace_bytes(N), dtype=torch.uint8, device=dev)
+    nbr = torch.empty((N, 27), dtype=torch.int32, device=dev)
+    out = torch.empty((N, O), dtype=f.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
+        subm3d_forward(f, nbr, w, b, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    subm3d_forward_status()
+    P = int((nbr >= 0).sum().item())
+    flops = 2.0 * P * I * O
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = subm3d_kernel_launches()
+    e0.record(stream)
+    for s in range(K):
+        ev[s][0].record(stream)
+        subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
+        ev[s][1].record(stream)
+        subm3d_forward(f, nbr, w, b, out=out)
+        ev[s][2].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = subm3d_kernel_launches() - launches0
+    clk = clocks.stop()
+    barrier(world)
+    subm3d_forward_status()
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    kmap_ms = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(K))
+    fwd_ms = statistics.mean(ev[s][1].elapsed_time(ev[s][2]) for s in range(K))
+    ms_per_step = total_ms / K
+    value = world * flops / (ms_per_step / 1e3) / 1e12
+
+    # end to end through the Python API: pinned host -> device, path, device -> host
+    out_h = torch.empty((N, O), dtype=f.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (coords_h, feats_h, weight_h, bias_h))
+    d2h = out_h.numel() * out_h.element_size()
+    cd, fd, wd, bd = (torch.empty_like(t, device=dev) for t in (coords_h, feats_h, weight_h, bias_h))
+
+    def e2e_step():
+        cd.copy_(coords_h, non_blocking=True)
+        fd.copy_(feats_h, non_blocking=True)
+        wd.copy_(weight_h, non_blocking=True)
+        bd.copy_(bias_h, non_blocking=True)
+        nb = subm3d_build_kmap(cd, res, workspace=ws)
+        o = subm3d_forward(fd, nb, wd, bd)
+        out_h.copy_(o, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world)
+    subm3d_forward_status()
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic",
+        "config": dict(workload_desc(case, P),
+                       l2="inputs larger than L2 (feats, nbr, hash table each > 126 MB); "
+                          "no flush between steps",
+                       parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "mvoxels_per_s": world * N / (ms_per_step / 1e3) / 1e6,
+        "kmap_ms": kmap_ms, "forward_us": fwd_ms * 1e3,
+        "forward_tflops": flops / (fwd_ms / 1e3) / 1e12,
+        "roofline": roof,
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+/*
+ * subm3d.h -- submanifold sparse 3D convolution (SubMConv3d: kernel 3, stride 1,
+ * no padding) for NVIDIA B300 (sm_103a). C ABI of libsubm3d.so.
+ *
+ * What is computed (sources are the pages' titles and sections):
+ *   "pixal3d_mrp_mlx README", scope table "Scope, measured against the shared
+ *   core", and "pixal3d_mrp_mlx CLAUDE.md", "Measured facts": every SparseConv3d
+ *   of the decoders is (c, out, 3) with stride 1 and no padding, which dispatches
+ *   to the submanifold convolution; the README's introduction calls it the
+ *   expensive part of the sparse decoders. Outputs exist only at the active input
+ *   voxels:
+ *
+ *     out[i, o] = bias[o] + sum_{k : nbr[i,k] >= 0} sum_c W[o, kz, ky, kx, c] * feats[nbr[i,k], c]
+ *
+ *   with k = 9 (dz+1) + 3 (dy+1) + (dx+1) for the neighbour offset (dz, dy, dx) in
+ *   {-1, 0, 1}^3 and (kz, ky, kx) = (dz+1, dy+1, dx+1) (cross-correlation, as a
+ *   dense Conv3d). The weight layout [O, kz, ky, kx, I] with channels-last
+ *   features is the one the README's commit header gives for the checkpoints.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory; scratch space is the caller's `workspace`.
+ *   - Arrays are dense row-major ("contiguous"); every pointer must be 16-byte
+ *     aligned. Row strides are exactly the logical widths given.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *     enqueued on it; subm3d_build_kmap additionally waits for it (see there).
+ *   - Every call returns a subm3d_status. On failure, subm3d_last_error() gives a
+ *     message (thread-local, valid until this thread's next call into the
+ *     library) that names the argument and its value.
+ *   - One process, one GPU: the calls use the current CUDA device.
+ */
+#ifndef SUBM3D_H
+#define SUBM3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SUBM3D_API __attribute__((visibility("default")))
+#else
+#define SUBM3D_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SUBM3D_OK = 0,
+  SUBM3D_ERR_ARG = -1,          /* a host-side argument check failed                    */
+  SUBM3D_ERR_COORD_RANGE = -2,  /* a coordinate outside 0 <= z,y,x < res or 0 <= b <= 65534 */
+  SUBM3D_ERR_DUPLICATE = -3,    /* two input rows share one (b, z, y, x)                */
+  SUBM3D_ERR_HASH_FULL = -4,    /* a hash insert or lookup exceeded its probe limit     */
+  SUBM3D_ERR_CUDA = -5,         /* a CUDA runtime call failed (message has the code)    */
+  SUBM3D_ERR_UNSUPPORTED = -6,  /* valid but unsupported shape / dtype combination      */
+  SUBM3D_ERR_WORKSPACE = -7,    /* workspace too small or misaligned                    */
+  SUBM3D_ERR_DEVICE = -8        /* a kernel recorded an error: a bounded wait ran out,
+                                   or nbr held an index outside [-1, N)                 */
+} subm3d_status;
+
+typedef enum { SUBM3D_F32 = 0, SUBM3D_BF16 = 1 } subm3d_dtype;
+
+/* Largest accepted grid side and batch index. */
+#define SUBM3D_MAX_RES 65535
+#define SUBM3D_MAX_BATCH 65534
+
+/*
+ * Workspace bytes that subm3d_build_kmap needs for N voxels (default hash
+ * capacity: the smallest power of two >= 2N, at least 64 slots). Host-only, no CUDA
+ * call. Returns 0 for N < 0.
+ */
+SUBM3D_API size_t subm3d_kmap_workspace_bytes(int64_t N);
+
+/* Same, for an explicit hash capacity (a power of two >= 8; 0 = the default). */
+SUBM3D_API size_t subm3d_kmap_workspace_bytes_ex(int64_t N, int64_t hash_capacity);
+
+/*
+ * Kernel map (neighbour table) of an active voxel set.
+ *
+ * The pages define the operation as submanifold (outputs only at active sites),
+ * which needs, per active voxel, the index of each of its 27 neighbours; the map
+ * is what the README's "spatial cache" lets several convolutions on one voxel set
+ * share.
+ *
+ *   coords    device int32 [N, 4], rows (b, z, y, x); 0 <= b <= 65534, 0 <= z,y,x < res.
+ *   N         number of active voxels, 0 <= N < 2^31. N = 0 is a no-op (OK).
+ *   res       grid side, 1 <= res <= 65535.
+ *   nbr       device int32 [N, 27], written: nbr[i, k] = index of the row of coords
+ *             at coords[i] + offset k (same batch item), or -1 if that voxel is not
+ *             active or lies outside [0, res)^3. Rows and values are in the caller's
+ *             input order. Bit-exact (the answer is unique).
+ *   workspace device scratch of at least subm3d_kmap_workspace_bytes(N) bytes,
+ *             256-byte aligned; its contents on entry do not matter.
+ *
+ * Steps (all CUDA kernels on `stream`): validate and pack each coordinate into a
+ * 64-bit key b<<48 | z<<32 | y<<16 | x; Morton-order the voxels (LSD radix sort
+ * of (b, interleaved z/y/x bits)); insert the keys into an open-addressing hash
+ * table with bounded linear probing; probe the 27 offsets per voxel with
+ * warp-cooperative lookups and coalesced writes of nbr.
+ *
+ * Synchronisation: the call waits for `stream` once, at its end, to read the
+ * device status word, so it is not capturable into a CUDA graph. Errors found on
+ * the device (COORD_RANGE, DUPLICATE, HASH_FULL) are returned by this same call;
+ * nbr is then unspecified.
+ */
+SUBM3D_API int subm3d_build_kmap(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * subm3d_build_kmap with two extras:
+ *   order          device int32 [N] or NULL. If given, receives the Morton order:
+ *                  order[s] = the input row at position s of the (b, Morton code)
+ *                  ascending sort (stable, so ties keep input order).
+ *   hash_capacity  0 for the default, else a power of two >= 8 (slots). A capacity
+ *                  below N makes the insert fail with SUBM3D_ERR_HASH_FULL.
+ */
+SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                         int32_t* order, int64_t hash_capacity, void* workspace,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Forward pass of the submanifold convolution (the formula at the top of this file).
+ *
+ *   feats   device [N, I] of `dtype`, channels-last.
+ *   nbr     device int32 [N, 27] as written by subm3d_build_kmap. An entry outside
+ *           [-1, N) is treated as absent and recorded as SUBM3D_ERR_DEVICE (see
+ *           subm3d_forward_status); it is never dereferenced.
+ *   weight  device [O, 3, 3, 3, I] of `dtype` (the checkpoints' [O, kz, ky, kx, I]).
+ *   bias    device [O] of `dtype`, or NULL for no bias.
+ *   out     device [N, O] of `dtype`, written once per row (no atomics, no
+ *           read-modify-write). Must not overlap the inputs.
+ *   dtype   SUBM3D_BF16: bf16 inputs, fp32 accumulation (tcgen05 tensor cores,
+ *           accumulator in tensor memory), bias added in fp32, output rounded to
+ *           bf16 (nearest-even). Needs I % 8 == 0 and O % 8 == 0; O <= 256 runs on
+ *           the tensor cores, larger O on the CUDA-core kernel.
+ *           SUBM3D_F32: fp32 inputs and accumulation on the CUDA cores.
+ *   N, I, O N >= 0 (0 is a no-op), 1 <= I, O <= 4096.
+ *
+ * Fully asynchronous: only host-side argument checks are reported by the return
+ * value. Device-side conditions are reported by subm3d_forward_status().
+ */
+SUBM3D_API int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight,
+                   const void* bias, void* out, int64_t N, int32_t I, int32_t O,
+                   subm3d_dtype dtype, cudaStream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the forward kernels' device error word:
+ * SUBM3D_OK, or SUBM3D_ERR_DEVICE (message says which condition: an nbr entry
+ * outside [-1, N), or a bounded pipeline wait that ran out). The word is shared by
+ * all streams of the process.
+ */
+SUBM3D_API int subm3d_forward_status(cudaStream_t stream);
+
+/* Thread-local message describing the last failure of this thread ("" if none). */
+SUBM3D_API const char* subm3d_last_error(void);
+
+/* Number of CUDA kernels this library has launched in this process (host counter). */
+SUBM3D_API int64_t subm3d_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SUBM3D_H */

@@ -1,0 +1,19 @@
+"""Submanifold sparse 3D convolution (SubMConv3d: kernel 3, stride 1, no padding)
+for NVIDIA B300 (sm_103a).
+
+The convolution runs in libsubm3d.so (CUDA kernels behind the C ABI of
+include/subm3d.h); this package is its Python binding, with the same names:
+
+    nbr = subm3d_build_kmap(coords, res)                 # int32 [N, 27]
+    out = subm3d_forward(feats, nbr, weight, bias)       # [N, O]
+
+coords int32 [N, 4] (b, z, y, x); feats [N, I] bf16 or fp32 (channels-last);
+weight [O, 3, 3, 3, I] ([O, kz, ky, kx, I]); bias [O] or None.
+"""
+from ._binding import (BF16, F32, LIB_PATH, Subm3dError, lib, subm3d_build_kmap,
+                       subm3d_build_kmap_ex, subm3d_forward, subm3d_forward_status,
+                       subm3d_kernel_launches, subm3d_kmap_workspace_bytes, subm3d_last_error)
+
+__all__ = ["BF16", "F32", "LIB_PATH", "Subm3dError", "lib", "subm3d_build_kmap",
+           "subm3d_build_kmap_ex", "subm3d_forward", "subm3d_forward_status",
+           "subm3d_kernel_launches", "subm3d_kmap_workspace_bytes", "subm3d_last_error"]

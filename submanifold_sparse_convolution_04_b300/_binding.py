@@ -1,0 +1,162 @@
+"""ctypes binding of libsubm3d.so (include/subm3d.h). Argument marshalling only:
+every step of the convolution runs in the library's CUDA kernels; PyTorch supplies
+device memory and the current stream. There is no other code path: if the library
+is missing or the tensors are not on a CUDA device, the calls raise."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsubm3d.so")
+
+OK, ERR_ARG, ERR_COORD_RANGE, ERR_DUPLICATE, ERR_HASH_FULL, ERR_CUDA, ERR_UNSUPPORTED, \
+    ERR_WORKSPACE, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7, -8
+F32, BF16 = 0, 1
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_COORD_RANGE", -3: "ERR_DUPLICATE", -4: "ERR_HASH_FULL",
+          -5: "ERR_CUDA", -6: "ERR_UNSUPPORTED", -7: "ERR_WORKSPACE", -8: "ERR_DEVICE"}
+
+_lib = None
+
+
+class Subm3dError(RuntimeError):
+    """A libsubm3d call returned a non-zero status."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_NAMES.get(code, code)}: {message}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m submanifold_sparse_convolution_04_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        L.subm3d_kmap_workspace_bytes.argtypes = [i64]
+        L.subm3d_kmap_workspace_bytes.restype = sz
+        L.subm3d_kmap_workspace_bytes_ex.argtypes = [i64, i64]
+        L.subm3d_kmap_workspace_bytes_ex.restype = sz
+        L.subm3d_build_kmap.argtypes = [vp, i64, i32, vp, vp, sz, vp]
+        L.subm3d_build_kmap.restype = ctypes.c_int
+        L.subm3d_build_kmap_ex.argtypes = [vp, i64, i32, vp, vp, i64, vp, sz, vp]
+        L.subm3d_build_kmap_ex.restype = ctypes.c_int
+        L.subm3d_forward.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, vp]
+        L.subm3d_forward.restype = ctypes.c_int
+        L.subm3d_forward_status.argtypes = [vp]
+        L.subm3d_forward_status.restype = ctypes.c_int
+        L.subm3d_last_error.argtypes = []
+        L.subm3d_last_error.restype = ctypes.c_char_p
+        L.subm3d_kernel_launches.argtypes = []
+        L.subm3d_kernel_launches.restype = ctypes.c_int64
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise Subm3dError(rc, subm3d_last_error())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def subm3d_last_error() -> str:
+    return lib().subm3d_last_error().decode()
+
+
+def subm3d_kernel_launches() -> int:
+    return int(lib().subm3d_kernel_launches())
+
+
+def subm3d_kmap_workspace_bytes(N: int, hash_capacity: int = 0) -> int:
+    if hash_capacity:
+        return int(lib().subm3d_kmap_workspace_bytes_ex(N, hash_capacity))
+    return int(lib().subm3d_kmap_workspace_bytes(N))
+
+
+def _workspace(N, hash_capacity, workspace, device):
+    need = subm3d_kmap_workspace_bytes(N, hash_capacity)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, _dev(workspace, "workspace", torch.uint8), workspace.numel()
+
+
+def subm3d_build_kmap(coords: torch.Tensor, res: int, nbr: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """nbr int32 [N, 27] of the voxel set coords int32 [N, 4] (b, z, y, x)."""
+    N = coords.shape[0]
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    if nbr is None:
+        nbr = torch.empty((N, 27), dtype=torch.int32, device=coords.device)
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    workspace, pw, nbytes = _workspace(N, 0, workspace, coords.device)
+    _check(lib().subm3d_build_kmap(pc, N, int(res), pn, pw, nbytes, _stream(stream)))
+    return nbr
+
+
+def subm3d_build_kmap_ex(coords: torch.Tensor, res: int, nbr: torch.Tensor | None = None,
+                         order: torch.Tensor | bool | None = None, hash_capacity: int = 0,
+                         workspace: torch.Tensor | None = None, stream=None):
+    """(nbr, order): order int32 [N] is the Morton order if requested (order=True or a
+    tensor), else None."""
+    N = coords.shape[0]
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    if nbr is None:
+        nbr = torch.empty((N, 27), dtype=torch.int32, device=coords.device)
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    if order is True:
+        order = torch.empty(N, dtype=torch.int32, device=coords.device)
+    elif order is False:
+        order = None
+    po = None if order is None else _dev(order, "order", torch.int32, (N,))
+    workspace, pw, nbytes = _workspace(N, hash_capacity, workspace, coords.device)
+    _check(lib().subm3d_build_kmap_ex(pc, N, int(res), pn, po, int(hash_capacity), pw, nbytes,
+                                      _stream(stream)))
+    return nbr, order
+
+
+def subm3d_forward(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tensor,
+                   bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """out [N, O] = submanifold convolution of feats [N, I] with weight [O, 3, 3, 3, I]."""
+    if feats.dtype not in _DTYPES:
+        raise ValueError(f"feats dtype {feats.dtype} is not float32 or bfloat16")
+    N, I = feats.shape
+    O = weight.shape[0]
+    pf = _dev(feats, "feats")
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    pw = _dev(weight, "weight", feats.dtype, (O, 3, 3, 3, I))
+    pb = None if bias is None else _dev(bias, "bias", feats.dtype, (O,))
+    if out is None:
+        out = torch.empty((N, O), dtype=feats.dtype, device=feats.device)
+    po = _dev(out, "out", feats.dtype, (N, O))
+    _check(lib().subm3d_forward(pf, pn, pw, pb, po, N, I, O, _DTYPES[feats.dtype],
+                                _stream(stream)))
+    return out
+
+
+def subm3d_forward_status(stream=None) -> None:
+    """Waits for the stream and raises Subm3dError if a forward kernel recorded an error."""
+    _check(lib().subm3d_forward_status(_stream(stream)))

@@ -1,0 +1,116 @@
+// C-ABI entry points of libsubm3d.so (declared in include/subm3d.h): host-side
+// argument checks, the thread-local error message, the launch counter, and
+// dispatch to the kernel-map and forward launchers.
+#include <cstdarg>
+
+#include "common.cuh"
+
+namespace subm3d {
+
+namespace {
+thread_local char g_msg[512] = "";
+std::atomic<int64_t> g_launches{0};
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+void clear_error() { g_msg[0] = '\0'; }
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace subm3d
+
+using namespace subm3d;
+
+extern "C" {
+
+size_t subm3d_kmap_workspace_bytes(int64_t N) { return kmap_workspace_bytes(N, 0); }
+
+size_t subm3d_kmap_workspace_bytes_ex(int64_t N, int64_t hash_capacity) {
+  if (hash_capacity < 0) return 0;
+  return kmap_workspace_bytes(N, hash_capacity);
+}
+
+int subm3d_build_kmap(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  clear_error();
+  return kmap_build(coords, N, res, nbr, nullptr, 0, workspace, ws_bytes, stream);
+}
+
+int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                         int32_t* order, int64_t hash_capacity, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
+  clear_error();
+  return kmap_build(coords, N, res, nbr, order, hash_capacity, workspace, ws_bytes, stream);
+}
+
+int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
+                   void* out, int64_t N, int32_t I, int32_t O, subm3d_dtype dtype,
+                   cudaStream_t stream) {
+  clear_error();
+  if (N < 0 || N > 0x7FFFFFFFll) {
+    set_error("subm3d_forward: N=%lld outside [0, 2^31)", (long long)N);
+    return SUBM3D_ERR_ARG;
+  }
+  if (I < 1 || I > 4096 || O < 1 || O > 4096) {
+    set_error("subm3d_forward: I=%d, O=%d must lie in [1, 4096]", I, O);
+    return SUBM3D_ERR_ARG;
+  }
+  if (dtype != SUBM3D_F32 && dtype != SUBM3D_BF16) {
+    set_error("subm3d_forward: unknown dtype %d", static_cast<int>(dtype));
+    return SUBM3D_ERR_ARG;
+  }
+  if (N == 0) return SUBM3D_OK;
+  if (!feats || !nbr || !weight || !out) {
+    set_error("subm3d_forward: NULL pointer (feats=%p nbr=%p weight=%p out=%p)", feats,
+              (const void*)nbr, weight, out);
+    return SUBM3D_ERR_ARG;
+  }
+  const uintptr_t any = reinterpret_cast<uintptr_t>(feats) | reinterpret_cast<uintptr_t>(nbr) |
+                        reinterpret_cast<uintptr_t>(weight) | reinterpret_cast<uintptr_t>(out) |
+                        reinterpret_cast<uintptr_t>(bias);
+  if (any & 15) {
+    set_error("subm3d_forward: feats=%p nbr=%p weight=%p bias=%p out=%p must be 16-byte aligned",
+              feats, (const void*)nbr, weight, bias, out);
+    return SUBM3D_ERR_ARG;
+  }
+  if (dtype == SUBM3D_BF16) {
+    if (I % 8 || O % 8) {
+      set_error("subm3d_forward: bf16 needs I %% 8 == 0 and O %% 8 == 0 (got I=%d, O=%d)", I, O);
+      return SUBM3D_ERR_UNSUPPORTED;
+    }
+    if (O <= 256)
+      return forward_launch_tc(static_cast<const __nv_bfloat16*>(feats), nbr,
+                               static_cast<const __nv_bfloat16*>(weight),
+                               static_cast<const __nv_bfloat16*>(bias),
+                               static_cast<__nv_bfloat16*>(out), N, I, O, stream);
+  }
+  return forward_launch_simt(feats, nbr, weight, bias, out, N, I, O, dtype, stream);
+}
+
+int subm3d_forward_status(cudaStream_t stream) {
+  clear_error();
+  SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
+  int* word = forward_error_word();
+  if (!word) {
+    set_error("subm3d_forward_status: device error word not available");
+    return SUBM3D_ERR_CUDA;
+  }
+  int host = 0;
+  const int zero = 0;
+  SUBM3D_CUDA_TRY(cudaMemcpy(&host, word, sizeof(int), cudaMemcpyDeviceToHost));
+  SUBM3D_CUDA_TRY(cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  if (host == 0) return SUBM3D_OK;
+  set_error("subm3d_forward: device reported%s%s", (host & kDevErrBadNbr) ? " an nbr entry outside [-1, N)" : "",
+            (host & kDevErrTimeout) ? " a pipeline wait that ran out (kernel stopped early)" : "");
+  return SUBM3D_ERR_DEVICE;
+}
+
+const char* subm3d_last_error(void) { return g_msg; }
+
+int64_t subm3d_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

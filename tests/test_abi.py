@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/subm3d.h declares, and host-side argument checks return before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from submanifold_sparse_convolution_04_b300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "subm3d.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SUBM3D_API\s+[\w\s\*]+?\b(subm3d_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from submanifold_sparse_convolution_04_b300.build import build
+    build()
+    return B.lib()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("subm3d_build_kmap", "subm3d_forward", "subm3d_kmap_workspace_bytes",
+                 "subm3d_last_error"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read().split()
+    exported = sorted(s for s in out if s.startswith("subm3d_"))
+    assert exported == declared_symbols()
+
+
+def test_workspace_bytes_host_only(L):
+    assert L.subm3d_kmap_workspace_bytes(-1) == 0
+    w0 = L.subm3d_kmap_workspace_bytes(0)
+    w1 = L.subm3d_kmap_workspace_bytes(1000)
+    w2 = L.subm3d_kmap_workspace_bytes(3_000_000)
+    assert 0 < w0 < w1 < w2
+    # table (16 B x 8M slots) + keys + two sort buffers + indices dominate at 3 M voxels
+    assert 3_000_000 * (8 * 3 + 4 * 2) + 16 * (1 << 23) <= w2 < 1.1 * (3_000_000 * 32 + 16 * (1 << 23)) + (1 << 22)
+    assert L.subm3d_kmap_workspace_bytes_ex(1000, 64) < w1
+    assert L.subm3d_kmap_workspace_bytes_ex(1000, 0) == w1
+
+
+def test_empty_inputs_are_noops(L):
+    assert L.subm3d_build_kmap(None, 0, 16, None, None, 0, None) == B.OK
+    assert L.subm3d_forward(None, None, None, None, None, 0, 32, 32, B.BF16, None) == B.OK
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, -1, 16, None, None, 0, None), B.ERR_ARG),               # N < 0
+    ((None, 10, 0, None, None, 0, None), B.ERR_ARG),                # res < 1
+    ((None, 10, 65536, None, None, 0, None), B.ERR_ARG),            # res too large
+    ((None, 10, 16, None, None, 0, None), B.ERR_ARG),               # NULL pointers
+    ((16, 10, 16, 24, 256, 1 << 20, None), B.ERR_ARG),              # nbr not 16-byte aligned
+    ((16, 10, 16, 32, 128, 1 << 20, None), B.ERR_WORKSPACE),        # workspace not 256-aligned
+    ((16, 10, 16, 32, 256, 100, None), B.ERR_WORKSPACE),            # workspace too small
+])
+def test_build_kmap_argument_errors(L, args, code):
+    vp = [ctypes.c_void_p(a) if isinstance(a, int) and i in (0, 3, 4) else a
+          for i, a in enumerate(args)]
+    assert L.subm3d_build_kmap(*vp) == code
+    assert B.subm3d_last_error()
+
+
+def test_build_kmap_ex_capacity_checks(L):
+    p = ctypes.c_void_p
+    for cap in (-8, 3, 12, 1 << 41):
+        assert L.subm3d_build_kmap_ex(p(16), 10, 16, p(32), None, cap, p(256), 1 << 20, None) == B.ERR_ARG
+
+
+@pytest.mark.parametrize("N,I,O,dtype,code", [
+    (-1, 32, 32, B.BF16, B.ERR_ARG), (10, 0, 32, B.BF16, B.ERR_ARG), (10, 32, 5000, B.F32, B.ERR_ARG),
+    (10, 32, 32, 7, B.ERR_ARG), (10, 12, 32, B.BF16, B.ERR_UNSUPPORTED),
+    (10, 32, 20, B.BF16, B.ERR_UNSUPPORTED)])
+def test_forward_argument_errors(L, N, I, O, dtype, code):
+    p = ctypes.c_void_p
+    assert L.subm3d_forward(p(256), p(512), p(768), None, p(1024), N, I, O, dtype, None) == code
+
+
+def test_forward_null_and_alignment(L):
+    p = ctypes.c_void_p
+    assert L.subm3d_forward(None, p(512), p(768), None, p(1024), 10, 32, 32, B.BF16, None) == B.ERR_ARG
+    assert L.subm3d_forward(p(256), p(512), p(768), p(8), p(1024), 10, 32, 32, B.BF16, None) == B.ERR_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    from submanifold_sparse_convolution_04_b300 import subm3d_build_kmap, subm3d_forward
+    with pytest.raises(ValueError):
+        subm3d_build_kmap(torch.zeros((4, 4), dtype=torch.int32), 8)
+    with pytest.raises(ValueError):
+        subm3d_forward(torch.zeros((4, 8)), torch.zeros((4, 27), dtype=torch.int32),
+                       torch.zeros((8, 3, 3, 3, 8)))

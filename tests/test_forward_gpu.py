@@ -1,0 +1,181 @@
+"""Forward pass on the GPU against the CPU oracle (float64), within max|err| <=
+1e-4 max|ref| (fp32) and 2e-2 max|ref| (bf16; the tests also hold bf16 to a tighter
+4e-3). Small workloads are compared on every element; the full-size workloads on
+sampled rows (tile edges, the ragged last tile, random rows), in the same launch
+configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import cpu, ref
+from submanifold_sparse_convolution_04_b300 import (Subm3dError, subm3d_build_kmap,
+                                                    subm3d_forward, subm3d_forward_status,
+                                                    subm3d_kernel_launches)
+from submanifold_sparse_convolution_04_b300 import _binding as B
+from synth import ellipsoid_shell, make_values, union_coords, uniform_rotation
+from tests.conftest import cached_case
+from tests.gpu_util import assert_close, bf16_tensor, require_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def run(case, dev, rows=None):
+    c, f, w, b = to_device(case, dev)
+    nbr = subm3d_build_kmap(c, case["res"])
+    out = subm3d_forward(f, nbr, w, b)
+    subm3d_forward_status()
+    out = out.float().cpu().numpy()
+    return out if rows is None else out[rows]
+
+
+def sample_rows(N, seed, n_random=1500):
+    rng = np.random.default_rng(seed)
+    edges = [r for t in range(0, N, 128) for r in (t, t + 127) if r < N][:400]
+    tail = list(range(max(0, N - 300), N))
+    rows = np.unique(np.concatenate([rng.integers(0, N, n_random), edges, tail]))
+    return rows.astype(np.int64)
+
+
+@pytest.mark.parametrize("cfg_id", [1, 2])
+def test_forward_small_workloads_every_element(dev, cfg_id):
+    case = cached_case(cfg_id)
+    got = run(case, dev)
+    want = ref.subm_conv3d(case["coords"], case["feats"], case["weight"], case["bias"], case["res"])
+    assert_close(got, want, case["dtype"], case["name"])
+
+
+@pytest.mark.parametrize("cfg_id", [3, 4, 5])
+def test_forward_full_workloads_sampled(dev, cfg_id):
+    case = cached_case(cfg_id)
+    N = case["coords"].shape[0]
+    rows = sample_rows(N, cfg_id)
+    got = run(case, dev, rows)
+    want = cpu.forward_rows(case["coords"], case["feats"], case["weight"], case["bias"],
+                            case["res"], rows=rows)
+    assert_close(got, want, case["dtype"], case["name"])
+
+
+def test_forward_shuffled_order(dev):
+    case = cached_case(4, "shuffled")
+    rows = sample_rows(case["coords"].shape[0], 44, 800)
+    got = run(case, dev, rows)
+    want = cpu.forward_rows(case["coords"], case["feats"], case["weight"], case["bias"],
+                            case["res"], rows=rows)
+    assert_close(got, want, "bf16", "shuffled")
+
+
+def shell_case(seed, res, I, O, dtype, batch=1):
+    rng = np.random.default_rng(seed)
+    parts = []
+    for b in range(batch):
+        a = res * (0.2 + 0.15 * rng.random(3))
+        parts.append((b, ellipsoid_shell(res, res / 2 + rng.random(3), a, uniform_rotation(rng))))
+    coords = union_coords(parts, res)
+    v = make_values(coords.shape[0], I, O, dtype, seed)
+    return coords, v
+
+
+@pytest.mark.parametrize("I,O", [(16, 16), (32, 64), (64, 32), (96, 96), (128, 256), (256, 128),
+                                 (8, 8), (24, 40), (72, 136), (264, 48), (64, 256), (256, 256),
+                                 (40, 264), (8, 520)])
+def test_forward_bf16_shapes(dev, I, O):
+    coords, v = shell_case(I * 7 + O, 40, I, O, "bf16", batch=2)
+    N = coords.shape[0]
+    assert N % 128 != 0
+    c = torch.from_numpy(coords).to(dev)
+    nbr = subm3d_build_kmap(c, 40)
+    use_bias = (I + O) % 3 != 0
+    out = subm3d_forward(bf16_tensor(v["feats"], dev), nbr, bf16_tensor(v["weight"], dev),
+                         bf16_tensor(v["bias"], dev) if use_bias else None)
+    subm3d_forward_status()
+    rows = np.arange(N) if N * I * O < 3e8 else sample_rows(N, 1, 600)
+    want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"] if use_bias else None, 40,
+                            rows=rows)
+    assert_close(out.float().cpu().numpy()[rows], want, "bf16", f"I={I} O={O}")
+
+
+@pytest.mark.parametrize("I,O", [(32, 32), (16, 8), (3, 5), (64, 96), (1, 1), (130, 70)])
+def test_forward_fp32_shapes(dev, I, O):
+    coords, v = shell_case(I + 1000 * O, 24, I, O, "f32")
+    c = torch.from_numpy(coords).to(dev)
+    nbr = subm3d_build_kmap(c, 24)
+    out = subm3d_forward(torch.from_numpy(v["feats"]).to(dev), nbr,
+                         torch.from_numpy(v["weight"]).to(dev), torch.from_numpy(v["bias"]).to(dev))
+    subm3d_forward_status()
+    want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"], 24)
+    assert_close(out.cpu().numpy(), want, "f32", f"I={I} O={O}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_forward_tiny_and_isolated(dev, dtype):
+    # N = 1, then a handful of isolated voxels: only the centre tap contributes
+    for coords in (np.array([[0, 3, 3, 3]], np.int32),
+                   np.array([[0, 1, 1, 1], [0, 5, 5, 5], [1, 1, 1, 1], [2, 9, 0, 9]], np.int32)):
+        v = make_values(coords.shape[0], 64, 64, dtype, 5)
+        mk = (lambda a: bf16_tensor(a, dev)) if dtype == "bf16" else (lambda a: torch.from_numpy(a).to(dev))
+        nbr = subm3d_build_kmap(torch.from_numpy(coords).to(dev), 10)
+        out = subm3d_forward(mk(v["feats"]), nbr, mk(v["weight"]), mk(v["bias"]))
+        subm3d_forward_status()
+        want = v["feats"].astype(np.float64) @ v["weight"][:, 1, 1, 1, :].astype(np.float64).T + v["bias"]
+        assert_close(out.float().cpu().numpy(), want, dtype, "isolated")
+
+
+def test_forward_empty(dev):
+    f = torch.zeros((0, 64), dtype=torch.bfloat16, device=dev)
+    nbr = torch.zeros((0, 27), dtype=torch.int32, device=dev)
+    w = torch.zeros((64, 3, 3, 3, 64), dtype=torch.bfloat16, device=dev)
+    assert subm3d_forward(f, nbr, w).shape == (0, 64)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_forward_invalid_nbr_is_reported_not_dereferenced(dev, dtype):
+    coords, v = shell_case(9, 20, 32, 32, dtype)
+    N = coords.shape[0]
+    c = torch.from_numpy(coords).to(dev)
+    nbr = subm3d_build_kmap(c, 20)
+    bad = nbr.clone()
+    bad[5, 0] = N + 1000
+    bad[7, 26] = -7
+    mk = (lambda a: bf16_tensor(a, dev)) if dtype == "bf16" else (lambda a: torch.from_numpy(a).to(dev))
+    out = subm3d_forward(mk(v["feats"]), bad, mk(v["weight"]), mk(v["bias"]))
+    with pytest.raises(Subm3dError) as e:
+        subm3d_forward_status()
+    assert e.value.code == B.ERR_DEVICE
+    subm3d_forward_status()   # the word was cleared
+    # the bad entries were treated as absent
+    fixed = nbr.clone().cpu().numpy()
+    fixed[5, 0] = -1
+    fixed[7, 26] = -1
+    o2 = subm3d_forward(mk(v["feats"]), torch.from_numpy(fixed).to(dev), mk(v["weight"]), mk(v["bias"]))
+    subm3d_forward_status()
+    assert torch.equal(out, o2)
+
+
+def test_forward_is_deterministic_and_counts_launches(dev):
+    case = cached_case(2)
+    c, f, w, b = to_device(case, dev)
+    nbr = subm3d_build_kmap(c, case["res"])
+    n0 = subm3d_kernel_launches()
+    o1 = subm3d_forward(f, nbr, w, b)
+    o2 = subm3d_forward(f, nbr, w, b)
+    subm3d_forward_status()
+    assert subm3d_kernel_launches() - n0 == 2
+    assert torch.equal(o1, o2)
+
+
+def test_forward_on_side_stream(dev):
+    case = cached_case(2)
+    c, f, w, b = to_device(case, dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        nbr = subm3d_build_kmap(c, case["res"])
+        out = subm3d_forward(f, nbr, w, b)
+    subm3d_forward_status(s)
+    torch.cuda.synchronize()
+    want = ref.subm_conv3d(case["coords"], case["feats"], case["weight"], case["bias"], case["res"])
+    assert_close(out.float().cpu().numpy(), want, "bf16", "side stream")

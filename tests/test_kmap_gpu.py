@@ -1,0 +1,129 @@
+"""Kernel map on the GPU, bit-exact against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import cpu, ref
+from submanifold_sparse_convolution_04_b300 import (Subm3dError, subm3d_build_kmap,
+                                                    subm3d_build_kmap_ex,
+                                                    subm3d_kmap_workspace_bytes)
+from submanifold_sparse_convolution_04_b300 import _binding as B
+from tests.conftest import cached_case
+from tests.gpu_util import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def gpu_nbr(coords_np, res, dev, **kw):
+    c = torch.from_numpy(np.ascontiguousarray(coords_np, np.int32)).to(dev)
+    return subm3d_build_kmap(c, res, **kw).cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
+def test_kmap_bit_exact_on_workloads(dev, cfg_id):
+    case = cached_case(cfg_id)
+    got = gpu_nbr(case["coords"], case["res"], dev)
+    np.testing.assert_array_equal(got, cpu.kernel_map(case["coords"], case["res"]))
+
+
+@pytest.mark.parametrize("cfg_id", [2, 4])
+def test_kmap_bit_exact_shuffled_order(dev, cfg_id):
+    case = cached_case(cfg_id, "shuffled")
+    got = gpu_nbr(case["coords"], case["res"], dev)
+    np.testing.assert_array_equal(got, cpu.kernel_map(case["coords"], case["res"]))
+
+
+def random_set(rng, res, batch, n):
+    rows = []
+    for b in range(batch):
+        flat = rng.choice(res ** 3, size=n, replace=False)
+        z, rem = np.divmod(flat, res * res)
+        y, x = np.divmod(rem, res)
+        rows.append(np.stack([np.full(n, b), z, y, x], axis=1))
+    c = np.concatenate(rows).astype(np.int32)
+    return c[rng.permutation(c.shape[0])]
+
+
+@pytest.mark.parametrize("seed,res,batch,n", [(0, 4, 1, 1), (1, 3, 1, 27), (2, 5, 3, 70),
+                                               (3, 8, 2, 500), (4, 2, 4, 8), (5, 31, 1, 4000),
+                                               (6, 1, 5, 1), (7, 17, 7, 333)])
+def test_kmap_random_sets(dev, seed, res, batch, n):
+    rng = np.random.default_rng(seed)
+    c = random_set(rng, res, batch, n)
+    np.testing.assert_array_equal(gpu_nbr(c, res, dev), ref.kernel_map(c, res))
+
+
+def test_kmap_extreme_coordinates(dev):
+    res = 65535
+    c = np.array([[0, 0, 0, 0], [0, 65534, 65534, 65534], [0, 65533, 65534, 65534],
+                  [65534, 65534, 0, 1], [65534, 65534, 1, 1], [3, 1, 1, 1], [3, 0, 0, 0]],
+                 np.int32)
+    np.testing.assert_array_equal(gpu_nbr(c, res, dev), ref.kernel_map(c, res))
+
+
+def test_kmap_empty(dev):
+    c = torch.zeros((0, 4), dtype=torch.int32, device=dev)
+    assert subm3d_build_kmap(c, 16).shape == (0, 27)
+
+
+def test_kmap_morton_order(dev):
+    case = cached_case(3)
+    c = torch.from_numpy(case["coords"]).to(dev)
+    nbr, order = subm3d_build_kmap_ex(c, case["res"], order=True)
+    o = order.cpu().numpy()
+    assert np.array_equal(np.sort(o), np.arange(len(o)))
+    # Morton key written out independently: interleave bits of z, y, x (z highest of each triple)
+    co = case["coords"].astype(np.int64)
+    m = np.zeros(len(co), np.int64)
+    for t in range(8):
+        m |= ((co[:, 3] >> t) & 1) << (3 * t)
+        m |= ((co[:, 2] >> t) & 1) << (3 * t + 1)
+        m |= ((co[:, 1] >> t) & 1) << (3 * t + 2)
+    key = (co[:, 0] << 24) | m
+    want = np.lexsort((np.arange(len(co)), key))       # stable ascending order
+    np.testing.assert_array_equal(o, want)
+    np.testing.assert_array_equal(nbr.cpu().numpy(), cpu.kernel_map(case["coords"], case["res"]))
+
+
+def test_kmap_errors_and_recovery(dev):
+    good = np.array([[0, 1, 1, 1], [0, 1, 1, 2]], np.int32)
+    for bad, code in [
+        (np.array([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], np.int32), B.ERR_DUPLICATE),
+        (np.array([[0, 1, 1, 1], [0, 8, 0, 0]], np.int32), B.ERR_COORD_RANGE),
+        (np.array([[0, 1, 1, 1], [0, 0, -1, 0]], np.int32), B.ERR_COORD_RANGE),
+        (np.array([[-1, 1, 1, 1]], np.int32), B.ERR_COORD_RANGE),
+        (np.array([[65535, 1, 1, 1]], np.int32), B.ERR_COORD_RANGE),
+    ]:
+        with pytest.raises(Subm3dError) as e:
+            gpu_nbr(bad, 8, dev)
+        assert e.value.code == code
+        np.testing.assert_array_equal(gpu_nbr(good, 8, dev), ref.kernel_map(good, 8))
+
+
+def test_kmap_hash_full_is_reported(dev):
+    rng = np.random.default_rng(3)
+    c = torch.from_numpy(random_set(rng, 10, 1, 100)).to(dev)
+    with pytest.raises(Subm3dError) as e:
+        subm3d_build_kmap_ex(c, 10, hash_capacity=64)
+    assert e.value.code == B.ERR_HASH_FULL
+    # the smallest capacity that holds the set works, with long probe chains
+    nbr, _ = subm3d_build_kmap_ex(c, 10, hash_capacity=128)
+    np.testing.assert_array_equal(nbr.cpu().numpy(), ref.kernel_map(c.cpu().numpy(), 10))
+
+
+def test_kmap_reuses_dirty_workspace(dev):
+    case = cached_case(2)
+    c = torch.from_numpy(case["coords"]).to(dev)
+    ws = torch.full((subm3d_kmap_workspace_bytes(c.shape[0]),), 0xA5, dtype=torch.uint8, device=dev)
+    a = subm3d_build_kmap(c, case["res"], workspace=ws).cpu().numpy()
+    b = subm3d_build_kmap(c, case["res"], workspace=ws).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a, cpu.kernel_map(case["coords"], case["res"]))
+    with pytest.raises(Subm3dError) as e:
+        subm3d_build_kmap(c, case["res"], workspace=ws[:1024])
+    assert e.value.code == B.ERR_WORKSPACE

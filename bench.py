@@ -33,8 +33,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SubMConv3d bf16 TFLOP/s & Mvoxels/s (fraction of roofline); kmap build ms"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-CPU_SAMPLE_VOXELS = 1_000_000      # oracle CPU baseline: first 1 M voxels (raster order)
-REF_STEP_VOXELS = 20_000           # reference arm: voxels per step
+CPU_SAMPLE_VOXELS = 4_000_000      # oracle CPU baseline: up to the first 4 M voxels (raster order)
+REF_STEP_FLOPS = 2e9               # reference arm: ~2 GFLOP of oracle work per step
 PROFILE = os.path.join(ROOT, "profiles", "fwd_tc_shells16_1024.md")
 KERNEL_SRC = os.path.join(ROOT, "submanifold_sparse_convolution_04_b300", "csrc", "forward_tc.cu")
 
@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--max-voxels", type=int, default=0,
+                   help="keep only the first M voxels (raster order): a slab of the workload")
     return p.parse_args()
 
 
@@ -68,6 +70,19 @@ def workload_desc(case, P):
             "name": cfg["name"], "res": cfg["res"], "N": int(cfg["coords"].shape[0]),
             "pairs": None if P is None else int(P), "I": cfg["I"], "O": cfg["O"],
             "order": cfg["info"]["order"]}
+
+
+def load_case(args):
+    from synth import make_case
+    case = make_case(args.workload, args.order)
+    M = args.max_voxels
+    if M and M < case["coords"].shape[0]:
+        for k in ("coords", "feats", "feats_bits"):
+            if k in case:
+                case[k] = case[k][:M]
+        case["name"] += f"_first{M}"
+        case["info"] = dict(case["info"], N=M)
+    return case
 
 
 # ------------------------------------------------------------------------- distributed
@@ -240,11 +255,11 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from oracle import cpu
-    from synth import make_case
-    case = make_case(args.workload, args.order)
+    case = load_case(args)
+    per_step = max(256, int(REF_STEP_FLOPS / (2.0 * 11 * case["I"] * case["O"])))
     steps = []
     for s in range(args.warmup + args.steps):
-        steps.append(oracle_sample(case, s * REF_STEP_VOXELS, REF_STEP_VOXELS))
+        steps.append(oracle_sample(case, s * per_step, per_step))
     times, flops = [], []
     for s, (sub, feats, P) in enumerate(steps):
         dt, fl = time_oracle(case, sub, feats, P)
@@ -261,8 +276,9 @@ def run_reference(args, world, rank):
         "config": dict(workload_desc(case, None), parallelism="1 process, host cores"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu.threads(),
                          "kind": "oracle",
-                         "sample": f"each step: the C++ oracle on {REF_STEP_VOXELS} consecutive "
-                                   "voxels (raster order) as a voxel set of their own"},
+                         "sample": f"each step: the C++ oracle (map build + all rows, fp64) on "
+                                   f"{per_step} consecutive voxels (raster order) as a voxel "
+                                   "set of their own"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -276,13 +292,11 @@ def run_ours(args, world, rank, local):
                                                         subm3d_forward_status,
                                                         subm3d_kernel_launches,
                                                         subm3d_kmap_workspace_bytes)
-    from synth import make_case
-
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    case = make_case(args.workload, args.order)
+    case = load_case(args)
     N, I, O, res = case["coords"].shape[0], case["I"], case["O"], case["res"]
     bf16 = case["dtype"] == "bf16"
 

@@ -22,8 +22,11 @@
 // tile t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> one store per
 // element) while the tensor core works on tile t + 1.
 //
-// Warp roles (288 threads): warps 0-3 producers (thread 0 also issues the TMA),
-// warp 4 tensor-memory allocation + MMA issue (one lane), warps 5-8 epilogue.
+// Warp roles (320 threads): warps 0-3 producers (thread 0 also issues the weight
+// TMA), warp 4 tensor-memory allocation + MMA issue (one lane), warps 5-8 epilogue,
+// warp 9 stages each tile's 128 x 27 block of nbr (13.8 KB, contiguous in memory)
+// into a double-buffered shared-memory ring with one bulk async copy, a tile
+// ahead, so the producers never wait on a global load before issuing a gather.
 // Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the
 // device error word, stops the CTA's pipeline, drains what is in flight and
 // releases tensor memory before the CTA exits.
@@ -45,9 +48,11 @@ namespace {
 
 constexpr int kBM = 128;          // output rows per tile (tensor-memory lanes)
 constexpr int kKC = 64;           // channels per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 288;
+constexpr int kThreads = 320;
 constexpr int kProducerThreads = 128;
 constexpr int kMmaWarp = 4;
+constexpr int kNbrWarp = 9;
+constexpr int kNbrTileBytes = kBM * 27 * 4;   // one tile's rows of nbr
 constexpr int kSmemLimit = 227 * 1024;
 
 template <int NMMA>
@@ -55,10 +60,11 @@ struct Cfg {
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = NMMA * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kMisc = 1024 /*alignment slack*/ + 512 /*barriers*/ + 4 * 256 /*bias*/;
+  static constexpr int kMisc = 1024 /*alignment slack*/ + 2 * kNbrTileBytes /*nbr ring*/ +
+                               512 /*barriers*/ + 4 * 256 /*bias*/;
   static constexpr int kFit = (kSmemLimit - kMisc) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kLag = kStages >= 6 ? 4 : kStages - 2;   // cp.async groups in flight
+  static constexpr int kLag = kStages - 1;   // cp.async groups a producer keeps in flight
   static constexpr int kTmemCols = (2 * NMMA <= 32) ? 32 : (2 * NMMA <= 64) ? 64
                                  : (2 * NMMA <= 128) ? 128 : (2 * NMMA <= 256) ? 256 : 512;
   static constexpr int kSmemBytes = kMisc + kStages * kStageBytes;
@@ -118,14 +124,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sA = base;                              // S x 16 KB
   const uint32_t sB = base + S * C::kABytes;             // S x NMMA*128 B
-  uint8_t* misc = base_ptr + S * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);   // full[S], empty[S], accf[2], acce[2], drain
+  const uint32_t sNbr = base + S * C::kStageBytes;       // 2 x 13.8 KB
+  const int32_t* nbr_sm = reinterpret_cast<const int32_t*>(base_ptr + S * C::kStageBytes);
+  uint8_t* misc = base_ptr + S * C::kStageBytes + 2 * kNbrTileBytes;
+  // barriers: full[S], empty[S], accf[2], acce[2], drain, nbrf[2], nbre[2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
+  const uint32_t nbrf0 = drain + 8;
+  const uint32_t nbre0 = nbrf0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 9));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* bias_sm = reinterpret_cast<float*>(misc + 512);
 
@@ -141,13 +152,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
       mbar_init(acce0 + 8 * b, 128);
+      mbar_init(nbrf0 + 8 * b, 1);
+      mbar_init(nbre0 + 8 * b, kProducerThreads);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&wmap);
   }
-  if (tid >= 160) {
+  if (tid >= 160 && tid < 288) {
     for (int o = tid - 160; o < NMMA; o += 128)
       bias_sm[o] = (p.bias && o < p.O) ? __bfloat162float(p.bias[o]) : 0.f;
   }
@@ -164,18 +177,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producers
     const int q = tid & 7;          // 16-byte column chunk inside the 128-byte row
     const int rsub = tid >> 3;      // rows rsub + 16 m, m = 0..7
-    uint32_t g = 0;
+    uint32_t g = 0, lt = 0;
     bool bad = false, aborted = false;
-    for (int tile = blockIdx.x; tile < p.ntiles && !aborted; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < p.ntiles && !aborted; tile += gridDim.x, ++lt) {
       const int64_t row0 = int64_t(tile) * kBM;
+      const uint32_t nb = lt & 1u;
+      if (!mbar_wait(nbrf0 + 8 * nb, (lt >> 1) & 1u, abort_flag)) {
+        aborted = true;
+        break;
+      }
+      const int32_t* tile_nbr = nbr_sm + nb * (kBM * 27);
       for (int k = 0; k < 27 && !aborted; ++k) {
         int32_t j[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const int64_t i = row0 + rsub + 16 * m;
+          const int r = rsub + 16 * m;
           int32_t v = -1;
-          if (i < p.N) {
-            v = __ldg(p.nbr + i * 27 + k);
+          if (row0 + r < p.N) {
+            v = tile_nbr[r * 27 + k];
             if (v < -1 || v >= p.N) {
               bad = true;
               v = -1;
@@ -183,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           j[m] = v;
         }
+        if (k == 26) mbar_arrive(nbre0 + 8 * nb);   // this tile's nbr block is no longer read
         for (int c = 0; c < p.nchunks; ++c) {
           const uint32_t s = g % S;
           const uint32_t ph = (g / S) & 1u;
@@ -229,6 +249,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(full0 + 8 * (x % S), (x / S) & 1u);
       }
     }
+  } else if (warp == kNbrWarp) {
+    // ------------------------------------------------------------------ nbr staging
+    if (lane == 0) {
+      uint32_t lt = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++lt) {
+        const uint32_t nb = lt & 1u;
+        if (!mbar_wait(nbre0 + 8 * nb, ((lt >> 1) & 1u) ^ 1u, abort_flag)) {
+          aborted = true;
+          break;
+        }
+        const int64_t row0 = int64_t(tile) * kBM;
+        const int64_t rows = (p.N - row0) < kBM ? (p.N - row0) : kBM;
+        const uint32_t bytes = static_cast<uint32_t>(rows) * 108u;
+        const uint32_t bulk = bytes & ~15u;
+        int32_t* dst = const_cast<int32_t*>(nbr_sm) + nb * (kBM * 27);
+        for (uint32_t off = bulk; off < bytes; off += 4)   // ragged tail of the last tile
+          dst[off / 4] = __ldg(p.nbr + row0 * 27 + off / 4);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(nbrf0 + 8 * nb, bulk);
+        bulk_load(sNbr + nb * kNbrTileBytes, p.nbr + row0 * 27, bulk, nbrf0 + 8 * nb);
+      }
+      // every copy this warp issued has landed before the CTA may exit
+      const uint32_t issued = lt;
+      for (uint32_t x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
+        drain_wait(nbrf0 + 8 * (x & 1u), (x >> 1) & 1u);
+      if (aborted) {
+        *abort_flag = 1;
+        atomicOr(p.err, kDevErrTimeout);
+      }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
     if (lane == 0) {

@@ -136,6 +136,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Arrives on `bar` (counted in its expected count) once every cp.async this thread
+// issued so far has landed in shared memory; the thread itself does not wait.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA / tensor core) accesses.

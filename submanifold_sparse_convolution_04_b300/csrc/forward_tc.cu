@@ -12,7 +12,11 @@
 //   A = the 128 gathered neighbour rows, 64 channels each (16 KB), staged by 128
 //       producer threads with 16-byte cp.async (an absent neighbour, nbr = -1,
 //       zero-fills and reads nothing), written in the 128-byte-swizzled K-major
-//       layout the tensor core reads;
+//       layout the tensor core reads. Each producer marks the stage full with
+//       cp.async.mbarrier.arrive.noinc, so a slot counts as full the moment its
+//       rows land and no producer ever blocks on its own copies; the MMA thread
+//       orders those generic-proxy writes before its tensor-core reads with
+//       fence.proxy.async after the barrier wait;
 //   B = W_k[:, chunk] = weight[:, kz, ky, kx, chunk], an [O x 64] K-major tile (I is
 //       contiguous in the checkpoint layout, so no transpose), fetched by TMA with
 //       the same 128-byte swizzle; out-of-range rows/columns are zero-filled.
@@ -64,12 +68,10 @@ struct Cfg {
                                512 /*barriers*/ + 4 * 256 /*bias*/;
   static constexpr int kFit = (kSmemLimit - kMisc) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kLag = kStages - 1;   // cp.async groups a producer keeps in flight
   static constexpr int kTmemCols = (2 * NMMA <= 32) ? 32 : (2 * NMMA <= 64) ? 64
                                  : (2 * NMMA <= 128) ? 128 : (2 * NMMA <= 256) ? 256 : 512;
   static constexpr int kSmemBytes = kMisc + kStages * kStageBytes;
   static_assert(kStages >= 3, "pipeline too shallow");
-  static_assert(kLag >= 1 && kLag <= kStages - 1, "lag must leave a stage for the MMA");
 };
 
 struct Params {
@@ -225,21 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat16* src = ok ? p.feats + int64_t(j[m]) * p.I + col : p.feats;
             cp_async_16(dst, src, ok ? 16u : 0u);
           }
-          cp_async_commit();
-          if (g >= static_cast<uint32_t>(C::kLag)) {
-            cp_async_wait<C::kLag>();
-            fence_proxy_async_smem();
-            mbar_arrive(full0 + 8 * ((g - C::kLag) % S));
-          }
+          cp_async_arrive_noinc(full0 + 8 * s);   // stage s is full once these land
           ++g;
         }
       }
     }
-    // retire the stages still in flight (also after an abort, so their phases can complete)
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    for (uint32_t x = (g > static_cast<uint32_t>(C::kLag) ? g - C::kLag : 0u); x < g; ++x)
-      mbar_arrive(full0 + 8 * (x % S));
+    cp_async_wait_all();   // no gather of this thread is still landing when the CTA exits
     if (bad) atomicOr(p.err, kDevErrBadNbr);
     if (aborted) {
       *abort_flag = 1;

@@ -120,6 +120,26 @@ SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t re
                          size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Kernel map without any device allocation. The pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory themselves -- a host
+ * application that owns all device memory through its own pool and hands a plugin
+ * only its input and output buffers, or a latency-critical loop where an allocation,
+ * which may synchronise the device, is not acceptable.
+ *
+ * Same result and errors as subm3d_build_kmap (coords, N, res, nbr and stream as
+ * there), but the scratch space (hash table, sort buffers, status word) is a 9 MiB
+ * array compiled into the library, so N is limited to SUBM3D_NOALLOC_MAX_VOXELS; a
+ * larger N returns SUBM3D_ERR_ARG before any device work. Every GPU that loads the
+ * library keeps that array until the process exits. The first call on a device looks
+ * up the array's device address (make it before any stream capture). All calls
+ * share the one array: each call re-initialises what it reads, but calls that
+ * overlap on the GPU (from several host threads or streams) race on it.
+ */
+#define SUBM3D_NOALLOC_MAX_VOXELS 131072
+SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32_t res,
+                                         int32_t* nbr, cudaStream_t stream);
+
+/*
  * Forward pass of the submanifold convolution (the formula at the top of this file).
  *
  *   feats   device [N, I] of `dtype`, channels-last.

@@ -11,9 +11,9 @@ coords int32 [N, 4] (b, z, y, x); feats [N, I] bf16 or fp32 (channels-last);
 weight [O, 3, 3, 3, I] ([O, kz, ky, kx, I]); bias [O] or None.
 """
 from ._binding import (BF16, F32, LIB_PATH, Subm3dError, lib, subm3d_build_kmap,
-                       subm3d_build_kmap_ex, subm3d_forward, subm3d_forward_status,
+                       subm3d_build_kmap_ex, subm3d_build_kmap_noalloc, subm3d_forward, subm3d_forward_status,
                        subm3d_kernel_launches, subm3d_kmap_workspace_bytes, subm3d_last_error)
 
 __all__ = ["BF16", "F32", "LIB_PATH", "Subm3dError", "lib", "subm3d_build_kmap",
-           "subm3d_build_kmap_ex", "subm3d_forward", "subm3d_forward_status",
+           "subm3d_build_kmap_ex", "subm3d_build_kmap_noalloc", "subm3d_forward", "subm3d_forward_status",
            "subm3d_kernel_launches", "subm3d_kmap_workspace_bytes", "subm3d_last_error"]

@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
         L.subm3d_build_kmap.restype = ctypes.c_int
         L.subm3d_build_kmap_ex.argtypes = [vp, i64, i32, vp, vp, i64, vp, sz, vp]
         L.subm3d_build_kmap_ex.restype = ctypes.c_int
+        L.subm3d_build_kmap_noalloc.argtypes = [vp, i64, i32, vp, vp]
+        L.subm3d_build_kmap_noalloc.restype = ctypes.c_int
         L.subm3d_forward.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, vp]
         L.subm3d_forward.restype = ctypes.c_int
         L.subm3d_forward_status.argtypes = [vp]
@@ -135,6 +137,17 @@ def subm3d_build_kmap_ex(coords: torch.Tensor, res: int, nbr: torch.Tensor | Non
     _check(lib().subm3d_build_kmap_ex(pc, N, int(res), pn, po, int(hash_capacity), pw, nbytes,
                                       _stream(stream)))
     return nbr, order
+
+
+def subm3d_build_kmap_noalloc(coords: torch.Tensor, res: int, nbr: torch.Tensor,
+                              stream=None) -> torch.Tensor:
+    """nbr int32 [N, 27] of coords int32 [N, 4], written into the caller's nbr, with the
+    library's built-in scratch instead of a workspace (N <= 131072). Allocates nothing."""
+    N = coords.shape[0]
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    _check(lib().subm3d_build_kmap_noalloc(pc, N, int(res), pn, _stream(stream)))
+    return nbr
 
 
 def subm3d_forward(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tensor,

@@ -9,28 +9,39 @@
 // One persistent CTA per SM loops over tiles of 128 output rows. For each tile the
 // reduction runs over 27 offsets x ceil(I / 64) channel chunks; every (offset,
 // chunk) step is one pipeline stage in shared memory:
-//   A = the 128 gathered neighbour rows, 64 channels each (16 KB), staged by 128
-//       producer threads with 16-byte cp.async (an absent neighbour, nbr = -1,
-//       zero-fills and reads nothing), written in the 128-byte-swizzled K-major
-//       layout the tensor core reads. Each producer marks the stage full with
-//       cp.async.mbarrier.arrive.noinc, so a slot counts as full the moment its
-//       rows land and no producer ever blocks on its own copies; the MMA thread
-//       orders those generic-proxy writes before its tensor-core reads with
-//       fence.proxy.async after the barrier wait;
+//   A = the 128 gathered neighbour rows, 64 channels each (16 KB), written with
+//       16-byte cp.async (an absent neighbour, nbr = -1, zero-fills and reads
+//       nothing) in the 128-byte-swizzled K-major layout the tensor core reads;
 //   B = W_k[:, chunk] = weight[:, kz, ky, kx, chunk], an [O x 64] K-major tile (I is
 //       contiguous in the checkpoint layout, so no transpose), fetched by TMA with
 //       the same 128-byte swizzle; out-of-range rows/columns are zero-filled.
-// One thread issues tcgen05.mma (M = 128, N = round_up(O, 16), K = 16 per
-// instruction) into a tensor-memory accumulator; tcgen05.commit frees the stage.
-// Two accumulators (double-buffered tensor memory) let four epilogue warps drain
-// tile t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> one store per
-// element) while the tensor core works on tile t + 1.
+// The row gathers are many small independent loads, and one warp can keep only a
+// few kilobytes of cp.async in flight, so the gather rate grows with the number of
+// warps issuing them, not with the depth of one warp's queue. The producers are
+// therefore G groups of four warps (G = 6 for O <= 128): stage g belongs to group
+// g mod G, and each group owns its own slots of the shared-memory ring, so G
+// stages are gathered at once by 4G warps. Each producer thread fetches its eight
+// nbr entries for its group's next stage while the current stage's copies are in
+// flight (read-only loads, cached in L1), and the MMA thread asks L2 to prefetch
+// the next tile's 13.8 KB nbr block when it starts a tile. A producer marks its
+// stage full with cp.async.mbarrier.arrive.noinc (the slot counts as full the
+// moment its rows land; no producer blocks on its own copies); the MMA thread
+// orders those generic-proxy writes before its tensor-core reads with
+// fence.proxy.async after the barrier wait.
+// The MMA warp runs converged and one elected lane issues a stage's tcgen05.mma
+// instructions (M = 128, N = round_up(O, 16), K = 16 each, up to four per stage) from a
+// single asm block with a separate descriptor register per instruction: an MMA
+// reads its register operands after issue, so reusing one register for the next
+// instruction's descriptor serialises the MMAs (about 300 cycles each instead of
+// 85 at N = 64 or 128 at N = 256). tcgen05.commit then frees the stage. Two
+// accumulators (double-buffered tensor memory) let four epilogue warps drain tile t
+// (tcgen05.ld, 8 columns at a time -> + bias -> bf16 round-to-nearest-even -> one
+// 16-byte store per 8 outputs) while the tensor core works on tile t + 1.
 //
-// Warp roles (320 threads): warps 0-3 producers (thread 0 also issues the weight
-// TMA), warp 4 tensor-memory allocation + MMA issue (one lane), warps 5-8 epilogue,
-// warp 9 stages each tile's 128 x 27 block of nbr (13.8 KB, contiguous in memory)
-// into a double-buffered shared-memory ring with one bulk async copy, a tile
-// ahead, so the producers never wait on a global load before issuing a gather.
+// Warp roles: warps 0 .. 4G-1 producers (the first thread of each group also issues
+// its stages' weight TMA), warp 4G tensor-memory allocation + MMA issue (one lane),
+// warps 4G+1 .. 4G+4 epilogue (warp w reads tensor-memory lanes 32 (w % 4) ..
+// 32 (w % 4) + 31).
 // Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the
 // device error word, stops the CTA's pipeline, drains what is in flight and
 // releases tensor memory before the CTA exits.
@@ -52,26 +63,32 @@ namespace {
 
 constexpr int kBM = 128;          // output rows per tile (tensor-memory lanes)
 constexpr int kKC = 64;           // channels per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 320;
-constexpr int kProducerThreads = 128;
-constexpr int kMmaWarp = 4;
-constexpr int kNbrWarp = 9;
-constexpr int kNbrTileBytes = kBM * 27 * 4;   // one tile's rows of nbr
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxGroups = 6;     // producer groups of four warps
+constexpr int kGroupThreads = 128;
 
 template <int NMMA>
 struct Cfg {
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = NMMA * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kMisc = 1024 /*alignment slack*/ + 2 * kNbrTileBytes /*nbr ring*/ +
-                               512 /*barriers*/ + 4 * 256 /*bias*/;
+  static constexpr int kMisc = 1024 /*alignment slack*/ + 512 /*barriers*/ + 4 * 256 /*bias*/;
   static constexpr int kFit = (kSmemLimit - kMisc) / kStageBytes;
-  static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kTmemCols = (2 * NMMA <= 32) ? 32 : (2 * NMMA <= 64) ? 64
-                                 : (2 * NMMA <= 128) ? 128 : (2 * NMMA <= 256) ? 256 : 512;
+  static constexpr int kGroups = kFit < kMaxGroups ? kFit : kMaxGroups;
+  static constexpr int kSlots = kFit / kGroups;            // ring slots per group
+  static constexpr int kStages = kGroups * kSlots;
+  static constexpr int kMmaWarp = 4 * kGroups;
+  static constexpr int kEpiWarp0 = kMmaWarp + 1;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+  // one tile's accumulator: NMMA columns, placed at a power-of-two column stride
+  static constexpr int kBufCols = NMMA <= 16 ? 16 : NMMA <= 32 ? 32 : NMMA <= 64 ? 64
+                                : NMMA <= 128 ? 128 : 256;
+  static constexpr int kTmemCols = 2 * kBufCols < 32 ? 32 : 2 * kBufCols;
   static constexpr int kSmemBytes = kMisc + kStages * kStageBytes;
-  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kGroups >= 3, "too few producer groups");
+  static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor memory");
+  static_assert(kThreads <= 1024, "block too large");
+  static_assert(8 * (2 * kStages + 5) + 8 <= 512, "barrier area too small");
 };
 
 struct Params {
@@ -115,58 +132,133 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Warp-uniform bounded wait: every lane polls the barrier; the warp proceeds only if
+// all lanes saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One stage's MMAs, K = 16 each (ksteps of them, 1..4), issued by one elected lane of a
+// converged warp. K step kk starts 32 bytes further into both 128-byte-swizzled
+// tiles, i.e. +2 in the descriptors' address field. The first MMA accumulates only if
+// `acc` is set; the later ones always do. Every MMA gets its own descriptor
+// registers (see the file comment).
+__device__ __forceinline__ void mma_stage(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          int ksteps, uint32_t acc) {
+  const uint64_t a1 = a + 2, a2 = a + 4, a3 = a + 6;
+  const uint64_t b1 = b + 2, b2 = b + 4, b3 = b + 6;
+#define SUBM3D_MMA_HEAD                                                   \
+  "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %9, 0;\n\t"                    \
+  "elect.sync _|e, 0xffffffff;\n\t"                                       \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n\t"
+#define SUBM3D_MMA(A, B) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], " A ", " B ", %10, 1;\n\t"
+#define SUBM3D_MMA_ARGS                                                                  \
+  "r"(d), "l"(a), "l"(a1), "l"(a2), "l"(a3), "l"(b), "l"(b1), "l"(b2), "l"(b3), "r"(acc), \
+      "r"(idesc)
+  switch (ksteps) {
+    case 4:
+      asm volatile(SUBM3D_MMA_HEAD SUBM3D_MMA("%2", "%6") SUBM3D_MMA("%3", "%7")
+                       SUBM3D_MMA("%4", "%8") "}" ::SUBM3D_MMA_ARGS
+                   : "memory");
+      break;
+    case 3:
+      asm volatile(SUBM3D_MMA_HEAD SUBM3D_MMA("%2", "%6") SUBM3D_MMA("%3", "%7") "}" ::SUBM3D_MMA_ARGS
+                   : "memory");
+      break;
+    case 2:
+      asm volatile(SUBM3D_MMA_HEAD SUBM3D_MMA("%2", "%6") "}" ::SUBM3D_MMA_ARGS : "memory");
+      break;
+    default:
+      asm volatile(SUBM3D_MMA_HEAD "}" ::SUBM3D_MMA_ARGS : "memory");
+      break;
+  }
+#undef SUBM3D_MMA_HEAD
+#undef SUBM3D_MMA
+#undef SUBM3D_MMA_ARGS
+}
+
+// tcgen05.commit from one elected lane of a converged warp.
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+
+// The eight nbr entries producer thread (rsub, q) needs for a stage of tile-row
+// block row0 at offset k: rows rsub + 16 m, m = 0..7 (-1 past N). An entry outside
+// [-1, N) is reported through `bad` and treated as absent.
+__device__ __forceinline__ void load_rows(const Params& p, int64_t row0, int k, int rsub,
+                                          int32_t (&j)[8], bool& bad) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int64_t row = row0 + rsub + 16 * m;
+    int32_t v = -1;
+    if (row < p.N) {
+      v = __ldg(p.nbr + row * 27 + k);
+      if (v < -1 || v >= p.N) {
+        bad = true;
+        v = -1;
+      }
+    }
+    j[m] = v;
+  }
+}
+
 template <int NMMA>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
     fwd_tc(const __grid_constant__ CUtensorMap wmap, const Params p) {
   using C = Cfg<NMMA>;
   constexpr int S = C::kStages;
+  constexpr int G = C::kGroups;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sA = base;                              // S x 16 KB
   const uint32_t sB = base + S * C::kABytes;             // S x NMMA*128 B
-  const uint32_t sNbr = base + S * C::kStageBytes;       // 2 x 13.8 KB
-  const int32_t* nbr_sm = reinterpret_cast<const int32_t*>(base_ptr + S * C::kStageBytes);
-  uint8_t* misc = base_ptr + S * C::kStageBytes + 2 * kNbrTileBytes;
-  // barriers: full[S], empty[S], accf[2], acce[2], drain, nbrf[2], nbre[2]
+  uint8_t* misc = base_ptr + S * C::kStageBytes;
+  // barriers: full[S], empty[S], accf[2], acce[2], drain
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
-  const uint32_t nbrf0 = drain + 8;
-  const uint32_t nbre0 = nbrf0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 9));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* bias_sm = reinterpret_cast<float*>(misc + 512);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // tiles of this CTA: blockIdx.x + t * gridDim.x, t < ntl; stages per tile: spt
+  const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                  static_cast<int>(gridDim.x);
+  const uint32_t spt = 27u * static_cast<uint32_t>(p.nchunks);
+  const uint32_t total = static_cast<uint32_t>(ntl) * spt;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, kProducerThreads + 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, kGroupThreads + 1);   // a group's noinc arrivals + the TMA's
+      mbar_init(empty0 + 8 * s, 1);                  // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
       mbar_init(acce0 + 8 * b, 128);
-      mbar_init(nbrf0 + 8 * b, 1);
-      mbar_init(nbre0 + 8 * b, kProducerThreads);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&wmap);
   }
-  if (tid >= 160 && tid < 288) {
-    for (int o = tid - 160; o < NMMA; o += 128)
+  if (warp >= C::kEpiWarp0) {
+    for (int o = tid - C::kEpiWarp0 * 32; o < NMMA; o += 128)
       bias_sm[o] = (p.bias && o < p.O) ? __bfloat162float(p.bias[o]) : 0.f;
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -175,159 +267,119 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < C::kMmaWarp) {
     // ------------------------------------------------------------------ producers
-    const int q = tid & 7;          // 16-byte column chunk inside the 128-byte row
-    const int rsub = tid >> 3;      // rows rsub + 16 m, m = 0..7
-    uint32_t g = 0, lt = 0;
+    const int grp = warp >> 2;
+    const int gt = tid & (kGroupThreads - 1);
+    const int q = gt & 7;           // 16-byte column chunk inside the 128-byte row
+    const int rsub = gt >> 3;       // rows rsub + 16 m, m = 0..7
     bool bad = false, aborted = false;
-    for (int tile = blockIdx.x; tile < p.ntiles && !aborted; tile += gridDim.x, ++lt) {
-      const int64_t row0 = int64_t(tile) * kBM;
-      const uint32_t nb = lt & 1u;
-      if (!mbar_wait(nbrf0 + 8 * nb, (lt >> 1) & 1u, abort_flag)) {
+    uint32_t last = 0;              // one past the last stage this group issued
+    int32_t jn[8];
+    if (static_cast<uint32_t>(grp) < total) {
+      const uint32_t lt = grp / spt, kc = grp - lt * spt;
+      load_rows(p, int64_t(blockIdx.x + lt * gridDim.x) * kBM, kc / p.nchunks, rsub, jn, bad);
+    }
+    for (uint32_t g = grp; g < total; g += G) {
+      const uint32_t lt = g / spt;
+      const uint32_t kc = g - lt * spt;
+      const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
+      const int k = static_cast<int>(kc / static_cast<uint32_t>(p.nchunks));
+      int32_t j[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) j[m] = jn[m];
+      if (g + G < total) {   // next stage's rows: in flight while this stage is issued
+        const uint32_t lt2 = (g + G) / spt, kc2 = (g + G) - lt2 * spt;
+        load_rows(p, int64_t(blockIdx.x + lt2 * gridDim.x) * kBM, kc2 / p.nchunks, rsub, jn,
+                  bad);
+      }
+      const uint32_t s = g % S;
+      const uint32_t ph = (g / S) & 1u;
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
         aborted = true;
         break;
       }
-      const int32_t* tile_nbr = nbr_sm + nb * (kBM * 27);
-      for (int k = 0; k < 27 && !aborted; ++k) {
-        int32_t j[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int r = rsub + 16 * m;
-          int32_t v = -1;
-          if (row0 + r < p.N) {
-            v = tile_nbr[r * 27 + k];
-            if (v < -1 || v >= p.N) {
-              bad = true;
-              v = -1;
-            }
-          }
-          j[m] = v;
-        }
-        if (k == 26) mbar_arrive(nbre0 + 8 * nb);   // this tile's nbr block is no longer read
-        for (int c = 0; c < p.nchunks; ++c) {
-          const uint32_t s = g % S;
-          const uint32_t ph = (g / S) & 1u;
-          if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
-            aborted = true;
-            break;
-          }
-          if (tid == 0) {
-            mbar_arrive_expect_tx(full0 + 8 * s, C::kBBytes);
-            tma_load_3d(sB + s * C::kBBytes, &wmap, full0 + 8 * s, c * kKC, k, 0);
-          }
-          const int col = c * kKC + q * 8;
-          const bool col_ok = col < p.I;
-          const uint32_t a_stage = sA + s * C::kABytes;
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const int r = rsub + 16 * m;
-            const uint32_t dst = a_stage + r * 128 + ((q ^ (r & 7)) << 4);
-            const bool ok = col_ok && j[m] >= 0;
-            const __nv_bfloat16* src = ok ? p.feats + int64_t(j[m]) * p.I + col : p.feats;
-            cp_async_16(dst, src, ok ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(full0 + 8 * s);   // stage s is full once these land
-          ++g;
-        }
+      if (gt == 0) {
+        mbar_arrive_expect_tx(full0 + 8 * s, C::kBBytes);
+        tma_load_3d(sB + s * C::kBBytes, &wmap, full0 + 8 * s, c * kKC, k, 0);
       }
+      const int col = c * kKC + q * 8;
+      const bool col_ok = col < p.I;
+      const uint32_t a_stage = sA + s * C::kABytes;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int r = rsub + 16 * m;
+        const uint32_t dst = a_stage + r * 128 + ((q ^ (r & 7)) << 4);
+        const bool ok = col_ok && j[m] >= 0;
+        const __nv_bfloat16* src = ok ? p.feats + int64_t(j[m]) * p.I + col : p.feats;
+        cp_async_16(dst, src, ok ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(full0 + 8 * s);   // stage s is full once these land
+      last = g + G;
     }
     cp_async_wait_all();   // no gather of this thread is still landing when the CTA exits
     if (bad) atomicOr(p.err, kDevErrBadNbr);
     if (aborted) {
       *abort_flag = 1;
       atomicOr(p.err, kDevErrTimeout);
-      if (tid == 0) {   // make sure no TMA write is still landing in this CTA's memory
-        for (uint32_t x = (g > static_cast<uint32_t>(S) ? g - S : 0u); x < g; ++x)
-          drain_wait(full0 + 8 * (x % S), (x / S) & 1u);
+      if (gt == 0) {   // no weight TMA of this group may still be landing in shared memory
+        for (uint32_t x = last >= static_cast<uint32_t>(S) ? last - S : 0u; x < last; ++x)
+          if (x % G == static_cast<uint32_t>(grp)) drain_wait(full0 + 8 * (x % S), (x / S) & 1u);
       }
     }
-  } else if (warp == kNbrWarp) {
-    // ------------------------------------------------------------------ nbr staging
-    if (lane == 0) {
-      uint32_t lt = 0;
-      bool aborted = false;
-      for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++lt) {
-        const uint32_t nb = lt & 1u;
-        if (!mbar_wait(nbre0 + 8 * nb, ((lt >> 1) & 1u) ^ 1u, abort_flag)) {
-          aborted = true;
-          break;
-        }
-        const int64_t row0 = int64_t(tile) * kBM;
-        const int64_t rows = (p.N - row0) < kBM ? (p.N - row0) : kBM;
-        const uint32_t bytes = static_cast<uint32_t>(rows) * 108u;
-        const uint32_t bulk = bytes & ~15u;
-        int32_t* dst = const_cast<int32_t*>(nbr_sm) + nb * (kBM * 27);
-        for (uint32_t off = bulk; off < bytes; off += 4)   // ragged tail of the last tile
-          dst[off / 4] = __ldg(p.nbr + row0 * 27 + off / 4);
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(nbrf0 + 8 * nb, bulk);
-        bulk_load(sNbr + nb * kNbrTileBytes, p.nbr + row0 * 27, bulk, nbrf0 + 8 * nb);
-      }
-      // every copy this warp issued has landed before the CTA may exit
-      const uint32_t issued = lt;
-      for (uint32_t x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
-        drain_wait(nbrf0 + 8 * (x & 1u), (x >> 1) & 1u);
-      if (aborted) {
-        *abort_flag = 1;
-        atomicOr(p.err, kDevErrTimeout);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc<NMMA>();
-      uint32_t g = 0, t = 0;
-      bool aborted = false;
-      for (int tile = blockIdx.x; tile < p.ntiles && !aborted; tile += gridDim.x, ++t) {
-        const uint32_t buf = t & 1u;
-        const uint32_t use = t >> 1;
-        if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag)) {
+    const uint32_t idesc = make_idesc<NMMA>();
+    uint32_t g = 0;
+    bool aborted = false;
+    for (int t = 0; t < ntl && !aborted; ++t) {
+      if (t + 1 < ntl && lane == 0) {   // the next tile's nbr block into L2 while this tile runs
+        const int64_t row1 = int64_t(blockIdx.x + (t + 1) * gridDim.x) * kBM;
+        const int64_t rows = (p.N - row1) < kBM ? (p.N - row1) : kBM;
+        const uint32_t bytes = static_cast<uint32_t>(rows * 108) & ~15u;
+        if (bytes) bulk_prefetch_l2(p.nbr + row1 * 27, bytes);
+      }
+      const uint32_t buf = t & 1u;
+      const uint32_t use = t >> 1;
+      if (!warp_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * C::kBufCols;
+      for (uint32_t kc = 0; kc < spt; ++kc) {
+        const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
+        const uint32_t s = g % S;
+        const uint32_t ph = (g / S) & 1u;
+        if (!warp_wait(full0 + 8 * s, ph, abort_flag)) {
           aborted = true;
           break;
         }
+        fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * NMMA;
-        uint32_t accumulate = 0;
-        for (int k = 0; k < 27 && !aborted; ++k) {
-          for (int c = 0; c < p.nchunks; ++c) {
-            const uint32_t s = g % S;
-            const uint32_t ph = (g / S) & 1u;
-            if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) {
-              aborted = true;
-              break;
-            }
-            fence_proxy_async_smem();
-            tc_fence_after();
-            const int rem = p.I - c * kKC;
-            const int ksteps = rem >= kKC ? 4 : (rem + 15) / 16;
-            const uint32_t a0 = sA + s * C::kABytes;
-            const uint32_t b0 = sB + s * C::kBBytes;
-            for (int kk = 0; kk < ksteps; ++kk) {
-              tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                         accumulate);
-              accumulate = 1;
-            }
-            tc_commit(empty0 + 8 * s);
-            ++g;
-          }
-        }
-        if (!aborted) tc_commit(accf0 + 8 * buf);
+        const int rem = p.I - c * kKC;
+        const int ksteps = rem >= kKC ? 4 : (rem + 15) / 16;
+        mma_stage(d_tmem, sw128_desc(sA + s * C::kABytes), sw128_desc(sB + s * C::kBBytes), idesc,
+                  ksteps, kc == 0 ? 0u : 1u);
+        tc_commit_elect(empty0 + 8 * s);
+        ++g;
       }
-      if (aborted) {
+      if (!aborted) tc_commit_elect(accf0 + 8 * buf);
+    }
+    if (aborted) {
+      if (lane == 0) {
         *abort_flag = 1;
         atomicOr(p.err, kDevErrTimeout);
-        tc_commit(drain);            // wait for every MMA already issued
-        drain_wait(drain, 0);
       }
+      tc_commit_elect(drain);   // wait for every MMA already issued
+      if (lane == 0) drain_wait(drain, 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue
     const int lg = warp & 3;                  // tensor-memory lane group of this warp
-    uint32_t t = 0;
-    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++t) {
+    for (int t = 0; t < ntl; ++t) {
+      const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
       if (!mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag)) {
@@ -337,30 +389,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + buf * NMMA;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + buf * C::kBufCols;
       __nv_bfloat16* orow = p.out + row * p.O;
 #pragma unroll 1
-      for (int cc = 0; cc < NMMA / 16; ++cc) {
-        uint32_t v[16];
-        tmem_ld16(taddr + cc * 16, v);
+      for (int cc = 0; cc < NMMA / 8; ++cc) {   // 8 columns at a time
+        uint32_t v[8];
+        tmem_ld8(taddr + cc * 8, v);
         tmem_ld_wait();
-        if (cc == NMMA / 16 - 1) {
+        if (cc == NMMA / 8 - 1) {
           tc_fence_before();
           mbar_arrive(acce0 + 8 * buf);
         }
-        const int col0 = cc * 16;
+        const int col0 = cc * 8;
         if (row < p.N && col0 < p.O) {
-          uint32_t packed[8];
+          uint32_t packed[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 4; ++e) {
             const float lo = __uint_as_float(v[2 * e]) + bias_sm[col0 + 2 * e];
             const float hi = __uint_as_float(v[2 * e + 1]) + bias_sm[col0 + 2 * e + 1];
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
             packed[e] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          if (col0 + 8 < p.O) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          *reinterpret_cast<uint4*>(orow + col0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
       }
     }
@@ -369,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == C::kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -421,7 +472,7 @@ int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) 
     return SUBM3D_ERR_CUDA;
   }
   const int grid = prm.ntiles < num_sms() ? prm.ntiles : num_sms();
-  fwd_tc<NMMA><<<grid, kThreads, C::kSmemBytes, stream>>>(map, prm);
+  fwd_tc<NMMA><<<grid, C::kThreads, C::kSmemBytes, stream>>>(map, prm);
   SUBM3D_LAUNCHED("fwd_tc");
   return SUBM3D_OK;
 }

@@ -66,8 +66,9 @@ typedef enum { SUBM3D_F32 = 0, SUBM3D_BF16 = 1 } subm3d_dtype;
 #define SUBM3D_MAX_BATCH 65534
 
 /*
- * Workspace bytes that subm3d_build_kmap needs for N voxels (default hash
- * capacity: the smallest power of two >= 2N, at least 64 slots). Host-only, no CUDA
+ * Workspace bytes that subm3d_build_kmap needs for N voxels (the default hash table
+ * is reserved for its worst case, one occupied block per voxel: the smallest power
+ * of two >= 2N slots, at least 64, of 20 bytes each). Host-only, no CUDA
  * call. Returns 0 for N < 0.
  */
 SUBM3D_API size_t subm3d_kmap_workspace_bytes(int64_t N);
@@ -93,11 +94,15 @@ SUBM3D_API size_t subm3d_kmap_workspace_bytes_ex(int64_t N, int64_t hash_capacit
  *   workspace device scratch of at least subm3d_kmap_workspace_bytes(N) bytes,
  *             256-byte aligned; its contents on entry do not matter.
  *
- * Steps (all CUDA kernels on `stream`): validate and pack each coordinate into a
- * 64-bit key b<<48 | z<<32 | y<<16 | x; Morton-order the voxels (LSD radix sort
- * of (b, interleaved z/y/x bits)); insert the keys into an open-addressing hash
- * table with bounded linear probing; probe the 27 offsets per voxel with
- * warp-cooperative lookups and coalesced writes of nbr.
+ * Steps (all CUDA kernels on `stream`): validate each coordinate and pack it into a
+ * 64-bit sort key (b above the interleaved z/y/x bits: its Morton code); Morton-order
+ * the voxels (LSD radix sort). In that order every aligned 4x4x4 block is one run
+ * (the low 6 bits of the code are the place inside the block), so duplicates are
+ * adjacent equal codes; each occupied block is inserted into an open-addressing hash
+ * table (key b<<42 | (z>>2)<<28 | (y>>2)<<14 | (x>>2), a 64-bit occupancy mask, the
+ * block's first sorted position; bounded linear probing). The 27 offsets of each
+ * voxel are probed by warps that take 32 voxels of the sorted order and write each
+ * voxel's row of nbr contiguously.
  *
  * Synchronisation: the call waits for `stream` once, at its end, to read the
  * device status word, so it is not capturable into a CUDA graph. Errors found on
@@ -112,8 +117,12 @@ SUBM3D_API int subm3d_build_kmap(const int32_t* coords, int64_t N, int32_t res, 
  *   order          device int32 [N] or NULL. If given, receives the Morton order:
  *                  order[s] = the input row at position s of the (b, Morton code)
  *                  ascending sort (stable, so ties keep input order).
- *   hash_capacity  0 for the default, else a power of two >= 8 (slots). A capacity
- *                  below N makes the insert fail with SUBM3D_ERR_HASH_FULL.
+ *   hash_capacity  0 for the default (the smallest power of two >= 2 x the number of
+ *                  occupied 4x4x4 blocks, chosen on the device; the workspace is sized
+ *                  for the worst case of one block per voxel), else a fixed power of
+ *                  two >= 8 (slots, one per occupied block). A capacity below the
+ *                  number of occupied blocks makes the call fail with
+ *                  SUBM3D_ERR_HASH_FULL.
  */
 SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
                          int32_t* order, int64_t hash_capacity, void* workspace,

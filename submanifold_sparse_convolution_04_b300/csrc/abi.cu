@@ -82,6 +82,11 @@ int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, co
       set_error("subm3d_forward: bf16 needs I %% 8 == 0 and O %% 8 == 0 (got I=%d, O=%d)", I, O);
       return SUBM3D_ERR_UNSUPPORTED;
     }
+    if (forward_tm_applies(feats, I, O))
+      return forward_launch_tm(static_cast<const __nv_bfloat16*>(feats), nbr,
+                               static_cast<const __nv_bfloat16*>(weight),
+                               static_cast<const __nv_bfloat16*>(bias),
+                               static_cast<__nv_bfloat16*>(out), N, I, O, stream);
     if (O <= 256)
       return forward_launch_tc(static_cast<const __nv_bfloat16*>(feats), nbr,
                                static_cast<const __nv_bfloat16*>(weight),

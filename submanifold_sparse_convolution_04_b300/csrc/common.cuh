@@ -62,6 +62,12 @@ int* forward_error_word();                      // device address of the word
 int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
                       __nv_bfloat16* out, int64_t N, int I, int O, cudaStream_t stream);
+// The narrow-layer kernel (A operand in tensor memory, resident weight): I and O in
+// {16, 32, 48, 64} and feats 32-byte aligned.
+bool forward_tm_applies(const void* feats, int I, int O);
+int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr,
+                      const __nv_bfloat16* weight, const __nv_bfloat16* bias,
+                      __nv_bfloat16* out, int64_t N, int I, int O, cudaStream_t stream);
 int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weight,
                         const void* bias, void* out, int64_t N, int I, int O,
                         subm3d_dtype dtype, cudaStream_t stream);

@@ -1,0 +1,456 @@
+// Forward pass for narrow layers (I <= 64, O <= 64, both multiples of 16): implicit
+// gather-GEMM on the 5th-generation tensor cores with the gathered operand in
+// tensor memory and the whole weight resident in shared memory.
+//
+// out[i, o] = bias[o] + sum_k sum_c W[o, kz, ky, kx, c] * feats[nbr[i, k], c]
+// (submanifold convolution, kernel 3, stride 1, no padding, "pixal3d_mrp_mlx
+// README" scope table; weight [O, kz, ky, kx, I], channels-last features, same
+// README's commit header).
+//
+// Why a second kernel: with the gathered rows staged in shared memory, every 128-row
+// stage costs 48 KB of shared-memory traffic at O = 64 (16 KB of cp.async writes,
+// most of them zero-fill, the MMA re-reading them, and the weight tile written and
+// read), and the shared-memory port, not HBM, sets the pace. Here:
+//   * the weight, 27 x [O x 64] K-major tiles with 128-byte swizzle (216 KB at
+//     I = O = 64), is loaded once per CTA by TMA and stays resident;
+//   * each producer thread gathers one neighbour row (I bf16 <= 128 bytes) into
+//     registers with 32-byte read-only loads, an absent neighbour costing no load at
+//     all (zeros), and writes it with tcgen05.st into a tensor-memory stage, the row
+//     in the lane of its output row, channels 2c and 2c+1 in column c;
+//   * tcgen05.mma reads A from tensor memory and only B (the resident weight tap)
+//     from shared memory.
+// Tensor memory (512 columns): two accumulators of 64 columns (double buffer) and
+// twelve A stages of 32 columns. Stage g of the CTA (tile, offset k) is written by
+// producer group g mod 6 (four warps, warp w writing lanes 32 (w % 4) .. + 31) and
+// lives in slot g mod 12. A group has one stage's loads in flight while it waits for
+// its slot; it marks the stage full (one arrival per warp) after tcgen05.wait::st.
+// One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
+// up to four) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
+// t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> 16-byte stores) while
+// the tensor core works on tile t + 1.
+//
+// Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the device
+// error word, stops the CTA's pipeline, drains what is in flight and releases tensor
+// memory before the CTA exits.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace subm3d {
+namespace {
+
+constexpr int kBM = 128;              // output rows per tile = tensor-memory lanes
+constexpr int kGroups = 6;            // producer groups of four warps
+constexpr int kStages = 12;           // A stages in tensor memory
+constexpr int kStageCols = 32;        // 64 bf16 per row = 32 columns of 32 bits
+constexpr int kAccCols = 64;          // one accumulator (N <= 64)
+constexpr int kAColBase = 2 * kAccCols;
+constexpr int kMmaWarp = 4 * kGroups;
+constexpr int kEpiWarp0 = kMmaWarp + 1;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);   // 928
+constexpr int kSmemLimit = 227 * 1024;
+static_assert(kAColBase + kStages * kStageCols == 512, "tensor memory layout");
+static_assert(kStages % kGroups == 0, "slots per group");
+
+template <int NMMA>
+struct TmCfg {
+  static constexpr int kTapBytes = NMMA * 128;            // one [NMMA x 64] weight tile
+  static constexpr int kWBytes = 27 * kTapBytes;
+  static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 512 /*barriers*/ + 256 * 4 /*bias*/;
+  // at least half the SM's shared memory, so that one CTA (which takes all of tensor
+  // memory) runs per SM
+  static constexpr int kSmemBytes = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
+  static_assert(kSmemBytes <= kSmemLimit, "resident weight does not fit");
+};
+
+struct TmParams {
+  const __nv_bfloat16* feats;
+  const int32_t* nbr;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  int64_t N;
+  int I, O;
+  int ntiles;
+  int* err;
+};
+
+__device__ __forceinline__ uint64_t tm_sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                    // leading offset (unused: swizzled)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128.
+template <int NMMA>
+__device__ __forceinline__ uint32_t tm_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(NMMA >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tm_drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// One stage's MMAs with A in tensor memory: K step kk reads A columns a + 8 kk and
+// the weight tile 32 bytes further (+2 in the descriptor's address field). Each MMA
+// has its own operand registers; the first accumulates only if `acc` is set.
+__device__ __forceinline__ void tm_mma_stage(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                             int ksteps, uint32_t acc) {
+  const uint32_t a1 = a + 8, a2 = a + 16, a3 = a + 24;
+  const uint64_t b1 = b + 2, b2 = b + 4, b3 = b + 6;
+#define TM_MMA_HEAD                                                        \
+  "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %9, 0;\n\t"                     \
+  "elect.sync _|e, 0xffffffff;\n\t"                                        \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p;\n\t"
+#define TM_MMA(A, B) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [" A "], " B ", %10, 1;\n\t"
+#define TM_MMA_ARGS                                                                          \
+  "r"(d), "r"(a), "r"(a1), "r"(a2), "r"(a3), "l"(b), "l"(b1), "l"(b2), "l"(b3), "r"(acc), \
+      "r"(idesc)
+  switch (ksteps) {
+    case 4:
+      asm volatile(TM_MMA_HEAD TM_MMA("%2", "%6") TM_MMA("%3", "%7") TM_MMA("%4", "%8") "}" ::TM_MMA_ARGS
+                   : "memory");
+      break;
+    case 3:
+      asm volatile(TM_MMA_HEAD TM_MMA("%2", "%6") TM_MMA("%3", "%7") "}" ::TM_MMA_ARGS : "memory");
+      break;
+    case 2:
+      asm volatile(TM_MMA_HEAD TM_MMA("%2", "%6") "}" ::TM_MMA_ARGS : "memory");
+      break;
+    default:
+      asm volatile(TM_MMA_HEAD "}" ::TM_MMA_ARGS : "memory");
+      break;
+  }
+#undef TM_MMA_HEAD
+#undef TM_MMA
+#undef TM_MMA_ARGS
+}
+
+__device__ __forceinline__ void tm_commit(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+
+// 32 lanes x 32 bit, 32 consecutive columns from this thread's 32 registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 read-only bytes (8 words) from a 32-byte-aligned global address.
+__device__ __forceinline__ void ld32B(const void* p, uint32_t* w) {
+  asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+template <int NMMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tm(const __grid_constant__ CUtensorMap wmap, const TmParams p) {
+  using C = TmCfg<NMMA>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sW = base;                                   // 27 weight taps
+  uint8_t* misc = base_ptr + C::kWBytes;
+  // barriers: afull[12], aempty[12], accf[2], acce[2], wfull, drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+  const uint32_t afull0 = smem_u32(bars);
+  const uint32_t aempty0 = afull0 + 8 * kStages;
+  const uint32_t accf0 = aempty0 + 8 * kStages;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t wfull = acce0 + 16;
+  const uint32_t drain = wfull + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * kStages + 6));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* bias_sm = reinterpret_cast<float*>(misc + 512);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                  static_cast<int>(gridDim.x);
+  const uint32_t total = static_cast<uint32_t>(ntl) * 27u;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(afull0 + 8 * s, 4);     // one arrival per producer warp
+      mbar_init(aempty0 + 8 * s, 1);    // one tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 128);
+    }
+    mbar_init(wfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&wmap);
+    // the whole weight, once: tap k -> [NMMA x 64] K-major tile at sW + k * kTapBytes
+    mbar_arrive_expect_tx(wfull, C::kWBytes);
+    for (int k = 0; k < 27; ++k) tma_load_3d(sW + k * C::kTapBytes, &wmap, wfull, 0, k, 0);
+  }
+  if (warp >= kEpiWarp0) {
+    for (int o = tid - kEpiWarp0 * 32; o < NMMA; o += 128)
+      bias_sm[o] = (p.bias && o < p.O) ? __bfloat162float(p.bias[o]) : 0.f;
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kMmaWarp) {
+    // ------------------------------------------------------------------ producers
+    const int grp = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;       // row of the tile = tensor-memory lane
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    bool bad = false, aborted = false;
+    auto row_of = [&](uint32_t g) -> int32_t {
+      const uint32_t lt = g / 27u, k = g - lt * 27u;
+      const int64_t row = int64_t(blockIdx.x + lt * gridDim.x) * kBM + r;
+      int32_t v = -1;
+      if (row < p.N) {
+        v = __ldg(p.nbr + row * 27 + k);
+        if (v < -1 || v >= p.N) {
+          bad = true;
+          v = -1;
+        }
+      }
+      return v;
+    };
+    int32_t jn = static_cast<uint32_t>(grp) < total ? row_of(grp) : -1;
+    for (uint32_t g = grp; g < total; g += kGroups) {
+      const int32_t j = jn;
+      if (g + kGroups < total) jn = row_of(g + kGroups);   // next stage's row, in flight
+      uint32_t v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // 16 channels (32 bytes) per load
+        if (j >= 0 && q * 16 < p.I) {
+          ld32B(p.feats + int64_t(j) * p.I + q * 16, v + 8 * q);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * q + e] = 0u;
+        }
+      }
+      const uint32_t s = g % kStages;
+      const uint32_t use = g / kStages;
+      const bool ok = mbar_wait(aempty0 + 8 * s, (use & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tmem_base + lane_addr + kAColBase + s * kStageCols, v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull0 + 8 * s);
+    }
+    if (bad) atomicOr(p.err, kDevErrBadNbr);
+    if (aborted && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, kDevErrTimeout);
+    }
+    if (tid == 0) tm_drain_wait(wfull, 0);   // the weight TMA has landed before the CTA exits
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issue
+    const uint32_t idesc = tm_idesc<NMMA>();
+    const int ksteps = (p.I + 15) / 16;
+    const uint64_t w0 = tm_sw128_desc(sW);
+    bool aborted = !__all_sync(0xffffffffu, mbar_wait(wfull, 0, abort_flag));
+    uint32_t g = 0;
+    for (int t = 0; t < ntl && !aborted; ++t) {
+      if (t + 1 < ntl && lane == 0) {   // the next tile's nbr block into L2 while this tile runs
+        const int64_t row1 = int64_t(blockIdx.x + (t + 1) * gridDim.x) * kBM;
+        const int64_t rows = (p.N - row1) < kBM ? (p.N - row1) : kBM;
+        const uint32_t bytes = static_cast<uint32_t>(rows * 108) & ~15u;
+        if (bytes) bulk_prefetch_l2(p.nbr + row1 * 27, bytes);
+      }
+      const uint32_t buf = t & 1u;
+      const uint32_t use = t >> 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag))) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * kAccCols;
+      for (int k = 0; k < 27; ++k, ++g) {
+        const uint32_t s = g % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * s, (g / kStages) & 1u, abort_flag))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        tm_mma_stage(d_tmem, tmem_base + kAColBase + s * kStageCols,
+                     w0 + static_cast<uint64_t>(k) * (C::kTapBytes >> 4), idesc, ksteps,
+                     k == 0 ? 0u : 1u);
+        tm_commit(aempty0 + 8 * s);
+      }
+      if (!aborted) tm_commit(accf0 + 8 * buf);
+    }
+    if (aborted) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        atomicOr(p.err, kDevErrTimeout);
+      }
+      tm_commit(drain);   // wait for every MMA already issued
+      if (lane == 0) tm_drain_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int lg = warp & 3;                  // tensor-memory lane group of this warp
+    for (int t = 0; t < ntl; ++t) {
+      const int tile = blockIdx.x + t * gridDim.x;
+      const uint32_t buf = t & 1u;
+      const uint32_t use = t >> 1;
+      if (!mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag)) {
+        *abort_flag = 1;
+        atomicOr(p.err, kDevErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + buf * kAccCols;
+      __nv_bfloat16* orow = p.out + row * p.O;
+#pragma unroll 1
+      for (int cc = 0; cc < NMMA / 8; ++cc) {   // 8 columns at a time
+        uint32_t v[8];
+        tmem_ld8(taddr + cc * 8, v);
+        tmem_ld_wait();
+        if (cc == NMMA / 8 - 1) {
+          tc_fence_before();
+          mbar_arrive(acce0 + 8 * buf);
+        }
+        const int col0 = cc * 8;
+        if (row < p.N) {
+          uint32_t packed[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(v[2 * e]) + bias_sm[col0 + 2 * e];
+            const float hi = __uint_as_float(v[2 * e + 1]) + bias_sm[col0 + 2 * e + 1];
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+            packed[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(orow + col0) =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, 512);
+}
+
+typedef CUresult (*TmEncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+TmEncodeTiledFn tm_get_encode() {
+  static TmEncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TmEncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+template <int NMMA>
+int tm_launch(const TmParams& prm, const __nv_bfloat16* weight, cudaStream_t stream) {
+  using C = TmCfg<NMMA>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(fwd_tm<NMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes));
+    attr_set = true;
+  }
+  TmEncodeTiledFn encode = tm_get_encode();
+  if (!encode) {
+    set_error("subm3d_forward: cuTensorMapEncodeTiled is not available from the driver");
+    return SUBM3D_ERR_CUDA;
+  }
+  // weight [O, 3, 3, 3, I] as a 3-D tensor {I, 27, O}; box = one tap's [O x 64] slice
+  CUtensorMap wmap;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(prm.I), 27, static_cast<cuuint64_t>(prm.O)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(prm.I) * 2,
+                                 static_cast<cuuint64_t>(prm.I) * 27 * 2};
+  const cuuint32_t box[3] = {64, 1, NMMA};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                            const_cast<__nv_bfloat16*>(weight), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("subm3d_forward: cuTensorMapEncodeTiled failed (%d) for weight=%p I=%d O=%d",
+              static_cast<int>(r), (const void*)weight, prm.I, prm.O);
+    return SUBM3D_ERR_CUDA;
+  }
+  const int grid = prm.ntiles < num_sms() ? prm.ntiles : num_sms();
+  fwd_tm<NMMA><<<grid, kThreads, C::kSmemBytes, stream>>>(wmap, prm);
+  SUBM3D_LAUNCHED("fwd_tm");
+  return SUBM3D_OK;
+}
+
+}  // namespace
+
+bool forward_tm_applies(const void* feats, int I, int O) {
+  return I >= 16 && I <= 64 && I % 16 == 0 && O >= 16 && O <= 64 && O % 16 == 0 &&
+         (reinterpret_cast<uintptr_t>(feats) & 31) == 0;
+}
+
+int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv_bfloat16* weight,
+                      const __nv_bfloat16* bias, __nv_bfloat16* out, int64_t N, int I, int O,
+                      cudaStream_t stream) {
+  const int64_t ntiles = (N + kBM - 1) / kBM;
+  if (ntiles > 0x7FFFFFFFll) {
+    set_error("subm3d_forward: N=%lld too large", (long long)N);
+    return SUBM3D_ERR_UNSUPPORTED;
+  }
+  TmParams prm{feats, nbr, bias, out, N, I, O, static_cast<int>(ntiles), forward_error_word()};
+  switch (O) {
+    case 16: return tm_launch<16>(prm, weight, stream);
+    case 32: return tm_launch<32>(prm, weight, stream);
+    case 48: return tm_launch<48>(prm, weight, stream);
+    case 64: return tm_launch<64>(prm, weight, stream);
+    default:
+      set_error("subm3d_forward: O=%d outside the narrow tensor-core kernel's range", O);
+      return SUBM3D_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace subm3d

@@ -7,21 +7,32 @@
 // lets one table serve several convolutions on one voxel set.
 //
 // Pipeline (one stream, one host sync at the end to read the status word):
-//   1. init    : status word, digit histograms and hash table cleared
-//   2. pack    : validate (b, z, y, x), packed key b<<48|z<<32|y<<16|x, sort key
-//                (b << 3*bits) | Morton(z, y, x), all-pass digit histograms
+//   1. init    : status word and digit histograms cleared
+//   2. pack    : validate (b, z, y, x); sort key (b << 3*bits) | Morton(z, y, x) with
+//                bits >= 2; all-pass digit histograms
 //   3. plan    : which 8-bit radix passes are not constant (others are skipped)
-//   4. passes  : LSD radix sort of (sort key, row) -- count / scan / stable scatter
-//   5. insert  : keys into an open-addressing table in Morton order (atomicCAS,
-//                bounded linear probing; equal keys = duplicate coordinates)
-//   6. probe   : a warp takes 32 consecutive voxels and spreads their 32 x 27
-//                (voxel, offset) lookups over its lanes, so lane l of round t
-//                writes nbr[v0*27 + 32 t + l]: fully coalesced rows of the table.
+//   4. passes  : LSD radix sort of (sort key, row) -- count / scan / stable scatter;
+//                the scatter ranks a 4096-key tile in shared memory and writes each
+//                digit's run contiguously
+//   5. blocks  : the low 6 bits of a Morton code are the voxel's place inside its
+//                aligned 4x4x4 block and the bits above name the block, so in sorted
+//                order every block is one contiguous run. Adjacent equal codes are
+//                duplicate coordinates; the run starts are counted
+//   6. table   : hash capacity = the smallest power of two >= 2 x blocks (unless the
+//                caller fixed it), chosen and cleared on the device
+//   7. insert  : one slot per block, {packed block key b<<42|bz<<28|by<<14|bx,
+//                64-bit occupancy mask}, plus the block's first sorted position;
+//                open addressing, atomicCAS, bounded linear probing
+//   8. probe   : a warp takes 32 consecutive voxels (input order) and spreads their
+//                32 x 27 (voxel, offset) lookups over its lanes. A lookup finds the
+//                neighbour's block, tests its bit and turns the bit's rank inside
+//                the mask into a sorted position, whose input row is the answer.
+//                Lane l of round t writes nbr[v0 * 27 + 32 t + l]: the warp writes
+//                one contiguous stretch of the table.
 //
-// Hash: a slot is 16 bytes {key, row}; the home slot of a key is
-// mix(key of its 2x2x2 block) * 8 + (position inside the block), so the 27
-// lookups of a voxel touch at most eight 128-byte lines and neighbouring voxels
-// share them. mix is the splitmix64 finaliser (Steele, Lea and Flood, 2014).
+// The blocks of a shell hold ~10 voxels each, so the table is about a tenth of a
+// per-voxel table and stays in L2.
+// Hash of a block key: the splitmix64 finaliser (Steele, Lea and Flood, 2014).
 #include "common.cuh"
 
 namespace subm3d {
@@ -33,6 +44,7 @@ constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;   // keys per sort block
 constexpr int kMaxPasses = 8;
 constexpr int kMaxProbe = 4096;
+constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 256 * 4;
 
 enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8 };
 
@@ -41,18 +53,20 @@ struct KmapStatus {
   int pad;
   long long bad_row;
   int plan[kMaxPasses + 1];   // plan[p]: bit1 = pass active, bit0 = source buffer; plan[8] = final buffer
+  int pad2;
+  unsigned long long nblocks;    // occupied 4x4x4 blocks
+  unsigned long long cap;        // hash capacity in use (a power of two)
 };
 
 struct __align__(16) Slot {
-  unsigned long long key;
-  int row;
-  int pad;
+  unsigned long long key;    // packed block key, kEmptyKey when free
+  unsigned long long mask;   // bit (Morton order of the voxel inside the block) per active voxel
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, hist, keys, mk0, mk1, ix0, ix1, cnt, table, total;
+  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table, base, total;
   int64_t nblk;
 };
 
@@ -62,22 +76,15 @@ Layout make_layout(int64_t N, int64_t cap) {
   size_t o = 0;
   L.status = o; o = align256(o + sizeof(KmapStatus));
   L.hist = o;   o = align256(o + sizeof(uint32_t) * kMaxPasses * 256);
-  L.keys = o;   o = align256(o + sizeof(uint64_t) * N);
   L.mk0 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.mk1 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
   L.ix1 = o;    o = align256(o + sizeof(int32_t) * N);
   L.cnt = o;    o = align256(o + sizeof(uint32_t) * 256 * L.nblk);
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
+  L.base = o;   o = align256(o + sizeof(int32_t) * cap);
   L.total = o;
   return L;
-}
-
-__device__ __forceinline__ unsigned long long pack_key(int b, int z, int y, int x) {
-  return (static_cast<unsigned long long>(static_cast<uint32_t>(b) & 0xFFFFu) << 48) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(z) & 0xFFFFu) << 32) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(y) & 0xFFFFu) << 16) |
-         static_cast<unsigned long long>(static_cast<uint32_t>(x) & 0xFFFFu);
 }
 
 // Interleaves the low `bits` bits of z, y, x: bit t of x -> 3t, of y -> 3t+1, of z -> 3t+2.
@@ -91,21 +98,29 @@ __device__ __forceinline__ unsigned long long morton3(uint32_t z, uint32_t y, ui
   return m;
 }
 
+// Place of (z, y, x) inside its 4x4x4 block: the low 6 bits of the Morton code.
+__device__ __forceinline__ uint32_t in_block_bit(uint32_t z, uint32_t y, uint32_t x) {
+  return (x & 1u) | ((y & 1u) << 1) | ((z & 1u) << 2) | ((x & 2u) << 2) | ((y & 2u) << 3) |
+         ((z & 2u) << 4);
+}
+
+// b << 42 | (z >> 2) << 28 | (y >> 2) << 14 | (x >> 2): 16 + 3 x 14 bits, never all ones.
+__device__ __forceinline__ unsigned long long block_key(uint32_t b, uint32_t z, uint32_t y,
+                                                        uint32_t x) {
+  return (static_cast<unsigned long long>(b & 0xFFFFu) << 42) |
+         (static_cast<unsigned long long>((z >> 2) & 0x3FFFu) << 28) |
+         (static_cast<unsigned long long>((y >> 2) & 0x3FFFu) << 14) |
+         static_cast<unsigned long long>((x >> 2) & 0x3FFFu);
+}
+
 __device__ __forceinline__ unsigned long long mix64(unsigned long long v) {
   v = (v ^ (v >> 30)) * 0xbf58476d1ce4e5b9ull;
   v = (v ^ (v >> 27)) * 0x94d049bb133111ebull;
   return v ^ (v >> 31);
 }
 
-__device__ __forceinline__ unsigned long long home_slot(unsigned long long key,
-                                                        unsigned long long mask) {
-  const unsigned long long low = 0x0000000100010001ull;   // lowest bit of z, y and x
-  const unsigned long long inner = ((key >> 30) & 4ull) | ((key >> 15) & 2ull) | (key & 1ull);
-  return ((mix64(key & ~low) << 3) | inner) & mask;
-}
-
 // 1. ------------------------------------------------------------------------------
-__global__ void kmap_init(KmapStatus* st, uint32_t* hist, Slot* table, int64_t cap) {
+__global__ void kmap_init(KmapStatus* st, uint32_t* hist) {
   const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   if (tid == 0) {
@@ -113,21 +128,16 @@ __global__ void kmap_init(KmapStatus* st, uint32_t* hist, Slot* table, int64_t c
     st->pad = 0;
     st->bad_row = 0x7FFFFFFFFFFFFFFFll;
     for (int p = 0; p <= kMaxPasses; ++p) st->plan[p] = 0;
+    st->pad2 = 0;
+    st->nblocks = 0;
+    st->cap = 0;
   }
   for (int64_t i = tid; i < kMaxPasses * 256; i += stride) hist[i] = 0;
-  for (int64_t i = tid; i < cap; i += stride) {
-    Slot s;
-    s.key = kEmptyKey;
-    s.row = -1;
-    s.pad = 0;
-    table[i] = s;
-  }
 }
 
 // 2. ------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords, int64_t N,
                                                  int res, int bits, int npass,
-                                                 unsigned long long* __restrict__ keys,
                                                  unsigned long long* __restrict__ mk,
                                                  int32_t* __restrict__ ix, uint32_t* hist,
                                                  KmapStatus* st) {
@@ -146,10 +156,8 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
       atomicMin(&st->bad_row, static_cast<long long>(i));
       c = make_int4(0, 0, 0, 0);
     }
-    const unsigned long long key = pack_key(c.x, c.y, c.z, c.w);
     const unsigned long long m =
         (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w, bits);
-    keys[i] = key;
     mk[i] = m;
     ix[i] = static_cast<int32_t>(i);
     for (int p = 0; p < npass; ++p) atomicAdd(&sh[p][(m >> (8 * p)) & 255u], 1u);
@@ -199,52 +207,60 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_count(
   cnt[threadIdx.x * nblk + blockIdx.x] = sh[threadIdx.x];
 }
 
+// Exclusive prefix sum of one value per thread over a 256-thread block; returns the
+// thread's prefix and leaves the block total in *total. `tmp` holds 8 words.
+__device__ __forceinline__ uint32_t block_exclusive_scan256(uint32_t x, uint32_t* tmp,
+                                                            uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = x;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  uint32_t wpre = 0, all = 0;
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t t = tmp[w];
+    if (w < warp) wpre += t;
+    all += t;
+  }
+  __syncthreads();
+  *total = all;
+  return wpre + incl - x;
+}
+
 // 4b. one block per digit: exclusive scan over blocks plus the digit's base --------
 __global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict__ hist, int pass,
                                                       int64_t nblk, uint32_t* __restrict__ cnt,
                                                       const KmapStatus* st) {
   if (!(st->plan[pass] & 2)) return;
   const int d = blockIdx.x;
-  __shared__ uint32_t warp_sums[8];
-  __shared__ uint32_t carry;
+  __shared__ uint32_t tmp[8];
+  uint32_t total;
   // base = sum of the histogram bins below d
-  uint32_t v = threadIdx.x < static_cast<unsigned>(d) ? hist[pass * 256 + threadIdx.x] : 0u;
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t s = 0;
-    for (int w = 0; w < 8; ++w) s += warp_sums[w];
-    carry = s;
-  }
-  __syncthreads();
+  block_exclusive_scan256(threadIdx.x < static_cast<unsigned>(d) ? hist[pass * 256 + threadIdx.x]
+                                                                  : 0u,
+                          tmp, &total);
+  uint32_t carry = total;
   uint32_t* row = cnt + d * nblk;
   for (int64_t b0 = 0; b0 < nblk; b0 += 256) {
     const int64_t b = b0 + threadIdx.x;
     const uint32_t x = b < nblk ? row[b] : 0u;
-    // block-wide inclusive scan of x
-    uint32_t incl = x;
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if ((threadIdx.x & 31) >= o) incl += y;
-    }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 31) warp_sums[threadIdx.x >> 5] = incl;
-    __syncthreads();
-    uint32_t wpre = 0;
-    for (int w = 0; w < static_cast<int>(threadIdx.x >> 5); ++w) wpre += warp_sums[w];
-    const uint32_t c0 = carry;
-    if (b < nblk) row[b] = c0 + wpre + incl - x;
-    __syncthreads();
-    if (threadIdx.x == 255) carry = c0 + wpre + incl;
-    __syncthreads();
+    uint32_t sum;
+    const uint32_t pre = block_exclusive_scan256(x, tmp, &sum);
+    if (b < nblk) row[b] = carry + pre;
+    carry += sum;
   }
 }
 
-// 4c. stable scatter: rank inside the tile = earlier warps + earlier rounds + earlier lanes
+// 4c. stable scatter. A tile of 4096 keys is ranked (rank = earlier warps + earlier
+// rounds + earlier lanes with the same digit), laid out digit-sorted in shared
+// memory, then written out in that order, so consecutive threads write consecutive
+// addresses of one digit's run.
 __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     unsigned long long* mk0, unsigned long long* mk1, int32_t* ix0, int32_t* ix1, int64_t N,
-    int pass, int64_t nblk, const uint32_t* __restrict__ cnt, const KmapStatus* st) {
+    int pass, int64_t nblk, const uint32_t* __restrict__ cnt, KmapStatus* st) {
   const int plan = st->plan[pass];
   if (!(plan & 2)) return;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
@@ -254,12 +270,18 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
   constexpr int kWarps = kSortThreads / 32;
   constexpr int kPerWarp = kSortTile / kWarps;           // 512
   constexpr int kRounds = kPerWarp / 32;                 // 16
-  __shared__ uint32_t wcnt[kWarps][257];
+  extern __shared__ __align__(16) unsigned char sort_sm[];
+  unsigned long long* skey = reinterpret_cast<unsigned long long*>(sort_sm);
+  int32_t* srow = reinterpret_cast<int32_t*>(sort_sm + kSortTile * 8);
+  uint32_t* wcnt = reinterpret_cast<uint32_t*>(sort_sm + kSortTile * 12);   // [kWarps][257]
+  uint32_t* loff = wcnt + kWarps * 257;                                       // [256]
+  __shared__ uint32_t tmp[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * 257; i += kSortThreads) (&wcnt[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kWarps * 257; i += kSortThreads) wcnt[i] = 0;
   __syncthreads();
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t base = blockIdx.x * int64_t(kSortTile) + warp * kPerWarp;
+  const int64_t tile0 = blockIdx.x * int64_t(kSortTile);
+  const int64_t base = tile0 + warp * kPerWarp;
   unsigned long long key[kRounds];
   int32_t row[kRounds];
   uint32_t rank[kRounds];
@@ -272,21 +294,23 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     const uint32_t d = valid ? static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u) : 256u;
     const unsigned peers = __match_any_sync(0xffffffffu, d);
     const uint32_t before = __popc(peers & lt_mask);
-    const uint32_t prior = wcnt[warp][d];
+    const uint32_t prior = wcnt[warp * 257 + d];
     __syncwarp();
-    if (before == 0) wcnt[warp][d] = prior + __popc(peers);
+    if (before == 0) wcnt[warp * 257 + d] = prior + __popc(peers);
     __syncwarp();
     rank[r] = prior + before;
   }
   __syncthreads();
-  {   // exclusive scan over warps, one thread per digit
+  {   // per digit: exclusive over warps, then the digit's start inside the tile
     const int d = threadIdx.x;
     uint32_t run = 0;
     for (int w = 0; w < kWarps; ++w) {
-      const uint32_t c = wcnt[w][d];
-      wcnt[w][d] = run;
+      const uint32_t c = wcnt[w * 257 + d];
+      wcnt[w * 257 + d] = run;
       run += c;
     }
+    uint32_t total;
+    loff[d] = block_exclusive_scan256(run, tmp, &total);
   }
   __syncthreads();
 #pragma unroll
@@ -294,61 +318,149 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     const int64_t e = base + r * 32 + lane;
     if (e < N) {
       const uint32_t d = static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u);
-      const int64_t pos =
-          int64_t(cnt[d * nblk + blockIdx.x]) + wcnt[warp][d] + rank[r];
-      if (pos < N) {
-        dst[pos] = key[r];
-        idst[pos] = row[r];
-      } else {
-        atomicOr(const_cast<int*>(&st->flags), kFlagInternal);
-      }
+      const uint32_t local = loff[d] + wcnt[warp * 257 + d] + rank[r];
+      skey[local] = key[r];
+      srow[local] = row[r];
+    }
+  }
+  __syncthreads();
+  const int nvalid = static_cast<int>((N - tile0) < kSortTile ? (N - tile0) : kSortTile);
+  for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
+    const unsigned long long k = skey[i];
+    const uint32_t d = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
+    const int64_t pos = int64_t(cnt[d * nblk + blockIdx.x]) + (i - static_cast<int>(loff[d]));
+    if (pos >= 0 && pos < N) {
+      dst[pos] = k;
+      idst[pos] = srow[i];
+    } else {
+      atomicOr(&st->flags, kFlagInternal);
     }
   }
 }
 
 // 5. ------------------------------------------------------------------------------
-__global__ void kmap_insert(const unsigned long long* __restrict__ keys,
-                            const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1,
-                            int64_t N, Slot* table, unsigned long long mask, int max_probe,
-                            int32_t* __restrict__ order, KmapStatus* st) {
-  const int32_t* sorted = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
+// Over the sorted order: duplicates (adjacent equal codes; the stable sort puts the
+// later input row second), block runs counted, the order written if asked for.
+__global__ void __launch_bounds__(256) kmap_blocks_count(
+    const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
+    const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N,
+    int32_t* __restrict__ order, KmapStatus* st) {
+  const bool second = st->plan[kMaxPasses] & 1;
+  const unsigned long long* mk = second ? mk1 : mk0;
+  const int32_t* ix = second ? ix1 : ix0;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  unsigned long long starts = 0;
+  for (int64_t s = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; s < N; s += stride) {
+    const unsigned long long m = mk[s];
+    const int32_t row = ix[s];
+    if (static_cast<uint64_t>(row) >= static_cast<uint64_t>(N)) atomicOr(&st->flags, kFlagInternal);
+    if (order) order[s] = row;
+    if (s == 0) {
+      ++starts;
+    } else {
+      const unsigned long long prev = mk[s - 1];
+      if ((prev >> 6) != (m >> 6)) ++starts;
+      if (prev == m) {
+        atomicOr(&st->flags, kFlagDup);
+        atomicMin(&st->bad_row, static_cast<long long>(row));
+      }
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) starts += __shfl_xor_sync(0xffffffffu, starts, o);
+  if ((threadIdx.x & 31) == 0 && starts) atomicAdd(&st->nblocks, starts);
+}
+
+// 6. ------------------------------------------------------------------------------
+// Capacity in use: the caller's, or the smallest power of two >= 2 x blocks (>= 64,
+// <= the workspace's). Clears exactly that many slots.
+__global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max, KmapStatus* st) {
+  unsigned long long cap = static_cast<unsigned long long>(cap_fixed);
+  if (cap == 0) {
+    cap = 64;
+    while (cap < 2 * st->nblocks && cap < static_cast<unsigned long long>(cap_max)) cap <<= 1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) st->cap = cap;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+       i < static_cast<int64_t>(cap); i += stride) {
+    Slot s;
+    s.key = kEmptyKey;
+    s.mask = 0;
+    table[i] = s;
+  }
+}
+
+// 7. ------------------------------------------------------------------------------
+// One thread per block run: its occupancy mask from the run's codes, its key from
+// the first voxel's coordinates, inserted with its first sorted position.
+__global__ void __launch_bounds__(256) kmap_blocks_insert(
+    const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
+    const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
+    const int32_t* __restrict__ ix1, int64_t N, Slot* table, int32_t* __restrict__ base,
+    KmapStatus* st) {
+  const bool second = st->plan[kMaxPasses] & 1;
+  const unsigned long long* mk = second ? mk1 : mk0;
+  const int32_t* ix = second ? ix1 : ix0;
+  const unsigned long long cap = st->cap;
+  const unsigned long long cmask = cap - 1;
+  const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t s = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; s < N; s += stride) {
-    const int32_t i = sorted[s];
-    if (static_cast<uint64_t>(i) >= static_cast<uint64_t>(N)) {
-      atomicOr(&st->flags, kFlagInternal);
-      continue;
+    const unsigned long long blk = mk[s] >> 6;
+    if (s > 0 && (mk[s - 1] >> 6) == blk) continue;
+    unsigned long long mask = 0;
+    for (int64_t j0 = s; j0 < N && j0 < s + 128; j0 += 8) {   // a run: <= 64 codes unless duplicated
+      unsigned long long m[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m[u] = j0 + u < N ? mk[j0 + u] : ~0ull;   // loads in flight together
+      bool ended = false;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ended = ended || (m[u] >> 6) != blk;
+        if (!ended) mask |= 1ull << (m[u] & 63u);
+      }
+      if (ended) break;
     }
-    if (order) order[s] = i;
-    const unsigned long long key = keys[i];
-    unsigned long long h = home_slot(key, mask);
+    const int32_t row = ix[s];
+    if (static_cast<uint64_t>(row) >= static_cast<uint64_t>(N)) continue;   // flagged in step 5
+    const int4 c = coords[row];
+    const unsigned long long key = block_key(c.x, c.y, c.z, c.w);
+    unsigned long long h = mix64(key) & cmask;
     int probe = 0;
     for (; probe < max_probe; ++probe) {
       const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, key);
       if (prev == kEmptyKey) {
-        table[h].row = i;
+        table[h].mask = mask;
+        base[h] = static_cast<int32_t>(s);
         break;
       }
-      if (prev == key) {
-        atomicOr(&st->flags, kFlagDup);
-        atomicMin(&st->bad_row, static_cast<long long>(i));
+      if (prev == key) {   // two runs of one block: only possible for rejected coordinates
+        atomicOr(&st->flags, kFlagInternal);
         break;
       }
-      h = (h + 1) & mask;
+      h = (h + 1) & cmask;
     }
     if (probe == max_probe) atomicOr(&st->flags, kFlagFull);
   }
 }
 
-// 6. ------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) kmap_probe(const int4* __restrict__ coords, int64_t N,
-                                                  int res, const Slot* __restrict__ table,
-                                                  unsigned long long mask, int max_probe,
-                                                  int32_t* __restrict__ nbr, KmapStatus* st) {
+// 8. ------------------------------------------------------------------------------
+// Voxels in input order, so that a warp's 32 x 27 results are one contiguous stretch
+// of nbr (3456 bytes, fully written lines); the block table is small enough to stay
+// in L2, so the lookups need no spatial order.
+__global__ void __launch_bounds__(256) kmap_probe(
+    const int4* __restrict__ coords, const int32_t* __restrict__ ix0,
+    const int32_t* __restrict__ ix1, int64_t N, int res, const Slot* __restrict__ table,
+    const int32_t* __restrict__ base, int32_t* __restrict__ nbr, KmapStatus* st) {
+  const bool second = st->plan[kMaxPasses] & 1;
+  const int32_t* ix = second ? ix1 : ix0;
+  const unsigned long long cap = st->cap;
+  const unsigned long long cmask = cap - 1;
+  const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  bool full = false;
+  bool full = false, bad = false;
   for (int64_t v0 = warp_global * 32; v0 < N; v0 += nwarps * 32) {
     int4 mine = make_int4(0, 0, 0, 0);
     if (v0 + lane < N) mine = coords[v0 + lane];
@@ -367,17 +479,23 @@ __global__ void __launch_bounds__(256) kmap_probe(const int4* __restrict__ coord
         if (static_cast<unsigned>(z) < static_cast<unsigned>(res) &&
             static_cast<unsigned>(y) < static_cast<unsigned>(res) &&
             static_cast<unsigned>(x) < static_cast<unsigned>(res)) {
-          const unsigned long long key = pack_key(b, z, y, x);
-          unsigned long long h = home_slot(key, mask);
+          const unsigned long long key = block_key(b, z, y, x);
+          unsigned long long h = mix64(key) & cmask;
           int probe = 0;
           for (; probe < max_probe; ++probe) {
             const ulonglong2 s = __ldg(reinterpret_cast<const ulonglong2*>(table + h));
+            const int32_t sb = __ldg(base + h);   // independent of the slot's contents
             if (s.x == key) {
-              found = static_cast<int32_t>(s.y & 0xFFFFFFFFull);
+              const uint32_t bit = in_block_bit(z, y, x);
+              if ((s.y >> bit) & 1ull) {
+                const int64_t pos = int64_t(sb) + __popcll(s.y & ((1ull << bit) - 1ull));
+                if (pos < N) found = __ldg(ix + pos);
+                else bad = true;
+              }
               break;
             }
             if (s.x == kEmptyKey) break;
-            h = (h + 1) & mask;
+            h = (h + 1) & cmask;
           }
           if (probe == max_probe) full = true;
         }
@@ -386,6 +504,7 @@ __global__ void __launch_bounds__(256) kmap_probe(const int4* __restrict__ coord
     }
   }
   if (full) atomicOr(&st->flags, kFlagFull);
+  if (bad) atomicOr(&st->flags, kFlagInternal);
 }
 
 int grid_for(int64_t work, int threads, int per_sm) {
@@ -436,8 +555,8 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
               (const void*)coords, (void*)nbr, (void*)order);
     return SUBM3D_ERR_ARG;
   }
-  const int64_t cap = hash_capacity > 0 ? hash_capacity : default_hash_capacity(N);
-  const Layout L = make_layout(N, cap);
+  const int64_t cap_max = hash_capacity > 0 ? hash_capacity : default_hash_capacity(N);
+  const Layout L = make_layout(N, cap_max);
   if (reinterpret_cast<uintptr_t>(workspace) & 255) {
     set_error("subm3d_build_kmap: workspace=%p must be 256-byte aligned", workspace);
     return SUBM3D_ERR_WORKSPACE;
@@ -447,28 +566,31 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
               (long long)N);
     return SUBM3D_ERR_WORKSPACE;
   }
+  static bool attr_set = false;
+  if (!attr_set) {
+    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(kmap_sort_scatter,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScatterSmem));
+    attr_set = true;
+  }
   char* ws = static_cast<char*>(workspace);
   KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(ws + L.keys);
   unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
   unsigned long long* mk1 = reinterpret_cast<unsigned long long*>(ws + L.mk1);
   int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
   int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   Slot* table = reinterpret_cast<Slot*>(ws + L.table);
+  int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
 
-  int bits = 1;
+  int bits = 2;   // at least one whole 4x4x4 block level below the batch bits
   while ((1 << bits) < res) ++bits;
   const int npass = (3 * bits + 16 + 7) / 8;
-  const unsigned long long mask = static_cast<unsigned long long>(cap - 1);
-  const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
 
-  kmap_init<<<grid_for(cap, 256, 8), 256, 0, stream>>>(st, hist, table, cap);
+  kmap_init<<<8, 256, 0, stream>>>(st, hist);
   SUBM3D_LAUNCHED("kmap_init");
-  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, npass, keys, mk0, ix0,
-                                                     hist, st);
+  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, npass, mk0, ix0, hist, st);
   SUBM3D_LAUNCHED("kmap_pack");
   kmap_plan<<<1, 256, 0, stream>>>(hist, npass, N, st);
   SUBM3D_LAUNCHED("kmap_plan");
@@ -478,36 +600,43 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
     SUBM3D_LAUNCHED("kmap_sort_count");
     kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, L.nblk, cnt, st);
     SUBM3D_LAUNCHED("kmap_sort_scan");
-    kmap_sort_scatter<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, ix0, ix1, N, p, L.nblk, cnt, st);
+    kmap_sort_scatter<<<nblk, kSortThreads, kScatterSmem, stream>>>(mk0, mk1, ix0, ix1, N, p,
+                                                                    L.nblk, cnt, st);
     SUBM3D_LAUNCHED("kmap_sort_scatter");
   }
-  kmap_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(keys, ix0, ix1, N, table, mask, max_probe,
-                                                       order, st);
-  SUBM3D_LAUNCHED("kmap_insert");
-  kmap_probe<<<grid_for(N * 8, 256, 8), 256, 0, stream>>>(c4, N, res, table, mask, max_probe, nbr,
+  kmap_blocks_count<<<grid_for(N, 256, 8), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
+  SUBM3D_LAUNCHED("kmap_blocks_count");
+  kmap_table_init<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, hash_capacity, cap_max, st);
+  SUBM3D_LAUNCHED("kmap_table_init");
+  kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
+                                                              base, st);
+  SUBM3D_LAUNCHED("kmap_blocks_insert");
+  kmap_probe<<<grid_for(N * 8, 256, 8), 256, 0, stream>>>(c4, ix0, ix1, N, res, table, base, nbr,
                                                           st);
   SUBM3D_LAUNCHED("kmap_probe");
 
   KmapStatus host;
   SUBM3D_CUDA_TRY(cudaMemcpyAsync(&host, st, sizeof(host), cudaMemcpyDeviceToHost, stream));
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
-  if (host.flags & kFlagInternal) {
-    set_error("subm3d_build_kmap: internal error (sort produced an index outside [0, N))");
-    return SUBM3D_ERR_DEVICE;
-  }
   if (host.flags & kFlagCoord) {
     set_error("subm3d_build_kmap: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d",
               host.bad_row, SUBM3D_MAX_BATCH, res);
     return SUBM3D_ERR_COORD_RANGE;
   }
+  if (host.flags & kFlagInternal) {
+    set_error("subm3d_build_kmap: internal error (sort or block table produced an index outside "
+              "[0, N))");
+    return SUBM3D_ERR_DEVICE;
+  }
   if (host.flags & kFlagDup) {
-    set_error("subm3d_build_kmap: duplicate coordinate (row %lld repeats an earlier key)",
+    set_error("subm3d_build_kmap: duplicate coordinate (row %lld repeats an earlier row)",
               host.bad_row);
     return SUBM3D_ERR_DUPLICATE;
   }
   if (host.flags & kFlagFull) {
-    set_error("subm3d_build_kmap: hash probe limit %d exceeded (capacity %lld, N=%lld)", max_probe,
-              (long long)cap, (long long)N);
+    set_error("subm3d_build_kmap: %llu occupied 4x4x4 blocks do not fit a hash capacity of %llu "
+              "within %d probes (N=%lld)",
+              host.nblocks, host.cap, kMaxProbe, (long long)N);
     return SUBM3D_ERR_HASH_FULL;
   }
   return SUBM3D_OK;

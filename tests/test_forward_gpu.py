@@ -99,6 +99,40 @@ def test_forward_bf16_shapes(dev, I, O):
     assert_close(out.float().cpu().numpy()[rows], want, "bf16", f"I={I} O={O}")
 
 
+@pytest.mark.parametrize("I,O", [(16, 48), (48, 16), (48, 48), (64, 64), (64, 16), (32, 32)])
+def test_forward_narrow_kernel_shapes(dev, I, O):
+    # I, O in {16, 32, 48, 64}: the kernel that keeps the gathered rows in tensor memory
+    coords, v = shell_case(I * 11 + O * 3, 40, I, O, "bf16", batch=2)
+    N = coords.shape[0]
+    assert N % 128 != 0
+    nbr = subm3d_build_kmap(torch.from_numpy(coords).to(dev), 40)
+    out = subm3d_forward(bf16_tensor(v["feats"], dev), nbr, bf16_tensor(v["weight"], dev),
+                         bf16_tensor(v["bias"], dev))
+    subm3d_forward_status()
+    want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"], 40)
+    assert_close(out.float().cpu().numpy(), want, "bf16", f"I={I} O={O}")
+
+
+def test_forward_narrow_shape_with_16_byte_aligned_feats(dev):
+    # the narrow kernel needs 32-byte-aligned rows; a feats pointer that is only 16-byte
+    # aligned takes the shared-memory kernel, and both match the oracle
+    coords, v = shell_case(77, 40, 64, 64, "bf16", batch=2)
+    N = coords.shape[0]
+    nbr = subm3d_build_kmap(torch.from_numpy(coords).to(dev), 40)
+    f32b = bf16_tensor(v["feats"], dev)
+    flat = torch.empty(N * 64 + 8, dtype=torch.bfloat16, device=dev)
+    f16b = flat[8:].view(N, 64)
+    f16b.copy_(f32b)
+    assert f32b.data_ptr() % 32 == 0 and f16b.data_ptr() % 32 == 16
+    w, b = bf16_tensor(v["weight"], dev), bf16_tensor(v["bias"], dev)
+    o1 = subm3d_forward(f32b, nbr, w, b)
+    o2 = subm3d_forward(f16b, nbr, w, b)
+    subm3d_forward_status()
+    want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"], 40)
+    assert_close(o1.float().cpu().numpy(), want, "bf16", "32-byte aligned")
+    assert_close(o2.float().cpu().numpy(), want, "bf16", "16-byte aligned")
+
+
 @pytest.mark.parametrize("I,O", [(32, 32), (16, 8), (3, 5), (64, 96), (1, 1), (130, 70)])
 def test_forward_fp32_shapes(dev, I, O):
     coords, v = shell_case(I + 1000 * O, 24, I, O, "f32")

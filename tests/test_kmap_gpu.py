@@ -106,14 +106,19 @@ def test_kmap_errors_and_recovery(dev):
 
 
 def test_kmap_hash_full_is_reported(dev):
+    # 100 voxels, each in an aligned 4x4x4 block of its own: 100 occupied blocks
     rng = np.random.default_rng(3)
-    c = torch.from_numpy(random_set(rng, 10, 1, 100)).to(dev)
+    cells = rng.choice(16 ** 3, size=100, replace=False)
+    c = np.zeros((100, 4), np.int32)
+    c[:, 1], c[:, 2], c[:, 3] = 4 * (cells // 256), 4 * ((cells // 16) % 16), 4 * (cells % 16)
+    c[:, 1:] += rng.integers(0, 4, size=(100, 3)).astype(np.int32)
+    ct = torch.from_numpy(c).to(dev)
     with pytest.raises(Subm3dError) as e:
-        subm3d_build_kmap_ex(c, 10, hash_capacity=64)
+        subm3d_build_kmap_ex(ct, 64, hash_capacity=64)
     assert e.value.code == B.ERR_HASH_FULL
-    # the smallest capacity that holds the set works, with long probe chains
-    nbr, _ = subm3d_build_kmap_ex(c, 10, hash_capacity=128)
-    np.testing.assert_array_equal(nbr.cpu().numpy(), ref.kernel_map(c.cpu().numpy(), 10))
+    # the smallest capacity that holds the blocks works, with long probe chains
+    nbr, _ = subm3d_build_kmap_ex(ct, 64, hash_capacity=128)
+    np.testing.assert_array_equal(nbr.cpu().numpy(), ref.kernel_map(c, 64))
 
 
 def test_kmap_reuses_dirty_workspace(dev):

@@ -11,21 +11,25 @@
 // stage costs 48 KB of shared-memory traffic at O = 64 (16 KB of cp.async writes,
 // most of them zero-fill, the MMA re-reading them, and the weight tile written and
 // read), and the shared-memory port, not HBM, sets the pace. Here:
-//   * the weight, 27 x [O x 64] K-major tiles with 128-byte swizzle (216 KB at
-//     I = O = 64), is loaded once per CTA by TMA and stays resident;
 //   * each producer thread gathers one neighbour row (I bf16 <= 128 bytes) into
 //     registers with 32-byte read-only loads, an absent neighbour costing no load at
 //     all (zeros), and writes it with tcgen05.st into a tensor-memory stage, the row
 //     in the lane of its output row, channels 2c and 2c+1 in column c;
-//   * tcgen05.mma reads A from tensor memory and only B (the resident weight tap)
-//     from shared memory.
+//   * tcgen05.mma reads A from tensor memory and only B, the stage's weight tap
+//     W_k = weight[:, kz, ky, kx, :] ([O x 64] K-major, 128-byte swizzle, fetched by
+//     TMA into the stage's weight slot), from shared memory;
+//   * a loader warp copies each tile's 128 x 27 block of nbr (13.8 KB, contiguous)
+//     into a double-buffered shared-memory ring with one bulk copy, a tile ahead, so
+//     a producer reads its row's index with one conflict-free shared load (27 is
+//     odd) instead of one 32-byte global sector per 4-byte index.
 // Tensor memory (512 columns): two accumulators of 64 columns (double buffer) and
 // twelve A stages of 32 columns. Stage g of the CTA (tile, offset k) is written by
 // producer group g mod 6 (four warps, warp w writing lanes 32 (w % 4) .. + 31) and
-// lives in slot g mod 12. A group has one stage's loads in flight while it waits for
-// its slot; it marks the stage full (one arrival per warp) after tcgen05.wait::st.
+// lives in slot g mod 12 (A in tensor memory, W_k in shared memory). A group has one
+// stage's loads in flight while it waits for its slot; the stage is full when its
+// four warps have arrived (after tcgen05.wait::st) and its weight bytes have landed.
 // One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
-// up to four) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
+// up to four) and frees the slot (both halves) with tcgen05.commit. Four epilogue warps drain tile
 // t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> 16-byte stores) while
 // the tensor core works on tile t + 1.
 //
@@ -45,9 +49,12 @@ constexpr int kStages = 12;           // A stages in tensor memory
 constexpr int kStageCols = 32;        // 64 bf16 per row = 32 columns of 32 bits
 constexpr int kAccCols = 64;          // one accumulator (N <= 64)
 constexpr int kAColBase = 2 * kAccCols;
-constexpr int kMmaWarp = 4 * kGroups;
-constexpr int kEpiWarp0 = kMmaWarp + 1;
-constexpr int kThreads = 32 * (kEpiWarp0 + 4);   // 928
+constexpr int kProducerWarps = 4 * kGroups;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 25..28: lane groups 1, 2, 3, 0
+constexpr int kNbrWarp = kEpiWarp0 + 4;
+constexpr int kThreads = 32 * (kNbrWarp + 1);    // 960
+constexpr int kNbrTileBytes = kBM * 27 * 4;      // one tile's rows of nbr
 constexpr int kSmemLimit = 227 * 1024;
 static_assert(kAColBase + kStages * kStageCols == 512, "tensor memory layout");
 static_assert(kStages % kGroups == 0, "slots per group");
@@ -55,8 +62,9 @@ static_assert(kStages % kGroups == 0, "slots per group");
 template <int NMMA>
 struct TmCfg {
   static constexpr int kTapBytes = NMMA * 128;            // one [NMMA x 64] weight tile
-  static constexpr int kWBytes = 27 * kTapBytes;
-  static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 512 /*barriers*/ + 256 * 4 /*bias*/;
+  static constexpr int kWBytes = kStages * kTapBytes;     // one weight slot per stage
+  static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 2 * kNbrTileBytes +
+                               512 /*barriers*/ + 256 * 4 /*bias*/;
   // at least half the SM's shared memory, so that one CTA (which takes all of tensor
   // memory) runs per SM
   static constexpr int kSmemBytes = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
@@ -172,17 +180,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sW = base;                                   // 27 weight taps
-  uint8_t* misc = base_ptr + C::kWBytes;
-  // barriers: afull[12], aempty[12], accf[2], acce[2], wfull, drain
+  const uint32_t sW = base;                                   // kStages weight slots
+  const uint32_t sNbr = base + C::kWBytes;                    // 2 x 13.8 KB
+  const int32_t* nbr_sm = reinterpret_cast<const int32_t*>(base_ptr + C::kWBytes);
+  uint8_t* misc = base_ptr + C::kWBytes + 2 * kNbrTileBytes;
+  // barriers: afull[12], aempty[12], accf[2], acce[2], nbrf[2], nbre[2], drain
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   const uint32_t afull0 = smem_u32(bars);
   const uint32_t aempty0 = afull0 + 8 * kStages;
   const uint32_t accf0 = aempty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 16;
-  const uint32_t wfull = acce0 + 16;
-  const uint32_t drain = wfull + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * kStages + 6));
+  const uint32_t nbrf0 = acce0 + 16;
+  const uint32_t nbre0 = nbrf0 + 16;
+  const uint32_t drain = nbre0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * kStages + 9));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* bias_sm = reinterpret_cast<float*>(misc + 512);
 
@@ -195,23 +206,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(afull0 + 8 * s, 4);     // one arrival per producer warp
+      mbar_init(afull0 + 8 * s, 5);     // the group's four warps + the weight TMA's expect_tx
       mbar_init(aempty0 + 8 * s, 1);    // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
       mbar_init(acce0 + 8 * b, 128);
+      mbar_init(nbrf0 + 8 * b, 1);
+      mbar_init(nbre0 + 8 * b, kProducerWarps);
     }
-    mbar_init(wfull, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&wmap);
-    // the whole weight, once: tap k -> [NMMA x 64] K-major tile at sW + k * kTapBytes
-    mbar_arrive_expect_tx(wfull, C::kWBytes);
-    for (int k = 0; k < 27; ++k) tma_load_3d(sW + k * C::kTapBytes, &wmap, wfull, 0, k, 0);
   }
-  if (warp >= kEpiWarp0) {
+  if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     for (int o = tid - kEpiWarp0 * 32; o < NMMA; o += 128)
       bias_sm[o] = (p.bias && o < p.O) ? __bfloat162float(p.bias[o]) : 0.f;
   }
@@ -224,30 +233,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < kMmaWarp) {
+  if (warp < kProducerWarps) {
     // ------------------------------------------------------------------ producers
     const int grp = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;       // row of the tile = tensor-memory lane
+    const bool leader = quarter == 0 && lane == 0;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     bool bad = false, aborted = false;
-    auto row_of = [&](uint32_t g) -> int32_t {
-      const uint32_t lt = g / 27u, k = g - lt * 27u;
+    int cur = -1;                            // tile whose nbr block this warp is reading
+    uint32_t last = 0;                       // one past the last stage this group issued
+    for (uint32_t g = grp; g < total; g += kGroups) {
+      const int lt = static_cast<int>(g / 27u);
+      const int k = static_cast<int>(g - static_cast<uint32_t>(lt) * 27u);
+      if (lt != cur) {   // move to tile lt's nbr block (and release the previous one)
+        if (cur >= 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(nbre0 + 8 * (cur & 1));
+        }
+        const bool ok = mbar_wait(nbrf0 + 8 * (lt & 1), (lt >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
+        }
+        cur = lt;
+      }
       const int64_t row = int64_t(blockIdx.x + lt * gridDim.x) * kBM + r;
-      int32_t v = -1;
+      int32_t j = -1;
       if (row < p.N) {
-        v = __ldg(p.nbr + row * 27 + k);
-        if (v < -1 || v >= p.N) {
+        j = nbr_sm[(lt & 1) * (kBM * 27) + r * 27 + k];
+        if (j < -1 || j >= p.N) {
           bad = true;
-          v = -1;
+          j = -1;
         }
       }
-      return v;
-    };
-    int32_t jn = static_cast<uint32_t>(grp) < total ? row_of(grp) : -1;
-    for (uint32_t g = grp; g < total; g += kGroups) {
-      const int32_t j = jn;
-      if (g + kGroups < total) jn = row_of(g + kGroups);   // next stage's row, in flight
       uint32_t v[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {   // 16 channels (32 bytes) per load
@@ -265,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         aborted = true;
         break;
       }
+      if (leader) {   // the stage's weight tap into its slot
+        mbar_arrive_expect_tx(afull0 + 8 * s, C::kTapBytes);
+        tma_load_3d(sW + s * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k, 0);
+      }
+      last = g + kGroups;
       tc_fence_after();
       tmem_st32(tmem_base + lane_addr + kAColBase + s * kStageCols, v);
       tmem_st_wait();
@@ -277,21 +301,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.err, kDevErrTimeout);
     }
-    if (tid == 0) tm_drain_wait(wfull, 0);   // the weight TMA has landed before the CTA exits
+    if (aborted && leader) {   // no weight TMA of this group may still be landing
+      for (uint32_t x = last >= static_cast<uint32_t>(kStages) ? last - kStages : 0u; x < last; ++x)
+        if (x % kGroups == static_cast<uint32_t>(grp))
+          tm_drain_wait(afull0 + 8 * (x % kStages), (x / kStages) & 1u);
+    }
+  } else if (warp == kNbrWarp) {
+    // ------------------------------------------------------------------ nbr staging
+    if (lane == 0) {
+      int issued = 0;
+      bool aborted = false;
+      for (int lt = 0; lt < ntl; ++lt, ++issued) {
+        const uint32_t nb = lt & 1;
+        if (!mbar_wait(nbre0 + 8 * nb, ((lt >> 1) & 1) ^ 1, abort_flag)) {
+          aborted = true;
+          break;
+        }
+        const int64_t row0 = int64_t(blockIdx.x + lt * gridDim.x) * kBM;
+        const int64_t rows = (p.N - row0) < kBM ? (p.N - row0) : kBM;
+        const uint32_t bytes = static_cast<uint32_t>(rows) * 108u;
+        const uint32_t bulk = bytes & ~15u;
+        int32_t* dst = const_cast<int32_t*>(nbr_sm) + nb * (kBM * 27);
+        for (uint32_t off = bulk; off < bytes; off += 4)   // ragged tail of the last tile
+          dst[off / 4] = __ldg(p.nbr + row0 * 27 + off / 4);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(nbrf0 + 8 * nb, bulk);
+        bulk_load(sNbr + nb * kNbrTileBytes, p.nbr + row0 * 27, bulk, nbrf0 + 8 * nb);
+        if (lt + 2 < ntl) {   // the block after next into L2
+          const int64_t row2 = int64_t(blockIdx.x + (lt + 2) * gridDim.x) * kBM;
+          const int64_t rows2 = (p.N - row2) < kBM ? (p.N - row2) : kBM;
+          const uint32_t b2 = static_cast<uint32_t>(rows2 * 108) & ~15u;
+          if (b2) bulk_prefetch_l2(p.nbr + row2 * 27, b2);
+        }
+      }
+      // every copy this warp issued has landed before the CTA may exit
+      for (int x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
+        tm_drain_wait(nbrf0 + 8 * (x & 1), (x >> 1) & 1);
+      if (aborted) {
+        *abort_flag = 1;
+        atomicOr(p.err, kDevErrTimeout);
+      }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
     const uint32_t idesc = tm_idesc<NMMA>();
     const int ksteps = (p.I + 15) / 16;
     const uint64_t w0 = tm_sw128_desc(sW);
-    bool aborted = !__all_sync(0xffffffffu, mbar_wait(wfull, 0, abort_flag));
+    bool aborted = false;
     uint32_t g = 0;
     for (int t = 0; t < ntl && !aborted; ++t) {
-      if (t + 1 < ntl && lane == 0) {   // the next tile's nbr block into L2 while this tile runs
-        const int64_t row1 = int64_t(blockIdx.x + (t + 1) * gridDim.x) * kBM;
-        const int64_t rows = (p.N - row1) < kBM ? (p.N - row1) : kBM;
-        const uint32_t bytes = static_cast<uint32_t>(rows * 108) & ~15u;
-        if (bytes) bulk_prefetch_l2(p.nbr + row1 * 27, bytes);
-      }
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag))) {
@@ -308,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         tm_mma_stage(d_tmem, tmem_base + kAColBase + s * kStageCols,
-                     w0 + static_cast<uint64_t>(k) * (C::kTapBytes >> 4), idesc, ksteps,
+                     w0 + static_cast<uint64_t>(s) * (C::kTapBytes >> 4), idesc, ksteps,
                      k == 0 ? 0u : 1u);
         tm_commit(aempty0 + 8 * s);
       }

@@ -23,12 +23,11 @@
 //   7. insert  : one slot per block, {packed block key b<<42|bz<<28|by<<14|bx,
 //                64-bit occupancy mask}, plus the block's first sorted position;
 //                open addressing, atomicCAS, bounded linear probing
-//   8. probe   : a warp takes 32 consecutive voxels (input order) and spreads their
-//                32 x 27 (voxel, offset) lookups over its lanes. A lookup finds the
-//                neighbour's block, tests its bit and turns the bit's rank inside
-//                the mask into a sorted position, whose input row is the answer.
-//                Lane l of round t writes nbr[v0 * 27 + 32 t + l]: the warp writes
-//                one contiguous stretch of the table.
+//   8. probe   : a thread per voxel (input order) looks up the at most 2 x 2 x 2
+//                blocks its 27 neighbours fall in; a neighbour is then a bit test,
+//                and the bit's rank inside the mask turns into a sorted position,
+//                whose input row is the answer. A block's 128 rows of results are
+//                staged in shared memory and written as one contiguous stretch.
 //
 // The blocks of a shell hold ~10 voxels each, so the table is about a tenth of a
 // per-voxel table and stays in L2.
@@ -445,63 +444,102 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 }
 
 // 8. ------------------------------------------------------------------------------
-// Voxels in input order, so that a warp's 32 x 27 results are one contiguous stretch
-// of nbr (3456 bytes, fully written lines); the block table is small enough to stay
-// in L2, so the lookups need no spatial order.
-__global__ void __launch_bounds__(256) kmap_probe(
+// One thread per voxel, in input order. Along each axis the three neighbour
+// coordinates fall in the voxel's own 4-block or, when the voxel sits on the block's
+// low (high) face, partly in the block below (above); so the 27 neighbours lie in
+// at most 2 x 2 x 2 blocks, looked up once each (about 3.4 per voxel on a shell) and
+// kept in shared memory. Each of the 27 offsets is then a bit test, a popcount and
+// one load of the input row at the sorted position. A block's 128 rows of results
+// are staged in shared memory and written out as one contiguous stretch of nbr.
+constexpr int kProbeThreads = 128;
+
+__device__ __forceinline__ void block_lookup(const Slot* __restrict__ table,
+                                             const int32_t* __restrict__ base,
+                                             unsigned long long key, unsigned long long cmask,
+                                             int max_probe, unsigned long long& mask,
+                                             int32_t& start, bool& full) {
+  unsigned long long h = mix64(key) & cmask;
+  mask = 0;
+  start = 0;
+  int probe = 0;
+  for (; probe < max_probe; ++probe) {
+    const ulonglong2 s = __ldg(reinterpret_cast<const ulonglong2*>(table + h));
+    if (s.x == key) {
+      mask = s.y;
+      start = __ldg(base + h);
+      return;
+    }
+    if (s.x == kEmptyKey) return;
+    h = (h + 1) & cmask;
+  }
+  full = true;
+}
+
+__global__ void __launch_bounds__(kProbeThreads) kmap_probe(
     const int4* __restrict__ coords, const int32_t* __restrict__ ix0,
     const int32_t* __restrict__ ix1, int64_t N, int res, const Slot* __restrict__ table,
     const int32_t* __restrict__ base, int32_t* __restrict__ nbr, KmapStatus* st) {
+  __shared__ unsigned long long s_mask[8][kProbeThreads];
+  __shared__ int32_t s_start[8][kProbeThreads];
+  __shared__ __align__(16) int32_t s_out[kProbeThreads * 27];
   const bool second = st->plan[kMaxPasses] & 1;
   const int32_t* ix = second ? ix1 : ix0;
   const unsigned long long cap = st->cap;
   const unsigned long long cmask = cap - 1;
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int t = threadIdx.x;
   bool full = false, bad = false;
-  for (int64_t v0 = warp_global * 32; v0 < N; v0 += nwarps * 32) {
-    int4 mine = make_int4(0, 0, 0, 0);
-    if (v0 + lane < N) mine = coords[v0 + lane];
-    const int64_t nv = (N - v0) < 32 ? (N - v0) : 32;
-#pragma unroll 1
-    for (int t = 0; t < 27; ++t) {
-      const int p = t * 32 + lane;          // flat (voxel, offset) index inside the warp's rows
-      const int vv = p / 27;
-      const int k = p - vv * 27;
-      const int b = __shfl_sync(0xffffffffu, mine.x, vv);
-      const int z = __shfl_sync(0xffffffffu, mine.y, vv) + (k / 9) - 1;
-      const int y = __shfl_sync(0xffffffffu, mine.z, vv) + ((k / 3) % 3) - 1;
-      const int x = __shfl_sync(0xffffffffu, mine.w, vv) + (k % 3) - 1;
-      if (vv < nv) {
-        int32_t found = -1;
-        if (static_cast<unsigned>(z) < static_cast<unsigned>(res) &&
-            static_cast<unsigned>(y) < static_cast<unsigned>(res) &&
-            static_cast<unsigned>(x) < static_cast<unsigned>(res)) {
-          const unsigned long long key = block_key(b, z, y, x);
-          unsigned long long h = mix64(key) & cmask;
-          int probe = 0;
-          for (; probe < max_probe; ++probe) {
-            const ulonglong2 s = __ldg(reinterpret_cast<const ulonglong2*>(table + h));
-            const int32_t sb = __ldg(base + h);   // independent of the slot's contents
-            if (s.x == key) {
-              const uint32_t bit = in_block_bit(z, y, x);
-              if ((s.y >> bit) & 1ull) {
-                const int64_t pos = int64_t(sb) + __popcll(s.y & ((1ull << bit) - 1ull));
-                if (pos < N) found = __ldg(ix + pos);
-                else bad = true;
-              }
-              break;
-            }
-            if (s.x == kEmptyKey) break;
-            h = (h + 1) & cmask;
+  for (int64_t v0 = blockIdx.x * int64_t(kProbeThreads); v0 < N;
+       v0 += int64_t(gridDim.x) * kProbeThreads) {
+    const int64_t i = v0 + t;
+    if (i < N) {
+      const int4 c = coords[i];   // (b, z, y, x)
+      const int z = c.y, y = c.z, x = c.w;
+      // direction of the second block along each axis (0: none needed)
+      const int oz = ((z & 3) == 0 && z > 0) ? -1 : ((z & 3) == 3 && z + 1 < res) ? 1 : 0;
+      const int oy = ((y & 3) == 0 && y > 0) ? -1 : ((y & 3) == 3 && y + 1 < res) ? 1 : 0;
+      const int ox = ((x & 3) == 0 && x > 0) ? -1 : ((x & 3) == 3 && x + 1 < res) ? 1 : 0;
+#pragma unroll
+      for (int combo = 0; combo < 8; ++combo) {
+        const int sz = combo >> 2, sy = (combo >> 1) & 1, sx = combo & 1;
+        if ((sz && !oz) || (sy && !oy) || (sx && !ox)) continue;
+        const unsigned long long key =
+            block_key(c.x, z + 4 * sz * oz, y + 4 * sy * oy, x + 4 * sx * ox);
+        unsigned long long m;
+        int32_t st0;
+        block_lookup(table, base, key, cmask, max_probe, m, st0, full);
+        s_mask[combo][t] = m;
+        s_start[combo][t] = st0;
+      }
+#pragma unroll
+      for (int k = 0; k < 27; ++k) {
+        const int dz = k / 9 - 1, dy = (k / 3) % 3 - 1, dx = k % 3 - 1;
+        const int zz = z + dz, yy = y + dy, xx = x + dx;
+        int32_t val = -1;
+        if (static_cast<unsigned>(zz) < static_cast<unsigned>(res) &&
+            static_cast<unsigned>(yy) < static_cast<unsigned>(res) &&
+            static_cast<unsigned>(xx) < static_cast<unsigned>(res)) {
+          const int combo = ((dz != 0 && dz == oz) ? 4 : 0) | ((dy != 0 && dy == oy) ? 2 : 0) |
+                            ((dx != 0 && dx == ox) ? 1 : 0);
+          const unsigned long long m = s_mask[combo][t];
+          const uint32_t bit = in_block_bit(zz, yy, xx);
+          if ((m >> bit) & 1ull) {
+            const int64_t pos = int64_t(s_start[combo][t]) + __popcll(m & ((1ull << bit) - 1ull));
+            if (pos < N) val = __ldg(ix + pos);
+            else bad = true;
           }
-          if (probe == max_probe) full = true;
         }
-        nbr[v0 * 27 + p] = found;
+        s_out[t * 27 + k] = val;
       }
     }
+    __syncthreads();
+    const int64_t nv = (N - v0) < kProbeThreads ? (N - v0) : kProbeThreads;
+    const int nwords = static_cast<int>(nv) * 27;
+    int4* dst4 = reinterpret_cast<int4*>(nbr + v0 * 27);   // v0 * 108 bytes: 16-byte aligned
+    const int4* src4 = reinterpret_cast<const int4*>(s_out);
+    for (int w = t; w < nwords / 4; w += kProbeThreads) dst4[w] = src4[w];
+    for (int w = (nwords / 4) * 4 + t; w < nwords; w += kProbeThreads) nbr[v0 * 27 + w] = s_out[w];
+    __syncthreads();
   }
   if (full) atomicOr(&st->flags, kFlagFull);
   if (bad) atomicOr(&st->flags, kFlagInternal);
@@ -611,8 +649,8 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
   kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
                                                               base, st);
   SUBM3D_LAUNCHED("kmap_blocks_insert");
-  kmap_probe<<<grid_for(N * 8, 256, 8), 256, 0, stream>>>(c4, ix0, ix1, N, res, table, base, nbr,
-                                                          st);
+  kmap_probe<<<grid_for(N, kProbeThreads, 16), kProbeThreads, 0, stream>>>(c4, ix0, ix1, N, res,
+                                                                           table, base, nbr, st);
   SUBM3D_LAUNCHED("kmap_probe");
 
   KmapStatus host;

@@ -35,8 +35,16 @@ METRIC = "SubMConv3d bf16 TFLOP/s & Mvoxels/s (fraction of roofline); kmap build
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 CPU_SAMPLE_VOXELS = 4_000_000      # oracle CPU baseline: up to the first 4 M voxels (raster order)
 REF_STEP_FLOPS = 2e9               # reference arm: ~2 GFLOP of oracle work per step
-PROFILE = os.path.join(ROOT, "profiles", "fwd_tc_shells16_1024.md")
-KERNEL_SRC = os.path.join(ROOT, "submanifold_sparse_convolution_04_b300", "csrc", "forward_tc.cu")
+CSRC = os.path.join(ROOT, "submanifold_sparse_convolution_04_b300", "csrc")
+
+
+def forward_kernel(I, O):
+    """(kernel name, source file) of the bf16 forward the library picks for I x O: the
+    narrow kernel (gathered rows in tensor memory) for I, O in {16, 32, 48, 64}, else
+    the shared-memory-staged one (torch allocations are 32-byte aligned)."""
+    if I in (16, 32, 48, 64) and O in (16, 32, 48, 64):
+        return "fwd_tm", os.path.join(CSRC, "forward_tm.cu")
+    return "fwd_tc", os.path.join(CSRC, "forward_tc.cu")
 
 
 def parse_args():
@@ -181,23 +189,25 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------- roofline
 
-def recorded_traffic():
-    """dram bytes per forward launch from the committed ncu summary, if it was taken on
-    the current kernel source (sha256 of forward_tc.cu recorded beside the number)."""
-    if not os.path.exists(PROFILE):
+def recorded_traffic(kernel, src, workload):
+    """dram bytes per forward launch from the committed ncu summary of this kernel on
+    this workload, if it was taken on the current kernel source (sha256 recorded beside
+    the number)."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(prof):
         return None, "no ncu summary"
-    text = open(PROFILE).read()
+    text = open(prof).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"forward_tc_sha256:\s*([0-9a-f]{64})", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None, "ncu summary has no traffic line"
-    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if h.group(1) != cur:
         return None, "kernel changed since the ncu capture"
-    return float(m.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum"
+    return float(m.group(1)), f"ncu dram__bytes_read.sum + dram__bytes_write.sum ({os.path.relpath(prof, ROOT)})"
 
 
-def roofline(N, P, I, O, fwd_s, peaks, peak_kind):
+def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload):
     e = 2
     gathered = P * I * e + N * O * e + 108 * N + 27 * I * O * e
     compulsory = N * I * e + N * O * e + 108 * N + 27 * I * O * e
@@ -206,9 +216,10 @@ def roofline(N, P, I, O, fwd_s, peaks, peak_kind):
     tc = float(peaks["bf16_tflops"])
     achieved = gathered / fwd_s / 1e9
     t_roof = max(flops / (tc * 1e12), gathered / (hbm * 1e9))
-    traffic, traffic_src = recorded_traffic()
+    kernel, src = forward_kernel(I, O)
+    traffic, traffic_src = recorded_traffic(kernel, src, workload)
     return {
-        "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
         "frac": achieved / hbm, "traffic": traffic, "peak_source": f"hbm_gbs, {peak_kind}",
         "algorithmic_bytes": gathered, "traffic_source": traffic_src,
         "compulsory_bytes": compulsory, "compulsory_frac": compulsory / fwd_s / 1e9 / hbm,
@@ -382,7 +393,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
-    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind)
+    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind, case["name"])
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -12,7 +12,7 @@
 //                bits >= 2; all-pass digit histograms
 //   3. plan    : which 8-bit radix passes are not constant (others are skipped)
 //   4. passes  : LSD radix sort of (sort key, row) -- count / scan / stable scatter;
-//                the scatter ranks a 4096-key tile in shared memory and writes each
+//                the scatter ranks a 2048-key tile in shared memory and writes each
 //                digit's run contiguously
 //   5. blocks  : the low 6 bits of a Morton code are the voxel's place inside its
 //                aligned 4x4x4 block and the bits above name the block, so in sorted
@@ -39,7 +39,7 @@ namespace {
 
 constexpr unsigned long long kEmptyKey = ~0ull;
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 16;
+constexpr int kSortItems = 8;   // 2048-key tiles: ~80 registers, three blocks per SM
 constexpr int kSortTile = kSortThreads * kSortItems;   // keys per sort block
 constexpr int kMaxPasses = 8;
 constexpr int kMaxProbe = 4096;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict
   }
 }
 
-// 4c. stable scatter. A tile of 4096 keys is ranked (rank = earlier warps + earlier
+// 4c. stable scatter. A tile of 2048 keys is ranked (rank = earlier warps + earlier
 // rounds + earlier lanes with the same digit), laid out digit-sorted in shared
 // memory, then written out in that order, so consecutive threads write consecutive
 // addresses of one digit's run.
@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
   const int32_t* isrc = (plan & 1) ? ix1 : ix0;
   int32_t* idst = (plan & 1) ? ix0 : ix1;
   constexpr int kWarps = kSortThreads / 32;
-  constexpr int kPerWarp = kSortTile / kWarps;           // 512
-  constexpr int kRounds = kPerWarp / 32;                 // 16
+  constexpr int kPerWarp = kSortTile / kWarps;           // 256
+  constexpr int kRounds = kPerWarp / 32;                 // 8
   extern __shared__ __align__(16) unsigned char sort_sm[];
   unsigned long long* skey = reinterpret_cast<unsigned long long*>(sort_sm);
   int32_t* srow = reinterpret_cast<int32_t*>(sort_sm + kSortTile * 8);
@@ -390,8 +390,12 @@ __global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max,
 }
 
 // 7. ------------------------------------------------------------------------------
-// One thread per block run: its occupancy mask from the run's codes, its key from
-// the first voxel's coordinates, inserted with its first sorted position.
+// A warp takes 32 consecutive sorted positions. Each lane's bit (its code's low 6
+// bits) is OR-ed into the first lane of its block's run by a segmented scan over
+// shuffles (runs are contiguous); the run's first lane inserts the block with its key
+// (from the first voxel's coordinates) and first sorted position. A run that goes on
+// past the warp's last lane is finished from memory by its first lane (a run holds at
+// most 64 distinct codes; longer runs are duplicates, reported in step 5).
 __global__ void __launch_bounds__(256) kmap_blocks_insert(
     const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
     const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
@@ -403,43 +407,54 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
   const unsigned long long cap = st->cap;
   const unsigned long long cmask = cap - 1;
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
+  const int lane = threadIdx.x & 31;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t s = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; s < N; s += stride) {
-    const unsigned long long blk = mk[s] >> 6;
-    if (s > 0 && (mk[s - 1] >> 6) == blk) continue;
-    unsigned long long mask = 0;
-    for (int64_t j0 = s; j0 < N && j0 < s + 128; j0 += 8) {   // a run: <= 64 codes unless duplicated
-      unsigned long long m[8];
+  for (int64_t w0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x - lane; w0 < N; w0 += stride) {
+    const int64_t s = w0 + lane;
+    const bool live = s < N;
+    const unsigned long long m = live ? mk[s] : ~0ull;
+    const unsigned long long blk = m >> 6;
+    unsigned long long prev = __shfl_up_sync(0xffffffffu, blk, 1);
+    if (lane == 0) prev = (s > 0 && live) ? (mk[s - 1] >> 6) : ~0ull;
+    const bool start = live && (s == 0 || prev != blk);
+    unsigned long long acc = live ? (1ull << (m & 63u)) : 0ull;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) m[u] = j0 + u < N ? mk[j0 + u] : ~0ull;   // loads in flight together
-      bool ended = false;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        ended = ended || (m[u] >> 6) != blk;
-        if (!ended) mask |= 1ull << (m[u] & 63u);
-      }
-      if (ended) break;
+    for (int off = 1; off < 32; off <<= 1) {   // OR of the lanes [lane, lane + 2 off) of the run
+      const unsigned long long o = __shfl_down_sync(0xffffffffu, acc, off);
+      const unsigned long long ob = __shfl_down_sync(0xffffffffu, blk, off);
+      if (lane + off < 32 && ob == blk) acc |= o;
     }
-    const int32_t row = ix[s];
-    if (static_cast<uint64_t>(row) >= static_cast<uint64_t>(N)) continue;   // flagged in step 5
-    const int4 c = coords[row];
-    const unsigned long long key = block_key(c.x, c.y, c.z, c.w);
-    unsigned long long h = mix64(key) & cmask;
-    int probe = 0;
-    for (; probe < max_probe; ++probe) {
-      const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, key);
-      if (prev == kEmptyKey) {
-        table[h].mask = mask;
-        base[h] = static_cast<int32_t>(s);
-        break;
+    const unsigned long long last_blk = __shfl_sync(0xffffffffu, blk, 31);
+    const int32_t row = start ? ix[s] : -1;
+    // rows outside [0, N) are flagged in step 5
+    if (start && static_cast<uint64_t>(row) < static_cast<uint64_t>(N)) {
+      unsigned long long mask = acc;
+      if (blk == last_blk) {   // the run reaches lane 31: finish it from memory
+        for (int64_t j = w0 + 32; j < N && j < s + 128; ++j) {
+          const unsigned long long mj = mk[j];
+          if ((mj >> 6) != blk) break;
+          mask |= 1ull << (mj & 63u);
+        }
       }
-      if (prev == key) {   // two runs of one block: only possible for rejected coordinates
-        atomicOr(&st->flags, kFlagInternal);
-        break;
+      const int4 c = coords[row];
+      const unsigned long long key = block_key(c.x, c.y, c.z, c.w);
+      unsigned long long h = mix64(key) & cmask;
+      int probe = 0;
+      for (; probe < max_probe; ++probe) {
+        const unsigned long long prevk = atomicCAS(&table[h].key, kEmptyKey, key);
+        if (prevk == kEmptyKey) {
+          table[h].mask = mask;
+          base[h] = static_cast<int32_t>(s);
+          break;
+        }
+        if (prevk == key) {   // two runs of one block: only possible for rejected coordinates
+          atomicOr(&st->flags, kFlagInternal);
+          break;
+        }
+        h = (h + 1) & cmask;
       }
-      h = (h + 1) & cmask;
+      if (probe == max_probe) atomicOr(&st->flags, kFlagFull);
     }
-    if (probe == max_probe) atomicOr(&st->flags, kFlagFull);
   }
 }
 

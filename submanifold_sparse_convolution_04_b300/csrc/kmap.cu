@@ -9,8 +9,9 @@
 // Pipeline (one stream, one host sync at the end to read the status word):
 //   1. init    : status word and digit histograms cleared
 //   2. pack    : validate (b, z, y, x); sort key (b << 3*bits) | Morton(z, y, x) with
-//                bits >= 2; all-pass digit histograms
-//   3. plan    : which 8-bit radix passes are not constant (others are skipped)
+//                bits >= 2; smallest and largest key
+//   3. plan    : passes whose digit lies above the highest bit in which the smallest
+//                and largest key differ are constant and skipped
 //   4. passes  : LSD radix sort of (sort key, row) -- count / scan / stable scatter;
 //                the scatter ranks a 2048-key tile in shared memory and writes each
 //                digit's run contiguously
@@ -43,6 +44,7 @@ constexpr int kSortItems = 8;   // 2048-key tiles: ~80 registers, three blocks p
 constexpr int kSortTile = kSortThreads * kSortItems;   // keys per sort block
 constexpr int kMaxPasses = 8;
 constexpr int kMaxProbe = 4096;
+constexpr int kHistParts = 16;   // partial digit histograms (spreads the count kernel's atomics)
 constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 256 * 4;
 
 enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8 };
@@ -55,6 +57,7 @@ struct KmapStatus {
   int pad2;
   unsigned long long nblocks;    // occupied 4x4x4 blocks
   unsigned long long cap;        // hash capacity in use (a power of two)
+  unsigned long long kmin, kmax; // smallest and largest sort key
 };
 
 struct __align__(16) Slot {
@@ -74,7 +77,7 @@ Layout make_layout(int64_t N, int64_t cap) {
   L.nblk = (N + kSortTile - 1) / kSortTile;
   size_t o = 0;
   L.status = o; o = align256(o + sizeof(KmapStatus));
-  L.hist = o;   o = align256(o + sizeof(uint32_t) * kMaxPasses * 256);
+  L.hist = o;   o = align256(o + sizeof(uint32_t) * kHistParts * kMaxPasses * 256);
   L.mk0 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.mk1 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
@@ -130,19 +133,18 @@ __global__ void kmap_init(KmapStatus* st, uint32_t* hist) {
     st->pad2 = 0;
     st->nblocks = 0;
     st->cap = 0;
+    st->kmin = ~0ull;
+    st->kmax = 0;
   }
-  for (int64_t i = tid; i < kMaxPasses * 256; i += stride) hist[i] = 0;
+  for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) hist[i] = 0;
 }
 
 // 2. ------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords, int64_t N,
-                                                 int res, int bits, int npass,
+                                                 int res, int bits,
                                                  unsigned long long* __restrict__ mk,
-                                                 int32_t* __restrict__ ix, uint32_t* hist,
-                                                 KmapStatus* st) {
-  __shared__ uint32_t sh[kMaxPasses][256];
-  for (int i = threadIdx.x; i < kMaxPasses * 256; i += blockDim.x) (&sh[0][0])[i] = 0;
-  __syncthreads();
+                                                 int32_t* __restrict__ ix, KmapStatus* st) {
+  unsigned long long lo = ~0ull, hi = 0;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
     int4 c = coords[i];   // (b, z, y, x)
@@ -159,38 +161,38 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
         (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w, bits);
     mk[i] = m;
     ix[i] = static_cast<int32_t>(i);
-    for (int p = 0; p < npass; ++p) atomicAdd(&sh[p][(m >> (8 * p)) & 255u], 1u);
+    lo = m < lo ? m : lo;
+    hi = m > hi ? m : hi;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < npass * 256; i += blockDim.x) {
-    const uint32_t v = (&sh[0][0])[i];
-    if (v) atomicAdd(&hist[i], v);
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    const unsigned long long h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&st->kmin, lo);
+    atomicMax(&st->kmax, hi);
   }
 }
 
 // 3. ------------------------------------------------------------------------------
-__global__ void kmap_plan(const uint32_t* hist, int npass, int64_t N, KmapStatus* st) {
-  __shared__ int constant_pass[kMaxPasses];
-  if (threadIdx.x < kMaxPasses) constant_pass[threadIdx.x] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < npass * 256; i += blockDim.x)
-    if (hist[i] == static_cast<uint64_t>(N)) constant_pass[i / 256] = 1;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int buf = 0;
-    for (int p = 0; p < kMaxPasses; ++p) {
-      const bool active = p < npass && !constant_pass[p];
-      st->plan[p] = active ? (2 | buf) : 0;
-      if (active) buf ^= 1;
-    }
-    st->plan[kMaxPasses] = buf;
+__global__ void kmap_plan(int npass, KmapStatus* st) {
+  const unsigned long long diff = st->kmax ^ st->kmin;
+  int buf = 0;
+  for (int p = 0; p < kMaxPasses; ++p) {
+    const bool active = p < npass && (diff >> (8 * p)) != 0;
+    st->plan[p] = active ? (2 | buf) : 0;
+    if (active) buf ^= 1;
   }
+  st->plan[kMaxPasses] = buf;
 }
 
 // 4a. per-block digit counts, digit-major: cnt[d * nblk + blk] -------------------------
 __global__ void __launch_bounds__(kSortThreads) kmap_sort_count(
     const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
-    int64_t N, int pass, int64_t nblk, uint32_t* __restrict__ cnt, const KmapStatus* st) {
+    int64_t N, int pass, int64_t nblk, uint32_t* __restrict__ cnt, uint32_t* __restrict__ hist,
+    const KmapStatus* st) {
   const int plan = st->plan[pass];
   if (!(plan & 2)) return;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
@@ -203,7 +205,10 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_count(
     if (e < N) atomicAdd(&sh[(src[e] >> (8 * pass)) & 255u], 1u);
   }
   __syncthreads();
-  cnt[threadIdx.x * nblk + blockIdx.x] = sh[threadIdx.x];
+  const uint32_t v = sh[threadIdx.x];
+  cnt[threadIdx.x * nblk + blockIdx.x] = v;
+  // the pass's digit totals, in kHistParts partial histograms [part][pass][digit]
+  if (v) atomicAdd(&hist[((blockIdx.x % kHistParts) * kMaxPasses + pass) * 256 + threadIdx.x], v);
 }
 
 // Exclusive prefix sum of one value per thread over a 256-thread block; returns the
@@ -237,10 +242,11 @@ __global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict
   const int d = blockIdx.x;
   __shared__ uint32_t tmp[8];
   uint32_t total;
-  // base = sum of the histogram bins below d
-  block_exclusive_scan256(threadIdx.x < static_cast<unsigned>(d) ? hist[pass * 256 + threadIdx.x]
-                                                                  : 0u,
-                          tmp, &total);
+  // base = sum of the histogram bins below d (over the partial histograms)
+  uint32_t below = 0;
+  if (threadIdx.x < static_cast<unsigned>(d))
+    for (int q = 0; q < kHistParts; ++q) below += hist[(q * kMaxPasses + pass) * 256 + threadIdx.x];
+  block_exclusive_scan256(below, tmp, &total);
   uint32_t carry = total;
   uint32_t* row = cnt + d * nblk;
   for (int64_t b0 = 0; b0 < nblk; b0 += 256) {
@@ -526,21 +532,36 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
         s_mask[combo][t] = m;
         s_start[combo][t] = st0;
       }
+      // per axis and step d in {-1, 0, 1}: is the coordinate inside the grid, which of
+      // the two blocks along the axis holds it (its bit of the block selector), and its
+      // share of the Morton place inside the block
+      bool vz[3], vy[3], vx[3];
+      uint32_t cz[3], cy[3], cx[3], bz[3], by[3], bx[3];
+#pragma unroll
+      for (int d = 0; d < 3; ++d) {
+        const int zz = z + d - 1, yy = y + d - 1, xx = x + d - 1;
+        vz[d] = static_cast<unsigned>(zz) < static_cast<unsigned>(res);
+        vy[d] = static_cast<unsigned>(yy) < static_cast<unsigned>(res);
+        vx[d] = static_cast<unsigned>(xx) < static_cast<unsigned>(res);
+        cz[d] = (d != 1 && d - 1 == oz) ? 4u : 0u;
+        cy[d] = (d != 1 && d - 1 == oy) ? 2u : 0u;
+        cx[d] = (d != 1 && d - 1 == ox) ? 1u : 0u;
+        bz[d] = ((zz & 1) << 2) | (((zz >> 1) & 1) << 5);
+        by[d] = ((yy & 1) << 1) | (((yy >> 1) & 1) << 4);
+        bx[d] = (xx & 1) | (((xx >> 1) & 1) << 3);
+      }
 #pragma unroll
       for (int k = 0; k < 27; ++k) {
-        const int dz = k / 9 - 1, dy = (k / 3) % 3 - 1, dx = k % 3 - 1;
-        const int zz = z + dz, yy = y + dy, xx = x + dx;
+        const int dz = k / 9, dy = (k / 3) % 3, dx = k % 3;
         int32_t val = -1;
-        if (static_cast<unsigned>(zz) < static_cast<unsigned>(res) &&
-            static_cast<unsigned>(yy) < static_cast<unsigned>(res) &&
-            static_cast<unsigned>(xx) < static_cast<unsigned>(res)) {
-          const int combo = ((dz != 0 && dz == oz) ? 4 : 0) | ((dy != 0 && dy == oy) ? 2 : 0) |
-                            ((dx != 0 && dx == ox) ? 1 : 0);
+        if (vz[dz] && vy[dy] && vx[dx]) {
+          const uint32_t combo = cz[dz] | cy[dy] | cx[dx];
+          const uint32_t bit = bz[dz] | by[dy] | bx[dx];
           const unsigned long long m = s_mask[combo][t];
-          const uint32_t bit = in_block_bit(zz, yy, xx);
           if ((m >> bit) & 1ull) {
-            const int64_t pos = int64_t(s_start[combo][t]) + __popcll(m & ((1ull << bit) - 1ull));
-            if (pos < N) val = __ldg(ix + pos);
+            const uint32_t pos = static_cast<uint32_t>(s_start[combo][t]) +
+                                 static_cast<uint32_t>(__popcll(m & ((1ull << bit) - 1ull)));
+            if (pos < static_cast<uint64_t>(N)) val = __ldg(ix + pos);
             else bad = true;
           }
         }
@@ -643,13 +664,13 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
 
   kmap_init<<<8, 256, 0, stream>>>(st, hist);
   SUBM3D_LAUNCHED("kmap_init");
-  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, npass, mk0, ix0, hist, st);
+  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, mk0, ix0, st);
   SUBM3D_LAUNCHED("kmap_pack");
-  kmap_plan<<<1, 256, 0, stream>>>(hist, npass, N, st);
+  kmap_plan<<<1, 1, 0, stream>>>(npass, st);
   SUBM3D_LAUNCHED("kmap_plan");
   const int nblk = static_cast<int>(L.nblk);
   for (int p = 0; p < npass; ++p) {
-    kmap_sort_count<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, N, p, L.nblk, cnt, st);
+    kmap_sort_count<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, N, p, L.nblk, cnt, hist, st);
     SUBM3D_LAUNCHED("kmap_sort_count");
     kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, L.nblk, cnt, st);
     SUBM3D_LAUNCHED("kmap_sort_scan");

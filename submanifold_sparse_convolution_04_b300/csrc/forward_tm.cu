@@ -22,14 +22,18 @@
 //     into a double-buffered shared-memory ring with one bulk copy, a tile ahead, so
 //     a producer reads its row's index with one conflict-free shared load (27 is
 //     odd) instead of one 32-byte global sector per 4-byte index.
-// Tensor memory (512 columns): two accumulators of 64 columns (double buffer) and
-// twelve A stages of 32 columns. Stage g of the CTA (tile, offset k) is written by
-// producer group g mod 6 (four warps, warp w writing lanes 32 (w % 4) .. + 31) and
-// lives in slot g mod 12 (A in tensor memory, W_k in shared memory). A group has one
-// stage's loads in flight while it waits for its slot; the stage is full when its
-// four warps have arrived (after tcgen05.wait::st) and its weight bytes have landed.
+// Tensor memory (512 columns): two accumulators of 64 columns (double buffer) and six
+// A stages of 64 columns. A stage carries two offsets (2p, 2p + 1; the last of a tile
+// only offset 26), because every stage costs the single MMA-issuing warp a barrier wait
+// and a commit, and that per-stage cost, not the memory system, bounded the kernel with
+// one offset per stage. Stage g of the CTA (tile, pair p) is written by producer group
+// g mod 6 (four warps, warp w writing lanes 32 (w % 4) .. + 31) into slot g mod 6: each
+// thread gathers its row of offset 2p (loads in flight while the slot frees), stores
+// it, then gathers and stores its row of offset 2p + 1; the group leader fetches both
+// weight taps into the stage's weight slot by TMA. The stage is full when its four
+// warps have arrived (after tcgen05.wait::st) and its weight bytes have landed.
 // One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
-// up to four) and frees the slot (both halves) with tcgen05.commit. Four epilogue warps drain tile
+// up to four per offset) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
 // t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> 16-byte stores) while
 // the tensor core works on tile t + 1.
 //
@@ -45,8 +49,10 @@ namespace {
 
 constexpr int kBM = 128;              // output rows per tile = tensor-memory lanes
 constexpr int kGroups = 6;            // producer groups of four warps
-constexpr int kStages = 12;           // A stages in tensor memory
-constexpr int kStageCols = 32;        // 64 bf16 per row = 32 columns of 32 bits
+constexpr int kStages = 6;            // A stages in tensor memory
+constexpr int kOffCols = 32;          // one offset's row: 64 bf16 = 32 columns of 32 bits
+constexpr int kStageCols = 2 * kOffCols;   // a stage holds two offsets (2p, 2p + 1)
+constexpr int kPairs = 14;            // stages per tile: offsets (0,1) .. (24,25), (26)
 constexpr int kAccCols = 64;          // one accumulator (N <= 64)
 constexpr int kAColBase = 2 * kAccCols;
 constexpr int kProducerWarps = 4 * kGroups;
@@ -62,7 +68,7 @@ static_assert(kStages % kGroups == 0, "slots per group");
 template <int NMMA>
 struct TmCfg {
   static constexpr int kTapBytes = NMMA * 128;            // one [NMMA x 64] weight tile
-  static constexpr int kWBytes = kStages * kTapBytes;     // one weight slot per stage
+  static constexpr int kWBytes = kStages * 2 * kTapBytes;  // two taps per stage
   static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 2 * kNbrTileBytes +
                                512 /*barriers*/ + 256 * 4 /*bias*/;
   // at least half the SM's shared memory, so that one CTA (which takes all of tensor
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sW = base;                                   // kStages weight slots
+  const uint32_t sW = base;                                   // kStages slots of two taps
   const uint32_t sNbr = base + C::kWBytes;                    // 2 x 13.8 KB
   const int32_t* nbr_sm = reinterpret_cast<const int32_t*>(base_ptr + C::kWBytes);
   uint8_t* misc = base_ptr + C::kWBytes + 2 * kNbrTileBytes;
@@ -202,11 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                   static_cast<int>(gridDim.x);
-  const uint32_t total = static_cast<uint32_t>(ntl) * 27u;
+  const uint32_t total = static_cast<uint32_t>(ntl) * kPairs;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(afull0 + 8 * s, 5);     // the group's four warps + the weight TMA's expect_tx
+      mbar_init(afull0 + 8 * s, 5);     // the group's four warps + the weight TMAs' expect_tx
       mbar_init(aempty0 + 8 * s, 1);    // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -243,9 +249,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool bad = false, aborted = false;
     int cur = -1;                            // tile whose nbr block this warp is reading
     uint32_t last = 0;                       // one past the last stage this group issued
+    // this thread's row of offset k of tile lt: its input row, -1 when absent
+    auto row_index = [&](int lt, int k) -> int32_t {
+      const int64_t row = int64_t(blockIdx.x + lt * gridDim.x) * kBM + r;
+      if (row >= p.N) return -1;
+      int32_t j = nbr_sm[(lt & 1) * (kBM * 27) + r * 27 + k];
+      if (j < -1 || j >= p.N) {
+        bad = true;
+        j = -1;
+      }
+      return j;
+    };
+    auto load_row = [&](int32_t j, uint32_t (&v)[32]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // 16 channels (32 bytes) per load
+        if (j >= 0 && q * 16 < p.I) {
+          ld32B(p.feats + int64_t(j) * p.I + q * 16, v + 8 * q);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * q + e] = 0u;
+        }
+      }
+    };
     for (uint32_t g = grp; g < total; g += kGroups) {
-      const int lt = static_cast<int>(g / 27u);
-      const int k = static_cast<int>(g - static_cast<uint32_t>(lt) * 27u);
+      const int lt = static_cast<int>(g / kPairs);
+      const int k0 = 2 * static_cast<int>(g - static_cast<uint32_t>(lt) * kPairs);
+      const bool two = k0 + 1 < 27;
       if (lt != cur) {   // move to tile lt's nbr block (and release the previous one)
         if (cur >= 0) {
           __syncwarp();
@@ -258,25 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cur = lt;
       }
-      const int64_t row = int64_t(blockIdx.x + lt * gridDim.x) * kBM + r;
-      int32_t j = -1;
-      if (row < p.N) {
-        j = nbr_sm[(lt & 1) * (kBM * 27) + r * 27 + k];
-        if (j < -1 || j >= p.N) {
-          bad = true;
-          j = -1;
-        }
-      }
       uint32_t v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {   // 16 channels (32 bytes) per load
-        if (j >= 0 && q * 16 < p.I) {
-          ld32B(p.feats + int64_t(j) * p.I + q * 16, v + 8 * q);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[8 * q + e] = 0u;
-        }
-      }
+      load_row(row_index(lt, k0), v);   // in flight while the slot frees
       const uint32_t s = g % kStages;
       const uint32_t use = g / kStages;
       const bool ok = mbar_wait(aempty0 + 8 * s, (use & 1u) ^ 1u, abort_flag);
@@ -284,13 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         aborted = true;
         break;
       }
-      if (leader) {   // the stage's weight tap into its slot
-        mbar_arrive_expect_tx(afull0 + 8 * s, C::kTapBytes);
-        tma_load_3d(sW + s * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k, 0);
+      if (leader) {   // the stage's weight taps into its slot
+        mbar_arrive_expect_tx(afull0 + 8 * s, (two ? 2 : 1) * C::kTapBytes);
+        tma_load_3d(sW + s * 2 * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k0, 0);
+        if (two) tma_load_3d(sW + (s * 2 + 1) * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k0 + 1, 0);
       }
       last = g + kGroups;
       tc_fence_after();
-      tmem_st32(tmem_base + lane_addr + kAColBase + s * kStageCols, v);
+      const uint32_t taddr = tmem_base + lane_addr + kAColBase + s * kStageCols;
+      tmem_st32(taddr, v);
+      if (two) {
+        tmem_st_wait();   // v is free again
+        load_row(row_index(lt, k0 + 1), v);
+        tmem_st32(taddr + kOffCols, v);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -359,16 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * kAccCols;
-      for (int k = 0; k < 27; ++k, ++g) {
+      for (int pr = 0; pr < kPairs; ++pr, ++g) {
         const uint32_t s = g % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * s, (g / kStages) & 1u, abort_flag))) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        tm_mma_stage(d_tmem, tmem_base + kAColBase + s * kStageCols,
-                     w0 + static_cast<uint64_t>(s) * (C::kTapBytes >> 4), idesc, ksteps,
-                     k == 0 ? 0u : 1u);
+        const uint32_t a = tmem_base + kAColBase + s * kStageCols;
+        const uint64_t b = w0 + static_cast<uint64_t>(2 * s) * (C::kTapBytes >> 4);
+        tm_mma_stage(d_tmem, a, b, idesc, ksteps, pr == 0 ? 0u : 1u);
+        if (2 * pr + 1 < 27)
+          tm_mma_stage(d_tmem, a + kOffCols, b + (C::kTapBytes >> 4), idesc, ksteps, 1u);
         tm_commit(aempty0 + 8 * s);
       }
       if (!aborted) tm_commit(accf0 + 8 * buf);

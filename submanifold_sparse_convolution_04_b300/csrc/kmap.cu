@@ -100,12 +100,6 @@ __device__ __forceinline__ unsigned long long morton3(uint32_t z, uint32_t y, ui
   return m;
 }
 
-// Place of (z, y, x) inside its 4x4x4 block: the low 6 bits of the Morton code.
-__device__ __forceinline__ uint32_t in_block_bit(uint32_t z, uint32_t y, uint32_t x) {
-  return (x & 1u) | ((y & 1u) << 1) | ((z & 1u) << 2) | ((x & 2u) << 2) | ((y & 2u) << 3) |
-         ((z & 2u) << 4);
-}
-
 // b << 42 | (z >> 2) << 28 | (y >> 2) << 14 | (x >> 2): 16 + 3 x 14 bits, never all ones.
 __device__ __forceinline__ unsigned long long block_key(uint32_t b, uint32_t z, uint32_t y,
                                                         uint32_t x) {

@@ -63,10 +63,7 @@ constexpr int kThreads = 32 * (kNbrWarp + 1);    // 960
 constexpr int kNbrTileBytes = kBM * 27 * 4;      // one tile's rows of nbr
 constexpr int kSmemLimit = 227 * 1024;
 static_assert(kAColBase + kStages * kStageCols == 512, "tensor memory layout");
-// Every slot must be filled by one producer group only: the slot waits use mbarrier phase
-// parity, which is only sound when a waiter can never be two phases ahead, i.e. when one
-// group takes each use of a slot in turn.
-static_assert(kStages % kGroups == 0, "each slot must belong to one producer group");
+static_assert(kStages % kGroups == 0, "slots per group");
 
 template <int NMMA>
 struct TmCfg {

@@ -161,8 +161,11 @@ SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32
  *           read-modify-write). Must not overlap the inputs.
  *   dtype   SUBM3D_BF16: bf16 inputs, fp32 accumulation (tcgen05 tensor cores,
  *           accumulator in tensor memory), bias added in fp32, output rounded to
- *           bf16 (nearest-even). Needs I % 8 == 0 and O % 8 == 0; O <= 256 runs on
- *           the tensor cores, larger O on the CUDA-core kernel.
+ *           bf16 (nearest-even). Needs I % 8 == 0 and O % 8 == 0. I and O in
+ *           {16, 32, 48, 64} with feats 32-byte aligned run the narrow kernel (the
+ *           gathered rows in tensor memory); other O <= 256 the kernel that stages
+ *           them in shared memory; larger O the CUDA-core kernel. All three compute
+ *           the same sums (fp32 accumulation order may differ between them).
  *           SUBM3D_F32: fp32 inputs and accumulation on the CUDA cores.
  *   N, I, O N >= 0 (0 is a no-op), 1 <= I, O <= 4096.
  *

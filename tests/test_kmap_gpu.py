@@ -90,6 +90,27 @@ def test_kmap_morton_order(dev):
     np.testing.assert_array_equal(nbr.cpu().numpy(), cpu.kernel_map(case["coords"], case["res"]))
 
 
+@pytest.mark.parametrize("res", [1, 2, 3, 4, 5])
+def test_kmap_morton_order_small_grids_with_batches(dev, res):
+    # grids below 4 per side: the sort key still keeps the batch above a whole 4x4x4
+    # block's Morton bits; the order is (b, Morton(z, y, x)) ascending, stable
+    rng = np.random.default_rng(res)
+    cells = np.array([(b, z, y, x) for b in range(3) for z in range(res) for y in range(res)
+                      for x in range(res)], np.int32)
+    c = cells[rng.permutation(len(cells))[: max(1, (2 * len(cells)) // 3)]]
+    ct = torch.from_numpy(c).to(dev)
+    nbr, order = subm3d_build_kmap_ex(ct, res, order=True)
+    co = c.astype(np.int64)
+    m = np.zeros(len(co), np.int64)
+    for t in range(4):
+        m |= ((co[:, 3] >> t) & 1) << (3 * t)
+        m |= ((co[:, 2] >> t) & 1) << (3 * t + 1)
+        m |= ((co[:, 1] >> t) & 1) << (3 * t + 2)
+    want = np.lexsort((np.arange(len(co)), m, co[:, 0]))   # by batch, then Morton, stable
+    np.testing.assert_array_equal(order.cpu().numpy(), want)
+    np.testing.assert_array_equal(nbr.cpu().numpy(), ref.kernel_map(c, res))
+
+
 def test_kmap_errors_and_recovery(dev):
     good = np.array([[0, 1, 1, 1], [0, 1, 1, 2]], np.int32)
     for bad, code in [

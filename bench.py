@@ -207,8 +207,8 @@ def recorded_traffic(kernel, src, workload):
     return float(m.group(1)), f"ncu dram__bytes_read.sum + dram__bytes_write.sum ({os.path.relpath(prof, ROOT)})"
 
 
-def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload):
-    e = 2
+def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload, e=2):
+    """e: bytes per element of feats, weight and out (2 for bf16, 4 for fp32)."""
     gathered = P * I * e + N * O * e + 108 * N + 27 * I * O * e
     compulsory = N * I * e + N * O * e + 108 * N + 27 * I * O * e
     flops = 2.0 * P * I * O
@@ -216,7 +216,7 @@ def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload):
     tc = float(peaks["bf16_tflops"])
     achieved = gathered / fwd_s / 1e9
     t_roof = max(flops / (tc * 1e12), gathered / (hbm * 1e9))
-    kernel, src = forward_kernel(I, O)
+    kernel, src = forward_kernel(I, O) if e == 2 else ("fwd_simt", os.path.join(CSRC, "forward_simt.cu"))
     traffic, traffic_src = recorded_traffic(kernel, src, workload)
     return {
         "bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -424,7 +424,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
-    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind, case["name"])
+    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind, case["name"], e=2 if bf16 else 4)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -32,12 +32,13 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["OFFSETS", "CENTER", "OracleError", "tap", "coordinate_dict", "kernel_map",
-           "subm_conv3d", "subm_conv3d_rows"]
+__all__ = ["OFFSETS", "CENTER", "ACTIVATIONS", "OracleError", "tap", "coordinate_dict",
+           "kernel_map", "subm_conv3d", "subm_conv3d_rows", "activation", "block_epilogue"]
 
 # k -> (dz, dy, dx), k = 9 (dz + 1) + 3 (dy + 1) + (dx + 1)
 OFFSETS = [(dz, dy, dx) for dz in (-1, 0, 1) for dy in (-1, 0, 1) for dx in (-1, 0, 1)]
 CENTER = 13
+ACTIVATIONS = ("none", "relu", "silu")
 MAX_BATCH = 65534
 MAX_RES = 65535
 
@@ -136,3 +137,36 @@ def subm_conv3d(coords, feats, weight, bias, res):
     """All output rows, float64 [N, O] (see subm_conv3d_rows)."""
     N = np.asarray(coords).shape[0]
     return subm_conv3d_rows(coords, feats, weight, bias, res, range(N))
+
+
+def activation(y, act):
+    """Elementwise activation in float64: "none" is the identity, "relu" is max(y, 0),
+    "silu" is y * sigmoid(y) = y / (1 + exp(-y))."""
+    y = np.asarray(y, dtype=np.float64)
+    if act == "none":
+        return y.copy()
+    if act == "relu":
+        return np.where(y > 0.0, y, 0.0)
+    if act == "silu":
+        with np.errstate(over="ignore"):      # exp(-y) = inf for y << 0 gives -0.0
+            return y / (1.0 + np.exp(-y))
+    raise OracleError(f"activation {act!r} is not one of {ACTIVATIONS}")
+
+
+def block_epilogue(conv, residual=None, act="none"):
+    """Tail of a residual block on top of the convolution, float64:
+
+    out = act(conv + residual), conv being the convolution output with its bias.
+
+    The "pixal3d_mrp_mlx README" scope table ("Scope, measured against the shared
+    core" and its correction) lists ResBlock-style and ConvNeXt-style sparse blocks and
+    activations beside SubMConv3d, but not their internals; a residual add and an
+    activation are the steps such a block applies to a convolution's output.
+    """
+    y = np.asarray(conv, dtype=np.float64)
+    if residual is not None:
+        residual = np.asarray(residual, dtype=np.float64)
+        if residual.shape != y.shape:
+            raise OracleError(f"residual shape {residual.shape} != output shape {y.shape}")
+        y = y + residual
+    return activation(y, act)

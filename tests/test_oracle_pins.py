@@ -303,3 +303,80 @@ def test_planted_offset_enumeration_mistake_is_caught(monkeypatch):
     rng = np.random.default_rng(0)
     c = random_set(rng, 4, 1, 20)
     assert not np.array_equal(ref.kernel_map(c, 4), brute_force_nbr(c))
+
+
+# ----------------------------------------------------------------- fused block epilogue
+
+_TORCH_ACT = {"none": lambda t: t, "relu": F.relu, "silu": F.silu}
+
+
+def dense_block(coords, feats, weight, bias, residual, act, res):
+    """act(dense masked Conv3d + residual) with torch's own activation routines."""
+    y = torch.from_numpy(dense_masked_conv3d(coords, feats, weight, bias, res))
+    if residual is not None:
+        y = y + torch.from_numpy(np.asarray(residual, np.float64))
+    return _TORCH_ACT[act](y).numpy()
+
+
+@pytest.mark.parametrize("act", ref.ACTIVATIONS)
+@pytest.mark.parametrize("with_residual", [False, True])
+def test_block_epilogue_matches_dense_block(act, with_residual):
+    rng = np.random.default_rng(20 + len(act) + with_residual)
+    c = random_set(rng, 6, 2, 60)
+    f, w, b = rand_values(rng, c.shape[0], 4, 5)
+    r = rng.standard_normal((c.shape[0], 5)) if with_residual else None
+    want = dense_block(c, f, w, b, r, act, 6)
+    got = ref.block_epilogue(ref.subm_conv3d(c, f, w, b, 6), r, act)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
+    # the negative side of every activation is exercised
+    assert (ref.subm_conv3d(c, f, w, b, 6) < -0.5).any()
+
+
+def test_activation_closed_forms_and_odd_part():
+    ln3 = np.log(3.0)
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4
+    np.testing.assert_allclose(ref.activation([ln3, -ln3, 0.0], "silu"),
+                               [0.75 * ln3, -0.25 * ln3, 0.0], rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(ref.activation([-2.0, 0.0, 3.5], "relu"), [0.0, 0.0, 3.5])
+    np.testing.assert_array_equal(ref.activation([-2.0, 3.5], "none"), [-2.0, 3.5])
+    y = np.random.default_rng(5).standard_normal(1000) * 6
+    # f(y) - f(-y) = y for relu and silu (y sigmoid(y) + y sigmoid(-y) = y)
+    for act in ("relu", "silu"):
+        np.testing.assert_allclose(ref.activation(y, act) - ref.activation(-y, act), y,
+                                   rtol=0, atol=1e-12)
+    # silu tends to the identity above and to 0 below, without overflow to nan
+    assert abs(ref.activation([40.0], "silu")[0] - 40.0) < 1e-14
+    big = ref.activation([-800.0, 800.0], "silu")
+    assert np.isfinite(big).all() and big[0] == 0.0 and big[1] == 800.0
+    with pytest.raises(ref.OracleError):
+        ref.activation([1.0], "gelu")
+
+
+def test_block_epilogue_residual_only_and_shape_check():
+    """Zero weight and bias leave act(residual): the epilogue sees only the skip path."""
+    rng = np.random.default_rng(8)
+    c = random_set(rng, 5, 1, 30)
+    f = rng.standard_normal((30, 3))
+    r = rng.standard_normal((30, 4))
+    conv = ref.subm_conv3d(c, f, np.zeros((4, 3, 3, 3, 3)), np.zeros(4), 5)
+    for act in ref.ACTIVATIONS:
+        np.testing.assert_allclose(ref.block_epilogue(conv, r, act),
+                                   _TORCH_ACT[act](torch.from_numpy(r)).numpy(), rtol=1e-15,
+                                   atol=1e-16)
+    with pytest.raises(ref.OracleError):
+        ref.block_epilogue(conv, r[:, :3], "relu")
+
+
+def test_planted_silu_sign_mistake_is_caught(monkeypatch):
+    """Planting y * sigmoid(-y) for silu in the oracle must break the dense-block pin."""
+    real = ref.activation
+
+    def wrong(y, act):
+        return -real(-np.asarray(y, np.float64), act) if act == "silu" else real(y, act)
+
+    monkeypatch.setattr(ref, "activation", wrong)
+    rng = np.random.default_rng(21)
+    c = random_set(rng, 6, 1, 40)
+    f, w, b = rand_values(rng, 40, 3, 3)
+    got = ref.block_epilogue(ref.subm_conv3d(c, f, w, b, 6), None, "silu")
+    assert not np.allclose(got, dense_block(c, f, w, b, None, "silu", 6), atol=1e-6)

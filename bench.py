@@ -8,6 +8,7 @@ subm3d_forward (tcgen05 gather-GEMM with fused bias). Default workload: the
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
     python bench.py --impl reference ...      # the CPU oracle, as the reference arm
+    python bench.py --residual --act relu     # forward with the fused block epilogue
 
 Prints one JSON line (rank 0). `value` = effective TFLOP/s of the whole step,
 2 * pairs * I * O / step time, summed over ranks (replicas: every rank runs the
@@ -57,6 +58,10 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--residual", action="store_true",
+                   help="fused block epilogue: add a residual [N, O] input (subm3d_forward_ex)")
+    p.add_argument("--act", default="none", choices=["none", "relu", "silu"],
+                   help="fused block epilogue: activation after bias (+ residual)")
     p.add_argument("--max-voxels", type=int, default=0,
                    help="keep only the first M voxels (raster order): a slab of the workload")
     return p.parse_args()
@@ -207,10 +212,11 @@ def recorded_traffic(kernel, src, workload):
     return float(m.group(1)), f"ncu dram__bytes_read.sum + dram__bytes_write.sum ({os.path.relpath(prof, ROOT)})"
 
 
-def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload, e=2):
-    """e: bytes per element of feats, weight and out (2 for bf16, 4 for fp32)."""
-    gathered = P * I * e + N * O * e + 108 * N + 27 * I * O * e
-    compulsory = N * I * e + N * O * e + 108 * N + 27 * I * O * e
+def roofline(N, P, I, O, fwd_s, peaks, peak_kind, workload, e=2, residual=False):
+    """e: bytes per element of feats, weight and out (2 for bf16, 4 for fp32); residual:
+    the fused epilogue reads an [N, O] residual as well."""
+    gathered = P * I * e + N * O * e + 108 * N + 27 * I * O * e + (N * O * e if residual else 0)
+    compulsory = N * I * e + N * O * e + 108 * N + 27 * I * O * e + (N * O * e if residual else 0)
     flops = 2.0 * P * I * O
     hbm = float(peaks["hbm_gbs"])
     tc = float(peaks["bf16_tflops"])
@@ -300,6 +306,7 @@ def run_ours(args, world, rank, local):
     import numpy as np
     import torch
     from submanifold_sparse_convolution_04_b300 import (subm3d_build_kmap, subm3d_forward,
+                                                        subm3d_forward_ex,
                                                         subm3d_forward_status,
                                                         subm3d_kernel_launches,
                                                         subm3d_kmap_workspace_bytes)
@@ -326,10 +333,24 @@ def run_ours(args, world, rank, local):
     nbr = torch.empty((N, 27), dtype=torch.int32, device=dev)
     out = torch.empty((N, O), dtype=f.dtype, device=dev)
     stream = torch.cuda.current_stream()
+    fused = args.residual or args.act != "none"
+    res_h = r = None
+    if args.residual:
+        from synth import make_residual
+        rv, rbits = make_residual(N, O, case["dtype"], case["cfg_id"])
+        res_h = (torch.from_numpy(rbits.view(np.int16)).view(torch.bfloat16) if bf16
+                 else torch.from_numpy(rv)).pin_memory()
+        r = res_h.to(dev)
+
+    def forward(f, nbr, w, b, r, out):
+        if fused:
+            subm3d_forward_ex(f, nbr, w, b, residual=r, act=args.act, out=out)
+        else:
+            subm3d_forward(f, nbr, w, b, out=out)
 
     def step():
         subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
-        subm3d_forward(f, nbr, w, b, out=out)
+        forward(f, nbr, w, b, r, out)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -352,7 +373,7 @@ def run_ours(args, world, rank, local):
         ev[s][0].record(stream)
         subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
         ev[s][1].record(stream)
-        subm3d_forward(f, nbr, w, b, out=out)
+        forward(f, nbr, w, b, r, out)
         ev[s][2].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -366,17 +387,44 @@ def run_ours(args, world, rank, local):
     ms_per_step = total_ms / K
     value = world * flops / (ms_per_step / 1e3) / 1e12
 
+    unfused_us = None
+    if fused:
+        # the same epilogue as separate passes (plain forward, then torch's add and
+        # activation over [N, O]): what the fusion saves
+        def unfused():
+            subm3d_forward(f, nbr, w, b, out=out)
+            if r is not None:
+                out.add_(r)
+            if args.act == "relu":
+                out.relu_()
+            elif args.act == "silu":
+                torch.nn.functional.silu(out, inplace=True)
+        for _ in range(3):
+            unfused()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        u0.record(stream)
+        for _ in range(min(K, 50)):
+            unfused()
+        u1.record(stream)
+        torch.cuda.synchronize()
+        unfused_us = u0.elapsed_time(u1) / min(K, 50) * 1e3
+        forward(f, nbr, w, b, r, out)      # leave the fused result in out
+        torch.cuda.synchronize()
+
     # end to end through the Python API: every step copies its inputs from pinned host
     # memory to the device, builds the map, runs the forward and copies the output back
     # to pinned host memory. Steps are pipelined over three streams with two buffer sets:
     # step i+1's inputs travel host -> device while step i computes and its output
     # travels device -> host (the copy engines run both directions at once).
-    h2d = sum(t.numel() * t.element_size() for t in (coords_h, feats_h, weight_h, bias_h))
+    ins = [("c", coords_h), ("f", feats_h), ("w", weight_h), ("b", bias_h)]
+    if res_h is not None:
+        ins.append(("r", res_h))
+    h2d = sum(t.numel() * t.element_size() for _, t in ins)
     d2h = N * O * f.element_size()
     s_cmp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    bufs = [dict(c=torch.empty_like(coords_h, device=dev), f=torch.empty_like(feats_h, device=dev),
-                 w=torch.empty_like(weight_h, device=dev), b=torch.empty_like(bias_h, device=dev),
+    bufs = [dict({"r": None}, **{key: torch.empty_like(src, device=dev) for key, src in ins},
                  nbr=torch.empty((N, 27), dtype=torch.int32, device=dev),
                  out=torch.empty((N, O), dtype=f.dtype, device=dev),
                  out_h=torch.empty((N, O), dtype=f.dtype).pin_memory(),
@@ -388,7 +436,7 @@ def run_ours(args, world, rank, local):
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(B["ev_cmp"])        # step i-2 has finished with these inputs
-            for key, src in (("c", coords_h), ("f", feats_h), ("w", weight_h), ("b", bias_h)):
+            for key, src in ins:
                 B[key].copy_(src, non_blocking=True)
             B["ev_in"].record(s_in)
 
@@ -398,7 +446,7 @@ def run_ours(args, world, rank, local):
         if i >= 2:
             s_cmp.wait_event(B["ev_out"])           # step i-2's output has left the device
         subm3d_build_kmap(B["c"], res, nbr=B["nbr"], workspace=ws)
-        subm3d_forward(B["f"], B["nbr"], B["w"], B["b"], out=B["out"])
+        forward(B["f"], B["nbr"], B["w"], B["b"], B["r"], B["out"])
         B["ev_cmp"].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(B["ev_cmp"])
@@ -424,7 +472,10 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
-    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind, case["name"], e=2 if bf16 else 4)
+    epi = "none" if not fused else ("residual+" if args.residual else "") + args.act
+    roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind,
+                    case["name"] + ("" if not fused else "_" + epi.replace("+", "_")),
+                    e=2 if bf16 else 4, residual=args.residual)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -433,11 +484,13 @@ def run_ours(args, world, rank, local):
         "config": dict(workload_desc(case, P),
                        l2="inputs larger than L2 (feats, nbr, hash table each > 126 MB); "
                           "no flush between steps",
-                       parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+                       parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       epilogue=epi),
         "mvoxels_per_s": world * N / (ms_per_step / 1e3) / 1e6,
         "kmap_ms": kmap_ms, "forward_us": fwd_ms * 1e3,
         "forward_tflops": flops / (fwd_ms / 1e3) / 1e12,
         "roofline": roof,
+        **({"unfused_epilogue_forward_us": unfused_us} if fused else {}),
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3, "steps": args.e2e_steps,

@@ -61,6 +61,13 @@ typedef enum {
 
 typedef enum { SUBM3D_F32 = 0, SUBM3D_BF16 = 1 } subm3d_dtype;
 
+/* Activation of the fused epilogue (subm3d_forward_ex). */
+typedef enum {
+  SUBM3D_ACT_NONE = 0,  /* identity                                                  */
+  SUBM3D_ACT_RELU = 1,  /* max(y, 0)                                                 */
+  SUBM3D_ACT_SILU = 2   /* y * sigmoid(y) = y / (1 + exp(-y))                        */
+} subm3d_act;
+
 /* Largest accepted grid side and batch index. */
 #define SUBM3D_MAX_RES 65535
 #define SUBM3D_MAX_BATCH 65534
@@ -175,6 +182,35 @@ SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32
 SUBM3D_API int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight,
                    const void* bias, void* out, int64_t N, int32_t I, int32_t O,
                    subm3d_dtype dtype, cudaStream_t stream);
+
+/*
+ * Forward pass with a fused block epilogue: the convolution above, then a residual
+ * add and an activation, in the same kernel and the same single store per row:
+ *
+ *   out[i, o] = act( bias[o] + residual[i, o]
+ *                    + sum_k sum_c weight[o, kz, ky, kx, c] * feats[nbr[i, k], c] )
+ *
+ * This is the tail of a residual block built on this convolution (the "pixal3d_mrp_mlx"
+ * page, section "Scope, measured against the shared core", lists ResBlock-style and
+ * ConvNeXt-style sparse blocks and activations next to SubMConv3d; the block
+ * internals are not given there, so the epilogue offers the two pieces every such
+ * block ends with). Several convolutions at one resolution share one nbr: build it
+ * once, pass it to each call.
+ *
+ *   residual  device [N, O] of `dtype`, or NULL for none; 16-byte aligned. It may be
+ *             the same buffer as `out` (an in-place residual block: each element is
+ *             read before it is overwritten, by the same thread); any other overlap
+ *             with `out`, and any overlap of `out` with feats, is not allowed.
+ *   act       SUBM3D_ACT_NONE, SUBM3D_ACT_RELU or SUBM3D_ACT_SILU, applied in fp32 to
+ *             the fp32 sum before the output is rounded to `dtype`.
+ *
+ * Other arguments, kernels, errors and asynchrony as subm3d_forward, which is this
+ * call with residual = NULL and act = SUBM3D_ACT_NONE.
+ */
+SUBM3D_API int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight,
+                                 const void* bias, const void* residual, subm3d_act act,
+                                 void* out, int64_t N, int32_t I, int32_t O,
+                                 subm3d_dtype dtype, cudaStream_t stream);
 
 /*
  * Waits for `stream`, then reads and clears the forward kernels' device error word:

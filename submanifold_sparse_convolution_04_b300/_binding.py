@@ -16,6 +16,7 @@ OK, ERR_ARG, ERR_COORD_RANGE, ERR_DUPLICATE, ERR_HASH_FULL, ERR_CUDA, ERR_UNSUPP
     ERR_WORKSPACE, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7, -8
 F32, BF16 = 0, 1
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+ACTIVATIONS = {"none": 0, "relu": 1, "silu": 2}   # subm3d_act
 _NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_COORD_RANGE", -3: "ERR_DUPLICATE", -4: "ERR_HASH_FULL",
           -5: "ERR_CUDA", -6: "ERR_UNSUPPORTED", -7: "ERR_WORKSPACE", -8: "ERR_DEVICE"}
 
@@ -51,6 +52,9 @@ def lib() -> ctypes.CDLL:
         L.subm3d_build_kmap_noalloc.restype = ctypes.c_int
         L.subm3d_forward.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, vp]
         L.subm3d_forward.restype = ctypes.c_int
+        L.subm3d_forward_ex.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, i32, i32,
+                                        ctypes.c_int, vp]
+        L.subm3d_forward_ex.restype = ctypes.c_int
         L.subm3d_forward_status.argtypes = [vp]
         L.subm3d_forward_status.restype = ctypes.c_int
         L.subm3d_last_error.argtypes = []
@@ -167,6 +171,33 @@ def subm3d_forward(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tensor,
     po = _dev(out, "out", feats.dtype, (N, O))
     _check(lib().subm3d_forward(pf, pn, pw, pb, po, N, I, O, _DTYPES[feats.dtype],
                                 _stream(stream)))
+    return out
+
+
+def subm3d_forward_ex(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tensor,
+                      bias: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                      act: str = "none", out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """out [N, O] = act(convolution + bias + residual), the fused block epilogue.
+
+    residual [N, O] of feats' dtype or None; it may be `out` itself (in place).
+    act is "none", "relu" or "silu"."""
+    if feats.dtype not in _DTYPES:
+        raise ValueError(f"feats dtype {feats.dtype} is not float32 or bfloat16")
+    if act not in ACTIVATIONS:
+        raise ValueError(f"act {act!r} is not one of {sorted(ACTIVATIONS)}")
+    N, I = feats.shape
+    O = weight.shape[0]
+    pf = _dev(feats, "feats")
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    pw = _dev(weight, "weight", feats.dtype, (O, 3, 3, 3, I))
+    pb = None if bias is None else _dev(bias, "bias", feats.dtype, (O,))
+    pr = None if residual is None else _dev(residual, "residual", feats.dtype, (N, O))
+    if out is None:
+        out = torch.empty((N, O), dtype=feats.dtype, device=feats.device)
+    po = _dev(out, "out", feats.dtype, (N, O))
+    _check(lib().subm3d_forward_ex(pf, pn, pw, pb, pr, ACTIVATIONS[act], po, N, I, O,
+                                   _DTYPES[feats.dtype], _stream(stream)))
     return out
 
 

@@ -47,9 +47,9 @@ int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t*
   return kmap_build(coords, N, res, nbr, order, hash_capacity, workspace, ws_bytes, stream);
 }
 
-int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
-                   void* out, int64_t N, int32_t I, int32_t O, subm3d_dtype dtype,
-                   cudaStream_t stream) {
+int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
+                      const void* residual, subm3d_act act, void* out, int64_t N, int32_t I,
+                      int32_t O, subm3d_dtype dtype, cudaStream_t stream) {
   clear_error();
   if (N < 0 || N > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld outside [0, 2^31)", (long long)N);
@@ -63,6 +63,10 @@ int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, co
     set_error("subm3d_forward: unknown dtype %d", static_cast<int>(dtype));
     return SUBM3D_ERR_ARG;
   }
+  if (act != SUBM3D_ACT_NONE && act != SUBM3D_ACT_RELU && act != SUBM3D_ACT_SILU) {
+    set_error("subm3d_forward_ex: unknown activation %d", static_cast<int>(act));
+    return SUBM3D_ERR_ARG;
+  }
   if (N == 0) return SUBM3D_OK;
   if (!feats || !nbr || !weight || !out) {
     set_error("subm3d_forward: NULL pointer (feats=%p nbr=%p weight=%p out=%p)", feats,
@@ -71,12 +75,26 @@ int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, co
   }
   const uintptr_t any = reinterpret_cast<uintptr_t>(feats) | reinterpret_cast<uintptr_t>(nbr) |
                         reinterpret_cast<uintptr_t>(weight) | reinterpret_cast<uintptr_t>(out) |
-                        reinterpret_cast<uintptr_t>(bias);
+                        reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(residual);
   if (any & 15) {
-    set_error("subm3d_forward: feats=%p nbr=%p weight=%p bias=%p out=%p must be 16-byte aligned",
-              feats, (const void*)nbr, weight, bias, out);
+    set_error("subm3d_forward: feats=%p nbr=%p weight=%p bias=%p residual=%p out=%p must be "
+              "16-byte aligned",
+              feats, (const void*)nbr, weight, bias, residual, out);
     return SUBM3D_ERR_ARG;
   }
+  if (residual && residual != out) {
+    // the one overlap allowed is residual == out (in place)
+    const size_t bytes = static_cast<size_t>(N) * O * (dtype == SUBM3D_BF16 ? 2 : 4);
+    const char* r = static_cast<const char*>(residual);
+    const char* q = static_cast<const char*>(out);
+    if (r < q + bytes && q < r + bytes) {
+      set_error("subm3d_forward_ex: residual=%p partially overlaps out=%p (only residual == out "
+                "is allowed)",
+                residual, out);
+      return SUBM3D_ERR_ARG;
+    }
+  }
+  const Epilogue epi{residual, static_cast<int>(act)};
   if (dtype == SUBM3D_BF16) {
     if (I % 8 || O % 8) {
       set_error("subm3d_forward: bf16 needs I %% 8 == 0 and O %% 8 == 0 (got I=%d, O=%d)", I, O);
@@ -86,14 +104,21 @@ int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, co
       return forward_launch_tm(static_cast<const __nv_bfloat16*>(feats), nbr,
                                static_cast<const __nv_bfloat16*>(weight),
                                static_cast<const __nv_bfloat16*>(bias),
-                               static_cast<__nv_bfloat16*>(out), N, I, O, stream);
+                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, stream);
     if (O <= 256)
       return forward_launch_tc(static_cast<const __nv_bfloat16*>(feats), nbr,
                                static_cast<const __nv_bfloat16*>(weight),
                                static_cast<const __nv_bfloat16*>(bias),
-                               static_cast<__nv_bfloat16*>(out), N, I, O, stream);
+                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, stream);
   }
-  return forward_launch_simt(feats, nbr, weight, bias, out, N, I, O, dtype, stream);
+  return forward_launch_simt(feats, nbr, weight, bias, out, N, I, O, dtype, epi, stream);
+}
+
+int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
+                   void* out, int64_t N, int32_t I, int32_t O, subm3d_dtype dtype,
+                   cudaStream_t stream) {
+  return subm3d_forward_ex(feats, nbr, weight, bias, nullptr, SUBM3D_ACT_NONE, out, N, I, O,
+                           dtype, stream);
 }
 
 int subm3d_forward_status(cudaStream_t stream) {

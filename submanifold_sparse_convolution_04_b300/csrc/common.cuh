@@ -59,18 +59,26 @@ inline int num_sms() {
 // Device error word of the forward kernels (bit flags below).
 enum : int { kDevErrBadNbr = 1, kDevErrTimeout = 2 };
 int* forward_error_word();                      // device address of the word
+// Fused epilogue of subm3d_forward_ex: out = act(acc + bias + residual); residual NULL
+// and act SUBM3D_ACT_NONE give the plain convolution.
+struct Epilogue {
+  const void* residual;   // [N, O] of the feature dtype, or NULL
+  int act;                // subm3d_act
+};
 int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
-                      __nv_bfloat16* out, int64_t N, int I, int O, cudaStream_t stream);
+                      __nv_bfloat16* out, int64_t N, int I, int O, Epilogue epi,
+                      cudaStream_t stream);
 // The narrow-layer kernel (A operand in tensor memory, resident weight): I and O in
 // {16, 32, 48, 64} and feats 32-byte aligned.
 bool forward_tm_applies(const void* feats, int I, int O);
 int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
-                      __nv_bfloat16* out, int64_t N, int I, int O, cudaStream_t stream);
+                      __nv_bfloat16* out, int64_t N, int I, int O, Epilogue epi,
+                      cudaStream_t stream);
 int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weight,
                         const void* bias, void* out, int64_t N, int I, int O,
-                        subm3d_dtype dtype, cudaStream_t stream);
+                        subm3d_dtype dtype, Epilogue epi, cudaStream_t stream);
 int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int32_t* order,
                int64_t hash_capacity, void* workspace, size_t ws_bytes, cudaStream_t stream);
 size_t kmap_workspace_bytes(int64_t N, int64_t hash_capacity);
@@ -211,5 +219,58 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Fused epilogue ------------------------------------------------------------------
+// silu(y) = y / (1 + e^-y) with the fast exponential and division intrinsics (a few
+// ulp, far below the bf16 output rounding and the fp32 tolerance; the exact expf and
+// IEEE division made the epilogue warps, not the gathers, set the pace). Below -80,
+// |silu(y)| < 1e-33 is returned as 0 (e^80 stays inside the intrinsic division's
+// range); NaN propagates.
+__device__ __forceinline__ float apply_act(float y, int act) {
+  if (act == SUBM3D_ACT_RELU) return fmaxf(y, 0.f);
+  if (act == SUBM3D_ACT_SILU) return y < -80.f ? 0.f : __fdividef(y, 1.f + __expf(-y));
+  return y;
+}
+// Asks L2 for every 128-byte line of a row of `bytes` (> 0) bytes at p; the addresses
+// must lie inside the allocation. A hint: no data comes back, nothing waits for it.
+__device__ __forceinline__ void prefetch_row_l2(const void* p, int bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + bytes - 1));
+}
+// 16 bytes of a row that may be the output buffer itself (an in-place residual): a
+// plain load, not the read-only path.
+__device__ __forceinline__ uint4 ld_row16(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+// Eight consecutive output columns of one row: acc (fp32 bit patterns) + bias, plus the
+// eight residual values in r when has_res, then the activation, rounded to bf16
+// (nearest-even) and packed for one 16-byte store.
+__device__ __forceinline__ uint4 epilogue8_bf16(const uint32_t (&acc)[8], const float* bias8,
+                                                bool has_res, uint4 r, int act) {
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = __uint_as_float(acc[e]) + bias8[e];
+  if (has_res) {
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[e]));
+      y[2 * e] += f.x;
+      y[2 * e + 1] += f.y;
+    }
+  }
+  if (act != SUBM3D_ACT_NONE) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = apply_act(y[e], act);
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+    packed[e] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  return make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
 
 }  // namespace subm3d

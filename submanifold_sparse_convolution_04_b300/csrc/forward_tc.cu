@@ -35,8 +35,9 @@
 // instruction's descriptor serialises the MMAs (about 300 cycles each instead of
 // 85 at N = 64 or 128 at N = 256). tcgen05.commit then frees the stage. Two
 // accumulators (double-buffered tensor memory) let four epilogue warps drain tile t
-// (tcgen05.ld, 8 columns at a time -> + bias -> bf16 round-to-nearest-even -> one
-// 16-byte store per 8 outputs) while the tensor core works on tile t + 1.
+// (tcgen05.ld, 8 columns at a time -> + bias [+ residual row, activation: the fused
+// block epilogue] -> bf16 round-to-nearest-even -> one 16-byte store per 8 outputs)
+// while the tensor core works on tile t + 1.
 //
 // Warp roles: warps 0 .. 4G-1 producers (the first thread of each group also issues
 // its stages' weight TMA), warp 4G tensor-memory allocation + MMA issue (one lane),
@@ -96,6 +97,8 @@ struct Params {
   const int32_t* nbr;
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
+  const __nv_bfloat16* residual;   // [N, O] or NULL (may equal out)
+  int act;                         // subm3d_act
   int64_t N;
   int I, O;
   int nchunks;
@@ -382,13 +385,21 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
       const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
+      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
+      // the residual row travels to L2, and its first 16 bytes to registers, while this
+      // warp waits for the accumulator
+      const __nv_bfloat16* rrow = (p.residual && row < p.N) ? p.residual + row * p.O : nullptr;
+      uint4 rnext = make_uint4(0, 0, 0, 0);
+      if (rrow) {
+        prefetch_row_l2(rrow, p.O * 2);
+        rnext = ld_row16(rrow);
+      }
       if (!mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag)) {
         *abort_flag = 1;
         atomicOr(p.err, kDevErrTimeout);
         break;
       }
       tc_fence_after();
-      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + buf * C::kBufCols;
       __nv_bfloat16* orow = p.out + row * p.O;
@@ -396,6 +407,8 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
       for (int cc = 0; cc < NMMA / 8; ++cc) {   // 8 columns at a time
         uint32_t v[8];
         tmem_ld8(taddr + cc * 8, v);
+        const uint4 rcur = rnext;   // the next group's residual loads during this one
+        if (rrow && cc * 8 + 8 < p.O) rnext = ld_row16(rrow + cc * 8 + 8);
         tmem_ld_wait();
         if (cc == NMMA / 8 - 1) {
           tc_fence_before();
@@ -403,15 +416,8 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
         }
         const int col0 = cc * 8;
         if (row < p.N && col0 < p.O) {
-          uint32_t packed[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(v[2 * e]) + bias_sm[col0 + 2 * e];
-            const float hi = __uint_as_float(v[2 * e + 1]) + bias_sm[col0 + 2 * e + 1];
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-            packed[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(orow + col0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          *reinterpret_cast<uint4*>(orow + col0) =
+              epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act);
         }
       }
     }
@@ -481,14 +487,14 @@ int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) 
 
 int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv_bfloat16* weight,
                       const __nv_bfloat16* bias, __nv_bfloat16* out, int64_t N, int I, int O,
-                      cudaStream_t stream) {
+                      Epilogue epi, cudaStream_t stream) {
   const int64_t ntiles = (N + kBM - 1) / kBM;
   if (ntiles > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld too large", (long long)N);
     return SUBM3D_ERR_UNSUPPORTED;
   }
-  Params prm{feats, nbr, bias, out, N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles),
-             forward_error_word()};
+  Params prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual), epi.act,
+             N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), forward_error_word()};
   const int nmma = (O + 15) / 16 * 16;
   switch (nmma) {
 #define SUBM3D_CASE(n) \

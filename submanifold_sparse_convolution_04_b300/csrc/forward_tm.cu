@@ -34,8 +34,8 @@
 // warps have arrived (after tcgen05.wait::st) and its weight bytes have landed.
 // One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
 // up to four per offset) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
-// t (tcgen05.ld -> + bias -> bf16 round-to-nearest-even -> 16-byte stores) while
-// the tensor core works on tile t + 1.
+// t (tcgen05.ld -> + bias [+ residual row, activation: the fused block epilogue] ->
+// bf16 round-to-nearest-even -> 16-byte stores) while the tensor core works on tile t + 1.
 //
 // Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the device
 // error word, stops the CTA's pipeline, drains what is in flight and releases tensor
@@ -82,6 +82,8 @@ struct TmParams {
   const int32_t* nbr;
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
+  const __nv_bfloat16* residual;   // [N, O] or NULL (may equal out)
+  int act;                         // subm3d_act
   int64_t N;
   int I, O;
   int ntiles;
@@ -410,19 +412,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
+      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
+      // the residual row travels to L2, and its first 16 bytes to registers, while this
+      // warp waits for the accumulator
+      const __nv_bfloat16* rrow = (p.residual && row < p.N) ? p.residual + row * p.O : nullptr;
+      uint4 rnext = make_uint4(0, 0, 0, 0);
+      if (rrow) {
+        prefetch_row_l2(rrow, p.O * 2);
+        rnext = ld_row16(rrow);
+      }
       if (!mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag)) {
         *abort_flag = 1;
         atomicOr(p.err, kDevErrTimeout);
         break;
       }
       tc_fence_after();
-      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + buf * kAccCols;
       __nv_bfloat16* orow = p.out + row * p.O;
 #pragma unroll 1
       for (int cc = 0; cc < NMMA / 8; ++cc) {   // 8 columns at a time
         uint32_t v[8];
         tmem_ld8(taddr + cc * 8, v);
+        const uint4 rcur = rnext;   // the next group's residual loads during this one
+        if (rrow && cc * 8 + 8 < p.O) rnext = ld_row16(rrow + cc * 8 + 8);
         tmem_ld_wait();
         if (cc == NMMA / 8 - 1) {
           tc_fence_before();
@@ -430,16 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int col0 = cc * 8;
         if (row < p.N) {
-          uint32_t packed[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(v[2 * e]) + bias_sm[col0 + 2 * e];
-            const float hi = __uint_as_float(v[2 * e + 1]) + bias_sm[col0 + 2 * e + 1];
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-            packed[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
           *reinterpret_cast<uint4*>(orow + col0) =
-              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act);
         }
       }
     }
@@ -515,13 +519,14 @@ bool forward_tm_applies(const void* feats, int I, int O) {
 
 int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv_bfloat16* weight,
                       const __nv_bfloat16* bias, __nv_bfloat16* out, int64_t N, int I, int O,
-                      cudaStream_t stream) {
+                      Epilogue epi, cudaStream_t stream) {
   const int64_t ntiles = (N + kBM - 1) / kBM;
   if (ntiles > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld too large", (long long)N);
     return SUBM3D_ERR_UNSUPPORTED;
   }
-  TmParams prm{feats, nbr, bias, out, N, I, O, static_cast<int>(ntiles), forward_error_word()};
+  TmParams prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual),
+               epi.act, N, I, O, static_cast<int>(ntiles), forward_error_word()};
   switch (O) {
     case 16: return tm_launch<16>(prm, weight, stream);
     case 32: return tm_launch<32>(prm, weight, stream);

@@ -6,7 +6,8 @@ no part of the convolution itself: it only draws integer lattice coordinates
 values. Both the CUDA path and the CPU oracle consume what it produces.
 """
 from .shells import ellipsoid_shell, torus_shell, union_coords, uniform_rotation
-from .configs import CONFIGS, make_case, make_coords, make_values, round_to_bf16
+from .configs import (CONFIGS, make_case, make_coords, make_residual, make_values,
+                      round_to_bf16)
 
 __all__ = ["ellipsoid_shell", "torus_shell", "union_coords", "uniform_rotation", "CONFIGS",
-           "make_case", "make_coords", "make_values", "round_to_bf16"]
+           "make_case", "make_coords", "make_residual", "make_values", "round_to_bf16"]

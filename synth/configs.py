@@ -153,6 +153,19 @@ def make_values(N: int, I: int, O: int, dtype: str, seed: int):
     return out
 
 
+def make_residual(N: int, O: int, dtype: str, seed: int):
+    """Skip-path input [N, O] of the fused block epilogue: N(0, 1) float32 values (its
+    own stream of the seed), rounded to bf16 for dtype "bf16". Returns (values, bf16
+    bits or None)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 2]))
+    r = rng.standard_normal((N, O), dtype=np.float32)
+    if dtype == "bf16":
+        return round_to_bf16(r)
+    if dtype != "f32":
+        raise ValueError(dtype)
+    return r, None
+
+
 def make_case(cfg_id: int, order: str = "raster"):
     """Coordinates and values of workload cfg_id (see the module docstring)."""
     cfg = CONFIGS[cfg_id]

@@ -32,13 +32,15 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["OFFSETS", "CENTER", "ACTIVATIONS", "OracleError", "tap", "coordinate_dict",
-           "kernel_map", "subm_conv3d", "subm_conv3d_rows", "activation", "block_epilogue"]
+__all__ = ["OFFSETS", "CENTER", "ACTIVATIONS", "POOL_MODES", "OracleError", "tap",
+           "coordinate_dict", "kernel_map", "subm_conv3d", "subm_conv3d_rows", "activation",
+           "block_epilogue", "morton_code", "child_bit", "downsample", "upsample"]
 
 # k -> (dz, dy, dx), k = 9 (dz + 1) + 3 (dy + 1) + (dx + 1)
 OFFSETS = [(dz, dy, dx) for dz in (-1, 0, 1) for dy in (-1, 0, 1) for dx in (-1, 0, 1)]
 CENTER = 13
 ACTIVATIONS = ("none", "relu", "silu")
+POOL_MODES = ("mean", "max")
 MAX_BATCH = 65534
 MAX_RES = 65535
 
@@ -170,3 +172,73 @@ def block_epilogue(conv, residual=None, act="none"):
             raise OracleError(f"residual shape {residual.shape} != output shape {y.shape}")
         y = y + residual
     return activation(y, act)
+
+
+def morton_code(z, y, x):
+    """Z-order code of a lattice point: bit t of x goes to bit 3t, of y to 3t + 1, of z to
+    3t + 2 (z the most significant axis of each bit triple)."""
+    m, t = 0, 0
+    while (z >> t) or (y >> t) or (x >> t):
+        m |= ((x >> t) & 1) << (3 * t)
+        m |= ((y >> t) & 1) << (3 * t + 1)
+        m |= ((z >> t) & 1) << (3 * t + 2)
+        t += 1
+    return m
+
+
+def child_bit(z, y, x):
+    """Place of a fine voxel inside its parent's 2x2x2 cell: (z&1)<<2 | (y&1)<<1 | (x&1)."""
+    return ((z & 1) << 2) | ((y & 1) << 1) | (x & 1)
+
+
+def downsample(coords, feats, res, mode="mean"):
+    """SparseDownsample(2) and the subdivision it stores for its paired upsample.
+
+    The "pixal3d_mrp_mlx README" scope table lists SparseDownsample(2) (its status notes
+    say the shared core's downsample takes a pooling mode) and SparseUpsample(2) as the
+    cache-paired inverse that needs the subdivision stored by the matching downsample.
+    Readings: the coarse voxel of a fine voxel (b, z, y, x) is (b, z//2, y//2, x//2);
+    the coarse set is the set of those parents, ordered by batch, then Morton code;
+    a coarse feature pools its children's features ("mean" or "max"); the subdivision
+    is each fine row's parent row plus each parent's 8-bit child mask (child_bit).
+
+    Returns (coarse_coords int32 [M, 4], coarse_feats float64 [M, C] or None,
+    parent int32 [N], child_mask uint8 [M]).
+    """
+    if mode not in POOL_MODES:
+        raise OracleError(f"pooling mode {mode!r} is not one of {POOL_MODES}")
+    coordinate_dict(coords, res)    # validates range and duplicates
+    clist = np.asarray(coords).tolist()
+    groups = {}
+    for i, (b, z, y, x) in enumerate(clist):
+        groups.setdefault((b, z // 2, y // 2, x // 2), []).append(i)
+    order = sorted(groups, key=lambda q: (q[0], morton_code(q[1], q[2], q[3])))
+    M = len(order)
+    coarse = np.array(order, dtype=np.int32).reshape(M, 4)
+    parent = np.empty(len(clist), dtype=np.int32)
+    mask = np.zeros(M, dtype=np.uint8)
+    for p, q in enumerate(order):
+        for i in groups[q]:
+            parent[i] = p
+            b, z, y, x = clist[i]
+            mask[p] |= 1 << child_bit(z, y, x)
+    pooled = None
+    if feats is not None:
+        f = np.asarray(feats, dtype=np.float64)
+        if f.ndim != 2 or f.shape[0] != len(clist):
+            raise OracleError("feats must be [N, C]")
+        pooled = np.empty((M, f.shape[1]), dtype=np.float64)
+        for p, q in enumerate(order):
+            rows = f[groups[q]]
+            pooled[p] = rows.sum(axis=0) / len(rows) if mode == "mean" else rows.max(axis=0)
+    return coarse, pooled, parent, mask
+
+
+def upsample(coarse_feats, parent):
+    """SparseUpsample(2) with a stored subdivision: each fine row takes its parent's
+    coarse row (the fine set is exactly the one the paired downsample saw), float64."""
+    c = np.asarray(coarse_feats, dtype=np.float64)
+    parent = np.asarray(parent)
+    if parent.size and (parent.min() < 0 or parent.max() >= c.shape[0]):
+        raise OracleError("parent index outside the coarse rows")
+    return c[parent]

@@ -380,3 +380,103 @@ def test_planted_silu_sign_mistake_is_caught(monkeypatch):
     f, w, b = rand_values(rng, 40, 3, 3)
     got = ref.block_epilogue(ref.subm_conv3d(c, f, w, b, 6), None, "silu")
     assert not np.allclose(got, dense_block(c, f, w, b, None, "silu", 6), atol=1e-6)
+
+
+# ------------------------------------------------- SparseDownsample(2) / SparseUpsample(2)
+
+def _morton_less(p, q):
+    """Z-order comparison without building a code: the axis whose coordinates differ in
+    the highest bit decides; on equal highest bits z outranks y outranks x."""
+    j, best = 0, 0
+    for k in range(3):
+        d = p[k] ^ q[k]
+        if best < d and best < (best ^ d):    # msb(best) < msb(d)
+            j, best = k, d
+    return p[j] < q[j]
+
+
+def dense_pool(coords, feats, res, mode):
+    """Parents, pooled features and child counts from torch's dense 2x2x2 pooling on the
+    densified grid (ceil mode for odd sides)."""
+    coords = np.asarray(coords)
+    B = int(coords[:, 0].max()) + 1
+    C = feats.shape[1]
+    b, z, y, x = (torch.from_numpy(coords[:, k].astype(np.int64)) for k in range(4))
+    occ = torch.zeros(B, 1, res, res, res, dtype=torch.float64)
+    occ[b, 0, z, y, x] = 1.0
+    cnt = F.avg_pool3d(occ, 2, 2, ceil_mode=True, divisor_override=1)
+    if mode == "mean":
+        g = torch.zeros(B, C, res, res, res, dtype=torch.float64)
+        g[b, :, z, y, x] = torch.from_numpy(np.asarray(feats, np.float64))
+        pooled = F.avg_pool3d(g, 2, 2, ceil_mode=True, divisor_override=1) / cnt.clamp(min=1)
+    else:
+        g = torch.full((B, C, res, res, res), -np.inf, dtype=torch.float64)
+        g[b, :, z, y, x] = torch.from_numpy(np.asarray(feats, np.float64))
+        pooled = F.max_pool3d(g, 2, 2, ceil_mode=True)
+    return cnt[:, 0], pooled
+
+
+@pytest.mark.parametrize("mode", ref.POOL_MODES)
+@pytest.mark.parametrize("seed,res,batch,n", [(0, 4, 1, 30), (1, 7, 2, 120), (2, 9, 3, 200),
+                                               (3, 2, 1, 8), (4, 5, 2, 1)])
+def test_downsample_matches_dense_pooling(mode, seed, res, batch, n):
+    rng = np.random.default_rng(seed)
+    c = random_set(rng, res, batch, n)
+    f = rng.standard_normal((c.shape[0], 3))
+    coarse, pooled, parent, mask = ref.downsample(c, f, res, mode)
+    cnt, dense = dense_pool(c, f, res, mode)
+    # the coarse set is exactly the occupied 2x2x2 cells
+    occ = torch.nonzero(cnt > 0).numpy()
+    assert sorted(map(tuple, coarse.tolist())) == sorted(map(tuple, occ.tolist()))
+    # pooled rows and child counts equal the dense pooling at those cells
+    cb, cz, cy, cx = (coarse[:, k] for k in range(4))
+    np.testing.assert_allclose(pooled, dense.numpy()[cb, :, cz, cy, cx], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal([bin(int(m)).count("1") for m in mask], cnt.numpy()[cb, cz, cy, cx])
+    # every fine row points at the cell that holds it, with its own bit set in the mask
+    for i, (b, z, y, x) in enumerate(c.tolist()):
+        assert tuple(coarse[parent[i]]) == (b, z // 2, y // 2, x // 2)
+        assert mask[parent[i]] >> ((z & 1) << 2 | (y & 1) << 1 | (x & 1)) & 1
+
+
+def test_downsample_order_is_batch_then_z_order():
+    rng = np.random.default_rng(12)
+    c = random_set(rng, 32, 3, 400)
+    coarse = ref.downsample(c, None, 32)[0].tolist()
+    for p, q in zip(coarse, coarse[1:]):
+        assert p[0] < q[0] or (p[0] == q[0] and _morton_less(p[1:], q[1:])), (p, q)
+
+
+def test_upsample_inverts_structure_and_max_of_single_children():
+    rng = np.random.default_rng(13)
+    c = random_set(rng, 8, 2, 100)
+    f = rng.standard_normal((c.shape[0], 4))
+    coarse, pooled, parent, mask = ref.downsample(c, f, 8, "mean")
+    up = ref.upsample(pooled, parent)
+    # each fine row gets its cell's mean; summing a cell's children gives count x mean
+    for p in range(len(coarse)):
+        kids = np.nonzero(parent == p)[0]
+        np.testing.assert_allclose(up[kids].sum(axis=0), f[kids].sum(axis=0), rtol=0, atol=1e-12)
+    # voxels alone in their cell come back unchanged (both modes)
+    iso = np.array([[0, 0, 0, 0], [0, 2, 4, 6], [1, 5, 5, 5]], np.int32)
+    g = rng.standard_normal((3, 2))
+    for mode in ref.POOL_MODES:
+        _, pl, par, mk = ref.downsample(iso, g, 8, mode)
+        np.testing.assert_array_equal(ref.upsample(pl, par), g)
+        assert all(bin(int(m)).count("1") == 1 for m in mk)
+    with pytest.raises(ref.OracleError):
+        ref.upsample(pooled, np.array([len(coarse)]))
+    with pytest.raises(ref.OracleError):
+        ref.downsample(c, f, 8, "sum")
+    with pytest.raises(ref.OracleError):
+        ref.downsample(np.array([[0, 1, 1, 1], [0, 1, 1, 1]], np.int32), None, 4)
+
+
+def test_planted_morton_axis_swap_is_caught(monkeypatch):
+    """Planting x as the most significant axis of the Z-order code in the oracle must
+    break the order pin."""
+    monkeypatch.setattr(ref, "morton_code", lambda z, y, x: sum(
+        (((z >> t) & 1) << (3 * t) | ((y >> t) & 1) << (3 * t + 1) | ((x >> t) & 1) << (3 * t + 2))
+        for t in range(16)))
+    c = random_set(np.random.default_rng(12), 32, 1, 300)
+    coarse = ref.downsample(c, None, 32)[0].tolist()
+    assert not all(_morton_less(p[1:], q[1:]) for p, q in zip(coarse, coarse[1:]))

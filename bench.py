@@ -9,6 +9,7 @@ subm3d_forward (tcgen05 gather-GEMM with fused bias). Default workload: the
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
     python bench.py --impl reference ...      # the CPU oracle, as the reference arm
     python bench.py --residual --act relu     # forward with the fused block epilogue
+    python bench.py --op downsample|upsample  # SparseDownsample(2) / SparseUpsample(2)
 
 Prints one JSON line (rank 0). `value` = effective TFLOP/s of the whole step,
 2 * pairs * I * O / step time, summed over ranks (replicas: every rank runs the
@@ -58,6 +59,11 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--op", default="conv", choices=["conv", "downsample", "upsample"],
+                   help="conv: kmap + forward (the default step); downsample / upsample: "
+                        "SparseDownsample(2) / its paired SparseUpsample(2) on the workload")
+    p.add_argument("--pool", default="mean", choices=["mean", "max"],
+                   help="pooling of --op downsample (and of the coarse rows --op upsample uses)")
     p.add_argument("--residual", action="store_true",
                    help="fused block epilogue: add a residual [N, O] input (subm3d_forward_ex)")
     p.add_argument("--act", default="none", choices=["none", "relu", "silu"],
@@ -504,11 +510,118 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_resample(args, world, rank, local):
+    """SparseDownsample(2) (`--op downsample`: the Morton sort, the parent scan and the
+    pooling, with its one host sync) or the cache-paired SparseUpsample(2) (`--op
+    upsample`: one gather kernel) on the workload's voxels and features. Metric: fine
+    voxels per second. Roofline bytes: downsample 16 N (coords) + N C e (feats) + 4 N
+    (parent) + M (16 + 1 + C e) (coarse coords, masks, pooled rows); upsample 4 N + M C e
+    + N C e."""
+    import numpy as np
+    import torch
+    from submanifold_sparse_convolution_04_b300 import (lib, subm3d_downsample,
+                                                        subm3d_forward_status,
+                                                        subm3d_kernel_launches, subm3d_upsample)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = load_case(args)
+    N, C, res = case["coords"].shape[0], case["I"], case["res"]
+    bf16 = case["dtype"] == "bf16"
+    e = 2 if bf16 else 4
+    c = torch.from_numpy(case["coords"]).to(dev)
+    f = (torch.from_numpy(case["feats_bits"].view(np.int16)).view(torch.bfloat16) if bf16
+         else torch.from_numpy(case["feats"])).to(dev)
+    ws = torch.empty(max(256, lib().subm3d_downsample_workspace_bytes(N)), dtype=torch.uint8,
+                     device=dev)
+    cc, cf, parent, mask = subm3d_downsample(c, res, f, args.pool, workspace=ws)
+    M = cc.shape[0]
+    up = torch.empty((N, C), dtype=f.dtype, device=dev)
+    if args.op == "downsample":
+        def step():
+            subm3d_downsample(c, res, f, args.pool, workspace=ws)
+        nbytes = 16 * N + N * C * e + 4 * N + M * (16 + 1 + C * e)
+        kernel = "downsample: sort + ds_count/ds_scan/ds_emit + ds_pool"
+    else:
+        def step():
+            subm3d_upsample(cf, parent, out=up)
+        nbytes = 4 * N + M * C * e + N * C * e
+        kernel = "us_gather"
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    subm3d_forward_status()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = subm3d_kernel_launches()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = subm3d_kernel_launches() - launches0
+    clk = clocks.stop()
+    barrier(world)
+    subm3d_forward_status()
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    op_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    ms_per_step = total_ms / K
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = nbytes / (op_ms / 1e3) / 1e9
+    line = {
+        "metric": f"Sparse{args.op.capitalize()}(2) Mvoxels/s (fine voxels; fraction of roofline)",
+        "value": world * N / (ms_per_step / 1e3) / 1e6, "unit": "Mvoxels/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32",
+        "data": "synthetic",
+        "config": dict(workload_desc(case, None), op=args.op, pool=args.pool, coarse_M=int(M),
+                       l2="inputs larger than L2; no flush between steps",
+                       parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "op_us": op_ms * 1e3,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "traffic_source": "no ncu summary", "peak_source": f"hbm_gbs, {peak_kind}",
+                     "algorithmic_bytes": nbytes},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import ref
+        S = min(N, 1_000_000)
+        sub, fs = case["coords"][:S], case["feats"][:S]
+        t0 = time.perf_counter()
+        _, cfs, par, _ = ref.downsample(sub, fs, res, args.pool)
+        t1 = time.perf_counter()
+        if args.op == "upsample":
+            ref.upsample(cfs, par)
+        dt = (time.perf_counter() - t1) if args.op == "upsample" else (t1 - t0)
+        line["cpu_baseline"] = {"value": S / dt / 1e6, "unit": "Mvoxels/s", "cores": 1,
+                                "kind": "oracle", "seconds": dt,
+                                "sample": f"Python oracle ({args.op}) on the first {S} voxels in "
+                                          f"raster order, single thread"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.op != "conv":
+        run_resample(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -61,6 +61,12 @@ typedef enum {
 
 typedef enum { SUBM3D_F32 = 0, SUBM3D_BF16 = 1 } subm3d_dtype;
 
+/* Pooling of subm3d_downsample. */
+typedef enum {
+  SUBM3D_POOL_MEAN = 0,  /* mean of the children present (fp32 sum / count)            */
+  SUBM3D_POOL_MAX = 1    /* elementwise maximum of the children present                */
+} subm3d_pool;
+
 /* Activation of the fused epilogue (subm3d_forward_ex). */
 typedef enum {
   SUBM3D_ACT_NONE = 0,  /* identity                                                  */
@@ -213,10 +219,68 @@ SUBM3D_API int subm3d_forward_ex(const void* feats, const int32_t* nbr, const vo
                                  subm3d_dtype dtype, cudaStream_t stream);
 
 /*
- * Waits for `stream`, then reads and clears the forward kernels' device error word:
- * SUBM3D_OK, or SUBM3D_ERR_DEVICE (message says which condition: an nbr entry
- * outside [-1, N), or a bounded pipeline wait that ran out). The word is shared by
- * all streams of the process.
+ * SparseDownsample(2) and the subdivision its paired upsample needs. The
+ * "pixal3d_mrp_mlx README" scope table lists SparseDownsample(2) (with a pooling mode,
+ * per its status notes) and SparseUpsample(2) as the cache-paired inverse that reuses
+ * the subdivision stored by the matching downsample; the pages give no more detail,
+ * so this is the plain reading:
+ *
+ *   parent voxel of (b, z, y, x)  = (b, z >> 1, y >> 1, x >> 1)
+ *   coarse voxels                 = the distinct parents, in (batch, Morton code) order
+ *                                   (Morton: bit t of x -> 3t, of y -> 3t+1, of z -> 3t+2)
+ *   coarse_feats[p, :]            = mean or max of feats over the children of p
+ *   parent[i]                     = coarse row of fine row i
+ *   child_mask[p]                 = OR over children of 1 << ((z&1)<<2 | (y&1)<<1 | (x&1))
+ *
+ * Steps: validate + pack and the kernel map's Morton radix sort (children of one
+ * parent end up adjacent, since a parent's key is its children's key >> 3); parent
+ * starts counted per 2048-position tile and scanned; one pass writes parent, coarse
+ * coordinates, child masks and each parent's first sorted position; the pooling runs
+ * a thread per (parent, 16 bytes of channels) in fp32, rounded once to the dtype.
+ *
+ *   coords        device int32 [N, 4] (b, z, y, x): as subm3d_build_kmap (range, no
+ *                 duplicates; res as there). The coarse grid has side (res + 1) / 2.
+ *   feats         device [N, C] of `dtype`, or NULL for the structure alone.
+ *   mode          SUBM3D_POOL_MEAN or SUBM3D_POOL_MAX.
+ *   coarse_coords device int32 [N, 4] (room for N rows; the first M are written).
+ *   coarse_feats  device [N, C] of `dtype` (first M rows written); ignored if feats is NULL.
+ *   parent        device int32 [N].
+ *   child_mask    device uint8 [N] (first M written).
+ *   M_out         HOST int64: the number of coarse voxels M (0 on failure).
+ *   workspace     device scratch of subm3d_downsample_workspace_bytes(N), 256-byte
+ *                 aligned; other pointers 16-byte aligned.
+ *
+ * Synchronises `stream` once (to read M and the status word), like subm3d_build_kmap;
+ * the pooling kernel is then enqueued after it. Errors: ERR_ARG, ERR_WORKSPACE,
+ * ERR_COORD_RANGE, ERR_DUPLICATE (outputs unspecified), ERR_CUDA, ERR_DEVICE.
+ */
+SUBM3D_API size_t subm3d_downsample_workspace_bytes(int64_t N);
+SUBM3D_API int subm3d_downsample(const int32_t* coords, int64_t N, int32_t res, const void* feats,
+                                 int32_t C, subm3d_dtype dtype, subm3d_pool mode,
+                                 int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
+                                 uint8_t* child_mask, int64_t* M_out, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * SparseUpsample(2) with the subdivision a subm3d_downsample stored:
+ *   fine_feats[i, :] = coarse_feats[parent[i], :]
+ * (the fine voxel set is the one the downsample saw, in its row order).
+ *
+ *   coarse_feats  device [M, C] of `dtype`.
+ *   parent        device int32 [N] from subm3d_downsample; an entry outside [0, M)
+ *                 gives a zero row and is reported by subm3d_forward_status.
+ *   fine_feats    device [N, C] of `dtype`; must not overlap coarse_feats.
+ * All pointers 16-byte aligned. Fully asynchronous.
+ */
+SUBM3D_API int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C,
+                               const int32_t* parent, int64_t N, subm3d_dtype dtype,
+                               void* fine_feats, cudaStream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word of the forward and
+ * upsample kernels: SUBM3D_OK, or SUBM3D_ERR_DEVICE (message says which condition: an
+ * nbr entry outside [-1, N), a bounded pipeline wait that ran out, or a parent entry
+ * outside [0, M)). The word is shared by all streams of the process.
  */
 SUBM3D_API int subm3d_forward_status(cudaStream_t stream);
 

@@ -17,6 +17,7 @@ OK, ERR_ARG, ERR_COORD_RANGE, ERR_DUPLICATE, ERR_HASH_FULL, ERR_CUDA, ERR_UNSUPP
 F32, BF16 = 0, 1
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 ACTIVATIONS = {"none": 0, "relu": 1, "silu": 2}   # subm3d_act
+POOL_MODES = {"mean": 0, "max": 1}                 # subm3d_pool
 _NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_COORD_RANGE", -3: "ERR_DUPLICATE", -4: "ERR_HASH_FULL",
           -5: "ERR_CUDA", -6: "ERR_UNSUPPORTED", -7: "ERR_WORKSPACE", -8: "ERR_DEVICE"}
 
@@ -55,6 +56,13 @@ def lib() -> ctypes.CDLL:
         L.subm3d_forward_ex.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, i32, i32,
                                         ctypes.c_int, vp]
         L.subm3d_forward_ex.restype = ctypes.c_int
+        L.subm3d_downsample_workspace_bytes.argtypes = [i64]
+        L.subm3d_downsample_workspace_bytes.restype = sz
+        L.subm3d_downsample.argtypes = [vp, i64, i32, vp, i32, ctypes.c_int, ctypes.c_int, vp, vp,
+                                        vp, vp, ctypes.POINTER(ctypes.c_int64), vp, sz, vp]
+        L.subm3d_downsample.restype = ctypes.c_int
+        L.subm3d_upsample.argtypes = [vp, i64, i32, vp, i64, ctypes.c_int, vp, vp]
+        L.subm3d_upsample.restype = ctypes.c_int
         L.subm3d_forward_status.argtypes = [vp]
         L.subm3d_forward_status.restype = ctypes.c_int
         L.subm3d_last_error.argtypes = []
@@ -198,6 +206,59 @@ def subm3d_forward_ex(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tens
     po = _dev(out, "out", feats.dtype, (N, O))
     _check(lib().subm3d_forward_ex(pf, pn, pw, pb, pr, ACTIVATIONS[act], po, N, I, O,
                                    _DTYPES[feats.dtype], _stream(stream)))
+    return out
+
+
+def subm3d_downsample(coords: torch.Tensor, res: int, feats: torch.Tensor | None = None,
+                      mode: str = "mean", workspace: torch.Tensor | None = None, stream=None):
+    """SparseDownsample(2): (coarse_coords int32 [M, 4], coarse_feats [M, C] or None,
+    parent int32 [N], child_mask uint8 [M]) for coords int32 [N, 4] (b, z, y, x) on a
+    grid of side res. Coarse voxels come in (batch, Morton) order; parent and
+    child_mask are the subdivision subm3d_upsample takes. Synchronises the stream once."""
+    if mode not in POOL_MODES:
+        raise ValueError(f"mode {mode!r} is not one of {sorted(POOL_MODES)}")
+    N = coords.shape[0]
+    dev = coords.device
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    C, dt, pf, cf, pcf = 0, F32, None, None, None
+    if feats is not None:
+        if feats.dtype not in _DTYPES:
+            raise ValueError(f"feats dtype {feats.dtype} is not float32 or bfloat16")
+        C = feats.shape[1]
+        dt = _DTYPES[feats.dtype]
+        pf = _dev(feats, "feats", feats.dtype, (N, C))
+        cf = torch.empty((N, C), dtype=feats.dtype, device=dev)
+        pcf = _dev(cf, "coarse_feats")
+    cc = torch.empty((N, 4), dtype=torch.int32, device=dev)
+    parent = torch.empty(N, dtype=torch.int32, device=dev)
+    mask = torch.empty(N, dtype=torch.uint8, device=dev)
+    need = lib().subm3d_downsample_workspace_bytes(N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    pw = _dev(workspace, "workspace", torch.uint8)
+    M = ctypes.c_int64(0)
+    _check(lib().subm3d_downsample(pc, N, int(res), pf, C, dt, POOL_MODES[mode], _dev(cc, "cc"),
+                                   pcf, _dev(parent, "parent"), _dev(mask, "mask"),
+                                   ctypes.byref(M), pw, workspace.numel(), _stream(stream)))
+    m = M.value
+    return cc[:m], (None if cf is None else cf[:m]), parent, mask[:m]
+
+
+def subm3d_upsample(coarse_feats: torch.Tensor, parent: torch.Tensor,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """SparseUpsample(2) with a stored subdivision: out [N, C] with out[i] =
+    coarse_feats[parent[i]] (parent from subm3d_downsample)."""
+    if coarse_feats.dtype not in _DTYPES:
+        raise ValueError(f"coarse_feats dtype {coarse_feats.dtype} is not float32 or bfloat16")
+    M, C = coarse_feats.shape
+    N = parent.shape[0]
+    pcf = _dev(coarse_feats, "coarse_feats")
+    pp = _dev(parent, "parent", torch.int32, (N,))
+    if out is None:
+        out = torch.empty((N, C), dtype=coarse_feats.dtype, device=coarse_feats.device)
+    po = _dev(out, "out", coarse_feats.dtype, (N, C))
+    _check(lib().subm3d_upsample(pcf, M, C, pp, N, _DTYPES[coarse_feats.dtype], po,
+                                 _stream(stream)))
     return out
 
 

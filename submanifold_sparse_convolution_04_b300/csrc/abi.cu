@@ -121,6 +121,23 @@ int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, co
                            dtype, stream);
 }
 
+size_t subm3d_downsample_workspace_bytes(int64_t N) { return downsample_workspace_bytes(N); }
+
+int subm3d_downsample(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,
+                      subm3d_dtype dtype, subm3d_pool mode, int32_t* coarse_coords,
+                      void* coarse_feats, int32_t* parent, uint8_t* child_mask, int64_t* M_out,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  clear_error();
+  return downsample_build(coords, N, res, feats, C, dtype, static_cast<int>(mode), coarse_coords,
+                          coarse_feats, parent, child_mask, M_out, workspace, ws_bytes, stream);
+}
+
+int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
+                    int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream) {
+  clear_error();
+  return upsample_launch(coarse_feats, M, C, parent, N, dtype, fine_feats, stream);
+}
+
 int subm3d_forward_status(cudaStream_t stream) {
   clear_error();
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
@@ -134,8 +151,10 @@ int subm3d_forward_status(cudaStream_t stream) {
   SUBM3D_CUDA_TRY(cudaMemcpy(&host, word, sizeof(int), cudaMemcpyDeviceToHost));
   SUBM3D_CUDA_TRY(cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice));
   if (host == 0) return SUBM3D_OK;
-  set_error("subm3d_forward: device reported%s%s", (host & kDevErrBadNbr) ? " an nbr entry outside [-1, N)" : "",
-            (host & kDevErrTimeout) ? " a pipeline wait that ran out (kernel stopped early)" : "");
+  set_error("subm3d_forward_status: device reported%s%s%s",
+            (host & kDevErrBadNbr) ? " an nbr entry outside [-1, N)" : "",
+            (host & kDevErrTimeout) ? " a pipeline wait that ran out (kernel stopped early)" : "",
+            (host & kDevErrBadParent) ? " a parent entry outside [0, M)" : "");
   return SUBM3D_ERR_DEVICE;
 }
 

@@ -56,8 +56,8 @@ inline int num_sms() {
   return sms;
 }
 
-// Device error word of the forward kernels (bit flags below).
-enum : int { kDevErrBadNbr = 1, kDevErrTimeout = 2 };
+// Device error word of the forward and upsample kernels (bit flags below).
+enum : int { kDevErrBadNbr = 1, kDevErrTimeout = 2, kDevErrBadParent = 4 };
 int* forward_error_word();                      // device address of the word
 // Fused epilogue of subm3d_forward_ex: out = act(acc + bias + residual); residual NULL
 // and act SUBM3D_ACT_NONE give the plain convolution.
@@ -82,6 +82,13 @@ int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weigh
 int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int32_t* order,
                int64_t hash_capacity, void* workspace, size_t ws_bytes, cudaStream_t stream);
 size_t kmap_workspace_bytes(int64_t N, int64_t hash_capacity);
+size_t downsample_workspace_bytes(int64_t N);
+int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,
+                     subm3d_dtype dtype, int mode, int32_t* coarse_coords, void* coarse_feats,
+                     int32_t* parent, uint8_t* child_mask, int64_t* M_out, void* workspace,
+                     size_t ws_bytes, cudaStream_t stream);
+int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
+                    int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
 int64_t default_hash_capacity(int64_t N);
 
 // ---------------------------------------------------------------------------- device side

@@ -581,6 +581,280 @@ int grid_for(int64_t work, int threads, int per_sm) {
   return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
+// Validate + pack (Morton keys, batch above them) and the stable LSD radix sort of
+// (key, input row), shared by the kernel map and the downsample. Leaves the status
+// word's plan saying which of (mk0, ix0) / (mk1, ix1) holds the sorted result.
+int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* ws,
+                cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(kmap_sort_scatter,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScatterSmem));
+    attr_set = true;
+  }
+  KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
+  unsigned long long* mk1 = reinterpret_cast<unsigned long long*>(ws + L.mk1);
+  int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
+  int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+  int bits = 2;   // at least one whole 4x4x4 block level below the batch bits
+  while ((1 << bits) < res) ++bits;
+  const int npass = (3 * bits + 16 + 7) / 8;
+  kmap_init<<<8, 256, 0, stream>>>(st, hist);
+  SUBM3D_LAUNCHED("kmap_init");
+  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, mk0, ix0, st);
+  SUBM3D_LAUNCHED("kmap_pack");
+  kmap_plan<<<1, 1, 0, stream>>>(npass, st);
+  SUBM3D_LAUNCHED("kmap_plan");
+  const int nblk = static_cast<int>(L.nblk);
+  for (int p = 0; p < npass; ++p) {
+    kmap_sort_count<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, N, p, L.nblk, cnt, hist, st);
+    SUBM3D_LAUNCHED("kmap_sort_count");
+    kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, L.nblk, cnt, st);
+    SUBM3D_LAUNCHED("kmap_sort_scan");
+    kmap_sort_scatter<<<nblk, kSortThreads, kScatterSmem, stream>>>(mk0, mk1, ix0, ix1, N, p,
+                                                                    L.nblk, cnt, st);
+    SUBM3D_LAUNCHED("kmap_sort_scatter");
+  }
+  return SUBM3D_OK;
+}
+
+// SparseDownsample(2) / SparseUpsample(2) ------------------------------------------
+// The parent of a fine voxel (b, z, y, x) is (b, z>>1, y>>1, x>>1). Its sort key is the
+// fine key >> 3 (the lowest Morton triple is the place inside the 2x2x2 cell), so in the
+// sorted order each parent's children are adjacent and parents come in (batch, Morton)
+// order. A parent starts where key >> 3 changes; a scan over 2048-position tiles numbers
+// the parents.
+
+constexpr int kDsTile = kSortTile;   // sorted positions per tile (256 threads x 8)
+
+struct DsLayout {
+  Layout k;              // status, histograms and sort buffers (no hash table)
+  size_t tsum;           // uint32 [ntile + 1]: parents before each tile, then M
+  size_t pstart;         // int32 [N + 1]: first sorted position of each parent, then N
+  size_t total;
+  int64_t ntile;
+};
+
+DsLayout make_ds_layout(int64_t N) {
+  DsLayout D;
+  D.k = make_layout(N, 0);
+  D.ntile = (N + kDsTile - 1) / kDsTile;
+  size_t o = D.k.total;
+  D.tsum = o;   o = align256(o + sizeof(uint32_t) * (D.ntile + 1));
+  D.pstart = o; o = align256(o + sizeof(int32_t) * (N + 1));
+  D.total = o;
+  return D;
+}
+
+__device__ __forceinline__ bool parent_starts(const unsigned long long* mk, int64_t s) {
+  return s == 0 || (mk[s - 1] >> 3) != (mk[s] >> 3);
+}
+
+// Parents per tile; duplicate keys (adjacent equal) and sort indices out of range are
+// flagged in the status word.
+__global__ void __launch_bounds__(kSortThreads) ds_count(
+    const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
+    const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N,
+    uint32_t* __restrict__ tsum, KmapStatus* st) {
+  const bool second = st->plan[kMaxPasses] & 1;
+  const unsigned long long* mk = second ? mk1 : mk0;
+  const int32_t* ix = second ? ix1 : ix0;
+  const int64_t base = blockIdx.x * int64_t(kDsTile);
+  uint32_t heads = 0;
+  for (int r = 0; r < kSortItems; ++r) {
+    const int64_t s = base + r * kSortThreads + threadIdx.x;
+    if (s >= N) break;
+    const int32_t row = ix[s];
+    if (static_cast<uint64_t>(row) >= static_cast<uint64_t>(N)) atomicOr(&st->flags, kFlagInternal);
+    if (parent_starts(mk, s)) ++heads;
+    if (s > 0 && mk[s - 1] == mk[s]) {
+      atomicOr(&st->flags, kFlagDup);
+      atomicMin(&st->bad_row, static_cast<long long>(row));
+    }
+  }
+  __shared__ uint32_t tmp[8];
+  uint32_t total;
+  block_exclusive_scan256(heads, tmp, &total);
+  if (threadIdx.x == 0) tsum[blockIdx.x] = total;
+}
+
+// One block: exclusive scan of the per-tile counts; tsum[ntile] and nblocks get M.
+__global__ void __launch_bounds__(256) ds_scan(uint32_t* __restrict__ tsum, int64_t ntile,
+                                               KmapStatus* st) {
+  __shared__ uint32_t tmp[8];
+  uint32_t carry = 0;
+  for (int64_t b0 = 0; b0 < ntile; b0 += 256) {
+    const int64_t b = b0 + threadIdx.x;
+    const uint32_t x = b < ntile ? tsum[b] : 0u;
+    uint32_t sum;
+    const uint32_t pre = block_exclusive_scan256(x, tmp, &sum);
+    if (b < ntile) tsum[b] = carry + pre;
+    carry += sum;
+  }
+  if (threadIdx.x == 0) {
+    tsum[ntile] = carry;
+    st->nblocks = carry;
+  }
+}
+
+// Each thread takes 8 consecutive sorted positions of its tile: the parent index of a
+// position is the number of parent starts before it (tile offset + block scan + own
+// run). Writes parent[row] for every fine row and, at each start, the parent's
+// coordinates, its first sorted position and its child mask (the run is at most the
+// 8 cells of a 2x2x2 block when there are no duplicates; the loop never looks further).
+__global__ void __launch_bounds__(kSortThreads) ds_emit(
+    const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
+    const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
+    const int32_t* __restrict__ ix1, int64_t N, const uint32_t* __restrict__ tsum,
+    int4* __restrict__ coarse, int32_t* __restrict__ parent, uint8_t* __restrict__ cmask,
+    int32_t* __restrict__ pstart, const KmapStatus* st) {
+  if (st->flags & kFlagInternal) return;
+  const bool second = st->plan[kMaxPasses] & 1;
+  const unsigned long long* mk = second ? mk1 : mk0;
+  const int32_t* ix = second ? ix1 : ix0;
+  const int64_t s0 = blockIdx.x * int64_t(kDsTile) + threadIdx.x * int64_t(kSortItems);
+  uint32_t h = 0;
+  for (int j = 0; j < kSortItems; ++j) {
+    const int64_t s = s0 + j;
+    if (s < N && parent_starts(mk, s)) ++h;
+  }
+  __shared__ uint32_t tmp[8];
+  uint32_t total;
+  const uint32_t pre = block_exclusive_scan256(h, tmp, &total);
+  int64_t p = int64_t(tsum[blockIdx.x]) + pre - 1;   // parent of the position before s0
+  for (int j = 0; j < kSortItems; ++j) {
+    const int64_t s = s0 + j;
+    if (s >= N) break;
+    const bool head = parent_starts(mk, s);
+    if (head) ++p;
+    const int32_t row = ix[s];
+    parent[row] = static_cast<int32_t>(p);
+    if (head) {
+      const int4 c = coords[row];   // (b, z, y, x)
+      coarse[p] = make_int4(c.x, c.y >> 1, c.z >> 1, c.w >> 1);
+      pstart[p] = static_cast<int32_t>(s);
+      const unsigned long long key = mk[s] >> 3;
+      uint32_t mask = 0;
+      for (int t = 0; t < 8 && s + t < N; ++t) {
+        if ((mk[s + t] >> 3) != key) break;
+        const int4 d = coords[ix[s + t]];
+        mask |= 1u << (((d.y & 1) << 2) | ((d.z & 1) << 1) | (d.w & 1));
+      }
+      cmask[p] = static_cast<uint8_t>(mask);
+    }
+    if (s == N - 1) pstart[p + 1] = static_cast<int32_t>(N);
+  }
+}
+
+template <typename T, int V>
+struct Vec;
+template <>
+struct Vec<float, 1> {
+  static __device__ __forceinline__ void load(const float* p, float (&v)[1]) { v[0] = __ldg(p); }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[1]) { *p = v[0]; }
+};
+template <>
+struct Vec<float, 4> {
+  static __device__ __forceinline__ void load(const float* p, float (&v)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 1> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[1]) {
+    v[0] = __bfloat162float(__ldg(p));
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[1]) {
+    *p = __float2bfloat16_rn(v[0]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      v[2 * e] = f.x;
+      v[2 * e + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Pools each parent's children: a thread per (parent, V consecutive channels), fp32
+// accumulation, mean = sum / count, rounded once to the feature dtype.
+template <typename T, int V>
+__global__ void __launch_bounds__(256) ds_pool(const T* __restrict__ feats, int C,
+                                               const int32_t* __restrict__ ix,
+                                               const int32_t* __restrict__ pstart, int64_t M,
+                                               int mode, T* __restrict__ out) {
+  const int cv = C / V;
+  const int64_t total = M * cv;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
+    const int64_t p = e / cv;
+    const int c0 = static_cast<int>(e - p * cv) * V;
+    const int32_t a = pstart[p], b = pstart[p + 1];
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = mode == SUBM3D_POOL_MAX ? -INFINITY : 0.f;
+    for (int32_t s = a; s < b; ++s) {
+      float v[V];
+      Vec<T, V>::load(feats + int64_t(ix[s]) * C + c0, v);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] = mode == SUBM3D_POOL_MAX ? fmaxf(acc[k], v[k]) : acc[k] + v[k];
+    }
+    if (mode == SUBM3D_POOL_MEAN) {
+      const float n = static_cast<float>(b - a);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] = acc[k] / n;
+    }
+    Vec<T, V>::store(out + p * C + c0, acc);
+  }
+}
+
+// fine[i, :] = coarse[parent[i], :]; a parent outside [0, M) gives a zero row and sets
+// the device error word.
+template <typename T, int V>
+__global__ void __launch_bounds__(256) us_gather(const T* __restrict__ coarse, int64_t M, int C,
+                                                 const int32_t* __restrict__ parent, int64_t N,
+                                                 T* __restrict__ fine, int* err) {
+  const int cv = C / V;
+  const int64_t total = N * cv;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
+    const int64_t i = e / cv;
+    const int c0 = static_cast<int>(e - i * cv) * V;
+    const int32_t p = parent[i];
+    float v[V];
+    if (p >= 0 && p < M) {
+      Vec<T, V>::load(coarse + int64_t(p) * C + c0, v);
+    } else {
+      if (c0 == 0) atomicOr(err, kDevErrBadParent);
+#pragma unroll
+      for (int k = 0; k < V; ++k) v[k] = 0.f;
+    }
+    Vec<T, V>::store(fine + i * C + c0, v);
+  }
+}
+
 }  // namespace
 
 int64_t default_hash_capacity(int64_t N) {
@@ -634,43 +908,19 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
               (long long)N);
     return SUBM3D_ERR_WORKSPACE;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(kmap_sort_scatter,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScatterSmem));
-    attr_set = true;
-  }
   char* ws = static_cast<char*>(workspace);
   KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
   unsigned long long* mk1 = reinterpret_cast<unsigned long long*>(ws + L.mk1);
   int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
   int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   Slot* table = reinterpret_cast<Slot*>(ws + L.table);
   int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
 
-  int bits = 2;   // at least one whole 4x4x4 block level below the batch bits
-  while ((1 << bits) < res) ++bits;
-  const int npass = (3 * bits + 16 + 7) / 8;
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-
-  kmap_init<<<8, 256, 0, stream>>>(st, hist);
-  SUBM3D_LAUNCHED("kmap_init");
-  kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, mk0, ix0, st);
-  SUBM3D_LAUNCHED("kmap_pack");
-  kmap_plan<<<1, 1, 0, stream>>>(npass, st);
-  SUBM3D_LAUNCHED("kmap_plan");
-  const int nblk = static_cast<int>(L.nblk);
-  for (int p = 0; p < npass; ++p) {
-    kmap_sort_count<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, N, p, L.nblk, cnt, hist, st);
-    SUBM3D_LAUNCHED("kmap_sort_count");
-    kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, L.nblk, cnt, st);
-    SUBM3D_LAUNCHED("kmap_sort_scan");
-    kmap_sort_scatter<<<nblk, kSortThreads, kScatterSmem, stream>>>(mk0, mk1, ix0, ix1, N, p,
-                                                                    L.nblk, cnt, st);
-    SUBM3D_LAUNCHED("kmap_sort_scatter");
+  {
+    const int rc = launch_sort(c4, N, res, L, ws, stream);
+    if (rc != SUBM3D_OK) return rc;
   }
   kmap_blocks_count<<<grid_for(N, 256, 8), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
   SUBM3D_LAUNCHED("kmap_blocks_count");
@@ -708,6 +958,181 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
     return SUBM3D_ERR_HASH_FULL;
   }
   return SUBM3D_OK;
+}
+
+size_t downsample_workspace_bytes(int64_t N) {
+  if (N < 0 || N > 0x7FFFFFFFll) return 0;
+  return make_ds_layout(N).total;
+}
+
+namespace {
+template <typename T>
+int launch_pool(const void* feats, int C, const int32_t* ix, const int32_t* pstart, int64_t M,
+                int mode, void* out, cudaStream_t stream) {
+  constexpr int V = 16 / sizeof(T);
+  const T* f = static_cast<const T*>(feats);
+  T* o = static_cast<T*>(out);
+  if (C % V == 0) {
+    ds_pool<T, V><<<grid_for(M * (C / V), 256, 8), 256, 0, stream>>>(f, C, ix, pstart, M, mode, o);
+  } else {
+    ds_pool<T, 1><<<grid_for(M * C, 256, 8), 256, 0, stream>>>(f, C, ix, pstart, M, mode, o);
+  }
+  SUBM3D_LAUNCHED("ds_pool");
+  return SUBM3D_OK;
+}
+template <typename T>
+int launch_unpool(const void* coarse, int64_t M, int C, const int32_t* parent, int64_t N,
+                  void* fine, cudaStream_t stream) {
+  constexpr int V = 16 / sizeof(T);
+  const T* c = static_cast<const T*>(coarse);
+  T* f = static_cast<T*>(fine);
+  if (C % V == 0) {
+    us_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f,
+                                                                        forward_error_word());
+  } else {
+    us_gather<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f,
+                                                                  forward_error_word());
+  }
+  SUBM3D_LAUNCHED("us_gather");
+  return SUBM3D_OK;
+}
+}  // namespace
+
+int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,
+                     subm3d_dtype dtype, int mode, int32_t* coarse_coords, void* coarse_feats,
+                     int32_t* parent, uint8_t* child_mask, int64_t* M_out, void* workspace,
+                     size_t ws_bytes, cudaStream_t stream) {
+  if (!M_out) {
+    set_error("subm3d_downsample: M_out (host) is NULL");
+    return SUBM3D_ERR_ARG;
+  }
+  *M_out = 0;
+  if (N < 0 || N > 0x7FFFFFFFll) {
+    set_error("subm3d_downsample: N=%lld outside [0, 2^31)", (long long)N);
+    return SUBM3D_ERR_ARG;
+  }
+  if (res < 1 || res > SUBM3D_MAX_RES) {
+    set_error("subm3d_downsample: res=%d outside [1, %d]", res, SUBM3D_MAX_RES);
+    return SUBM3D_ERR_ARG;
+  }
+  if (mode != SUBM3D_POOL_MEAN && mode != SUBM3D_POOL_MAX) {
+    set_error("subm3d_downsample: unknown pooling mode %d", mode);
+    return SUBM3D_ERR_ARG;
+  }
+  if (feats && (C < 1 || C > 4096 || (dtype != SUBM3D_F32 && dtype != SUBM3D_BF16))) {
+    set_error("subm3d_downsample: C=%d must lie in [1, 4096] and dtype %d be F32 or BF16", C,
+              static_cast<int>(dtype));
+    return SUBM3D_ERR_ARG;
+  }
+  if (N == 0) return SUBM3D_OK;
+  if (!coords || !coarse_coords || !parent || !child_mask || !workspace || (feats && !coarse_feats)) {
+    set_error("subm3d_downsample: NULL pointer (coords=%p coarse_coords=%p parent=%p "
+              "child_mask=%p workspace=%p feats=%p coarse_feats=%p)",
+              (const void*)coords, (void*)coarse_coords, (void*)parent, (void*)child_mask,
+              workspace, feats, coarse_feats);
+    return SUBM3D_ERR_ARG;
+  }
+  const uintptr_t any = reinterpret_cast<uintptr_t>(coords) |
+                        reinterpret_cast<uintptr_t>(coarse_coords) |
+                        reinterpret_cast<uintptr_t>(parent) | reinterpret_cast<uintptr_t>(feats) |
+                        reinterpret_cast<uintptr_t>(coarse_feats);
+  if (any & 15) {
+    set_error("subm3d_downsample: coords, coarse_coords, parent, feats and coarse_feats must be "
+              "16-byte aligned");
+    return SUBM3D_ERR_ARG;
+  }
+  const DsLayout D = make_ds_layout(N);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) {
+    set_error("subm3d_downsample: workspace=%p must be 256-byte aligned", workspace);
+    return SUBM3D_ERR_WORKSPACE;
+  }
+  if (ws_bytes < D.total) {
+    set_error("subm3d_downsample: workspace of %zu bytes, need %zu for N=%lld", ws_bytes, D.total,
+              (long long)N);
+    return SUBM3D_ERR_WORKSPACE;
+  }
+  char* ws = static_cast<char*>(workspace);
+  const Layout& L = D.k;
+  KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
+  unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
+  unsigned long long* mk1 = reinterpret_cast<unsigned long long*>(ws + L.mk1);
+  int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
+  int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
+  uint32_t* tsum = reinterpret_cast<uint32_t*>(ws + D.tsum);
+  int32_t* pstart = reinterpret_cast<int32_t*>(ws + D.pstart);
+  const int4* c4 = reinterpret_cast<const int4*>(coords);
+  {
+    const int rc = launch_sort(c4, N, res, L, ws, stream);
+    if (rc != SUBM3D_OK) return rc;
+  }
+  const int ntile = static_cast<int>(D.ntile);
+  ds_count<<<ntile, kSortThreads, 0, stream>>>(mk0, mk1, ix0, ix1, N, tsum, st);
+  SUBM3D_LAUNCHED("ds_count");
+  ds_scan<<<1, 256, 0, stream>>>(tsum, D.ntile, st);
+  SUBM3D_LAUNCHED("ds_scan");
+  ds_emit<<<ntile, kSortThreads, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, tsum,
+                                              reinterpret_cast<int4*>(coarse_coords), parent,
+                                              child_mask, pstart, st);
+  SUBM3D_LAUNCHED("ds_emit");
+
+  KmapStatus host;
+  SUBM3D_CUDA_TRY(cudaMemcpyAsync(&host, st, sizeof(host), cudaMemcpyDeviceToHost, stream));
+  SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
+  if (host.flags & kFlagCoord) {
+    set_error("subm3d_downsample: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d",
+              host.bad_row, SUBM3D_MAX_BATCH, res);
+    return SUBM3D_ERR_COORD_RANGE;
+  }
+  if (host.flags & kFlagInternal) {
+    set_error("subm3d_downsample: internal error (the sort produced an index outside [0, N))");
+    return SUBM3D_ERR_DEVICE;
+  }
+  if (host.flags & kFlagDup) {
+    set_error("subm3d_downsample: duplicate coordinate (row %lld repeats an earlier row)",
+              host.bad_row);
+    return SUBM3D_ERR_DUPLICATE;
+  }
+  const int64_t M = static_cast<int64_t>(host.nblocks);
+  if (M < 1 || M > N) {
+    set_error("subm3d_downsample: internal error (%lld parents for %lld voxels)", (long long)M,
+              (long long)N);
+    return SUBM3D_ERR_DEVICE;
+  }
+  *M_out = M;
+  if (!feats) return SUBM3D_OK;
+  const int32_t* ix = (host.plan[kMaxPasses] & 1) ? ix1 : ix0;
+  return dtype == SUBM3D_BF16
+             ? launch_pool<__nv_bfloat16>(feats, C, ix, pstart, M, mode, coarse_feats, stream)
+             : launch_pool<float>(feats, C, ix, pstart, M, mode, coarse_feats, stream);
+}
+
+int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
+                    int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream) {
+  if (N < 0 || N > 0x7FFFFFFFll || M < 0 || M > 0x7FFFFFFFll) {
+    set_error("subm3d_upsample: N=%lld, M=%lld outside [0, 2^31)", (long long)N, (long long)M);
+    return SUBM3D_ERR_ARG;
+  }
+  if (C < 1 || C > 4096 || (dtype != SUBM3D_F32 && dtype != SUBM3D_BF16)) {
+    set_error("subm3d_upsample: C=%d must lie in [1, 4096] and dtype %d be F32 or BF16", C,
+              static_cast<int>(dtype));
+    return SUBM3D_ERR_ARG;
+  }
+  if (N == 0) return SUBM3D_OK;
+  if (!parent || !fine_feats || (M > 0 && !coarse_feats)) {
+    set_error("subm3d_upsample: NULL pointer (coarse_feats=%p parent=%p fine_feats=%p)",
+              coarse_feats, (const void*)parent, fine_feats);
+    return SUBM3D_ERR_ARG;
+  }
+  const uintptr_t any = reinterpret_cast<uintptr_t>(coarse_feats) |
+                        reinterpret_cast<uintptr_t>(parent) | reinterpret_cast<uintptr_t>(fine_feats);
+  if (any & 15) {
+    set_error("subm3d_upsample: coarse_feats=%p parent=%p fine_feats=%p must be 16-byte aligned",
+              coarse_feats, (const void*)parent, fine_feats);
+    return SUBM3D_ERR_ARG;
+  }
+  return dtype == SUBM3D_BF16
+             ? launch_unpool<__nv_bfloat16>(coarse_feats, M, C, parent, N, fine_feats, stream)
+             : launch_unpool<float>(coarse_feats, M, C, parent, N, fine_feats, stream);
 }
 
 }  // namespace subm3d

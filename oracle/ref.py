@@ -34,7 +34,8 @@ import numpy as np
 
 __all__ = ["OFFSETS", "CENTER", "ACTIVATIONS", "POOL_MODES", "OracleError", "tap",
            "coordinate_dict", "kernel_map", "subm_conv3d", "subm_conv3d_rows", "activation",
-           "block_epilogue", "morton_code", "child_bit", "downsample", "upsample"]
+           "block_epilogue", "morton_code", "child_bit", "downsample", "upsample",
+           "spatial2channel", "channel2spatial"]
 
 # k -> (dz, dy, dx), k = 9 (dz + 1) + 3 (dy + 1) + (dx + 1)
 OFFSETS = [(dz, dy, dx) for dz in (-1, 0, 1) for dy in (-1, 0, 1) for dx in (-1, 0, 1)]
@@ -242,3 +243,40 @@ def upsample(coarse_feats, parent):
     if parent.size and (parent.min() < 0 or parent.max() >= c.shape[0]):
         raise OracleError("parent index outside the coarse rows")
     return c[parent]
+
+
+def spatial2channel(coords, feats, res):
+    """SparseSpatial2Channel(2), the sparse pixel-unshuffle the "pixal3d_mrp_mlx README"
+    scope table lists beside the down/upsample (cache-backed, paired with the same
+    subdivision). Reading: each parent cell's row holds its eight children's feature
+    rows side by side in child_bit order, zeros where a child is absent:
+
+        out[p, k*C:(k+1)*C] = feats[i] if fine row i is child k of parent p, else 0.
+
+    Returns (coarse_coords [M, 4], out float64 [M, 8C], parent [N], child_mask [M]) with
+    the coarse set, order and subdivision of downsample()."""
+    coarse, _, parent, mask = downsample(coords, None, res)
+    f = np.asarray(feats, dtype=np.float64)
+    C = f.shape[1]
+    out = np.zeros((coarse.shape[0], 8 * C), dtype=np.float64)
+    for i, (b, z, y, x) in enumerate(np.asarray(coords).tolist()):
+        k = child_bit(z, y, x)
+        out[parent[i], k * C:(k + 1) * C] = f[i]
+    return coarse, out, parent, mask
+
+
+def channel2spatial(coarse_feats, coords, parent):
+    """The inverse of spatial2channel on the stored subdivision: fine row i takes the
+    C-wide slice of its parent's row at its child_bit, float64 [N, C]."""
+    c = np.asarray(coarse_feats, dtype=np.float64)
+    if c.shape[1] % 8:
+        raise OracleError("coarse rows must hold 8 x C channels")
+    C = c.shape[1] // 8
+    parent = np.asarray(parent)
+    if parent.size and (parent.min() < 0 or parent.max() >= c.shape[0]):
+        raise OracleError("parent index outside the coarse rows")
+    out = np.empty((parent.shape[0], C), dtype=np.float64)
+    for i, (b, z, y, x) in enumerate(np.asarray(coords).tolist()):
+        k = child_bit(z, y, x)
+        out[i] = c[parent[i], k * C:(k + 1) * C]
+    return out

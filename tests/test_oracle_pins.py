@@ -480,3 +480,60 @@ def test_planted_morton_axis_swap_is_caught(monkeypatch):
     c = random_set(np.random.default_rng(12), 32, 1, 300)
     coarse = ref.downsample(c, None, 32)[0].tolist()
     assert not all(_morton_less(p[1:], q[1:]) for p, q in zip(coarse, coarse[1:]))
+
+
+# ------------------------------------------- SparseSpatial2Channel(2) / channel2spatial
+
+def dense_unshuffle(coords, feats, res, coarse):
+    """3-D pixel-unshuffle of the densified grid by reshape and permute: channel block k
+    of a cell holds the child at (dz, dy, dx) with k = 4 dz + 2 dy + dx; read at the
+    coarse cells."""
+    coords = np.asarray(coords)
+    B = int(coords[:, 0].max()) + 1
+    C = feats.shape[1]
+    R = res + (res & 1)
+    g = torch.zeros(B, C, R, R, R, dtype=torch.float64)
+    b, z, y, x = (torch.from_numpy(coords[:, k].astype(np.int64)) for k in range(4))
+    g[b, :, z, y, x] = torch.from_numpy(np.asarray(feats, np.float64))
+    h = R // 2
+    g = g.view(B, C, h, 2, h, 2, h, 2).permute(0, 3, 5, 7, 1, 2, 4, 6).reshape(B, 8 * C, h, h, h)
+    cb, cz, cy, cx = (torch.from_numpy(coarse[:, k].astype(np.int64)) for k in range(4))
+    return g[cb, :, cz, cy, cx].numpy()
+
+
+@pytest.mark.parametrize("seed,res,batch,n,C", [(0, 6, 2, 100, 3), (1, 9, 1, 400, 2),
+                                                 (2, 2, 1, 8, 4), (3, 5, 3, 1, 1)])
+def test_spatial2channel_matches_dense_unshuffle(seed, res, batch, n, C):
+    rng = np.random.default_rng(seed)
+    c = random_set(rng, res, batch, n)
+    f = rng.standard_normal((c.shape[0], C))
+    coarse, out, parent, mask = ref.spatial2channel(c, f, res)
+    np.testing.assert_array_equal(out, dense_unshuffle(c, f, res, coarse))
+    ds = ref.downsample(c, None, res)
+    np.testing.assert_array_equal(coarse, ds[0])
+    np.testing.assert_array_equal(parent, ds[2])
+    # absent children are zero blocks, present ones are not (random features)
+    for p, m in enumerate(mask):
+        for k in range(8):
+            blk = out[p, k * C:(k + 1) * C]
+            assert (np.abs(blk).sum() > 0) == bool(m >> k & 1)
+    # channel2spatial undoes it exactly
+    np.testing.assert_array_equal(ref.channel2spatial(out, c, parent), f)
+
+
+def test_channel2spatial_errors_and_planted_bit_order(monkeypatch):
+    c = np.array([[0, 0, 0, 1], [0, 1, 0, 0]], np.int32)
+    f = np.array([[1.0], [2.0]])
+    coarse, out, parent, _ = ref.spatial2channel(c, f, 4)
+    np.testing.assert_array_equal(out, [[0, 1, 0, 0, 2, 0, 0, 0]])   # x -> block 1, z -> block 4
+    with pytest.raises(ref.OracleError):
+        ref.channel2spatial(out[:, :7], c, parent)
+    with pytest.raises(ref.OracleError):
+        ref.channel2spatial(out, c, np.array([0, 1]))
+    # planting x as the high bit of the child index must break the dense pin
+    monkeypatch.setattr(ref, "child_bit", lambda z, y, x: ((x & 1) << 2) | ((y & 1) << 1) | (z & 1))
+    rng = np.random.default_rng(3)
+    cs = random_set(rng, 6, 1, 80)
+    fs = rng.standard_normal((80, 2))
+    co, o2, _, _ = ref.spatial2channel(cs, fs, 6)
+    assert not np.array_equal(o2, dense_unshuffle(cs, fs, 6, co))

@@ -10,6 +10,7 @@ subm3d_forward (tcgen05 gather-GEMM with fused bias). Default workload: the
     python bench.py --impl reference ...      # the CPU oracle, as the reference arm
     python bench.py --residual --act relu     # forward with the fused block epilogue
     python bench.py --op downsample|upsample  # SparseDownsample(2) / SparseUpsample(2)
+    python bench.py --op spatial2channel|channel2spatial   # sparse pixel-(un)shuffle
 
 Prints one JSON line (rank 0). `value` = effective TFLOP/s of the whole step,
 2 * pairs * I * O / step time, summed over ranks (replicas: every rank runs the
@@ -59,9 +60,11 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", default="conv", choices=["conv", "downsample", "upsample"],
-                   help="conv: kmap + forward (the default step); downsample / upsample: "
-                        "SparseDownsample(2) / its paired SparseUpsample(2) on the workload")
+    p.add_argument("--op", default="conv",
+                   choices=["conv", "downsample", "upsample", "spatial2channel", "channel2spatial"],
+                   help="conv: kmap + forward (the default step); the others: SparseDownsample(2), "
+                        "its paired SparseUpsample(2), SparseSpatial2Channel(2) and its inverse on "
+                        "the workload's voxels and features")
     p.add_argument("--pool", default="mean", choices=["mean", "max"],
                    help="pooling of --op downsample (and of the coarse rows --op upsample uses)")
     p.add_argument("--residual", action="store_true",
@@ -512,16 +515,20 @@ def run_ours(args, world, rank, local):
 
 def run_resample(args, world, rank, local):
     """SparseDownsample(2) (`--op downsample`: the Morton sort, the parent scan and the
-    pooling, with its one host sync) or the cache-paired SparseUpsample(2) (`--op
-    upsample`: one gather kernel) on the workload's voxels and features. Metric: fine
-    voxels per second. Roofline bytes: downsample 16 N (coords) + N C e (feats) + 4 N
-    (parent) + M (16 + 1 + C e) (coarse coords, masks, pooled rows); upsample 4 N + M C e
-    + N C e."""
+    pooling, with its one host sync), the cache-paired SparseUpsample(2) (`--op
+    upsample`: one gather kernel), SparseSpatial2Channel(2) (`--op spatial2channel`: zero
+    fill of absent blocks + scatter) or its inverse (`--op channel2spatial`: one gather)
+    on the workload's voxels and features. Metric: fine voxels per second. Roofline
+    bytes: downsample 16 N (coords) + N C e (feats) + 4 N (parent) + M (16 + 1 + C e)
+    (coarse coords, masks, pooled rows); upsample 4 N + M C e + N C e; spatial2channel
+    N C e + 20 N + M + 8 M C e; channel2spatial 2 N C e + 20 N."""
     import numpy as np
     import torch
-    from submanifold_sparse_convolution_04_b300 import (lib, subm3d_downsample,
+    from submanifold_sparse_convolution_04_b300 import (lib, subm3d_channel2spatial,
+                                                        subm3d_downsample,
                                                         subm3d_forward_status,
-                                                        subm3d_kernel_launches, subm3d_upsample)
+                                                        subm3d_kernel_launches,
+                                                        subm3d_spatial2channel, subm3d_upsample)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
     dev = torch.device("cuda", local)
@@ -543,11 +550,24 @@ def run_resample(args, world, rank, local):
             subm3d_downsample(c, res, f, args.pool, workspace=ws)
         nbytes = 16 * N + N * C * e + 4 * N + M * (16 + 1 + C * e)
         kernel = "downsample: sort + ds_count/ds_scan/ds_emit + ds_pool"
-    else:
+    elif args.op == "upsample":
         def step():
             subm3d_upsample(cf, parent, out=up)
         nbytes = 4 * N + M * C * e + N * C * e
         kernel = "us_gather"
+    else:
+        s2c = torch.empty((M, 8 * C), dtype=f.dtype, device=dev)
+        subm3d_spatial2channel(f, c, parent, mask, out=s2c)
+        if args.op == "spatial2channel":
+            def step():
+                subm3d_spatial2channel(f, c, parent, mask, out=s2c)
+            nbytes = N * C * e + 20 * N + M + 8 * M * C * e
+            kernel = "s2c_zero + s2c_scatter"
+        else:
+            def step():
+                subm3d_channel2spatial(s2c, c, parent, out=up)
+            nbytes = 2 * N * C * e + 20 * N
+            kernel = "c2s_gather"
     stream = torch.cuda.current_stream()
     for _ in range(max(args.warmup, 3)):
         step()
@@ -607,11 +627,19 @@ def run_resample(args, world, rank, local):
         t1 = time.perf_counter()
         if args.op == "upsample":
             ref.upsample(cfs, par)
-        dt = (time.perf_counter() - t1) if args.op == "upsample" else (t1 - t0)
+        elif args.op in ("spatial2channel", "channel2spatial"):
+            _, s2cs, par, _ = ref.spatial2channel(sub, fs, res)
+            t2 = time.perf_counter()
+            if args.op == "channel2spatial":
+                ref.channel2spatial(s2cs, sub, par)
+                t1 = t2
+        dt = (t1 - t0) if args.op == "downsample" else (time.perf_counter() - t1)
         line["cpu_baseline"] = {"value": S / dt / 1e6, "unit": "Mvoxels/s", "cores": 1,
                                 "kind": "oracle", "seconds": dt,
                                 "sample": f"Python oracle ({args.op}) on the first {S} voxels in "
-                                          f"raster order, single thread"}
+                                          f"raster order, single thread"
+                                          + ("; includes the oracle's own subdivision"
+                                             if args.op == "spatial2channel" else "")}
     print(json.dumps(line), flush=True)
 
 

@@ -277,6 +277,38 @@ SUBM3D_API int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C,
                                void* fine_feats, cudaStream_t stream);
 
 /*
+ * SparseSpatial2Channel(2), the sparse pixel-unshuffle paired with the same subdivision
+ * (listed beside the down/upsample in the "pixal3d_mrp_mlx README" scope table; no
+ * layout is given there). Reading: a parent's row holds its eight children's rows side by
+ * side in child-bit order, zeros where a child is absent:
+ *
+ *   out[p, k*C .. k*C + C) = feats[i]  for the fine row i that is child k of p,
+ *                            0         for k not in child_mask[p],
+ *   k = (z&1)<<2 | (y&1)<<1 | (x&1) of coords[i].
+ *
+ *   feats       device [N, C] of `dtype`; coords device int32 [N, 4] (b, z, y, x), the
+ *               fine voxels; parent device int32 [N] and child_mask device uint8 [M] from
+ *               subm3d_downsample on the same coords.
+ *   out         device [M, 8 C] of `dtype`.
+ * A parent entry outside [0, M) is skipped and reported by subm3d_forward_status. All
+ * pointers but child_mask 16-byte aligned. Fully asynchronous.
+ */
+SUBM3D_API int subm3d_spatial2channel(const void* feats, const int32_t* coords,
+                                      const int32_t* parent, const uint8_t* child_mask, int64_t N,
+                                      int64_t M, int32_t C, subm3d_dtype dtype, void* out,
+                                      cudaStream_t stream);
+
+/*
+ * The inverse on the stored subdivision (channel2spatial):
+ *   fine_feats[i, :] = coarse_feats[parent[i], k*C .. k*C + C),  k the child bit of coords[i].
+ * coarse_feats device [M, 8 C]; fine_feats device [N, C]; a parent outside [0, M) gives a
+ * zero row and is reported by subm3d_forward_status. 16-byte aligned; asynchronous.
+ */
+SUBM3D_API int subm3d_channel2spatial(const void* coarse_feats, const int32_t* coords,
+                                      const int32_t* parent, int64_t N, int64_t M, int32_t C,
+                                      subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
+
+/*
  * Waits for `stream`, then reads and clears the device error word of the forward and
  * upsample kernels: SUBM3D_OK, or SUBM3D_ERR_DEVICE (message says which condition: an
  * nbr entry outside [-1, N), a bounded pipeline wait that ran out, or a parent entry

@@ -12,16 +12,18 @@ coords int32 [N, 4] (b, z, y, x); feats [N, I] bf16 or fp32 (channels-last);
 weight [O, 3, 3, 3, I] ([O, kz, ky, kx, I]); bias [O] or None. subm3d_forward_ex fuses a
 residual add and an activation (none, relu, silu) into the same kernel; one nbr serves
 every convolution at its resolution. subm3d_downsample / subm3d_upsample are
-SparseDownsample(2) (mean or max pooling) and its cache-paired SparseUpsample(2).
+SparseDownsample(2) (mean or max pooling) and its cache-paired SparseUpsample(2);
+subm3d_spatial2channel / subm3d_channel2spatial the sparse pixel-unshuffle and its
+inverse on the same subdivision.
 """
 from ._binding import (ACTIVATIONS, BF16, F32, LIB_PATH, POOL_MODES, Subm3dError, lib,
                        subm3d_build_kmap, subm3d_build_kmap_ex, subm3d_build_kmap_noalloc,
                        subm3d_downsample, subm3d_forward, subm3d_forward_ex, subm3d_forward_status,
                        subm3d_kernel_launches, subm3d_kmap_workspace_bytes, subm3d_last_error,
-                       subm3d_upsample)
+                       subm3d_upsample, subm3d_spatial2channel, subm3d_channel2spatial)
 
 __all__ = ["ACTIVATIONS", "BF16", "F32", "LIB_PATH", "POOL_MODES", "Subm3dError", "lib",
            "subm3d_build_kmap", "subm3d_build_kmap_ex", "subm3d_build_kmap_noalloc",
            "subm3d_downsample", "subm3d_forward", "subm3d_forward_ex", "subm3d_forward_status",
            "subm3d_kernel_launches", "subm3d_kmap_workspace_bytes", "subm3d_last_error",
-           "subm3d_upsample"]
+           "subm3d_upsample", "subm3d_spatial2channel", "subm3d_channel2spatial"]

@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
         L.subm3d_downsample.restype = ctypes.c_int
         L.subm3d_upsample.argtypes = [vp, i64, i32, vp, i64, ctypes.c_int, vp, vp]
         L.subm3d_upsample.restype = ctypes.c_int
+        L.subm3d_spatial2channel.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_int, vp, vp]
+        L.subm3d_spatial2channel.restype = ctypes.c_int
+        L.subm3d_channel2spatial.argtypes = [vp, vp, vp, i64, i64, i32, ctypes.c_int, vp, vp]
+        L.subm3d_channel2spatial.restype = ctypes.c_int
         L.subm3d_forward_status.argtypes = [vp]
         L.subm3d_forward_status.restype = ctypes.c_int
         L.subm3d_last_error.argtypes = []
@@ -259,6 +263,50 @@ def subm3d_upsample(coarse_feats: torch.Tensor, parent: torch.Tensor,
     po = _dev(out, "out", coarse_feats.dtype, (N, C))
     _check(lib().subm3d_upsample(pcf, M, C, pp, N, _DTYPES[coarse_feats.dtype], po,
                                  _stream(stream)))
+    return out
+
+
+def subm3d_spatial2channel(feats: torch.Tensor, coords: torch.Tensor, parent: torch.Tensor,
+                           child_mask: torch.Tensor, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """SparseSpatial2Channel(2): out [M, 8C], the eight children's rows of each parent side
+    by side in child-bit order (zeros for absent children); parent and child_mask from
+    subm3d_downsample on the same coords."""
+    if feats.dtype not in _DTYPES:
+        raise ValueError(f"feats dtype {feats.dtype} is not float32 or bfloat16")
+    N, C = feats.shape
+    M = child_mask.shape[0]
+    pf = _dev(feats, "feats")
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    pp = _dev(parent, "parent", torch.int32, (N,))
+    pm = _dev(child_mask, "child_mask", torch.uint8, (M,))
+    if out is None:
+        out = torch.empty((M, 8 * C), dtype=feats.dtype, device=feats.device)
+    po = _dev(out, "out", feats.dtype, (M, 8 * C))
+    _check(lib().subm3d_spatial2channel(pf, pc, pp, pm, N, M, C, _DTYPES[feats.dtype], po,
+                                        _stream(stream)))
+    return out
+
+
+def subm3d_channel2spatial(coarse_feats: torch.Tensor, coords: torch.Tensor, parent: torch.Tensor,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The inverse: out [N, C] with out[i] = the C-wide block of coarse_feats[parent[i]] at
+    fine voxel i's child bit."""
+    if coarse_feats.dtype not in _DTYPES:
+        raise ValueError(f"coarse_feats dtype {coarse_feats.dtype} is not float32 or bfloat16")
+    M, C8 = coarse_feats.shape
+    if C8 % 8:
+        raise ValueError(f"coarse_feats has {C8} channels, not a multiple of 8")
+    C = C8 // 8
+    N = parent.shape[0]
+    pcf = _dev(coarse_feats, "coarse_feats")
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    pp = _dev(parent, "parent", torch.int32, (N,))
+    if out is None:
+        out = torch.empty((N, C), dtype=coarse_feats.dtype, device=coarse_feats.device)
+    po = _dev(out, "out", coarse_feats.dtype, (N, C))
+    _check(lib().subm3d_channel2spatial(pcf, pc, pp, N, M, C, _DTYPES[coarse_feats.dtype], po,
+                                        _stream(stream)))
     return out
 
 

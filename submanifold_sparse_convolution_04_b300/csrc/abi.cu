@@ -138,6 +138,20 @@ int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C, const int32_
   return upsample_launch(coarse_feats, M, C, parent, N, dtype, fine_feats, stream);
 }
 
+int subm3d_spatial2channel(const void* feats, const int32_t* coords, const int32_t* parent,
+                           const uint8_t* child_mask, int64_t N, int64_t M, int32_t C,
+                           subm3d_dtype dtype, void* out, cudaStream_t stream) {
+  clear_error();
+  return spatial2channel_launch(feats, coords, parent, child_mask, N, M, C, dtype, out, stream);
+}
+
+int subm3d_channel2spatial(const void* coarse_feats, const int32_t* coords, const int32_t* parent,
+                           int64_t N, int64_t M, int32_t C, subm3d_dtype dtype, void* fine_feats,
+                           cudaStream_t stream) {
+  clear_error();
+  return channel2spatial_launch(coarse_feats, coords, parent, N, M, C, dtype, fine_feats, stream);
+}
+
 int subm3d_forward_status(cudaStream_t stream) {
   clear_error();
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));

@@ -89,6 +89,12 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* 
                      size_t ws_bytes, cudaStream_t stream);
 int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
                     int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
+int spatial2channel_launch(const void* feats, const int32_t* coords, const int32_t* parent,
+                           const uint8_t* child_mask, int64_t N, int64_t M, int32_t C,
+                           subm3d_dtype dtype, void* out, cudaStream_t stream);
+int channel2spatial_launch(const void* coarse_feats, const int32_t* coords, const int32_t* parent,
+                           int64_t N, int64_t M, int32_t C, subm3d_dtype dtype, void* fine_feats,
+                           cudaStream_t stream);
 int64_t default_hash_capacity(int64_t N);
 
 // ---------------------------------------------------------------------------- device side

@@ -855,6 +855,78 @@ __global__ void __launch_bounds__(256) us_gather(const T* __restrict__ coarse, i
   }
 }
 
+// SparseSpatial2Channel(2): fine row i's C values go to out[parent[i], k C .. k C + C)
+// with k its child bit; s2c_zero fills the blocks of absent children. The two kernels
+// write disjoint bytes.
+__device__ __forceinline__ int child_of(const int4 d) {   // d = (b, z, y, x)
+  return ((d.y & 1) << 2) | ((d.z & 1) << 1) | (d.w & 1);
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(256) s2c_scatter(const T* __restrict__ feats,
+                                                   const int4* __restrict__ coords,
+                                                   const int32_t* __restrict__ parent, int64_t N,
+                                                   int64_t M, int C, T* __restrict__ out, int* err) {
+  const int cv = C / V;
+  const int64_t total = N * cv;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
+    const int64_t i = e / cv;
+    const int c0 = static_cast<int>(e - i * cv) * V;
+    const int32_t p = parent[i];
+    if (p < 0 || p >= M) {
+      if (c0 == 0) atomicOr(err, kDevErrBadParent);
+      continue;
+    }
+    float v[V];
+    Vec<T, V>::load(feats + i * C + c0, v);
+    Vec<T, V>::store(out + (int64_t(p) * 8 + child_of(coords[i])) * C + c0, v);
+  }
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(256) s2c_zero(const uint8_t* __restrict__ mask, int64_t M, int C,
+                                                T* __restrict__ out) {
+  const int cv = C / V;
+  const int64_t total = M * 8 * cv;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
+    const int64_t pk = e / cv;   // parent * 8 + child
+    if ((mask[pk >> 3] >> (pk & 7)) & 1) continue;
+    const int c0 = static_cast<int>(e - pk * cv) * V;
+    float v[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) v[k] = 0.f;
+    Vec<T, V>::store(out + pk * C + c0, v);
+  }
+}
+
+// channel2spatial: fine[i, :] = coarse[parent[i], k C .. k C + C), k = child bit of i; a
+// parent outside [0, M) gives a zero row and sets the device error word.
+template <typename T, int V>
+__global__ void __launch_bounds__(256) c2s_gather(const T* __restrict__ coarse,
+                                                  const int4* __restrict__ coords,
+                                                  const int32_t* __restrict__ parent, int64_t N,
+                                                  int64_t M, int C, T* __restrict__ fine, int* err) {
+  const int cv = C / V;
+  const int64_t total = N * cv;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
+    const int64_t i = e / cv;
+    const int c0 = static_cast<int>(e - i * cv) * V;
+    const int32_t p = parent[i];
+    float v[V];
+    if (p >= 0 && p < M) {
+      Vec<T, V>::load(coarse + (int64_t(p) * 8 + child_of(coords[i])) * C + c0, v);
+    } else {
+      if (c0 == 0) atomicOr(err, kDevErrBadParent);
+#pragma unroll
+      for (int k = 0; k < V; ++k) v[k] = 0.f;
+    }
+    Vec<T, V>::store(fine + i * C + c0, v);
+  }
+}
+
 }  // namespace
 
 int64_t default_hash_capacity(int64_t N) {
@@ -1133,6 +1205,114 @@ int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_
   return dtype == SUBM3D_BF16
              ? launch_unpool<__nv_bfloat16>(coarse_feats, M, C, parent, N, fine_feats, stream)
              : launch_unpool<float>(coarse_feats, M, C, parent, N, fine_feats, stream);
+}
+
+namespace {
+template <typename T>
+int launch_s2c(const void* feats, const int4* coords, const int32_t* parent,
+               const uint8_t* mask, int64_t N, int64_t M, int C, void* out, cudaStream_t stream) {
+  constexpr int V = 16 / sizeof(T);
+  const T* f = static_cast<const T*>(feats);
+  T* o = static_cast<T*>(out);
+  const bool vec = C % V == 0;
+  if (M > 0) {
+    if (vec) {
+      s2c_zero<T, V><<<grid_for(M * 8 * (C / V), 256, 8), 256, 0, stream>>>(mask, M, C, o);
+    } else {
+      s2c_zero<T, 1><<<grid_for(M * 8 * C, 256, 8), 256, 0, stream>>>(mask, M, C, o);
+    }
+    SUBM3D_LAUNCHED("s2c_zero");
+  }
+  if (N > 0) {
+    if (vec) {
+      s2c_scatter<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(
+          f, coords, parent, N, M, C, o, forward_error_word());
+    } else {
+      s2c_scatter<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(f, coords, parent, N, M, C,
+                                                                    o, forward_error_word());
+    }
+    SUBM3D_LAUNCHED("s2c_scatter");
+  }
+  return SUBM3D_OK;
+}
+template <typename T>
+int launch_c2s(const void* coarse, const int4* coords, const int32_t* parent, int64_t N, int64_t M,
+               int C, void* fine, cudaStream_t stream) {
+  constexpr int V = 16 / sizeof(T);
+  const T* c = static_cast<const T*>(coarse);
+  T* f = static_cast<T*>(fine);
+  if (C % V == 0) {
+    c2s_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(
+        c, coords, parent, N, M, C, f, forward_error_word());
+  } else {
+    c2s_gather<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(c, coords, parent, N, M, C, f,
+                                                                 forward_error_word());
+  }
+  SUBM3D_LAUNCHED("c2s_gather");
+  return SUBM3D_OK;
+}
+
+int check_pixel_args(const char* fn, int64_t N, int64_t M, int32_t C, subm3d_dtype dtype) {
+  if (N < 0 || N > 0x7FFFFFFFll || M < 0 || M > 0x7FFFFFFFll) {
+    set_error("%s: N=%lld, M=%lld outside [0, 2^31)", fn, (long long)N, (long long)M);
+    return SUBM3D_ERR_ARG;
+  }
+  if (C < 1 || C > 4096 || (dtype != SUBM3D_F32 && dtype != SUBM3D_BF16)) {
+    set_error("%s: C=%d must lie in [1, 4096] and dtype %d be F32 or BF16", fn, C,
+              static_cast<int>(dtype));
+    return SUBM3D_ERR_ARG;
+  }
+  return SUBM3D_OK;
+}
+}  // namespace
+
+int spatial2channel_launch(const void* feats, const int32_t* coords, const int32_t* parent,
+                           const uint8_t* child_mask, int64_t N, int64_t M, int32_t C,
+                           subm3d_dtype dtype, void* out, cudaStream_t stream) {
+  const int rc = check_pixel_args("subm3d_spatial2channel", N, M, C, dtype);
+  if (rc != SUBM3D_OK) return rc;
+  if ((N > 0 && (!feats || !coords || !parent)) || (M > 0 && (!child_mask || !out))) {
+    set_error("subm3d_spatial2channel: NULL pointer (feats=%p coords=%p parent=%p child_mask=%p "
+              "out=%p)",
+              feats, (const void*)coords, (const void*)parent, (const void*)child_mask, out);
+    return SUBM3D_ERR_ARG;
+  }
+  const uintptr_t any = reinterpret_cast<uintptr_t>(feats) | reinterpret_cast<uintptr_t>(coords) |
+                        reinterpret_cast<uintptr_t>(parent) | reinterpret_cast<uintptr_t>(out);
+  if (any & 15) {
+    set_error("subm3d_spatial2channel: feats, coords, parent and out must be 16-byte aligned");
+    return SUBM3D_ERR_ARG;
+  }
+  const int4* c4 = reinterpret_cast<const int4*>(coords);
+  return dtype == SUBM3D_BF16
+             ? launch_s2c<__nv_bfloat16>(feats, c4, parent, child_mask, N, M, C, out, stream)
+             : launch_s2c<float>(feats, c4, parent, child_mask, N, M, C, out, stream);
+}
+
+int channel2spatial_launch(const void* coarse_feats, const int32_t* coords, const int32_t* parent,
+                           int64_t N, int64_t M, int32_t C, subm3d_dtype dtype, void* fine_feats,
+                           cudaStream_t stream) {
+  const int rc = check_pixel_args("subm3d_channel2spatial", N, M, C, dtype);
+  if (rc != SUBM3D_OK) return rc;
+  if (N == 0) return SUBM3D_OK;
+  if (!coords || !parent || !fine_feats || (M > 0 && !coarse_feats)) {
+    set_error("subm3d_channel2spatial: NULL pointer (coarse_feats=%p coords=%p parent=%p "
+              "fine_feats=%p)",
+              coarse_feats, (const void*)coords, (const void*)parent, fine_feats);
+    return SUBM3D_ERR_ARG;
+  }
+  const uintptr_t any = reinterpret_cast<uintptr_t>(coarse_feats) |
+                        reinterpret_cast<uintptr_t>(coords) | reinterpret_cast<uintptr_t>(parent) |
+                        reinterpret_cast<uintptr_t>(fine_feats);
+  if (any & 15) {
+    set_error("subm3d_channel2spatial: coarse_feats, coords, parent and fine_feats must be "
+              "16-byte aligned");
+    return SUBM3D_ERR_ARG;
+  }
+  const int4* c4 = reinterpret_cast<const int4*>(coords);
+  return dtype == SUBM3D_BF16
+             ? launch_c2s<__nv_bfloat16>(coarse_feats, c4, parent, N, M, C, fine_feats, stream)
+             : launch_c2s<float>(coarse_feats, c4, parent, N, M, C, fine_feats, stream);
 }
 
 }  // namespace subm3d

@@ -1,14 +1,16 @@
-"""SparseDownsample(2) / SparseUpsample(2) on the GPU against the CPU oracle
-(oracle.ref.downsample / upsample): coarse coordinates, parent rows and child masks
-bit-exact; pooled features within the forward's tolerances (fp32 1e-4, bf16 2e-2 of
-max|ref|, bf16 also the tighter 4e-3)."""
+"""SparseDownsample(2) / SparseUpsample(2) and SparseSpatial2Channel(2) /
+channel2spatial on the GPU against the CPU oracle (oracle.ref): coarse coordinates,
+parent rows and child masks bit-exact; pooled features within the forward's tolerances
+(fp32 1e-4, bf16 2e-2 of max|ref|, bf16 also the tighter 4e-3); the pixel-(un)shuffle
+pair moves values without arithmetic, so it is compared bit-exactly."""
 import numpy as np
 import pytest
 import torch
 
 from oracle import ref
-from submanifold_sparse_convolution_04_b300 import (Subm3dError, subm3d_downsample,
-                                                    subm3d_forward_status, subm3d_upsample)
+from submanifold_sparse_convolution_04_b300 import (Subm3dError, subm3d_channel2spatial,
+                                                    subm3d_downsample, subm3d_forward_status,
+                                                    subm3d_spatial2channel, subm3d_upsample)
 from submanifold_sparse_convolution_04_b300 import _binding as B
 from synth import round_to_bf16
 from tests.conftest import cached_case
@@ -171,3 +173,52 @@ def test_downsample_full_workload(dev, mode):
     subm3d_forward_status()
     np.testing.assert_array_equal(up[torch.from_numpy(rows).to(dev)].float().cpu().numpy(),
                                   cf.float().cpu().numpy()[parent[rows]])
+
+
+@pytest.mark.parametrize("dtype,C", [("f32", 3), ("f32", 8), ("bf16", 64), ("bf16", 12)])
+@pytest.mark.parametrize("seed,res,batch,n", [(0, 9, 2, 300), (1, 40, 3, 4000), (2, 1, 2, 1),
+                                               (3, 2, 1, 8)])
+def test_spatial2channel_matches_oracle(dev, dtype, C, seed, res, batch, n):
+    rng = np.random.default_rng(seed * 11 + C)
+    c = random_set(rng, res, batch, n)
+    f = values(rng, c.shape[0], C, dtype)
+    ct = torch.from_numpy(c).to(dev)
+    ft = as_tensor(f, dtype, dev)
+    _, _, parent, mask = subm3d_downsample(ct, res)
+    out = subm3d_spatial2channel(ft, ct, parent, mask)
+    back = subm3d_channel2spatial(out, ct, parent)
+    subm3d_forward_status()
+    want = ref.spatial2channel(c, f, res)
+    np.testing.assert_array_equal(out.float().cpu().numpy(), want[1])
+    np.testing.assert_array_equal(back.float().cpu().numpy(), f)
+
+
+def test_spatial2channel_full_workload_and_bad_parent(dev):
+    """The 1024^3 workload (2.9 M voxels, C = 64): the round trip is exact on every row,
+    sampled parents' rows equal the oracle's on their children, and a bad parent entry is
+    reported."""
+    case = cached_case(5)
+    co = case["coords"]
+    c, f, _, _ = to_device(case, dev)
+    cc, _, parent, mask = subm3d_downsample(c, case["res"])
+    out = subm3d_spatial2channel(f, c, parent, mask)
+    back = subm3d_channel2spatial(out, c, parent)
+    subm3d_forward_status()
+    assert torch.equal(back, f)
+    M = cc.shape[0]
+    p_np = parent.cpu().numpy()
+    rng = np.random.default_rng(9)
+    sample = np.unique(np.concatenate([rng.integers(0, M, 300), [0, M - 1]]))
+    rows = np.nonzero(np.isin(p_np, sample))[0]
+    sub = ref.spatial2channel(co[rows], case["feats"][rows], case["res"])
+    np.testing.assert_array_equal(sub[0], cc.cpu().numpy()[sample])
+    np.testing.assert_array_equal(out[torch.from_numpy(sample).to(dev)].float().cpu().numpy(),
+                                  sub[1])
+    bad = parent.clone()
+    bad[3] = M
+    fine = subm3d_channel2spatial(out, c, bad)
+    with pytest.raises(Subm3dError) as e:
+        subm3d_forward_status()
+    assert e.value.code == B.ERR_DEVICE and "parent" in str(e.value)
+    assert float(fine[3].float().abs().sum()) == 0.0
+    assert torch.equal(fine[4:], f[4:])

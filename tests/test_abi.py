@@ -102,3 +102,93 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         subm3d_forward(torch.zeros((4, 8)), torch.zeros((4, 27), dtype=torch.int32),
                        torch.zeros((8, 3, 3, 3, 8)))
+
+
+def test_forward_ex_argument_errors(L):
+    p = ctypes.c_void_p
+    args = lambda res, act, out: (p(256), p(512), p(768), None, res, act, out, 10, 32, 32, B.BF16, None)
+    assert L.subm3d_forward_ex(*args(None, 7, p(1024))) == B.ERR_ARG          # unknown activation
+    assert b"activation" in L.subm3d_last_error()
+    assert L.subm3d_forward_ex(*args(p(1032), 1, p(4096))) == B.ERR_ARG       # residual misaligned
+    assert L.subm3d_forward_ex(*args(p(4096 + 64), 2, p(4096))) == B.ERR_ARG  # partial overlap
+    assert b"overlaps" in L.subm3d_last_error()
+    assert L.subm3d_forward_ex(p(256), p(512), p(768), None, None, 1, None, 0, 32, 32, B.BF16,
+                               None) == B.OK                                    # N = 0
+
+
+def test_downsample_host_checks(L):
+    p = ctypes.c_void_p
+    M = ctypes.c_int64(-5)
+    ws = L.subm3d_downsample_workspace_bytes
+    assert ws(-1) == 0 and 0 < ws(0) < ws(1000) < ws(3_000_000)
+    # no block table: below the kernel map's workspace at the same N
+    assert ws(3_000_000) < L.subm3d_kmap_workspace_bytes(3_000_000)
+
+    def call(coords=16, N=10, res=16, feats=None, C=0, dtype=B.BF16, mode=0, cc=32, cf=None,
+             parent=48, mask=64, m=M, w=256, nbytes=1 << 30):
+        return L.subm3d_downsample(p(coords) if coords else None, N, res,
+                                   p(feats) if feats else None, C, dtype, mode,
+                                   p(cc) if cc else None, p(cf) if cf else None,
+                                   p(parent) if parent else None, p(mask) if mask else None,
+                                   ctypes.byref(m) if m is not None else None,
+                                   p(w) if w else None, nbytes, None)
+    assert call(m=None) == B.ERR_ARG
+    assert call(N=-1) == B.ERR_ARG and M.value == 0
+    assert call(res=0) == B.ERR_ARG
+    assert call(mode=5) == B.ERR_ARG
+    assert call(feats=80, C=0, cf=96) == B.ERR_ARG
+    assert call(feats=80, C=8, dtype=9, cf=96) == B.ERR_ARG
+    assert call(N=0) == B.OK and M.value == 0
+    assert call(coords=None) == B.ERR_ARG
+    assert call(feats=80, C=8, cf=None) == B.ERR_ARG          # feats without coarse_feats
+    assert call(parent=52) == B.ERR_ARG                       # misaligned
+    assert call(w=128) == B.ERR_WORKSPACE                     # workspace not 256-aligned
+    assert call(nbytes=100) == B.ERR_WORKSPACE
+    assert b"workspace" in L.subm3d_last_error()
+
+
+def test_upsample_and_pixel_shuffle_host_checks(L):
+    p = ctypes.c_void_p
+    assert L.subm3d_upsample(p(16), 4, 8, p(32), -1, B.BF16, p(64), None) == B.ERR_ARG
+    assert L.subm3d_upsample(p(16), 4, 0, p(32), 10, B.BF16, p(64), None) == B.ERR_ARG
+    assert L.subm3d_upsample(p(16), 4, 8, p(32), 10, 7, p(64), None) == B.ERR_ARG
+    assert L.subm3d_upsample(p(16), 4, 8, p(32), 0, B.BF16, p(64), None) == B.OK
+    assert L.subm3d_upsample(p(16), 4, 8, None, 10, B.BF16, p(64), None) == B.ERR_ARG
+    assert L.subm3d_upsample(p(16), 4, 8, p(36), 10, B.BF16, p(64), None) == B.ERR_ARG
+    s2c = L.subm3d_spatial2channel
+    assert s2c(p(16), p(32), p(48), p(60), 10, 4, 0, B.F32, p(64), None) == B.ERR_ARG
+    assert s2c(p(16), p(32), p(48), p(60), 10, -4, 8, B.F32, p(64), None) == B.ERR_ARG
+    assert s2c(None, None, None, None, 0, 0, 8, B.F32, None, None) == B.OK
+    assert s2c(p(16), p(32), p(48), None, 10, 4, 8, B.F32, p(64), None) == B.ERR_ARG
+    assert s2c(p(16), p(32), p(48), p(61), 10, 4, 8, B.F32, p(72), None) == B.ERR_ARG
+    c2s = L.subm3d_channel2spatial
+    assert c2s(p(16), p(32), p(48), 0, 4, 8, B.BF16, p(64), None) == B.OK
+    assert c2s(p(16), p(32), p(48), 10, 4, 4097, B.BF16, p(64), None) == B.ERR_ARG
+    assert c2s(p(16), None, p(48), 10, 4, 8, B.BF16, p(64), None) == B.ERR_ARG
+    assert c2s(p(24), p(32), p(48), 10, 4, 8, B.BF16, p(64), None) == B.ERR_ARG
+
+
+def test_binding_refuses_bad_arguments_without_a_gpu():
+    import torch
+    from submanifold_sparse_convolution_04_b300 import (subm3d_channel2spatial, subm3d_downsample,
+                                                        subm3d_forward_ex, subm3d_spatial2channel,
+                                                        subm3d_upsample)
+    f = torch.zeros((4, 8))
+    nbr = torch.zeros((4, 27), dtype=torch.int32)
+    w = torch.zeros((8, 3, 3, 3, 8))
+    with pytest.raises(ValueError):
+        subm3d_forward_ex(f, nbr, w, act="gelu")
+    with pytest.raises(ValueError):
+        subm3d_forward_ex(f, nbr, w, act="relu")                  # CPU tensors
+    with pytest.raises(ValueError):
+        subm3d_downsample(torch.zeros((4, 4), dtype=torch.int32), 8, mode="sum")
+    with pytest.raises(ValueError):
+        subm3d_downsample(torch.zeros((4, 4), dtype=torch.int32), 8)
+    with pytest.raises(ValueError):
+        subm3d_upsample(f, torch.zeros(4, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        subm3d_channel2spatial(torch.zeros((2, 12)), torch.zeros((4, 4), dtype=torch.int32),
+                               torch.zeros(4, dtype=torch.int32))   # 12 channels: not 8 x C
+    with pytest.raises(ValueError):
+        subm3d_spatial2channel(f, torch.zeros((4, 4), dtype=torch.int32),
+                               torch.zeros(4, dtype=torch.int32), torch.zeros(2, dtype=torch.uint8))

@@ -33,6 +33,11 @@
 // The blocks of a shell hold ~10 voxels each, so the table is about a tenth of a
 // per-voxel table and stays in L2.
 // Hash of a block key: the splitmix64 finaliser (Steele, Lea and Flood, 2014).
+//
+// The structure ops that share steps 1-4 live here too (their section is below the
+// probe): SparseDownsample(2), which numbers the parents of the sorted voxels and pools
+// their features; SparseUpsample(2), its cache-paired inverse; SparseSpatial2Channel(2)
+// and its inverse, the sparse pixel-(un)shuffle on the same subdivision.
 #include "common.cuh"
 
 namespace subm3d {

@@ -627,6 +627,9 @@ int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* w
 }
 
 // SparseDownsample(2) / SparseUpsample(2) ------------------------------------------
+// ("pixal3d_mrp_mlx README", scope table "Scope, measured against the shared core": a
+// downsample with a pooling mode, and the upsample as its cache-paired inverse that
+// reuses the stored subdivision.)
 // The parent of a fine voxel (b, z, y, x) is (b, z>>1, y>>1, x>>1). Its sort key is the
 // fine key >> 3 (the lowest Morton triple is the place inside the 2x2x2 cell), so in the
 // sorted order each parent's children are adjacent and parents come in (batch, Morton)
@@ -860,7 +863,8 @@ __global__ void __launch_bounds__(256) us_gather(const T* __restrict__ coarse, i
   }
 }
 
-// SparseSpatial2Channel(2): fine row i's C values go to out[parent[i], k C .. k C + C)
+// SparseSpatial2Channel(2), the sparse pixel-unshuffle of the same scope table, on the
+// downsample's subdivision: fine row i's C values go to out[parent[i], k C .. k C + C)
 // with k its child bit; s2c_zero fills the blocks of absent children. The two kernels
 // write disjoint bytes.
 __device__ __forceinline__ int child_of(const int4 d) {   // d = (b, z, y, x)

@@ -92,3 +92,35 @@ def test_values_distribution():
     assert abs(v["bias"].std() - 0.1) < 0.05
     back, _ = round_to_bf16(v["feats"])
     np.testing.assert_array_equal(back, v["feats"])
+
+
+def test_make_residual_is_seeded_bf16_exact_and_standard_normal():
+    from synth import make_residual, make_values
+    r1, bits1 = make_residual(5000, 64, "bf16", 5)
+    r2, bits2 = make_residual(5000, 64, "bf16", 5)
+    np.testing.assert_array_equal(bits1, bits2)
+    np.testing.assert_array_equal(r1, r2)
+    # bf16-exact: the low 16 bits of every float32 are zero, and the bits are the high half
+    u = r1.view(np.uint32)
+    assert not (u & 0xFFFF).any()
+    np.testing.assert_array_equal((u >> 16).astype(np.uint16), bits1)
+    assert abs(r1.mean()) < 0.02 and abs(r1.std() - 1) < 0.02
+    # its own stream: not a copy of the features drawn from the same seed
+    f = make_values(5000, 64, 64, "bf16", 5)["feats"]
+    assert not np.array_equal(f, r1)
+    r3, none = make_residual(10, 3, "f32", 1)
+    assert none is None and r3.dtype == np.float32 and r3.shape == (10, 3)
+
+
+def test_bench_roofline_bytes_with_and_without_residual():
+    import bench
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 1000.0}
+    N, P, I, O = 1000, 11000, 64, 64
+    a = bench.roofline(N, P, I, O, 1e-3, peaks, "measured", "none", e=2)
+    b = bench.roofline(N, P, I, O, 1e-3, peaks, "measured", "none", e=2, residual=True)
+    assert a["algorithmic_bytes"] == P * I * 2 + N * O * 2 + 108 * N + 27 * I * O * 2
+    assert b["algorithmic_bytes"] - a["algorithmic_bytes"] == N * O * 2
+    assert b["compulsory_bytes"] - a["compulsory_bytes"] == N * O * 2
+    assert abs(a["frac"] - a["algorithmic_bytes"] / 1e-3 / 1e9 / 1000.0) < 1e-12
+    c = bench.roofline(N, P, I, O, 1e-3, peaks, "measured", "none", e=4)
+    assert c["kernel"] == "fwd_simt" and c["algorithmic_bytes"] == 2 * a["algorithmic_bytes"] - 108 * N

@@ -17,6 +17,12 @@
  *   dense Conv3d). The weight layout [O, kz, ky, kx, I] with channels-last
  *   features is the one the README's commit header gives for the checkpoints.
  *
+ * Beside the convolution, on the same voxel structures (same pages, same scope table,
+ * which lists them next to SubMConv3d): a fused residual/activation epilogue
+ * (subm3d_forward_ex), SparseDownsample(2) with its cache-paired SparseUpsample(2)
+ * (subm3d_downsample, subm3d_upsample), and the sparse pixel-(un)shuffle on the same
+ * subdivision (subm3d_spatial2channel, subm3d_channel2spatial).
+ *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller. The library
  *     allocates no device memory; scratch space is the caller's `workspace`.

@@ -33,7 +33,10 @@
  *   - Every call returns a subm3d_status. On failure, subm3d_last_error() gives a
  *     message (thread-local, valid until this thread's next call into the
  *     library) that names the argument and its value.
- *   - One process, one GPU: the calls use the current CUDA device.
+ *   - The calls use the current CUDA device. Host-side state that belongs to a device
+ *     (kernel attributes, the device error word's address, the SM count) is looked up
+ *     on the first call made with that device current and kept per device, so one
+ *     process may use several devices (device ordinals below 64).
  */
 #ifndef SUBM3D_H
 #define SUBM3D_H
@@ -159,9 +162,11 @@ SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t re
  * array compiled into the library, so N is limited to SUBM3D_NOALLOC_MAX_VOXELS; a
  * larger N returns SUBM3D_ERR_ARG before any device work. Every GPU that loads the
  * library keeps that array until the process exits. The first call on a device looks
- * up the array's device address (make it before any stream capture). All calls
- * share the one array: each call re-initialises what it reads, but calls that
- * overlap on the GPU (from several host threads or streams) race on it.
+ * up the array's device address (make that first call before any stream capture
+ * begins). Like subm3d_build_kmap, the call waits for `stream` at its end, so calls
+ * from one host thread never overlap on the GPU. All calls share the one array: each
+ * call re-initialises what it reads, but calls made at the same time from several
+ * host threads race on it.
  */
 #define SUBM3D_NOALLOC_MAX_VOXELS 131072
 SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32_t res,

@@ -21,6 +21,68 @@ void set_error(const char* fmt, ...) {
 void clear_error() { g_msg[0] = '\0'; }
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int current_device(int* dev) {
+  *dev = -1;
+  SUBM3D_CUDA_TRY(cudaGetDevice(dev));
+  if (*dev < 0 || *dev >= kMaxDevices) {
+    set_error("device ordinal %d outside [0, %d)", *dev, kMaxDevices);
+    return SUBM3D_ERR_UNSUPPORTED;
+  }
+  return SUBM3D_OK;
+}
+
+namespace {
+PerDevice<int> g_sms;
+PerDevice<int*> g_err_word;
+}  // namespace
+
+int num_sms() {
+  int sms = 0;
+  const int rc = g_sms.get(&sms, [](int* v) -> int {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    *v = n;
+    return static_cast<int>(SUBM3D_OK);
+  });
+  return rc == SUBM3D_OK ? sms : 148;
+}
+
+int set_smem_limit_once(PerDevice<bool>& done, const void* kernel, int bytes, const char* name) {
+  bool ok = false;
+  return done.get(&ok, [&](bool* v) -> int {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute(%s, %d bytes of shared memory) failed: %s", name, bytes,
+                cudaGetErrorString(e));
+      return static_cast<int>(SUBM3D_ERR_CUDA);
+    }
+    *v = true;
+    return static_cast<int>(SUBM3D_OK);
+  });
+}
+
+// The device error word (kDevErr* bits) that the forward, upsample and pixel-shuffle
+// kernels report into; one per device that loads the library.
+__device__ int g_forward_err;
+
+int* forward_error_word() {
+  int* p = nullptr;
+  const int rc = g_err_word.get(&p, [](int** v) -> int {
+    void* a = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&a, g_forward_err);
+    if (e != cudaSuccess || !a) {
+      set_error("cudaGetSymbolAddress(device error word) failed: %s", cudaGetErrorString(e));
+      return static_cast<int>(SUBM3D_ERR_CUDA);
+    }
+    *v = static_cast<int*>(a);
+    return static_cast<int>(SUBM3D_OK);
+  });
+  return rc == SUBM3D_OK ? p : nullptr;
+}
+
 }  // namespace subm3d
 
 using namespace subm3d;
@@ -156,10 +218,7 @@ int subm3d_forward_status(cudaStream_t stream) {
   clear_error();
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
   int* word = forward_error_word();
-  if (!word) {
-    set_error("subm3d_forward_status: device error word not available");
-    return SUBM3D_ERR_CUDA;
-  }
+  if (!word) return SUBM3D_ERR_CUDA;
   int host = 0;
   const int zero = 0;
   SUBM3D_CUDA_TRY(cudaMemcpy(&host, word, sizeof(int), cudaMemcpyDeviceToHost));

@@ -10,6 +10,7 @@
 
 #include <atomic>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/subm3d.h"
@@ -45,20 +46,53 @@ void count_launch(int n = 1);                  // host-side kernel-launch counte
     }                                                                                  \
   } while (0)
 
-inline int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
+// Host state that belongs to one device (kernel attributes, symbol addresses, SM
+// counts) is kept per device ordinal, filled on the first call made with that device
+// current, under a mutex, so that calls on several devices or from several threads
+// each see their own device's values.
+constexpr int kMaxDevices = 64;
+
+// The current device in *dev; SUBM3D_ERR_CUDA or SUBM3D_ERR_UNSUPPORTED (ordinal
+// outside [0, kMaxDevices)) with the message set otherwise.
+int current_device(int* dev);
+
+template <typename T>
+class PerDevice {
+ public:
+  // The value for the current device in *out, made by make(T*) -> status on that
+  // device's first call (a failed make is retried on the next call).
+  template <typename F>
+  int get(T* out, F&& make) {
     int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
+    const int rc = current_device(&dev);
+    if (rc != SUBM3D_OK) return rc;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!ready_[dev]) {
+      const int mrc = make(&val_[dev]);
+      if (mrc != SUBM3D_OK) return mrc;
+      ready_[dev] = true;
+    }
+    *out = val_[dev];
+    return SUBM3D_OK;
   }
-  return sms;
-}
+
+ private:
+  std::mutex mu_;
+  bool ready_[kMaxDevices] = {};
+  T val_[kMaxDevices] = {};
+};
+
+// SM count of the current device (148 if it cannot be read: only grid sizes depend on it).
+int num_sms();
+
+// Sets a kernel's dynamic shared-memory limit once per device.
+int set_smem_limit_once(PerDevice<bool>& done, const void* kernel, int bytes, const char* name);
 
 // Device error word of the forward and upsample kernels (bit flags below).
 enum : int { kDevErrBadNbr = 1, kDevErrTimeout = 2, kDevErrBadParent = 4 };
-int* forward_error_word();                      // device address of the word
+// Device address of the word on the current device, or NULL (message set) when it
+// cannot be had; a launcher then returns SUBM3D_ERR_CUDA without launching.
+int* forward_error_word();
 // Fused epilogue of subm3d_forward_ex: out = act(acc + bias + residual); residual NULL
 // and act SUBM3D_ACT_NONE give the plain convolution.
 struct Epilogue {

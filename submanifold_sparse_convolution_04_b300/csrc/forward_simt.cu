@@ -146,17 +146,19 @@ int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weigh
     set_error("subm3d_forward: N=%lld too large for the CUDA-core kernel", (long long)N);
     return SUBM3D_ERR_UNSUPPORTED;
   }
+  int* err = forward_error_word();
+  if (!err) return SUBM3D_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>((O + kCols - 1) / kCols));
   if (dtype == SUBM3D_F32) {
     fwd_simt<float><<<grid, kThreads, 0, stream>>>(
         static_cast<const float*>(feats), nbr, static_cast<const float*>(weight),
         static_cast<const float*>(bias), static_cast<const float*>(epi.residual), epi.act,
-        static_cast<float*>(out), N, I, O, forward_error_word());
+        static_cast<float*>(out), N, I, O, err);
   } else {
     fwd_simt<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(feats), nbr, static_cast<const __nv_bfloat16*>(weight),
         static_cast<const __nv_bfloat16*>(bias), static_cast<const __nv_bfloat16*>(epi.residual),
-        epi.act, static_cast<__nv_bfloat16*>(out), N, I, O, forward_error_word());
+        epi.act, static_cast<__nv_bfloat16*>(out), N, I, O, err);
   }
   SUBM3D_LAUNCHED("fwd_simt");
   return SUBM3D_OK;

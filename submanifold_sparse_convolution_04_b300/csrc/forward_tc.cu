@@ -52,14 +52,6 @@
 
 namespace subm3d {
 
-__device__ int g_forward_err;
-
-int* forward_error_word() {
-  static int* ptr = nullptr;
-  if (!ptr) cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_forward_err);
-  return ptr;
-}
-
 namespace {
 
 constexpr int kBM = 128;          // output rows per tile (tensor-memory lanes)
@@ -451,12 +443,10 @@ EncodeTiledFn get_encode() {
 template <int NMMA>
 int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) {
   using C = Cfg<NMMA>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(fwd_tc<NMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-    attr_set = true;
-  }
+  static PerDevice<bool> attr_set;
+  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(fwd_tc<NMMA>),
+                                      C::kSmemBytes, "fwd_tc");
+  if (arc != SUBM3D_OK) return arc;
   EncodeTiledFn encode = get_encode();
   if (!encode) {
     set_error("subm3d_forward: cuTensorMapEncodeTiled is not available from the driver");
@@ -493,8 +483,10 @@ int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
     set_error("subm3d_forward: N=%lld too large", (long long)N);
     return SUBM3D_ERR_UNSUPPORTED;
   }
+  int* err = forward_error_word();
+  if (!err) return SUBM3D_ERR_CUDA;
   Params prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual), epi.act,
-             N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), forward_error_word()};
+             N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), err};
   const int nmma = (O + 15) / 16 * 16;
   switch (nmma) {
 #define SUBM3D_CASE(n) \

@@ -477,12 +477,10 @@ TmEncodeTiledFn tm_get_encode() {
 template <int NMMA>
 int tm_launch(const TmParams& prm, const __nv_bfloat16* weight, cudaStream_t stream) {
   using C = TmCfg<NMMA>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(fwd_tm<NMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-    attr_set = true;
-  }
+  static PerDevice<bool> attr_set;
+  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(fwd_tm<NMMA>),
+                                      C::kSmemBytes, "fwd_tm");
+  if (arc != SUBM3D_OK) return arc;
   TmEncodeTiledFn encode = tm_get_encode();
   if (!encode) {
     set_error("subm3d_forward: cuTensorMapEncodeTiled is not available from the driver");
@@ -525,8 +523,10 @@ int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
     set_error("subm3d_forward: N=%lld too large", (long long)N);
     return SUBM3D_ERR_UNSUPPORTED;
   }
+  int* err = forward_error_word();
+  if (!err) return SUBM3D_ERR_CUDA;
   TmParams prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual),
-               epi.act, N, I, O, static_cast<int>(ntiles), forward_error_word()};
+               epi.act, N, I, O, static_cast<int>(ntiles), err};
   switch (O) {
     case 16: return tm_launch<16>(prm, weight, stream);
     case 32: return tm_launch<32>(prm, weight, stream);

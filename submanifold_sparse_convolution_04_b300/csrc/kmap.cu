@@ -591,12 +591,10 @@ int grid_for(int64_t work, int threads, int per_sm) {
 // word's plan saying which of (mk0, ix0) / (mk1, ix1) holds the sorted result.
 int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* ws,
                 cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    SUBM3D_CUDA_TRY(cudaFuncSetAttribute(kmap_sort_scatter,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScatterSmem));
-    attr_set = true;
-  }
+  static PerDevice<bool> attr_set;
+  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(kmap_sort_scatter),
+                                      kScatterSmem, "kmap_sort_scatter");
+  if (arc != SUBM3D_OK) return arc;
   KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
@@ -1067,12 +1065,12 @@ int launch_unpool(const void* coarse, int64_t M, int C, const int32_t* parent, i
   constexpr int V = 16 / sizeof(T);
   const T* c = static_cast<const T*>(coarse);
   T* f = static_cast<T*>(fine);
+  int* err = forward_error_word();
+  if (!err) return SUBM3D_ERR_CUDA;
   if (C % V == 0) {
-    us_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f,
-                                                                        forward_error_word());
+    us_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f, err);
   } else {
-    us_gather<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f,
-                                                                  forward_error_word());
+    us_gather<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(c, M, C, parent, N, f, err);
   }
   SUBM3D_LAUNCHED("us_gather");
   return SUBM3D_OK;
@@ -1224,6 +1222,8 @@ int launch_s2c(const void* feats, const int4* coords, const int32_t* parent,
   const T* f = static_cast<const T*>(feats);
   T* o = static_cast<T*>(out);
   const bool vec = C % V == 0;
+  int* err = N > 0 ? forward_error_word() : nullptr;
+  if (N > 0 && !err) return SUBM3D_ERR_CUDA;
   if (M > 0) {
     if (vec) {
       s2c_zero<T, V><<<grid_for(M * 8 * (C / V), 256, 8), 256, 0, stream>>>(mask, M, C, o);
@@ -1235,10 +1235,10 @@ int launch_s2c(const void* feats, const int4* coords, const int32_t* parent,
   if (N > 0) {
     if (vec) {
       s2c_scatter<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(
-          f, coords, parent, N, M, C, o, forward_error_word());
+          f, coords, parent, N, M, C, o, err);
     } else {
       s2c_scatter<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(f, coords, parent, N, M, C,
-                                                                    o, forward_error_word());
+                                                                    o, err);
     }
     SUBM3D_LAUNCHED("s2c_scatter");
   }
@@ -1250,12 +1250,14 @@ int launch_c2s(const void* coarse, const int4* coords, const int32_t* parent, in
   constexpr int V = 16 / sizeof(T);
   const T* c = static_cast<const T*>(coarse);
   T* f = static_cast<T*>(fine);
+  int* err = forward_error_word();
+  if (!err) return SUBM3D_ERR_CUDA;
   if (C % V == 0) {
-    c2s_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(
-        c, coords, parent, N, M, C, f, forward_error_word());
+    c2s_gather<T, V><<<grid_for(N * (C / V), 256, 8), 256, 0, stream>>>(c, coords, parent, N, M,
+                                                                         C, f, err);
   } else {
     c2s_gather<T, 1><<<grid_for(N * C, 256, 8), 256, 0, stream>>>(c, coords, parent, N, M, C, f,
-                                                                 forward_error_word());
+                                                                 err);
   }
   SUBM3D_LAUNCHED("c2s_gather");
   return SUBM3D_OK;

@@ -12,10 +12,12 @@
 // g_kmap_scratch is a file-scope __device__ array: every GPU that loads the library
 // holds its 9 MiB until the process exits. In host code its name is only a host-side
 // stand-in, so its device address is fetched with cudaGetSymbolAddress, once per
-// device, with that device current (on the first call made on that device; make that
-// first call before any stream capture). All calls share the array and the build
-// re-initialises everything it reads, so each call starts clean; calls that overlap
-// on the GPU (several host threads, or several streams) race on it.
+// device, with that device current, by the first call made on that device (make that
+// first call before any stream capture begins). Like subm3d_build_kmap, each call
+// waits for its stream at its end, so two calls from one host thread never overlap on
+// the GPU. All calls share the array and the build re-initialises everything it reads,
+// so each call starts clean; calls made at the same time from several host threads race
+// on it.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,29 +27,19 @@ namespace {
 
 constexpr int64_t kNoAllocMaxVoxels = SUBM3D_NOALLOC_MAX_VOXELS;
 constexpr size_t kNoAllocScratchBytes = size_t(9) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_kmap_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+PerDevice<void*> g_scratch_ptr;
 
 // Device address of g_kmap_scratch on the current device (looked up once per device).
 int scratch_on_current_device(void** out) {
-  int dev = -1;
-  SUBM3D_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) {
-    set_error("subm3d_build_kmap_noalloc: device ordinal %d outside [0, %d)", dev, kMaxDevices);
-    return SUBM3D_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  return g_scratch_ptr.get(out, [](void** v) -> int {
     void* p = nullptr;
     SUBM3D_CUDA_TRY(cudaGetSymbolAddress(&p, g_kmap_scratch));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return SUBM3D_OK;
+    *v = p;
+    return static_cast<int>(SUBM3D_OK);
+  });
 }
 
 }  // namespace

@@ -192,3 +192,21 @@ def test_binding_refuses_bad_arguments_without_a_gpu():
     with pytest.raises(ValueError):
         subm3d_spatial2channel(f, torch.zeros((4, 4), dtype=torch.int32),
                                torch.zeros(4, dtype=torch.int32), torch.zeros(2, dtype=torch.uint8))
+
+
+def test_launchers_refuse_without_a_device_error_word(L):
+    # Every forward, upsample and pixel-shuffle launcher fetches its device's error word
+    # first and returns ERR_CUDA, launching nothing, when it cannot be had (here: no
+    # CUDA device). The pointers are never dereferenced on that path.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a CUDA device")
+    p = ctypes.c_void_p
+    for I, O, dt in ((64, 64, B.BF16), (128, 128, B.BF16), (64, 520, B.BF16), (32, 32, B.F32)):
+        assert L.subm3d_forward(p(256), p(512), p(768), None, p(1024), 10, I, O, dt, None) == B.ERR_CUDA
+        assert b"error word" in L.subm3d_last_error() or b"cudaGetDevice" in L.subm3d_last_error()
+    assert L.subm3d_upsample(p(16), 4, 8, p(32), 10, B.BF16, p(64), None) == B.ERR_CUDA
+    assert L.subm3d_spatial2channel(p(16), p(32), p(48), p(64), 10, 4, 8, B.F32, p(80),
+                                    None) == B.ERR_CUDA
+    assert L.subm3d_channel2spatial(p(16), p(32), p(48), 10, 4, 8, B.BF16, p(64), None) == B.ERR_CUDA
+    assert L.subm3d_forward_status(None) == B.ERR_CUDA

@@ -73,6 +73,14 @@ def parse_args():
                    help="fused block epilogue: activation after bias (+ residual)")
     p.add_argument("--max-voxels", type=int, default=0,
                    help="keep only the first M voxels (raster order): a slab of the workload")
+    p.add_argument("--path", default="grouped", choices=["grouped", "plain"],
+                   help="grouped: the kernel map as a tile plan and the forward on occupancy-"
+                        "grouped tiles; plain: the input-order nbr and the dense-offset tiles")
+    p.add_argument("--window", type=int, default=0,
+                   help="grouping window of the tile plan (0: the library default)")
+    p.add_argument("--sync-kmap", action="store_true",
+                   help="use the kernel-map call that waits for its stream (default: the "
+                        "asynchronous one, device status checked after the timed steps)")
     return p.parse_args()
 
 
@@ -311,14 +319,52 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def active_passes(coords, res):
+    """Radix passes the kernel map runs on these coords (constant high digits skipped)."""
+    import numpy as np
+    bits = 2
+    while (1 << bits) < res:
+        bits += 1
+    c = coords.astype(np.uint64)
+    key = c[:, 0] << np.uint64(3 * bits)
+    for t in range(bits):
+        key |= ((c[:, 3] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t)
+        key |= ((c[:, 2] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t + 1)
+        key |= ((c[:, 1] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t + 2)
+    diff = int(key.min()) ^ int(key.max())
+    npass = (3 * bits + 16 + 7) // 8
+    return sum(1 for p in range(npass) if (diff >> (8 * p)) != 0)
+
+
+def kmap_algorithmic_bytes(N, passes, grouped, window):
+    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N
+    if not grouped:
+        return base + 108 * N
+    last_window = (N - 1) // window
+    wbits = last_window.bit_length()
+    passes2 = (27 + wbits + 7) // 8
+    return base + 24 * N + 24 * N * passes2 + 20 * N + 4 * N + 108 * N
+
+
+def spread(xs):
+    s = sorted(xs)
+    return {"min": s[0], "median": statistics.median(s), "max": s[-1], "mean": statistics.mean(s)}
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
-    from submanifold_sparse_convolution_04_b300 import (subm3d_build_kmap, subm3d_forward,
-                                                        subm3d_forward_ex,
+    from submanifold_sparse_convolution_04_b300 import (GROUP_WINDOW, subm3d_build_kmap,
+                                                        subm3d_build_kmap_async,
+                                                        subm3d_build_kmap_grouped,
+                                                        subm3d_forward_ex, subm3d_forward_grouped,
                                                         subm3d_forward_status,
                                                         subm3d_kernel_launches,
-                                                        subm3d_kmap_workspace_bytes)
+                                                        subm3d_kmap_grouped_workspace_bytes,
+                                                        subm3d_kmap_stage_timing,
+                                                        subm3d_kmap_stage_times,
+                                                        subm3d_kmap_workspace_bytes,
+                                                        subm3d_plan_bytes)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
     dev = torch.device("cuda", local)
@@ -326,6 +372,8 @@ def run_ours(args, world, rank, local):
     case = load_case(args)
     N, I, O, res = case["coords"].shape[0], case["I"], case["O"], case["res"]
     bf16 = case["dtype"] == "bf16"
+    grouped = args.path == "grouped"
+    window = args.window or GROUP_WINDOW
 
     def host(name):
         if bf16:
@@ -338,11 +386,9 @@ def run_ours(args, world, rank, local):
     f = feats_h.to(dev)
     w = weight_h.to(dev)
     b = bias_h.to(dev)
-    ws = torch.empty(subm3d_kmap_workspace_bytes(N), dtype=torch.uint8, device=dev)
-    nbr = torch.empty((N, 27), dtype=torch.int32, device=dev)
-    out = torch.empty((N, O), dtype=f.dtype, device=dev)
+    ws_bytes = subm3d_kmap_grouped_workspace_bytes(N) if grouped else subm3d_kmap_workspace_bytes(N)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    fused = args.residual or args.act != "none"
     res_h = r = None
     if args.residual:
         from synth import make_residual
@@ -350,21 +396,42 @@ def run_ours(args, world, rank, local):
         res_h = (torch.from_numpy(rbits.view(np.int16)).view(torch.bfloat16) if bf16
                  else torch.from_numpy(rv)).pin_memory()
         r = res_h.to(dev)
+    fused = args.residual or args.act != "none"
 
-    def forward(f, nbr, w, b, r, out):
-        if fused:
-            subm3d_forward_ex(f, nbr, w, b, residual=r, act=args.act, out=out)
+    def new_map():
+        """The kernel map's output buffer: a tile plan or nbr [N, 27]."""
+        if grouped:
+            return torch.empty(max(subm3d_plan_bytes(N), 256), dtype=torch.uint8, device=dev)
+        return torch.empty((N, 27), dtype=torch.int32, device=dev)
+
+    def build(coords, kmap):
+        if grouped:
+            subm3d_build_kmap_grouped(coords, res, window=window, plan=kmap, workspace=ws,
+                                      async_=not args.sync_kmap)
+        elif args.sync_kmap:
+            subm3d_build_kmap(coords, res, nbr=kmap, workspace=ws)
         else:
-            subm3d_forward(f, nbr, w, b, out=out)
+            subm3d_build_kmap_async(coords, res, nbr=kmap, workspace=ws)
+
+    def forward(feats, kmap, wt, bs, resid, o):
+        if grouped:
+            subm3d_forward_grouped(feats, kmap, wt, bs, residual=resid, act=args.act, out=o)
+        else:
+            subm3d_forward_ex(feats, kmap, wt, bs, residual=resid, act=args.act, out=o)
+
+    kmap = new_map()
+    out = torch.empty((N, O), dtype=f.dtype, device=dev)
 
     def step():
-        subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
-        forward(f, nbr, w, b, r, out)
+        build(c, kmap)
+        forward(f, kmap, w, b, r, out)
 
     for _ in range(max(args.warmup, 3)):
         step()
     subm3d_forward_status()
-    P = int((nbr >= 0).sum().item())
+    nbr_check = subm3d_build_kmap(c, res)           # pair count from the plain map
+    P = int((nbr_check >= 0).sum().item())
+    del nbr_check
     flops = 2.0 * P * I * O
 
     K = args.steps
@@ -380,34 +447,50 @@ def run_ours(args, world, rank, local):
     e0.record(stream)
     for s in range(K):
         ev[s][0].record(stream)
-        subm3d_build_kmap(c, res, nbr=nbr, workspace=ws)
+        build(c, kmap)
         ev[s][1].record(stream)
-        forward(f, nbr, w, b, r, out)
+        forward(f, kmap, w, b, r, out)
         ev[s][2].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     launches = subm3d_kernel_launches() - launches0
     clk = clocks.stop()
     barrier(world)
-    subm3d_forward_status()
+    subm3d_forward_status()          # every step's kernel map and forward: no device error
     total_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    kmap_ms = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(K))
-    fwd_ms = statistics.mean(ev[s][1].elapsed_time(ev[s][2]) for s in range(K))
+    kmap_each = [ev[s][0].elapsed_time(ev[s][1]) for s in range(K)]
+    fwd_each = [ev[s][1].elapsed_time(ev[s][2]) for s in range(K)]
+    kmap_ms = statistics.mean(kmap_each)
+    fwd_ms = statistics.mean(fwd_each)
     ms_per_step = total_ms / K
     value = world * flops / (ms_per_step / 1e3) / 1e12
+
+    # per-stage GPU times of one more kernel-map build (outside the timed region)
+    subm3d_kmap_stage_timing(True)
+    build(c, kmap)
+    stages = subm3d_kmap_stage_times()
+    subm3d_kmap_stage_timing(False)
+    torch.cuda.synchronize()
+    subm3d_forward_status()
 
     unfused_us = None
     if fused:
         # the same epilogue as separate passes (plain forward, then torch's add and
         # activation over [N, O]): what the fusion saves
         def unfused():
-            subm3d_forward(f, nbr, w, b, out=out)
+            forward_plain_conv()
             if r is not None:
                 out.add_(r)
             if args.act == "relu":
                 out.relu_()
             elif args.act == "silu":
                 torch.nn.functional.silu(out, inplace=True)
+
+        def forward_plain_conv():
+            if grouped:
+                subm3d_forward_grouped(f, kmap, w, b, out=out)
+            else:
+                subm3d_forward_ex(f, kmap, w, b, out=out)
         for _ in range(3):
             unfused()
         u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -418,7 +501,7 @@ def run_ours(args, world, rank, local):
         u1.record(stream)
         torch.cuda.synchronize()
         unfused_us = u0.elapsed_time(u1) / min(K, 50) * 1e3
-        forward(f, nbr, w, b, r, out)      # leave the fused result in out
+        forward(f, kmap, w, b, r, out)      # leave the fused result in out
         torch.cuda.synchronize()
 
     # end to end through the Python API: every step copies its inputs from pinned host
@@ -434,7 +517,7 @@ def run_ours(args, world, rank, local):
     s_cmp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     bufs = [dict({"r": None}, **{key: torch.empty_like(src, device=dev) for key, src in ins},
-                 nbr=torch.empty((N, 27), dtype=torch.int32, device=dev),
+                 kmap=new_map(),
                  out=torch.empty((N, O), dtype=f.dtype, device=dev),
                  out_h=torch.empty((N, O), dtype=f.dtype).pin_memory(),
                  ev_in=torch.cuda.Event(), ev_cmp=torch.cuda.Event(), ev_out=torch.cuda.Event())
@@ -454,8 +537,8 @@ def run_ours(args, world, rank, local):
         s_cmp.wait_event(B["ev_in"])
         if i >= 2:
             s_cmp.wait_event(B["ev_out"])           # step i-2's output has left the device
-        subm3d_build_kmap(B["c"], res, nbr=B["nbr"], workspace=ws)
-        forward(B["f"], B["nbr"], B["w"], B["b"], B["r"], B["out"])
+        build(B["c"], B["kmap"])
+        forward(B["f"], B["kmap"], B["w"], B["b"], B["r"], B["out"])
         B["ev_cmp"].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(B["ev_cmp"])
@@ -483,8 +566,17 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = load_peaks()
     epi = "none" if not fused else ("residual+" if args.residual else "") + args.act
     roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind,
-                    case["name"] + ("" if not fused else "_" + epi.replace("+", "_")),
+                    case["name"] + ("_grouped" if grouped else "") +
+                    ("" if not fused else "_" + epi.replace("+", "_")),
                     e=2 if bf16 else 4, residual=args.residual)
+    passes = active_passes(case["coords"], res)
+    kbytes = kmap_algorithmic_bytes(N, passes, grouped, window)
+    hbm = float(peaks["hbm_gbs"])
+    kmap_roof = {"bound": "hbm", "achieved": kbytes / (kmap_ms / 1e3) / 1e9, "peak": hbm,
+                 "unit": "GB/s", "frac": kbytes / (kmap_ms / 1e3) / 1e9 / hbm,
+                 "algorithmic_bytes": kbytes, "radix_passes": passes,
+                 "peak_source": f"hbm_gbs, {peak_kind}",
+                 "stages_ms": [[n, round(t, 4)] for n, t in stages]}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -494,11 +586,19 @@ def run_ours(args, world, rank, local):
                        l2="inputs larger than L2 (feats, nbr, hash table each > 126 MB); "
                           "no flush between steps",
                        parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                       epilogue=epi),
+                       epilogue=epi,
+                       path=("tile plan (subm3d_build_kmap_grouped + subm3d_forward_grouped, "
+                             f"window {window})" if grouped else
+                             "input-order nbr (subm3d_build_kmap + subm3d_forward)"),
+                       kmap_wait="synchronous" if args.sync_kmap else
+                                 "asynchronous (device status checked after the timed steps)"),
         "mvoxels_per_s": world * N / (ms_per_step / 1e3) / 1e6,
         "kmap_ms": kmap_ms, "forward_us": fwd_ms * 1e3,
+        "kmap_ms_spread": spread(kmap_each),
+        "forward_us_spread": {k: v * 1e3 for k, v in spread(fwd_each).items()},
         "forward_tflops": flops / (fwd_ms / 1e3) / 1e12,
         "roofline": roof,
+        "kmap_roofline": kmap_roof,
         **({"unfused_epilogue_forward_us": unfused_us} if fused else {}),
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

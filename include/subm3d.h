@@ -151,6 +151,83 @@ SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t re
                          size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * subm3d_build_kmap without the wait: every step is enqueued on `stream` and the call
+ * returns at once, so a kernel-map build and the convolutions that use it can run back
+ * to back on the GPU (or be captured together into a CUDA graph). Errors found on the
+ * device (a coordinate out of range, a duplicate, a full hash table) are not returned
+ * here: they are folded into the device error word, and the next
+ * subm3d_forward_status() returns SUBM3D_ERR_COORD_RANGE, SUBM3D_ERR_DUPLICATE or
+ * SUBM3D_ERR_HASH_FULL. nbr is then unspecified, but every entry the forward kernels
+ * read is checked against [-1, N), so a forward on it never reads outside feats.
+ * Host-side argument errors are returned as by subm3d_build_kmap.
+ */
+SUBM3D_API int subm3d_build_kmap_async(const int32_t* coords, int64_t N, int32_t res,
+                                       int32_t* nbr, void* workspace, size_t ws_bytes,
+                                       cudaStream_t stream);
+
+/*
+ * Occupancy-grouped tiles ("tile plan"). The hot-path forward works on tiles of 128
+ * output rows and runs, for every tile, each of the 27 offsets at which any of its
+ * rows has a neighbour. In input (or Morton) order nearly every tile has a neighbour
+ * at nearly every offset, though on surfaces only about 11 of a voxel's 27 are there.
+ * A tile plan orders the rows so that a tile's rows share their neighbour offsets:
+ * within consecutive windows of the Morton order, voxels are sorted by their 27-bit
+ * neighbour mask (bit k set when nbr[i, k] >= 0), Morton order kept among equal masks.
+ * The forward then skips, per tile, every offset no row of the tile has (on the shell
+ * workloads it runs 0.43-0.55 of the offsets instead of all of them), and stores each
+ * output row through the plan's permutation, so `out` keeps the caller's input order.
+ * The result is the same convolution (the formula at the top of this file).
+ *
+ * Plan layout (device buffer of subm3d_plan_bytes(N) bytes, 256-byte aligned, owned by
+ * the caller; offsets from its start, each rounded up to 256 bytes):
+ *   perm       int32 [N]           at 0: perm[r] = input row at plan row r
+ *   nbr        int32 [N, 27]       next: row r = the neighbour-table row of input row
+ *                                  perm[r] (values are input rows, as in subm3d_build_kmap)
+ *   tile_mask  uint32 [ceil(N/128)] next: bit k of tile t set when some plan row in
+ *                                  [128 t, 128 t + 128) has a neighbour at offset k
+ * The window (voxels of the Morton order grouped together) trades the share of offsets
+ * skipped against the spread of the rows a tile gathers; SUBM3D_GROUP_WINDOW is the
+ * default.
+ */
+#define SUBM3D_GROUP_WINDOW 262144
+#define SUBM3D_KMAP_ASYNC 1u   /* flags: return without waiting (see subm3d_build_kmap_async) */
+SUBM3D_API size_t subm3d_plan_bytes(int64_t N);
+/* Workspace bytes subm3d_build_kmap_grouped needs for N voxels (0 for N outside [0, 2^31)). */
+SUBM3D_API size_t subm3d_kmap_grouped_workspace_bytes(int64_t N);
+
+/*
+ * Kernel map as a tile plan: the steps of subm3d_build_kmap up to the block table, then
+ * each voxel's neighbour mask (a warp-cooperative pass over the Morton order), a stable
+ * radix sort of the sorted positions by (window, mask), the plan's perm and tile masks,
+ * and the neighbour rows written in plan order.
+ *   coords, N, res  as subm3d_build_kmap.
+ *   window          0 for SUBM3D_GROUP_WINDOW, else a power of two in [128, 2^30].
+ *   plan            device buffer of at least subm3d_plan_bytes(N) bytes, written.
+ *   workspace       device scratch of subm3d_kmap_grouped_workspace_bytes(N) bytes,
+ *                   256-byte aligned.
+ *   flags           0: wait for `stream` and return device-side errors as
+ *                   subm3d_build_kmap does; SUBM3D_KMAP_ASYNC: do not wait (errors as
+ *                   subm3d_build_kmap_async).
+ * Bit-exact: the plan is a function of the voxel set and the window (stable sorts).
+ */
+SUBM3D_API int subm3d_build_kmap_grouped(const int32_t* coords, int64_t N, int32_t res,
+                                         int64_t window, void* plan, size_t plan_bytes,
+                                         void* workspace, size_t ws_bytes, unsigned flags,
+                                         cudaStream_t stream);
+
+/*
+ * subm3d_forward_ex on a tile plan instead of an input-order nbr: feats, weight, bias,
+ * residual, act, out, N, I, O, dtype and the kernels chosen are as there (feats,
+ * residual and out in the caller's input order); `plan` is what
+ * subm3d_build_kmap_grouped wrote for these N voxels. Asynchronous; a plan row whose
+ * perm entry lies outside [0, N) is skipped and reported by subm3d_forward_status.
+ */
+SUBM3D_API int subm3d_forward_grouped(const void* feats, const void* plan, const void* weight,
+                                      const void* bias, const void* residual, subm3d_act act,
+                                      void* out, int64_t N, int32_t I, int32_t O,
+                                      subm3d_dtype dtype, cudaStream_t stream);
+
+/*
  * Kernel map without any device allocation. The pages have no counterpart to this
  * call; it exists for callers that cannot allocate device memory themselves -- a host
  * application that owns all device memory through its own pool and hands a plugin
@@ -320,12 +397,29 @@ SUBM3D_API int subm3d_channel2spatial(const void* coarse_feats, const int32_t* c
                                       subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
 
 /*
- * Waits for `stream`, then reads and clears the device error word of the forward and
- * upsample kernels: SUBM3D_OK, or SUBM3D_ERR_DEVICE (message says which condition: an
- * nbr entry outside [-1, N), a bounded pipeline wait that ran out, or a parent entry
- * outside [0, M)). The word is shared by all streams of the process.
+ * Waits for `stream`, then reads and clears the device error word of the current
+ * device, which the forward, upsample and pixel-shuffle kernels and the asynchronous
+ * kernel-map builds report into. Returns SUBM3D_OK; SUBM3D_ERR_COORD_RANGE,
+ * SUBM3D_ERR_DUPLICATE or SUBM3D_ERR_HASH_FULL when an asynchronous build found that;
+ * else SUBM3D_ERR_DEVICE (the message says which condition: an nbr entry outside
+ * [-1, N), a bounded pipeline wait that ran out, a parent entry outside [0, M), a plan
+ * row naming no input row, an internal index error of a build). The word is shared by
+ * all streams of the process.
  */
 SUBM3D_API int subm3d_forward_status(cudaStream_t stream);
+
+/*
+ * Stage timing of the kernel-map builds, for measurement. While enabled (per host
+ * thread; off by default), every kernel-map build made by this thread records a CUDA
+ * event on its stream before its first stage and after each stage (pack, each radix
+ * pass, block table, probe; for the tile plan also the mask probe, each grouping-sort
+ * pass, the plan index and the plan probe). No extra synchronisation is added.
+ * subm3d_kmap_stage_times waits for the last build's events and writes, for up to `max`
+ * stages in order, the GPU milliseconds of each (ms[i]) and its name (names[i], a
+ * static string); it returns the number of stages written, or a negative status.
+ */
+SUBM3D_API void subm3d_kmap_stage_timing(int enable);
+SUBM3D_API int subm3d_kmap_stage_times(float* ms, const char** names, int max);
 
 /* Thread-local message describing the last failure of this thread ("" if none). */
 SUBM3D_API const char* subm3d_last_error(void);

@@ -35,7 +35,7 @@ import numpy as np
 __all__ = ["OFFSETS", "CENTER", "ACTIVATIONS", "POOL_MODES", "OracleError", "tap",
            "coordinate_dict", "kernel_map", "subm_conv3d", "subm_conv3d_rows", "activation",
            "block_epilogue", "morton_code", "child_bit", "downsample", "upsample",
-           "spatial2channel", "channel2spatial"]
+           "spatial2channel", "channel2spatial", "morton_codes", "neighbour_masks", "tile_plan"]
 
 # k -> (dz, dy, dx), k = 9 (dz + 1) + 3 (dy + 1) + (dx + 1)
 OFFSETS = [(dz, dy, dx) for dz in (-1, 0, 1) for dy in (-1, 0, 1) for dx in (-1, 0, 1)]
@@ -280,3 +280,50 @@ def channel2spatial(coarse_feats, coords, parent):
         k = child_bit(z, y, x)
         out[i] = c[parent[i], k * C:(k + 1) * C]
     return out
+
+
+# ---------------------------------------------------------------------------------
+# Occupancy-grouped tiles (the tile plan of the grouped forward). This is not part of
+# the convolution's definition -- the grouped forward computes the same sums -- but the
+# plan the GPU builds is a deterministic function of the voxel set and the window, so
+# it is written out here as plainly as the rest and compared bit-exactly.
+
+def morton_codes(coords):
+    """morton_code(z, y, x) of every row of coords [N, 4] (b, z, y, x), as uint64 (the
+    same bit interleave, one bit plane at a time over the whole array)."""
+    c = np.asarray(coords, dtype=np.int64)
+    m = np.zeros(c.shape[0], dtype=np.uint64)
+    for t in range(16):
+        for axis, col in ((0, 3), (1, 2), (2, 1)):       # x -> 3t, y -> 3t + 1, z -> 3t + 2
+            bitv = ((c[:, col] >> t) & 1).astype(np.uint64)
+            m |= bitv << np.uint64(3 * t + axis)
+    return m
+
+
+def neighbour_masks(nbr):
+    """27-bit mask per row of a kernel map: bit k set when nbr[i, k] >= 0."""
+    present = np.asarray(nbr) >= 0
+    return (present.astype(np.uint64) << np.arange(27, dtype=np.uint64)).sum(axis=1).astype(np.uint32)
+
+
+def tile_plan(coords, nbr, window, tile=128):
+    """(perm [N], plan_nbr [N, 27], tile_mask [ceil(N / tile)]) of the grouped forward.
+
+    The voxels in (batch, Morton code) order, ties by input row, are cut into windows of
+    `window` consecutive voxels; inside each window they are sorted by neighbour mask
+    (as an integer), keeping Morton order among equal masks. perm[r] is the input row
+    at plan row r, plan_nbr the kernel map's rows in that order, and tile_mask[t] the OR
+    of the masks of plan rows [tile t, tile t + tile)."""
+    c = np.asarray(coords, dtype=np.int64)
+    N = c.shape[0]
+    rows = np.arange(N)
+    morton_order = np.lexsort((rows, morton_codes(c), c[:, 0]))
+    masks = neighbour_masks(nbr)
+    window_of = rows // int(window)                       # window of each sorted position
+    grouped = np.lexsort((rows, masks[morton_order], window_of))
+    perm = morton_order[grouped].astype(np.int32)
+    ntiles = (N + tile - 1) // tile
+    padded = np.zeros(ntiles * tile, dtype=np.uint32)
+    padded[:N] = masks[perm]
+    tile_mask = np.bitwise_or.reduce(padded.reshape(ntiles, tile), axis=1).astype(np.uint32)
+    return perm, np.asarray(nbr)[perm], tile_mask

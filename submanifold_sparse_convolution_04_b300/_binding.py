@@ -51,6 +51,18 @@ def lib() -> ctypes.CDLL:
         L.subm3d_build_kmap_ex.restype = ctypes.c_int
         L.subm3d_build_kmap_noalloc.argtypes = [vp, i64, i32, vp, vp]
         L.subm3d_build_kmap_noalloc.restype = ctypes.c_int
+        L.subm3d_build_kmap_async.argtypes = [vp, i64, i32, vp, vp, sz, vp]
+        L.subm3d_build_kmap_async.restype = ctypes.c_int
+        L.subm3d_plan_bytes.argtypes = [i64]
+        L.subm3d_plan_bytes.restype = sz
+        L.subm3d_kmap_grouped_workspace_bytes.argtypes = [i64]
+        L.subm3d_kmap_grouped_workspace_bytes.restype = sz
+        L.subm3d_build_kmap_grouped.argtypes = [vp, i64, i32, i64, vp, sz, vp, sz, ctypes.c_uint,
+                                                vp]
+        L.subm3d_build_kmap_grouped.restype = ctypes.c_int
+        L.subm3d_forward_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, i32, i32,
+                                             ctypes.c_int, vp]
+        L.subm3d_forward_grouped.restype = ctypes.c_int
         L.subm3d_forward.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, ctypes.c_int, vp]
         L.subm3d_forward.restype = ctypes.c_int
         L.subm3d_forward_ex.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, i64, i32, i32,
@@ -69,6 +81,11 @@ def lib() -> ctypes.CDLL:
         L.subm3d_channel2spatial.restype = ctypes.c_int
         L.subm3d_forward_status.argtypes = [vp]
         L.subm3d_forward_status.restype = ctypes.c_int
+        L.subm3d_kmap_stage_timing.argtypes = [ctypes.c_int]
+        L.subm3d_kmap_stage_timing.restype = None
+        L.subm3d_kmap_stage_times.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                              ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]
+        L.subm3d_kmap_stage_times.restype = ctypes.c_int
         L.subm3d_last_error.argtypes = []
         L.subm3d_last_error.restype = ctypes.c_char_p
         L.subm3d_kernel_launches.argtypes = []
@@ -164,6 +181,96 @@ def subm3d_build_kmap_noalloc(coords: torch.Tensor, res: int, nbr: torch.Tensor,
     pn = _dev(nbr, "nbr", torch.int32, (N, 27))
     _check(lib().subm3d_build_kmap_noalloc(pc, N, int(res), pn, _stream(stream)))
     return nbr
+
+
+def subm3d_build_kmap_async(coords: torch.Tensor, res: int, nbr: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """subm3d_build_kmap without waiting for the stream; device-side errors surface at the
+    next subm3d_forward_status()."""
+    N = coords.shape[0]
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    if nbr is None:
+        nbr = torch.empty((N, 27), dtype=torch.int32, device=coords.device)
+    pn = _dev(nbr, "nbr", torch.int32, (N, 27))
+    workspace, pw, nbytes = _workspace(N, 0, workspace, coords.device)
+    _check(lib().subm3d_build_kmap_async(pc, N, int(res), pn, pw, nbytes, _stream(stream)))
+    return nbr
+
+
+KMAP_ASYNC = 1
+GROUP_WINDOW = 262144
+
+
+def subm3d_plan_bytes(N: int) -> int:
+    return int(lib().subm3d_plan_bytes(N))
+
+
+def subm3d_kmap_grouped_workspace_bytes(N: int) -> int:
+    return int(lib().subm3d_kmap_grouped_workspace_bytes(N))
+
+
+def plan_views(plan: torch.Tensor, N: int):
+    """(perm int32 [N], nbr int32 [N, 27], tile_mask int32 [ceil(N/128)]) views of a tile
+    plan buffer, at the offsets include/subm3d.h documents (each part 256-byte aligned;
+    tile_mask holds uint32 bit patterns)."""
+    a256 = lambda x: (x + 255) // 256 * 256
+    o_nbr = a256(4 * N)
+    o_mask = a256(o_nbr + 4 * 27 * N)
+    nt = (N + 127) // 128
+    b = plan.view(torch.uint8)
+    perm = b[0:4 * N].view(torch.int32)
+    nbr = b[o_nbr:o_nbr + 4 * 27 * N].view(torch.int32).view(N, 27)
+    mask = b[o_mask:o_mask + 4 * nt].view(torch.int32)
+    return perm, nbr, mask
+
+
+def subm3d_build_kmap_grouped(coords: torch.Tensor, res: int, window: int = 0,
+                              plan: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None, async_: bool = False,
+                              stream=None) -> torch.Tensor:
+    """The kernel map as a tile plan (uint8 device buffer; see plan_views). window 0 is
+    the default grouping window."""
+    N = coords.shape[0]
+    dev = coords.device
+    pc = _dev(coords, "coords", torch.int32, (N, 4))
+    if plan is None:
+        plan = torch.empty(max(subm3d_plan_bytes(N), 256), dtype=torch.uint8, device=dev)
+    pp = _dev(plan, "plan", torch.uint8)
+    need = subm3d_kmap_grouped_workspace_bytes(N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    pw = _dev(workspace, "workspace", torch.uint8)
+    _check(lib().subm3d_build_kmap_grouped(pc, N, int(res), int(window), pp, plan.numel(), pw,
+                                           workspace.numel(), KMAP_ASYNC if async_ else 0,
+                                           _stream(stream)))
+    return plan
+
+
+def subm3d_forward_grouped(feats: torch.Tensor, plan: torch.Tensor, weight: torch.Tensor,
+                           bias: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                           act: str = "none", out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """subm3d_forward_ex on a tile plan from subm3d_build_kmap_grouped (same voxels)."""
+    if feats.dtype not in _DTYPES:
+        raise ValueError(f"feats dtype {feats.dtype} is not float32 or bfloat16")
+    if act not in ACTIVATIONS:
+        raise ValueError(f"act {act!r} is not one of {sorted(ACTIVATIONS)}")
+    N, I = feats.shape
+    O = weight.shape[0]
+    pf = _dev(feats, "feats")
+    pp = _dev(plan, "plan", torch.uint8)
+    if plan.numel() < subm3d_plan_bytes(N):
+        raise ValueError(f"plan has {plan.numel()} bytes, a plan for N={N} needs "
+                         f"{subm3d_plan_bytes(N)}")
+    pw = _dev(weight, "weight", feats.dtype, (O, 3, 3, 3, I))
+    pb = None if bias is None else _dev(bias, "bias", feats.dtype, (O,))
+    pr = None if residual is None else _dev(residual, "residual", feats.dtype, (N, O))
+    if out is None:
+        out = torch.empty((N, O), dtype=feats.dtype, device=feats.device)
+    po = _dev(out, "out", feats.dtype, (N, O))
+    _check(lib().subm3d_forward_grouped(pf, pp, pw, pb, pr, ACTIVATIONS[act], po, N, I, O,
+                                        _DTYPES[feats.dtype], _stream(stream)))
+    return out
 
 
 def subm3d_forward(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tensor,
@@ -308,6 +415,22 @@ def subm3d_channel2spatial(coarse_feats: torch.Tensor, coords: torch.Tensor, par
     _check(lib().subm3d_channel2spatial(pcf, pc, pp, N, M, C, _DTYPES[coarse_feats.dtype], po,
                                         _stream(stream)))
     return out
+
+
+def subm3d_kmap_stage_timing(enable: bool) -> None:
+    """Turns the per-stage event recording of kernel-map builds on or off (this thread)."""
+    lib().subm3d_kmap_stage_timing(1 if enable else 0)
+
+
+def subm3d_kmap_stage_times() -> list:
+    """[(stage name, GPU ms)] of this thread's last kernel-map build made with stage
+    timing on (waits for its events)."""
+    ms = (ctypes.c_float * 40)()
+    names = (ctypes.c_char_p * 40)()
+    n = lib().subm3d_kmap_stage_times(ms, names, 40)
+    if n < 0:
+        _check(n)
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
 def subm3d_forward_status(stream=None) -> None:

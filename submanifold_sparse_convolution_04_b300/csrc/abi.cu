@@ -109,29 +109,31 @@ int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t*
   return kmap_build(coords, N, res, nbr, order, hash_capacity, workspace, ws_bytes, stream);
 }
 
-int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
-                      const void* residual, subm3d_act act, void* out, int64_t N, int32_t I,
-                      int32_t O, subm3d_dtype dtype, cudaStream_t stream) {
-  clear_error();
+namespace {
+// Host-side checks and kernel choice shared by the plain and the tile-plan forward.
+int forward_dispatch(const char* fn, const void* feats, const int32_t* nbr, const void* weight,
+                     const void* bias, const void* residual, subm3d_act act, void* out, int64_t N,
+                     int32_t I, int32_t O, subm3d_dtype dtype, TilePlan plan,
+                     cudaStream_t stream) {
   if (N < 0 || N > 0x7FFFFFFFll) {
-    set_error("subm3d_forward: N=%lld outside [0, 2^31)", (long long)N);
+    set_error("%s: N=%lld outside [0, 2^31)", fn, (long long)N);
     return SUBM3D_ERR_ARG;
   }
   if (I < 1 || I > 4096 || O < 1 || O > 4096) {
-    set_error("subm3d_forward: I=%d, O=%d must lie in [1, 4096]", I, O);
+    set_error("%s: I=%d, O=%d must lie in [1, 4096]", fn, I, O);
     return SUBM3D_ERR_ARG;
   }
   if (dtype != SUBM3D_F32 && dtype != SUBM3D_BF16) {
-    set_error("subm3d_forward: unknown dtype %d", static_cast<int>(dtype));
+    set_error("%s: unknown dtype %d", fn, static_cast<int>(dtype));
     return SUBM3D_ERR_ARG;
   }
   if (act != SUBM3D_ACT_NONE && act != SUBM3D_ACT_RELU && act != SUBM3D_ACT_SILU) {
-    set_error("subm3d_forward_ex: unknown activation %d", static_cast<int>(act));
+    set_error("%s: unknown activation %d", fn, static_cast<int>(act));
     return SUBM3D_ERR_ARG;
   }
   if (N == 0) return SUBM3D_OK;
   if (!feats || !nbr || !weight || !out) {
-    set_error("subm3d_forward: NULL pointer (feats=%p nbr=%p weight=%p out=%p)", feats,
+    set_error("%s: NULL pointer (feats=%p nbr=%p weight=%p out=%p)", fn, feats,
               (const void*)nbr, weight, out);
     return SUBM3D_ERR_ARG;
   }
@@ -139,9 +141,8 @@ int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight,
                         reinterpret_cast<uintptr_t>(weight) | reinterpret_cast<uintptr_t>(out) |
                         reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(residual);
   if (any & 15) {
-    set_error("subm3d_forward: feats=%p nbr=%p weight=%p bias=%p residual=%p out=%p must be "
-              "16-byte aligned",
-              feats, (const void*)nbr, weight, bias, residual, out);
+    set_error("%s: feats=%p nbr=%p weight=%p bias=%p residual=%p out=%p must be 16-byte aligned",
+              fn, feats, (const void*)nbr, weight, bias, residual, out);
     return SUBM3D_ERR_ARG;
   }
   if (residual && residual != out) {
@@ -150,8 +151,7 @@ int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight,
     const char* r = static_cast<const char*>(residual);
     const char* q = static_cast<const char*>(out);
     if (r < q + bytes && q < r + bytes) {
-      set_error("subm3d_forward_ex: residual=%p partially overlaps out=%p (only residual == out "
-                "is allowed)",
+      set_error("%s: residual=%p partially overlaps out=%p (only residual == out is allowed)", fn,
                 residual, out);
       return SUBM3D_ERR_ARG;
     }
@@ -159,22 +159,79 @@ int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight,
   const Epilogue epi{residual, static_cast<int>(act)};
   if (dtype == SUBM3D_BF16) {
     if (I % 8 || O % 8) {
-      set_error("subm3d_forward: bf16 needs I %% 8 == 0 and O %% 8 == 0 (got I=%d, O=%d)", I, O);
+      set_error("%s: bf16 needs I %% 8 == 0 and O %% 8 == 0 (got I=%d, O=%d)", fn, I, O);
       return SUBM3D_ERR_UNSUPPORTED;
     }
     if (forward_tm_applies(feats, I, O))
       return forward_launch_tm(static_cast<const __nv_bfloat16*>(feats), nbr,
                                static_cast<const __nv_bfloat16*>(weight),
                                static_cast<const __nv_bfloat16*>(bias),
-                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, stream);
+                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, plan, stream);
     if (O <= 256)
       return forward_launch_tc(static_cast<const __nv_bfloat16*>(feats), nbr,
                                static_cast<const __nv_bfloat16*>(weight),
                                static_cast<const __nv_bfloat16*>(bias),
-                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, stream);
+                               static_cast<__nv_bfloat16*>(out), N, I, O, epi, plan, stream);
   }
-  return forward_launch_simt(feats, nbr, weight, bias, out, N, I, O, dtype, epi, stream);
+  return forward_launch_simt(feats, nbr, weight, bias, out, N, I, O, dtype, epi, plan, stream);
 }
+}  // namespace
+
+int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
+                      const void* residual, subm3d_act act, void* out, int64_t N, int32_t I,
+                      int32_t O, subm3d_dtype dtype, cudaStream_t stream) {
+  clear_error();
+  return forward_dispatch("subm3d_forward", feats, nbr, weight, bias, residual, act, out, N, I, O,
+                          dtype, TilePlan{nullptr, nullptr}, stream);
+}
+
+size_t subm3d_plan_bytes(int64_t N) {
+  if (N < 0 || N > 0x7FFFFFFFll) return 0;
+  return plan_layout(N).total;
+}
+
+size_t subm3d_kmap_grouped_workspace_bytes(int64_t N) { return kmap_grouped_workspace_bytes(N); }
+
+int subm3d_build_kmap_grouped(const int32_t* coords, int64_t N, int32_t res, int64_t window,
+                              void* plan, size_t plan_bytes, void* workspace, size_t ws_bytes,
+                              unsigned flags, cudaStream_t stream) {
+  clear_error();
+  if (flags & ~static_cast<unsigned>(SUBM3D_KMAP_ASYNC)) {
+    set_error("subm3d_build_kmap_grouped: unknown flags 0x%x", flags);
+    return SUBM3D_ERR_ARG;
+  }
+  return kmap_build_grouped(coords, N, res, window, plan, plan_bytes, workspace, ws_bytes,
+                            !(flags & SUBM3D_KMAP_ASYNC), stream);
+}
+
+int subm3d_build_kmap_async(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  clear_error();
+  return kmap_build_async(coords, N, res, nbr, workspace, ws_bytes, stream);
+}
+
+int subm3d_forward_grouped(const void* feats, const void* plan, const void* weight,
+                           const void* bias, const void* residual, subm3d_act act, void* out,
+                           int64_t N, int32_t I, int32_t O, subm3d_dtype dtype,
+                           cudaStream_t stream) {
+  clear_error();
+  if (N > 0 && (!plan || (reinterpret_cast<uintptr_t>(plan) & 255))) {
+    set_error("subm3d_forward_grouped: plan=%p must be a 256-byte aligned tile plan", plan);
+    return SUBM3D_ERR_ARG;
+  }
+  if (N < 0 || N > 0x7FFFFFFFll) {
+    set_error("subm3d_forward_grouped: N=%lld outside [0, 2^31)", (long long)N);
+    return SUBM3D_ERR_ARG;
+  }
+  const PlanLayout PL = plan_layout(N);
+  const char* pl = static_cast<const char*>(plan);
+  const TilePlan tp{N > 0 ? reinterpret_cast<const int32_t*>(pl + PL.perm) : nullptr,
+                    N > 0 ? reinterpret_cast<const uint32_t*>(pl + PL.tmask) : nullptr};
+  return forward_dispatch("subm3d_forward_grouped", feats,
+                          N > 0 ? reinterpret_cast<const int32_t*>(pl + PL.nbr) : nullptr, weight,
+                          bias, residual, act, out, N, I, O, dtype, tp, stream);
+}
+
 
 int subm3d_forward(const void* feats, const int32_t* nbr, const void* weight, const void* bias,
                    void* out, int64_t N, int32_t I, int32_t O, subm3d_dtype dtype,
@@ -224,11 +281,32 @@ int subm3d_forward_status(cudaStream_t stream) {
   SUBM3D_CUDA_TRY(cudaMemcpy(&host, word, sizeof(int), cudaMemcpyDeviceToHost));
   SUBM3D_CUDA_TRY(cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice));
   if (host == 0) return SUBM3D_OK;
-  set_error("subm3d_forward_status: device reported%s%s%s",
+  set_error("subm3d_forward_status: device reported%s%s%s%s%s%s%s%s",
             (host & kDevErrBadNbr) ? " an nbr entry outside [-1, N)" : "",
             (host & kDevErrTimeout) ? " a pipeline wait that ran out (kernel stopped early)" : "",
-            (host & kDevErrBadParent) ? " a parent entry outside [0, M)" : "");
+            (host & kDevErrBadParent) ? " a parent entry outside [0, M)" : "",
+            (host & kDevErrBadPlan) ? " a tile-plan row naming no input row" : "",
+            (host & kDevErrKmapCoord) ? " [kernel map] a coordinate outside the grid" : "",
+            (host & kDevErrKmapDup) ? " [kernel map] a duplicate coordinate" : "",
+            (host & kDevErrKmapFull) ? " [kernel map] a full hash table" : "",
+            (host & kDevErrKmapInternal) ? " [kernel map] an internal index error" : "");
+  if (host & (kDevErrKmapCoord | kDevErrKmapDup | kDevErrKmapFull | kDevErrKmapInternal)) {
+    if (host & kDevErrKmapCoord) return SUBM3D_ERR_COORD_RANGE;
+    if (host & kDevErrKmapDup) return SUBM3D_ERR_DUPLICATE;
+    if (host & kDevErrKmapFull) return SUBM3D_ERR_HASH_FULL;
+  }
   return SUBM3D_ERR_DEVICE;
+}
+
+void subm3d_kmap_stage_timing(int enable) { kmap_stage_timing(enable != 0); }
+
+int subm3d_kmap_stage_times(float* ms, const char** names, int max) {
+  clear_error();
+  if (!ms || !names || max < 0) {
+    set_error("subm3d_kmap_stage_times: ms=%p names=%p max=%d", (void*)ms, (void*)names, max);
+    return SUBM3D_ERR_ARG;
+  }
+  return kmap_stage_times(ms, names, max);
 }
 
 const char* subm3d_last_error(void) { return g_msg; }

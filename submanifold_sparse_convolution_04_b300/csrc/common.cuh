@@ -88,8 +88,40 @@ int num_sms();
 // Sets a kernel's dynamic shared-memory limit once per device.
 int set_smem_limit_once(PerDevice<bool>& done, const void* kernel, int bytes, const char* name);
 
-// Device error word of the forward and upsample kernels (bit flags below).
-enum : int { kDevErrBadNbr = 1, kDevErrTimeout = 2, kDevErrBadParent = 4 };
+// Device error word of the forward, upsample and pixel-shuffle kernels and of the
+// asynchronous kernel-map builds (bit flags below).
+enum : int {
+  kDevErrBadNbr = 1, kDevErrTimeout = 2, kDevErrBadParent = 4, kDevErrKmapCoord = 8,
+  kDevErrKmapDup = 16, kDevErrKmapFull = 32, kDevErrKmapInternal = 64, kDevErrBadPlan = 128
+};
+
+// Tile plan (subm3d_build_kmap_grouped): the caller's buffer holds, 256-byte aligned,
+//   perm      int32 [N]       plan row -> input row
+//   nbr       int32 [N, 27]   row r: the neighbour table row of input row perm[r]
+//   tile_mask uint32 [ntiles] tile t (plan rows 128 t .. 128 t + 127): bit k set when
+//                             some row of the tile has a neighbour at offset k
+constexpr int kPlanTileRows = 128;
+struct PlanLayout {
+  size_t perm, nbr, tmask, total;
+  int64_t ntiles;
+};
+inline PlanLayout plan_layout(int64_t N) {
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  PlanLayout P;
+  P.ntiles = (N + kPlanTileRows - 1) / kPlanTileRows;
+  size_t o = 0;
+  P.perm = o;  o = a256(o + sizeof(int32_t) * N);
+  P.nbr = o;   o = a256(o + sizeof(int32_t) * 27 * N);
+  P.tmask = o; o = a256(o + sizeof(uint32_t) * P.ntiles);
+  P.total = o;
+  return P;
+}
+// What the forward kernels read of a plan: perm and tile_mask NULL for the plain
+// (input-order, all offsets) path.
+struct TilePlan {
+  const int32_t* perm;
+  const uint32_t* tmask;
+};
 // Device address of the word on the current device, or NULL (message set) when it
 // cannot be had; a launcher then returns SUBM3D_ERR_CUDA without launching.
 int* forward_error_word();
@@ -102,19 +134,27 @@ struct Epilogue {
 int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
                       __nv_bfloat16* out, int64_t N, int I, int O, Epilogue epi,
-                      cudaStream_t stream);
+                      TilePlan plan, cudaStream_t stream);
 // The narrow-layer kernel (A operand in tensor memory, resident weight): I and O in
 // {16, 32, 48, 64} and feats 32-byte aligned.
 bool forward_tm_applies(const void* feats, int I, int O);
 int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
                       __nv_bfloat16* out, int64_t N, int I, int O, Epilogue epi,
-                      cudaStream_t stream);
+                      TilePlan plan, cudaStream_t stream);
 int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weight,
                         const void* bias, void* out, int64_t N, int I, int O,
-                        subm3d_dtype dtype, Epilogue epi, cudaStream_t stream);
+                        subm3d_dtype dtype, Epilogue epi, TilePlan plan, cudaStream_t stream);
 int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int32_t* order,
                int64_t hash_capacity, void* workspace, size_t ws_bytes, cudaStream_t stream);
+int kmap_build_async(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                     void* workspace, size_t ws_bytes, cudaStream_t stream);
+size_t kmap_grouped_workspace_bytes(int64_t N);
+void kmap_stage_timing(bool on);
+int kmap_stage_times(float* ms, const char** names, int max);
+int kmap_build_grouped(const int32_t* coords, int64_t N, int32_t res, int64_t window, void* plan,
+                       size_t plan_bytes, void* workspace, size_t ws_bytes, bool sync,
+                       cudaStream_t stream);
 size_t kmap_workspace_bytes(int64_t N, int64_t hash_capacity);
 size_t downsample_workspace_bytes(int64_t N);
 int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ feats
                                                      const T* __restrict__ weight,
                                                      const T* __restrict__ bias, const T* residual,
                                                      int act, T* out, int64_t N, int I, int O,
-                                                     int* err) {
+                                                     int* err, const int32_t* __restrict__ perm) {
   __shared__ float g[kRows][kChunk + 1];     // gathered rows of one step
   __shared__ float w[kChunk][kCols + 1];     // weight slice of one step
   __shared__ int32_t jt[kRows * 27];         // this block's rows of nbr
@@ -127,7 +127,14 @@ __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ feats
   const float bv = bias ? load_ro(bias + o) : 0.f;
 #pragma unroll
   for (int m = 0; m < kRowsPerThread; ++m) {
-    const int64_t i = row0 + r4 + 4 * m;
+    int64_t i = row0 + r4 + 4 * m;   // row of the tile order; with a plan, perm[i] is the output row
+    if (perm && i < N) {
+      i = __ldg(perm + i);
+      if (i < 0 || i >= N) {
+        if (ol == 0) atomicOr(err, kDevErrBadPlan);
+        continue;
+      }
+    }
     if (i < N) {
       float y = acc[m] + bv;
       if (residual) y += load_rw(residual + i * O + o);
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ feats
 
 int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weight,
                         const void* bias, void* out, int64_t N, int I, int O, subm3d_dtype dtype,
-                        Epilogue epi, cudaStream_t stream) {
+                        Epilogue epi, TilePlan plan, cudaStream_t stream) {
   const int64_t tiles = (N + kRows - 1) / kRows;
   if (tiles > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld too large for the CUDA-core kernel", (long long)N);
@@ -153,12 +160,12 @@ int forward_launch_simt(const void* feats, const int32_t* nbr, const void* weigh
     fwd_simt<float><<<grid, kThreads, 0, stream>>>(
         static_cast<const float*>(feats), nbr, static_cast<const float*>(weight),
         static_cast<const float*>(bias), static_cast<const float*>(epi.residual), epi.act,
-        static_cast<float*>(out), N, I, O, err);
+        static_cast<float*>(out), N, I, O, err, plan.perm);
   } else {
     fwd_simt<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(feats), nbr, static_cast<const __nv_bfloat16*>(weight),
         static_cast<const __nv_bfloat16*>(bias), static_cast<const __nv_bfloat16*>(epi.residual),
-        epi.act, static_cast<__nv_bfloat16*>(out), N, I, O, err);
+        epi.act, static_cast<__nv_bfloat16*>(out), N, I, O, err, plan.perm);
   }
   SUBM3D_LAUNCHED("fwd_simt");
   return SUBM3D_OK;

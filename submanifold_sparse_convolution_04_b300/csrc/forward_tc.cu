@@ -96,6 +96,45 @@ struct Params {
   int nchunks;
   int ntiles;
   int* err;
+  const int32_t* perm;             // tile plan: plan row -> output row, or NULL (identity)
+  const uint32_t* tmask;           // tile plan: offsets present per tile, or NULL (all 27)
+};
+
+// Offsets a tile runs: its plan mask (the centre always included), or all 27.
+__device__ __forceinline__ uint32_t tile_mask(const Params& p, int tile) {
+  return p.tmask ? ((__ldg(p.tmask + tile) & 0x7FFFFFFu) | (1u << 13)) : 0x7FFFFFFu;
+}
+// The i-th set bit of m.
+__device__ __forceinline__ int nth_offset(uint32_t m, int i) {
+  for (int q = 0; q < i; ++q) m &= m - 1u;
+  return __ffs(m) - 1;
+}
+
+// Walks a CTA's stages in order: stage g is step g - g0 of local tile lt, a step being
+// one (offset, channel chunk); a tile has popcount(mask) x nchunks steps.
+struct StageCursor {
+  int lt = 0;
+  uint32_t g0 = 0, steps = 0, mask = 0;
+  __device__ __forceinline__ void start(const Params& p, int ntl) {
+    lt = 0;
+    g0 = 0;
+    if (ntl > 0) {
+      mask = tile_mask(p, blockIdx.x);
+      steps = __popc(mask) * static_cast<uint32_t>(p.nchunks);
+    }
+  }
+  // Moves to stage g (never backwards); false past the CTA's last stage.
+  __device__ __forceinline__ bool seek(const Params& p, int ntl, uint32_t g) {
+    while (lt < ntl && g >= g0 + steps) {
+      g0 += steps;
+      ++lt;
+      if (lt < ntl) {
+        mask = tile_mask(p, blockIdx.x + lt * gridDim.x);
+        steps = __popc(mask) * static_cast<uint32_t>(p.nchunks);
+      }
+    }
+    return lt < ntl;
+  }
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -232,8 +271,6 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
   // tiles of this CTA: blockIdx.x + t * gridDim.x, t < ntl; stages per tile: spt
   const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                   static_cast<int>(gridDim.x);
-  const uint32_t spt = 27u * static_cast<uint32_t>(p.nchunks);
-  const uint32_t total = static_cast<uint32_t>(ntl) * spt;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -271,22 +308,26 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
     bool bad = false, aborted = false;
     uint32_t last = 0;              // one past the last stage this group issued
     int32_t jn[8];
-    if (static_cast<uint32_t>(grp) < total) {
-      const uint32_t lt = grp / spt, kc = grp - lt * spt;
-      load_rows(p, int64_t(blockIdx.x + lt * gridDim.x) * kBM, kc / p.nchunks, rsub, jn, bad);
+    // cur: this group's stage; nxt: the one after it (its rows load a stage ahead)
+    StageCursor cur, nxt;
+    cur.start(p, ntl);
+    nxt.start(p, ntl);
+    if (nxt.seek(p, ntl, grp)) {
+      const uint32_t kc = grp - nxt.g0;
+      load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM,
+                nth_offset(nxt.mask, static_cast<int>(kc / p.nchunks)), rsub, jn, bad);
     }
-    for (uint32_t g = grp; g < total; g += G) {
-      const uint32_t lt = g / spt;
-      const uint32_t kc = g - lt * spt;
+    for (uint32_t g = grp; cur.seek(p, ntl, g); g += G) {
+      const uint32_t kc = g - cur.g0;
       const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
-      const int k = static_cast<int>(kc / static_cast<uint32_t>(p.nchunks));
+      const int k = nth_offset(cur.mask, static_cast<int>(kc / static_cast<uint32_t>(p.nchunks)));
       int32_t j[8];
 #pragma unroll
       for (int m = 0; m < 8; ++m) j[m] = jn[m];
-      if (g + G < total) {   // next stage's rows: in flight while this stage is issued
-        const uint32_t lt2 = (g + G) / spt, kc2 = (g + G) - lt2 * spt;
-        load_rows(p, int64_t(blockIdx.x + lt2 * gridDim.x) * kBM, kc2 / p.nchunks, rsub, jn,
-                  bad);
+      if (nxt.seek(p, ntl, g + G)) {   // next stage's rows: in flight while this stage is issued
+        const uint32_t kc2 = g + G - nxt.g0;
+        load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM,
+                  nth_offset(nxt.mask, static_cast<int>(kc2 / p.nchunks)), rsub, jn, bad);
       }
       const uint32_t s = g % S;
       const uint32_t ph = (g / S) & 1u;
@@ -342,6 +383,8 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * C::kBufCols;
+      const uint32_t spt = __popc(tile_mask(p, blockIdx.x + t * gridDim.x)) *
+                           static_cast<uint32_t>(p.nchunks);
       for (uint32_t kc = 0; kc < spt; ++kc) {
         const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
         const uint32_t s = g % S;
@@ -377,7 +420,15 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
       const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
-      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
+      const int64_t prow = int64_t(tile) * kBM + lg * 32 + lane;   // row of the tile order
+      int64_t row = prow;                                          // output row
+      if (p.perm && prow < p.N) {
+        row = __ldg(p.perm + prow);
+        if (row < 0 || row >= p.N) {   // a plan row that names no input row: skipped
+          atomicOr(p.err, kDevErrBadPlan);
+          row = p.N;
+        }
+      }
       // the residual row travels to L2, and its first 16 bytes to registers, while this
       // warp waits for the accumulator
       const __nv_bfloat16* rrow = (p.residual && row < p.N) ? p.residual + row * p.O : nullptr;
@@ -477,7 +528,7 @@ int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) 
 
 int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv_bfloat16* weight,
                       const __nv_bfloat16* bias, __nv_bfloat16* out, int64_t N, int I, int O,
-                      Epilogue epi, cudaStream_t stream) {
+                      Epilogue epi, TilePlan plan, cudaStream_t stream) {
   const int64_t ntiles = (N + kBM - 1) / kBM;
   if (ntiles > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld too large", (long long)N);
@@ -486,7 +537,7 @@ int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
   int* err = forward_error_word();
   if (!err) return SUBM3D_ERR_CUDA;
   Params prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual), epi.act,
-             N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), err};
+             N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
   const int nmma = (O + 15) / 16 * 16;
   switch (nmma) {
 #define SUBM3D_CASE(n) \

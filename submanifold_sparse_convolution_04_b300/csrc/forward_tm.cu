@@ -88,7 +88,23 @@ struct TmParams {
   int I, O;
   int ntiles;
   int* err;
+  const int32_t* perm;             // tile plan: plan row -> output row, or NULL (identity)
+  const uint32_t* tmask;           // tile plan: offsets present per tile, or NULL (all 27)
 };
+
+// Offsets a tile runs: its plan mask (the centre always included, so that every tile
+// has a stage), or all 27 without a plan.
+__device__ __forceinline__ uint32_t tm_tile_mask(const TmParams& p, int tile) {
+  return p.tmask ? ((__ldg(p.tmask + tile) & 0x7FFFFFFu) | (1u << 13)) : 0x7FFFFFFu;
+}
+// The offsets of pair j of a tile with mask m: its (2j)-th and (2j + 1)-th set bits
+// (k1 = -1 when the pair has only one).
+__device__ __forceinline__ void tm_pair_offsets(uint32_t m, int j, int& k0, int& k1) {
+  for (int i = 0; i < 2 * j; ++i) m &= m - 1u;
+  k0 = __ffs(m) - 1;
+  m &= m - 1u;
+  k1 = m ? __ffs(m) - 1 : -1;
+}
 
 __device__ __forceinline__ uint64_t tm_sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -210,7 +226,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int ntl = (p.ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                   static_cast<int>(gridDim.x);
-  const uint32_t total = static_cast<uint32_t>(ntl) * kPairs;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -273,21 +288,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    for (uint32_t g = grp; g < total; g += kGroups) {
-      const int lt = static_cast<int>(g / kPairs);
-      const int k0 = 2 * static_cast<int>(g - static_cast<uint32_t>(lt) * kPairs);
-      const bool two = k0 + 1 < 27;
-      if (lt != cur) {   // move to tile lt's nbr block (and release the previous one)
-        if (cur >= 0) {
+    // Moves this warp's hold on the double-buffered nbr blocks forward to tile `to`,
+    // taking part in every tile on the way (a tile with fewer stages than there are
+    // groups has none for some groups): each tile's block is waited for, then released
+    // when the next one is taken, so that every block's phases see all producer warps.
+    auto advance_to = [&](int to) -> bool {
+      for (int x = cur + 1; x <= to; ++x) {
+        if (x > 0) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(nbre0 + 8 * (cur & 1));
+          if (lane == 0) mbar_arrive(nbre0 + 8 * ((x - 1) & 1));
         }
-        const bool ok = mbar_wait(nbrf0 + 8 * (lt & 1), (lt >> 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          aborted = true;
-          break;
+        const bool ok = mbar_wait(nbrf0 + 8 * (x & 1), (x >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        cur = x;
+      }
+      return true;
+    };
+    // stage g of this CTA is pair g - g0 of local tile lt (whose pairs start at g0)
+    int lt = 0;
+    uint32_t g0 = 0, tm = ntl > 0 ? tm_tile_mask(p, blockIdx.x) : 1u;
+    uint32_t np = (__popc(tm) + 1) / 2;
+    for (uint32_t g = grp;; g += kGroups) {
+      while (lt < ntl && g >= g0 + np) {
+        g0 += np;
+        ++lt;
+        if (lt < ntl) {
+          tm = tm_tile_mask(p, blockIdx.x + lt * gridDim.x);
+          np = (__popc(tm) + 1) / 2;
         }
-        cur = lt;
+      }
+      if (lt >= ntl) break;
+      int k0, k1;
+      tm_pair_offsets(tm, static_cast<int>(g - g0), k0, k1);
+      const bool two = k1 >= 0;
+      if (lt != cur && !advance_to(lt)) {
+        aborted = true;
+        break;
       }
       uint32_t v[32];
       load_row(row_index(lt, k0), v);   // in flight while the slot frees
@@ -301,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {   // the stage's weight taps into its slot
         mbar_arrive_expect_tx(afull0 + 8 * s, (two ? 2 : 1) * C::kTapBytes);
         tma_load_3d(sW + s * 2 * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k0, 0);
-        if (two) tma_load_3d(sW + (s * 2 + 1) * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k0 + 1, 0);
+        if (two) tma_load_3d(sW + (s * 2 + 1) * C::kTapBytes, &wmap, afull0 + 8 * s, 0, k1, 0);
       }
       last = g + kGroups;
       tc_fence_after();
@@ -309,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(taddr, v);
       if (two) {
         tmem_st_wait();   // v is free again
-        load_row(row_index(lt, k0 + 1), v);
+        load_row(row_index(lt, k1), v);
         tmem_st32(taddr + kOffCols, v);
       }
       tmem_st_wait();
@@ -317,6 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(afull0 + 8 * s);
     }
+    // the tiles after this group's last stage: taken and released like the others, so
+    // that the loader warp can refill their buffers
+    if (!aborted && cur < ntl - 1 && !advance_to(ntl - 1)) aborted = true;
     if (bad) atomicOr(p.err, kDevErrBadNbr);
     if (aborted && lane == 0) {
       *abort_flag = 1;
@@ -380,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * kAccCols;
-      for (int pr = 0; pr < kPairs; ++pr, ++g) {
+      const int noff = __popc(tm_tile_mask(p, blockIdx.x + t * gridDim.x));
+      const int npairs = (noff + 1) / 2;
+      for (int pr = 0; pr < npairs; ++pr, ++g) {
         const uint32_t s = g % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(afull0 + 8 * s, (g / kStages) & 1u, abort_flag))) {
           aborted = true;
@@ -390,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = tmem_base + kAColBase + s * kStageCols;
         const uint64_t b = w0 + static_cast<uint64_t>(2 * s) * (C::kTapBytes >> 4);
         tm_mma_stage(d_tmem, a, b, idesc, ksteps, pr == 0 ? 0u : 1u);
-        if (2 * pr + 1 < 27)
+        if (2 * pr + 1 < noff)
           tm_mma_stage(d_tmem, a + kOffCols, b + (C::kTapBytes >> 4), idesc, ksteps, 1u);
         tm_commit(aempty0 + 8 * s);
       }
@@ -412,7 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
       const uint32_t use = t >> 1;
-      const int64_t row = int64_t(tile) * kBM + lg * 32 + lane;
+      const int64_t prow = int64_t(tile) * kBM + lg * 32 + lane;   // row of the tile order
+      int64_t row = prow;                                          // output row
+      if (p.perm && prow < p.N) {
+        row = __ldg(p.perm + prow);
+        if (row < 0 || row >= p.N) {   // a plan row that names no input row: skipped
+          atomicOr(p.err, kDevErrBadPlan);
+          row = p.N;
+        }
+      }
       // the residual row travels to L2, and its first 16 bytes to registers, while this
       // warp waits for the accumulator
       const __nv_bfloat16* rrow = (p.residual && row < p.N) ? p.residual + row * p.O : nullptr;
@@ -517,7 +566,7 @@ bool forward_tm_applies(const void* feats, int I, int O) {
 
 int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv_bfloat16* weight,
                       const __nv_bfloat16* bias, __nv_bfloat16* out, int64_t N, int I, int O,
-                      Epilogue epi, cudaStream_t stream) {
+                      Epilogue epi, TilePlan plan, cudaStream_t stream) {
   const int64_t ntiles = (N + kBM - 1) / kBM;
   if (ntiles > 0x7FFFFFFFll) {
     set_error("subm3d_forward: N=%lld too large", (long long)N);
@@ -526,7 +575,7 @@ int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
   int* err = forward_error_word();
   if (!err) return SUBM3D_ERR_CUDA;
   TmParams prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual),
-               epi.act, N, I, O, static_cast<int>(ntiles), err};
+               epi.act, N, I, O, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
   switch (O) {
     case 16: return tm_launch<16>(prm, weight, stream);
     case 32: return tm_launch<32>(prm, weight, stream);

@@ -60,6 +60,8 @@ struct KmapStatus {
   long long bad_row;
   int plan[kMaxPasses + 1];   // plan[p]: bit1 = pass active, bit0 = source buffer; plan[8] = final buffer
   int pad2;
+  int plan2[kMaxPasses + 1];  // the same for the grouping sort of the tile plan
+  int pad3;
   unsigned long long nblocks;    // occupied 4x4x4 blocks
   unsigned long long cap;        // hash capacity in use (a power of two)
   unsigned long long kmin, kmax; // smallest and largest sort key
@@ -73,16 +75,21 @@ struct __align__(16) Slot {
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table, base, total;
+  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table, base;
+  // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and each
+  // sorted position's row of the plan
+  size_t k2a, k2b, v2a, v2b, hist2, plan_pos;
+  size_t total;
   int64_t nblk;
 };
 
-Layout make_layout(int64_t N, int64_t cap) {
+Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   Layout L;
   L.nblk = (N + kSortTile - 1) / kSortTile;
+  const size_t hist_bytes = sizeof(uint32_t) * kHistParts * kMaxPasses * 256;
   size_t o = 0;
   L.status = o; o = align256(o + sizeof(KmapStatus));
-  L.hist = o;   o = align256(o + sizeof(uint32_t) * kHistParts * kMaxPasses * 256);
+  L.hist = o;   o = align256(o + hist_bytes);
   L.mk0 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.mk1 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
@@ -90,6 +97,15 @@ Layout make_layout(int64_t N, int64_t cap) {
   L.cnt = o;    o = align256(o + sizeof(uint32_t) * 256 * L.nblk);
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
   L.base = o;   o = align256(o + sizeof(int32_t) * cap);
+  L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.plan_pos = 0;
+  if (grouped) {
+    L.k2a = o;      o = align256(o + sizeof(uint64_t) * N);
+    L.k2b = o;      o = align256(o + sizeof(uint64_t) * N);
+    L.v2a = o;      o = align256(o + sizeof(int32_t) * N);
+    L.v2b = o;      o = align256(o + sizeof(int32_t) * N);
+    L.hist2 = o;    o = align256(o + hist_bytes);
+    L.plan_pos = o; o = align256(o + sizeof(int32_t) * N);
+  }
   L.total = o;
   return L;
 }
@@ -121,21 +137,24 @@ __device__ __forceinline__ unsigned long long mix64(unsigned long long v) {
 }
 
 // 1. ------------------------------------------------------------------------------
-__global__ void kmap_init(KmapStatus* st, uint32_t* hist) {
+__global__ void kmap_init(KmapStatus* st, uint32_t* hist, uint32_t* hist2) {
   const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   if (tid == 0) {
     st->flags = 0;
     st->pad = 0;
     st->bad_row = 0x7FFFFFFFFFFFFFFFll;
-    for (int p = 0; p <= kMaxPasses; ++p) st->plan[p] = 0;
-    st->pad2 = 0;
+    for (int p = 0; p <= kMaxPasses; ++p) st->plan[p] = st->plan2[p] = 0;
+    st->pad2 = st->pad3 = 0;
     st->nblocks = 0;
     st->cap = 0;
     st->kmin = ~0ull;
     st->kmax = 0;
   }
-  for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) hist[i] = 0;
+  for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) {
+    hist[i] = 0;
+    if (hist2) hist2[i] = 0;
+  }
 }
 
 // 2. ------------------------------------------------------------------------------
@@ -187,12 +206,18 @@ __global__ void kmap_plan(int npass, KmapStatus* st) {
   st->plan[kMaxPasses] = buf;
 }
 
+// The grouping sort of the tile plan runs every one of its npass passes.
+__global__ void kmap_plan2(int npass, KmapStatus* st) {
+  for (int p = 0; p < kMaxPasses; ++p) st->plan2[p] = p < npass ? (2 | (p & 1)) : 0;
+  st->plan2[kMaxPasses] = npass & 1;
+}
+
 // 4a. per-block digit counts, digit-major: cnt[d * nblk + blk] -------------------------
 __global__ void __launch_bounds__(kSortThreads) kmap_sort_count(
     const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
     int64_t N, int pass, int64_t nblk, uint32_t* __restrict__ cnt, uint32_t* __restrict__ hist,
-    const KmapStatus* st) {
-  const int plan = st->plan[pass];
+    const int* plans) {
+  const int plan = plans[pass];
   if (!(plan & 2)) return;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
   __shared__ uint32_t sh[256];
@@ -236,8 +261,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan256(uint32_t x, uint32_t
 // 4b. one block per digit: exclusive scan over blocks plus the digit's base --------
 __global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict__ hist, int pass,
                                                       int64_t nblk, uint32_t* __restrict__ cnt,
-                                                      const KmapStatus* st) {
-  if (!(st->plan[pass] & 2)) return;
+                                                      const int* plans) {
+  if (!(plans[pass] & 2)) return;
   const int d = blockIdx.x;
   __shared__ uint32_t tmp[8];
   uint32_t total;
@@ -264,8 +289,8 @@ __global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict
 // addresses of one digit's run.
 __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     unsigned long long* mk0, unsigned long long* mk1, int32_t* ix0, int32_t* ix1, int64_t N,
-    int pass, int64_t nblk, const uint32_t* __restrict__ cnt, KmapStatus* st) {
-  const int plan = st->plan[pass];
+    int pass, int64_t nblk, const uint32_t* __restrict__ cnt, const int* plans, KmapStatus* st) {
+  const int plan = plans[pass];
   if (!(plan & 2)) return;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
   unsigned long long* dst = (plan & 1) ? mk0 : mk1;
@@ -464,14 +489,23 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 }
 
 // 8. ------------------------------------------------------------------------------
-// One thread per voxel, in input order. Along each axis the three neighbour
-// coordinates fall in the voxel's own 4-block or, when the voxel sits on the block's
-// low (high) face, partly in the block below (above); so the 27 neighbours lie in
-// at most 2 x 2 x 2 blocks, looked up once each (about 3.4 per voxel on a shell) and
-// kept in shared memory. Each of the 27 offsets is then a bit test, a popcount and
-// one load of the input row at the sorted position. A block's 128 rows of results
-// are staged in shared memory and written out as one contiguous stretch of nbr.
-constexpr int kProbeThreads = 128;
+// Warp-cooperative probe over the sorted order. A warp takes 32 consecutive sorted
+// positions and handles every block run that starts among them (a run may go on past
+// them). For a run, lanes 0..26 each look up one of the 27 blocks around the run's
+// block (lane k: block offset (k / 9 - 1, k / 3 % 3 - 1, k % 3 - 1)), so every
+// neighbour of every voxel of the run lies in a block one of the lanes holds. Then,
+// voxel by voxel, lane k resolves the voxel's neighbour at offset k: a table indexed by
+// the voxel's place inside its block (the low 6 bits of its Morton code) gives the
+// lane that holds the neighbour's block and the neighbour's bit there; that lane's
+// mask and first sorted position come over by shuffles; a bit test and a popcount
+// give the neighbour's sorted position, and the input row there is the answer.
+// Depending on the mode the warp then writes
+//   kProbeNbr   the voxel's row of nbr (lanes 0..26: 108 contiguous bytes) at its input row;
+//   kProbeMask  its 27-bit presence mask (a ballot over the lanes) as a grouping key
+//               (window << 27 | mask) with its sorted position as the value;
+//   kProbePlan  its row of nbr at its row of the tile plan.
+enum ProbeMode { kProbeNbr = 0, kProbeMask = 1, kProbePlan = 2 };
+constexpr int kProbeThreads = 256;
 
 __device__ __forceinline__ void block_lookup(const Slot* __restrict__ table,
                                              const int32_t* __restrict__ base,
@@ -495,89 +529,173 @@ __device__ __forceinline__ void block_lookup(const Slot* __restrict__ table,
   full = true;
 }
 
+// Morton place (bit t of x -> 3t, y -> 3t+1, z -> 3t+2) of (z, y, x) inside a 4x4x4 block.
+__host__ __device__ __forceinline__ int place_in_block(int z, int y, int x) {
+  return (x & 1) | ((y & 1) << 1) | ((z & 1) << 2) | ((x & 2) << 2) | ((y & 2) << 3) |
+         ((z & 2) << 4);
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
-    const int4* __restrict__ coords, const int32_t* __restrict__ ix0,
+    const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
+    const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
     const int32_t* __restrict__ ix1, int64_t N, int res, const Slot* __restrict__ table,
-    const int32_t* __restrict__ base, int32_t* __restrict__ nbr, KmapStatus* st) {
-  __shared__ unsigned long long s_mask[8][kProbeThreads];
-  __shared__ int32_t s_start[8][kProbeThreads];
-  __shared__ __align__(16) int32_t s_out[kProbeThreads * 27];
+    const int32_t* __restrict__ base, int32_t* __restrict__ nbr,
+    const int32_t* __restrict__ plan_pos, unsigned long long* __restrict__ key2,
+    int32_t* __restrict__ val2, int window_shift, KmapStatus* st) {
+  // tbl[p][lane] = (lane holding the block of the neighbour at offset `lane` of a voxel
+  // at place p) << 8 | (that neighbour's place in its block); lanes 27..31 repeat the
+  // centre and write nothing
+  __shared__ uint16_t tbl[64 * 32];
+  for (int e = threadIdx.x; e < 64 * 32; e += kProbeThreads) {
+    const int p = e >> 5, l = e & 31, k = l < 27 ? l : 13;
+    const int lz = ((p >> 2) & 1) | ((p >> 4) & 2), ly = ((p >> 1) & 1) | ((p >> 3) & 2),
+              lx = (p & 1) | ((p >> 2) & 2);
+    const int nz = lz + k / 9 - 1, ny = ly + (k / 3) % 3 - 1, nx = lx + k % 3 - 1;
+    const int kb = 9 * ((nz >> 2) + 1) + 3 * ((ny >> 2) + 1) + ((nx >> 2) + 1);
+    tbl[e] = static_cast<uint16_t>((kb << 8) | place_in_block(nz & 3, ny & 3, nx & 3));
+  }
+  __syncthreads();
   const bool second = st->plan[kMaxPasses] & 1;
+  const unsigned long long* mk = second ? mk1 : mk0;
   const int32_t* ix = second ? ix1 : ix0;
-  const unsigned long long cap = st->cap;
-  const unsigned long long cmask = cap - 1;
-  const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
-  const int t = threadIdx.x;
+  const unsigned long long cmask = st->cap - 1;
+  const int max_probe = st->cap < kMaxProbe ? static_cast<int>(st->cap) : kMaxProbe;
+  const int lane = threadIdx.x & 31;
+  const int kk = lane < 27 ? lane : 13;
+  const int dz = kk / 9 - 1, dy = (kk / 3) % 3 - 1, dx = kk % 3 - 1;
+  const int bmax = (res - 1) >> 2;   // largest block coordinate along an axis
+  constexpr unsigned kAll = 0xffffffffu;
   bool full = false, bad = false;
-  for (int64_t v0 = blockIdx.x * int64_t(kProbeThreads); v0 < N;
-       v0 += int64_t(gridDim.x) * kProbeThreads) {
-    const int64_t i = v0 + t;
-    if (i < N) {
-      const int4 c = coords[i];   // (b, z, y, x)
-      const int z = c.y, y = c.z, x = c.w;
-      // direction of the second block along each axis (0: none needed)
-      const int oz = ((z & 3) == 0 && z > 0) ? -1 : ((z & 3) == 3 && z + 1 < res) ? 1 : 0;
-      const int oy = ((y & 3) == 0 && y > 0) ? -1 : ((y & 3) == 3 && y + 1 < res) ? 1 : 0;
-      const int ox = ((x & 3) == 0 && x > 0) ? -1 : ((x & 3) == 3 && x + 1 < res) ? 1 : 0;
-#pragma unroll
-      for (int combo = 0; combo < 8; ++combo) {
-        const int sz = combo >> 2, sy = (combo >> 1) & 1, sx = combo & 1;
-        if ((sz && !oz) || (sy && !oy) || (sx && !ox)) continue;
-        const unsigned long long key =
-            block_key(c.x, z + 4 * sz * oz, y + 4 * sy * oy, x + 4 * sx * ox);
-        unsigned long long m;
-        int32_t st0;
-        block_lookup(table, base, key, cmask, max_probe, m, st0, full);
-        s_mask[combo][t] = m;
-        s_start[combo][t] = st0;
+  const int64_t nwarps = (int64_t(gridDim.x) * kProbeThreads) >> 5;
+  for (int64_t w = (blockIdx.x * int64_t(kProbeThreads) + threadIdx.x) >> 5; w * 32 < N;
+       w += nwarps) {
+    const int64_t s = w * 32 + lane;
+    const unsigned long long m = s < N ? mk[s] : ~0ull;
+    unsigned long long prev = __shfl_up_sync(kAll, m, 1);
+    if (lane == 0) prev = s > 0 ? mk[s - 1] : ~0ull;
+    unsigned starts = __ballot_sync(kAll, s < N && (s == 0 || (prev >> 6) != (m >> 6)));
+    while (starts) {
+      const int j0 = __ffs(starts) - 1;
+      starts &= starts - 1;
+      const int64_t s0 = w * 32 + j0;
+      const unsigned long long blk = __shfl_sync(kAll, m, j0) >> 6;
+      const int32_t v0 = __ldg(ix + s0);
+      if (static_cast<uint64_t>(v0) >= static_cast<uint64_t>(N)) {   // flagged by blocks_count
+        bad = true;
+        continue;
       }
-      // per axis and step d in {-1, 0, 1}: is the coordinate inside the grid, which of
-      // the two blocks along the axis holds it (its bit of the block selector), and its
-      // share of the Morton place inside the block
-      bool vz[3], vy[3], vx[3];
-      uint32_t cz[3], cy[3], cx[3], bz[3], by[3], bx[3];
-#pragma unroll
-      for (int d = 0; d < 3; ++d) {
-        const int zz = z + d - 1, yy = y + d - 1, xx = x + d - 1;
-        vz[d] = static_cast<unsigned>(zz) < static_cast<unsigned>(res);
-        vy[d] = static_cast<unsigned>(yy) < static_cast<unsigned>(res);
-        vx[d] = static_cast<unsigned>(xx) < static_cast<unsigned>(res);
-        cz[d] = (d != 1 && d - 1 == oz) ? 4u : 0u;
-        cy[d] = (d != 1 && d - 1 == oy) ? 2u : 0u;
-        cx[d] = (d != 1 && d - 1 == ox) ? 1u : 0u;
-        bz[d] = ((zz & 1) << 2) | (((zz >> 1) & 1) << 5);
-        by[d] = ((yy & 1) << 1) | (((yy >> 1) & 1) << 4);
-        bx[d] = (xx & 1) | (((xx >> 1) & 1) << 3);
+      const int4 c = __ldg(coords + v0);   // (b, z, y, x) of the run's first voxel
+      unsigned long long bm = 0;
+      int32_t bb = 0;
+      if (lane < 27) {
+        const int nz = (c.y >> 2) + dz, ny = (c.z >> 2) + dy, nx = (c.w >> 2) + dx;
+        if (nz >= 0 && ny >= 0 && nx >= 0 && nz <= bmax && ny <= bmax && nx <= bmax)
+          block_lookup(table, base, block_key(c.x, nz << 2, ny << 2, nx << 2), cmask, max_probe,
+                       bm, bb, full);
       }
-#pragma unroll
-      for (int k = 0; k < 27; ++k) {
-        const int dz = k / 9, dy = (k / 3) % 3, dx = k % 3;
-        int32_t val = -1;
-        if (vz[dz] && vy[dy] && vx[dx]) {
-          const uint32_t combo = cz[dz] | cy[dy] | cx[dx];
-          const uint32_t bit = bz[dz] | by[dy] | bx[dx];
-          const unsigned long long m = s_mask[combo][t];
-          if ((m >> bit) & 1ull) {
-            const uint32_t pos = static_cast<uint32_t>(s_start[combo][t]) +
-                                 static_cast<uint32_t>(__popcll(m & ((1ull << bit) - 1ull)));
-            if (pos < static_cast<uint64_t>(N)) val = __ldg(ix + pos);
-            else bad = true;
+      const uint32_t bm_lo = static_cast<uint32_t>(bm), bm_hi = static_cast<uint32_t>(bm >> 32);
+      // the run's voxels, 32 sorted positions at a time (a run without duplicates holds
+      // at most 64 voxels; duplicates, flagged by blocks_count, only make it longer)
+      for (int64_t c0 = s0;; c0 += 32) {
+        const int64_t sj = c0 + lane;
+        const unsigned long long mj = sj < N ? mk[sj] : ~0ull;
+        const unsigned inrun = __ballot_sync(kAll, sj < N && (mj >> 6) == blk);
+        const int len = inrun == kAll ? 32 : __ffs(~inrun) - 1;
+        int32_t orow = -1;   // lane j: the row voxel c0 + j is written to
+        if (MODE == kProbeNbr && lane < len) orow = __ldg(ix + sj);
+        if (MODE == kProbePlan && lane < len) orow = __ldg(plan_pos + sj);
+        uint32_t my_mask = 0;
+#pragma unroll 2
+        for (int j = 0; j < len; ++j) {
+          const uint32_t p = __shfl_sync(kAll, static_cast<uint32_t>(mj), j) & 63u;
+          const uint32_t e = tbl[p * 32 + lane];
+          const int kb = static_cast<int>(e >> 8);
+          const uint32_t bit = e & 63u;
+          const uint32_t lo = __shfl_sync(kAll, bm_lo, kb);
+          const uint32_t hi = __shfl_sync(kAll, bm_hi, kb);
+          const int32_t bs = __shfl_sync(kAll, bb, kb);
+          const uint32_t word = bit < 32 ? lo : hi;
+          const uint32_t b5 = bit & 31u;
+          const bool present = lane < 27 && ((word >> b5) & 1u);
+          if (MODE == kProbeMask) {
+            const unsigned pm = __ballot_sync(kAll, present) & 0x7FFFFFFu;
+            if (lane == j) my_mask = pm;
+          } else {
+            int32_t val = -1;
+            if (present) {
+              const uint32_t below =
+                  __popc(word & ((1u << b5) - 1u)) + (bit >= 32 ? __popc(lo) : 0u);
+              const int64_t pos = int64_t(bs) + below;
+              if (pos < N) val = __ldg(ix + pos);
+              else bad = true;
+            }
+            const int32_t r = __shfl_sync(kAll, orow, j);
+            if (lane < 27 && static_cast<uint64_t>(r) < static_cast<uint64_t>(N))
+              nbr[int64_t(r) * 27 + lane] = val;
           }
         }
-        s_out[t * 27 + k] = val;
+        if (MODE == kProbeMask && lane < len) {
+          key2[sj] = (static_cast<unsigned long long>(sj >> window_shift) << 27) | my_mask;
+          val2[sj] = static_cast<int32_t>(sj);
+        }
+        if (len < 32) break;
       }
     }
+  }
+  if (__any_sync(kAll, full) && lane == 0) atomicOr(&st->flags, kFlagFull);
+  if (__any_sync(kAll, bad) && lane == 0) atomicOr(&st->flags, kFlagInternal);
+}
+
+// The tile plan from the grouping sort, a block of 128 threads per tile: plan row r is
+// the voxel at sorted position s = v2[r] (grouping key k2[r] = window << 27 | mask);
+// plan_pos[s] = r, perm[r] = its input row, and the tile's offset mask is the OR of its
+// rows' presence masks (the centre offset always included).
+__global__ void __launch_bounds__(128) kmap_plan_index(
+    const unsigned long long* __restrict__ k2a, const unsigned long long* __restrict__ k2b,
+    const int32_t* __restrict__ v2a, const int32_t* __restrict__ v2b,
+    const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int64_t ntiles,
+    int32_t* __restrict__ plan_pos, int32_t* __restrict__ perm, uint32_t* __restrict__ tmask,
+    KmapStatus* st) {
+  const bool sec2 = st->plan2[kMaxPasses] & 1;
+  const unsigned long long* k2 = sec2 ? k2b : k2a;
+  const int32_t* v2 = sec2 ? v2b : v2a;
+  const int32_t* ix = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
+  __shared__ uint32_t wm[4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  bool bad = false;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r = t * 128 + threadIdx.x;
+    uint32_t m = 0;
+    if (r < N) {
+      const int32_t sp = v2[r];
+      if (static_cast<uint64_t>(sp) < static_cast<uint64_t>(N)) {
+        plan_pos[sp] = static_cast<int32_t>(r);
+        perm[r] = ix[sp];
+        m = static_cast<uint32_t>(k2[r]) & 0x7FFFFFFu;
+      } else {
+        perm[r] = -1;
+        bad = true;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
+    if (lane == 0) wm[warp] = m;
     __syncthreads();
-    const int64_t nv = (N - v0) < kProbeThreads ? (N - v0) : kProbeThreads;
-    const int nwords = static_cast<int>(nv) * 27;
-    int4* dst4 = reinterpret_cast<int4*>(nbr + v0 * 27);   // v0 * 108 bytes: 16-byte aligned
-    const int4* src4 = reinterpret_cast<const int4*>(s_out);
-    for (int w = t; w < nwords / 4; w += kProbeThreads) dst4[w] = src4[w];
-    for (int w = (nwords / 4) * 4 + t; w < nwords; w += kProbeThreads) nbr[v0 * 27 + w] = s_out[w];
+    if (threadIdx.x == 0) tmask[t] = wm[0] | wm[1] | wm[2] | wm[3] | (1u << 13);
     __syncthreads();
   }
-  if (full) atomicOr(&st->flags, kFlagFull);
   if (bad) atomicOr(&st->flags, kFlagInternal);
+}
+
+// Folds the build's status into the device error word (asynchronous builds).
+__global__ void kmap_report(const KmapStatus* st, int* err) {
+  const int f = st->flags;
+  int bits = 0;
+  if (f & kFlagCoord) bits |= kDevErrKmapCoord;
+  if (f & kFlagDup) bits |= kDevErrKmapDup;
+  if (f & kFlagFull) bits |= kDevErrKmapFull;
+  if (f & kFlagInternal) bits |= kDevErrKmapInternal;
+  if (bits) atomicOr(err, bits);
 }
 
 int grid_for(int64_t work, int threads, int per_sm) {
@@ -589,6 +707,51 @@ int grid_for(int64_t work, int threads, int per_sm) {
 // Validate + pack (Morton keys, batch above them) and the stable LSD radix sort of
 // (key, input row), shared by the kernel map and the downsample. Leaves the status
 // word's plan saying which of (mk0, ix0) / (mk1, ix1) holds the sorted result.
+// Stage timing of the kernel-map builds (subm3d_kmap_stage_timing): while enabled on a
+// host thread, each build on that thread records a CUDA event on its stream before its
+// first stage and after each stage, so that subm3d_kmap_stage_times can report the GPU
+// time of every stage of the last build. Off by default; recording events adds no
+// synchronisation.
+struct StageTimer {
+  static constexpr int kMax = 40;
+  bool on = false;
+  int n = 0;
+  cudaEvent_t ev[kMax] = {};
+  const char* name[kMax] = {};
+  void begin(cudaStream_t stream) {
+    n = 0;
+    mark("start", stream);
+  }
+  void mark(const char* what, cudaStream_t stream) {
+    if (!on || n >= kMax) return;
+    if (!ev[n] && cudaEventCreate(&ev[n]) != cudaSuccess) return;
+    if (cudaEventRecord(ev[n], stream) != cudaSuccess) return;
+    name[n++] = what;
+  }
+};
+thread_local StageTimer g_stage;
+
+// The count / scan / scatter passes of a stable LSD radix sort of (u64 key, i32 value)
+// pairs ping-ponging between (k0, v0) and (k1, v1); plans[p] (device) says whether pass p
+// runs and which buffer it reads, plans[kMaxPasses] which one holds the result.
+int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, int32_t* v1,
+                 int64_t N, int npass, uint32_t* hist, uint32_t* cnt, int64_t nblk,
+                 const int* plans, KmapStatus* st, cudaStream_t stream,
+                 const char* stage = "sort pass") {
+  const int grid = static_cast<int>(nblk);
+  for (int p = 0; p < npass; ++p) {
+    kmap_sort_count<<<grid, kSortThreads, 0, stream>>>(k0, k1, N, p, nblk, cnt, hist, plans);
+    SUBM3D_LAUNCHED("kmap_sort_count");
+    kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, nblk, cnt, plans);
+    SUBM3D_LAUNCHED("kmap_sort_scan");
+    kmap_sort_scatter<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, p, nblk,
+                                                                    cnt, plans, st);
+    SUBM3D_LAUNCHED("kmap_sort_scatter");
+    g_stage.mark(stage, stream);
+  }
+  return SUBM3D_OK;
+}
+
 int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* ws,
                 cudaStream_t stream) {
   static PerDevice<bool> attr_set;
@@ -605,23 +768,17 @@ int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* w
   int bits = 2;   // at least one whole 4x4x4 block level below the batch bits
   while ((1 << bits) < res) ++bits;
   const int npass = (3 * bits + 16 + 7) / 8;
-  kmap_init<<<8, 256, 0, stream>>>(st, hist);
+  uint32_t* hist2 = L.hist2 ? reinterpret_cast<uint32_t*>(ws + L.hist2) : nullptr;
+  kmap_init<<<8, 256, 0, stream>>>(st, hist, hist2);
   SUBM3D_LAUNCHED("kmap_init");
   kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, mk0, ix0, st);
   SUBM3D_LAUNCHED("kmap_pack");
   kmap_plan<<<1, 1, 0, stream>>>(npass, st);
   SUBM3D_LAUNCHED("kmap_plan");
-  const int nblk = static_cast<int>(L.nblk);
-  for (int p = 0; p < npass; ++p) {
-    kmap_sort_count<<<nblk, kSortThreads, 0, stream>>>(mk0, mk1, N, p, L.nblk, cnt, hist, st);
-    SUBM3D_LAUNCHED("kmap_sort_count");
-    kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, L.nblk, cnt, st);
-    SUBM3D_LAUNCHED("kmap_sort_scan");
-    kmap_sort_scatter<<<nblk, kSortThreads, kScatterSmem, stream>>>(mk0, mk1, ix0, ix1, N, p,
-                                                                    L.nblk, cnt, st);
-    SUBM3D_LAUNCHED("kmap_sort_scatter");
-  }
-  return SUBM3D_OK;
+  g_stage.mark("pack", stream);
+  const int* plans = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
+                                                  offsetof(KmapStatus, plan));
+  return launch_radix(mk0, mk1, ix0, ix1, N, npass, hist, cnt, L.nblk, plans, st, stream);
 }
 
 // SparseDownsample(2) / SparseUpsample(2) ------------------------------------------
@@ -948,44 +1105,71 @@ size_t kmap_workspace_bytes(int64_t N, int64_t hash_capacity) {
   return make_layout(N, cap).total;
 }
 
-int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int32_t* order,
-               int64_t hash_capacity, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+namespace {
+
+// The steps every kernel-map build shares (validate + pack, Morton sort, block runs,
+// table, insert) followed by the probe for `nbr` (input order), or, when `plan` is
+// given, by the tile plan's steps: presence masks in sorted order, the grouping sort,
+// the plan's index arrays and the probe that writes the plan's rows. With `sync` the
+// call waits for the stream and returns the device-side status; without it the status
+// is folded into the device error word (read by subm3d_forward_status) and nothing
+// waits.
+int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+             int32_t* order, int64_t hash_capacity, int64_t window, void* plan,
+             size_t plan_bytes, void* workspace, size_t ws_bytes, bool sync,
+             cudaStream_t stream) {
+  const bool grouped = plan != nullptr;
   if (N < 0 || N > 0x7FFFFFFFll) {
-    set_error("subm3d_build_kmap: N=%lld outside [0, 2^31)", (long long)N);
+    set_error("%s: N=%lld outside [0, 2^31)", fn, (long long)N);
     return SUBM3D_ERR_ARG;
   }
   if (res < 1 || res > SUBM3D_MAX_RES) {
-    set_error("subm3d_build_kmap: res=%d outside [1, %d]", res, SUBM3D_MAX_RES);
+    set_error("%s: res=%d outside [1, %d]", fn, res, SUBM3D_MAX_RES);
     return SUBM3D_ERR_ARG;
   }
   if (hash_capacity != 0 && (hash_capacity < 8 || (hash_capacity & (hash_capacity - 1)) ||
                              hash_capacity > (int64_t(1) << 40))) {
-    set_error("subm3d_build_kmap: hash_capacity=%lld is not 0 or a power of two in [8, 2^40]",
+    set_error("%s: hash_capacity=%lld is not 0 or a power of two in [8, 2^40]", fn,
               (long long)hash_capacity);
     return SUBM3D_ERR_ARG;
   }
+  if (grouped && (window < 128 || window > (int64_t(1) << 30) || (window & (window - 1)))) {
+    set_error("%s: window=%lld is not a power of two in [128, 2^30]", fn, (long long)window);
+    return SUBM3D_ERR_ARG;
+  }
   if (N == 0) return SUBM3D_OK;
-  if (!coords || !nbr || !workspace) {
-    set_error("subm3d_build_kmap: NULL pointer (coords=%p nbr=%p workspace=%p)", (const void*)coords,
-              (void*)nbr, workspace);
+  if (!coords || (!grouped && !nbr) || !workspace) {
+    set_error("%s: NULL pointer (coords=%p nbr=%p plan=%p workspace=%p)", fn, (const void*)coords,
+              (void*)nbr, plan, workspace);
     return SUBM3D_ERR_ARG;
   }
   if ((reinterpret_cast<uintptr_t>(coords) & 15) || (reinterpret_cast<uintptr_t>(nbr) & 15) ||
-      (order && (reinterpret_cast<uintptr_t>(order) & 15))) {
-    set_error("subm3d_build_kmap: coords=%p nbr=%p order=%p must be 16-byte aligned",
-              (const void*)coords, (void*)nbr, (void*)order);
+      (order && (reinterpret_cast<uintptr_t>(order) & 15)) ||
+      (reinterpret_cast<uintptr_t>(plan) & 255)) {
+    set_error("%s: coords=%p nbr=%p order=%p must be 16-byte aligned and plan=%p 256-byte aligned",
+              fn, (const void*)coords, (void*)nbr, (void*)order, plan);
+    return SUBM3D_ERR_ARG;
+  }
+  const PlanLayout PL = plan_layout(N);
+  if (grouped && plan_bytes < PL.total) {
+    set_error("%s: plan of %zu bytes, need %zu for N=%lld", fn, plan_bytes, PL.total, (long long)N);
     return SUBM3D_ERR_ARG;
   }
   const int64_t cap_max = hash_capacity > 0 ? hash_capacity : default_hash_capacity(N);
-  const Layout L = make_layout(N, cap_max);
+  const Layout L = make_layout(N, cap_max, grouped);
   if (reinterpret_cast<uintptr_t>(workspace) & 255) {
-    set_error("subm3d_build_kmap: workspace=%p must be 256-byte aligned", workspace);
+    set_error("%s: workspace=%p must be 256-byte aligned", fn, workspace);
     return SUBM3D_ERR_WORKSPACE;
   }
   if (ws_bytes < L.total) {
-    set_error("subm3d_build_kmap: workspace of %zu bytes, need %zu for N=%lld", ws_bytes, L.total,
+    set_error("%s: workspace of %zu bytes, need %zu for N=%lld", fn, ws_bytes, L.total,
               (long long)N);
     return SUBM3D_ERR_WORKSPACE;
+  }
+  int* err = nullptr;
+  if (!sync) {
+    err = forward_error_word();
+    if (!err) return SUBM3D_ERR_CUDA;
   }
   char* ws = static_cast<char*>(workspace);
   KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
@@ -997,6 +1181,7 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
   int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
 
   const int4* c4 = reinterpret_cast<const int4*>(coords);
+  g_stage.begin(stream);
   {
     const int rc = launch_sort(c4, N, res, L, ws, stream);
     if (rc != SUBM3D_OK) return rc;
@@ -1008,35 +1193,125 @@ int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int3
   kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
                                                               base, st);
   SUBM3D_LAUNCHED("kmap_blocks_insert");
-  kmap_probe<<<grid_for(N, kProbeThreads, 16), kProbeThreads, 0, stream>>>(c4, ix0, ix1, N, res,
-                                                                           table, base, nbr, st);
-  SUBM3D_LAUNCHED("kmap_probe");
+  g_stage.mark("block table", stream);
+  const int probe_grid = grid_for((N + 31) / 32 * 32, kProbeThreads, 8);
+  if (!grouped) {
+    kmap_probe<kProbeNbr><<<probe_grid, kProbeThreads, 0, stream>>>(
+        c4, mk0, mk1, ix0, ix1, N, res, table, base, nbr, nullptr, nullptr, nullptr, 0, st);
+    SUBM3D_LAUNCHED("kmap_probe");
+    g_stage.mark("probe", stream);
+  } else {
+    char* pl = static_cast<char*>(plan);
+    int32_t* perm = reinterpret_cast<int32_t*>(pl + PL.perm);
+    int32_t* pnbr = reinterpret_cast<int32_t*>(pl + PL.nbr);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(pl + PL.tmask);
+    unsigned long long* k2a = reinterpret_cast<unsigned long long*>(ws + L.k2a);
+    unsigned long long* k2b = reinterpret_cast<unsigned long long*>(ws + L.k2b);
+    int32_t* v2a = reinterpret_cast<int32_t*>(ws + L.v2a);
+    int32_t* v2b = reinterpret_cast<int32_t*>(ws + L.v2b);
+    int32_t* plan_pos = reinterpret_cast<int32_t*>(ws + L.plan_pos);
+    uint32_t* hist2 = reinterpret_cast<uint32_t*>(ws + L.hist2);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+    int wshift = 0;
+    while ((int64_t(1) << wshift) < window) ++wshift;
+    const int64_t last_window = (N - 1) >> wshift;
+    int wbits = 0;
+    while ((last_window >> wbits) != 0) ++wbits;
+    const int npass2 = (27 + wbits + 7) / 8;
+    kmap_probe<kProbeMask><<<probe_grid, kProbeThreads, 0, stream>>>(
+        c4, mk0, mk1, ix0, ix1, N, res, table, base, nullptr, nullptr, k2a, v2a, wshift, st);
+    SUBM3D_LAUNCHED("kmap_probe_mask");
+    g_stage.mark("mask probe", stream);
+    kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);
+    SUBM3D_LAUNCHED("kmap_plan2");
+    const int* plans2 = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
+                                                     offsetof(KmapStatus, plan2));
+    const int rc = launch_radix(k2a, k2b, v2a, v2b, N, npass2, hist2, cnt, L.nblk, plans2, st,
+                                stream, "grouping sort pass");
+    if (rc != SUBM3D_OK) return rc;
+    kmap_plan_index<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
+        k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, plan_pos, perm, tmask, st);
+    SUBM3D_LAUNCHED("kmap_plan_index");
+    g_stage.mark("plan index", stream);
+    kmap_probe<kProbePlan><<<probe_grid, kProbeThreads, 0, stream>>>(
+        c4, mk0, mk1, ix0, ix1, N, res, table, base, pnbr, plan_pos, nullptr, nullptr, 0, st);
+    SUBM3D_LAUNCHED("kmap_probe_plan");
+    g_stage.mark("plan probe", stream);
+  }
 
+  if (!sync) {
+    kmap_report<<<1, 1, 0, stream>>>(st, err);
+    SUBM3D_LAUNCHED("kmap_report");
+    return SUBM3D_OK;
+  }
   KmapStatus host;
   SUBM3D_CUDA_TRY(cudaMemcpyAsync(&host, st, sizeof(host), cudaMemcpyDeviceToHost, stream));
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
   if (host.flags & kFlagCoord) {
-    set_error("subm3d_build_kmap: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d",
-              host.bad_row, SUBM3D_MAX_BATCH, res);
+    set_error("%s: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d", fn, host.bad_row,
+              SUBM3D_MAX_BATCH, res);
     return SUBM3D_ERR_COORD_RANGE;
   }
   if (host.flags & kFlagInternal) {
-    set_error("subm3d_build_kmap: internal error (sort or block table produced an index outside "
-              "[0, N))");
+    set_error("%s: internal error (sort or block table produced an index outside [0, N))", fn);
     return SUBM3D_ERR_DEVICE;
   }
   if (host.flags & kFlagDup) {
-    set_error("subm3d_build_kmap: duplicate coordinate (row %lld repeats an earlier row)",
-              host.bad_row);
+    set_error("%s: duplicate coordinate (row %lld repeats an earlier row)", fn, host.bad_row);
     return SUBM3D_ERR_DUPLICATE;
   }
   if (host.flags & kFlagFull) {
-    set_error("subm3d_build_kmap: %llu occupied 4x4x4 blocks do not fit a hash capacity of %llu "
-              "within %d probes (N=%lld)",
-              host.nblocks, host.cap, kMaxProbe, (long long)N);
+    set_error("%s: %llu occupied 4x4x4 blocks do not fit a hash capacity of %llu within %d "
+              "probes (N=%lld)",
+              fn, host.nblocks, host.cap, kMaxProbe, (long long)N);
     return SUBM3D_ERR_HASH_FULL;
   }
   return SUBM3D_OK;
+}
+
+}  // namespace
+
+void kmap_stage_timing(bool on) { g_stage.on = on; }
+
+int kmap_stage_times(float* ms, const char** names, int max) {
+  const int n = g_stage.n;
+  if (n < 2) return 0;
+  SUBM3D_CUDA_TRY(cudaEventSynchronize(g_stage.ev[n - 1]));
+  int k = 0;
+  for (int i = 1; i < n && k < max; ++i, ++k) {
+    SUBM3D_CUDA_TRY(cudaEventElapsedTime(&ms[k], g_stage.ev[i - 1], g_stage.ev[i]));
+    names[k] = g_stage.name[i];
+  }
+  return k;
+}
+
+int kmap_build(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr, int32_t* order,
+               int64_t hash_capacity, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return kmap_run("subm3d_build_kmap", coords, N, res, nbr, order, hash_capacity, 0, nullptr, 0,
+                  workspace, ws_bytes, true, stream);
+}
+
+int kmap_build_async(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
+                     void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return kmap_run("subm3d_build_kmap_async", coords, N, res, nbr, nullptr, 0, 0, nullptr, 0,
+                  workspace, ws_bytes, false, stream);
+}
+
+size_t kmap_grouped_workspace_bytes(int64_t N) {
+  if (N < 0 || N > 0x7FFFFFFFll) return 0;
+  return make_layout(N, default_hash_capacity(N), true).total;
+}
+
+int kmap_build_grouped(const int32_t* coords, int64_t N, int32_t res, int64_t window, void* plan,
+                       size_t plan_bytes, void* workspace, size_t ws_bytes, bool sync,
+                       cudaStream_t stream) {
+  if (!plan && N > 0) {
+    set_error("subm3d_build_kmap_grouped: plan is NULL");
+    return SUBM3D_ERR_ARG;
+  }
+  return kmap_run("subm3d_build_kmap_grouped", coords, N, res, nullptr, nullptr, 0,
+                  window ? window : SUBM3D_GROUP_WINDOW, plan, plan_bytes,
+                  workspace, ws_bytes, sync, stream);
 }
 
 size_t downsample_workspace_bytes(int64_t N) {

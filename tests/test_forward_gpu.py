@@ -1,8 +1,9 @@
 """Forward pass on the GPU against the CPU oracle (float64), within max|err| <=
 1e-4 max|ref| (fp32) and 2e-2 max|ref| (bf16; the tests also hold bf16 to a tighter
-4e-3). Small workloads are compared on every element; the full-size workloads on
-sampled rows (tile edges, the ragged last tile, random rows), in the same launch
-configuration the benchmark times."""
+4e-3). Every workload, the full-size ones included, is compared on every output row,
+in the same launch configuration the benchmark times; sets large enough that every
+persistent CTA runs at least four tiles check the reuse of accumulators, stage slots
+and neighbour-block buffers element by element on every kernel."""
 import numpy as np
 import pytest
 import torch
@@ -50,23 +51,51 @@ def test_forward_small_workloads_every_element(dev, cfg_id):
 
 
 @pytest.mark.parametrize("cfg_id", [3, 4, 5])
-def test_forward_full_workloads_sampled(dev, cfg_id):
+def test_forward_full_workloads_every_row(dev, cfg_id):
     case = cached_case(cfg_id)
-    N = case["coords"].shape[0]
-    rows = sample_rows(N, cfg_id)
-    got = run(case, dev, rows)
+    got = run(case, dev)
     want = cpu.forward_rows(case["coords"], case["feats"], case["weight"], case["bias"],
-                            case["res"], rows=rows)
+                            case["res"])
     assert_close(got, want, case["dtype"], case["name"])
 
 
 def test_forward_shuffled_order(dev):
     case = cached_case(4, "shuffled")
-    rows = sample_rows(case["coords"].shape[0], 44, 800)
-    got = run(case, dev, rows)
+    got = run(case, dev)
     want = cpu.forward_rows(case["coords"], case["feats"], case["weight"], case["bias"],
-                            case["res"], rows=rows)
+                            case["res"])
     assert_close(got, want, "bf16", "shuffled")
+
+
+def multi_tile_case(seed, I, O, dtype, min_tiles_per_sm=4):
+    """Shells on a 256^3 grid (two batch items) with at least 148 x 128 x min_tiles_per_sm
+    voxels and a ragged last tile: every persistent CTA runs several tiles."""
+    rng = np.random.default_rng(seed)
+    res = 256
+    need = 148 * 128 * min_tiles_per_sm
+    parts = []
+    coords = np.zeros((0, 4), np.int32)
+    while coords.shape[0] < need or coords.shape[0] % 128 == 0:
+        b = len(parts) % 2
+        a = res * (0.18 + 0.12 * rng.random(3))
+        parts.append((b, ellipsoid_shell(res, res / 2 + rng.random(3), a, uniform_rotation(rng))))
+        coords = union_coords(parts, res)
+    return coords, make_values(coords.shape[0], I, O, dtype, seed)
+
+
+@pytest.mark.parametrize("I,O,dtype", [(64, 64, "bf16"), (32, 48, "bf16"), (16, 16, "bf16"),
+                                       (128, 128, "bf16"), (96, 256, "bf16"), (64, 264, "bf16"),
+                                       (32, 32, "f32")])
+def test_forward_several_tiles_per_cta_every_row(dev, I, O, dtype):
+    coords, v = multi_tile_case(I * 5 + O, I, O, dtype)
+    N = coords.shape[0]
+    assert N >= 148 * 128 * 4 and N % 128 != 0
+    mk = (lambda a: bf16_tensor(a, dev)) if dtype == "bf16" else (lambda a: torch.from_numpy(a).to(dev))
+    nbr = subm3d_build_kmap(torch.from_numpy(coords).to(dev), 256)
+    out = subm3d_forward(mk(v["feats"]), nbr, mk(v["weight"]), mk(v["bias"]))
+    subm3d_forward_status()
+    want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"], 256)
+    assert_close(out.float().cpu().numpy(), want, dtype, f"N={N} I={I} O={O}")
 
 
 def shell_case(seed, res, I, O, dtype, batch=1):

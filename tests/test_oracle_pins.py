@@ -537,3 +537,124 @@ def test_channel2spatial_errors_and_planted_bit_order(monkeypatch):
     fs = rng.standard_normal((80, 2))
     co, o2, _, _ = ref.spatial2channel(cs, fs, 6)
     assert not np.array_equal(o2, dense_unshuffle(cs, fs, 6, co))
+
+
+# ------------------------------------------------- tile plan of the grouped forward
+
+def test_morton_codes_give_z_order_and_match_the_scalar_code():
+    rng = np.random.default_rng(31)
+    c = np.concatenate([random_set(rng, 64, 2, 300),
+                        np.array([[0, 65534, 3, 40000], [1, 0, 65534, 1]], np.int32)])
+    m = ref.morton_codes(c)
+    for i in range(0, c.shape[0], 7):
+        assert int(m[i]) == ref.morton_code(int(c[i, 1]), int(c[i, 2]), int(c[i, 3]))
+    order = np.lexsort((m, c[:, 0]))
+    pts = [tuple(int(v) for v in c[i]) for i in order]
+    for p, q in zip(pts, pts[1:]):
+        assert p[0] < q[0] or (p[0] == q[0] and _morton_less(p[1:], q[1:])), (p, q)
+
+
+def test_neighbour_masks_by_hand():
+    # k = 9 (dz + 1) + 3 (dy + 1) + (dx + 1). From (5,5,5): (5,5,6) is (0,0,+1), k = 14, and
+    # (4,5,5) is (-1,0,0), k = 4. From (5,5,6): (5,5,5) is (0,0,-1), k = 12, and (4,5,5) is
+    # (-1,0,-1), k = 3. From (4,5,5): (5,5,5) is (+1,0,0), k = 22, and (5,5,6) is (+1,0,+1),
+    # k = 23. (9,9,9) is alone: the centre, k = 13, only.
+    c = np.array([[0, 5, 5, 5], [0, 5, 5, 6], [0, 4, 5, 5], [0, 9, 9, 9]], np.int32)
+    m = ref.neighbour_masks(ref.kernel_map(c, 16))
+    assert m.tolist() == [(1 << 13) | (1 << 14) | (1 << 4), (1 << 13) | (1 << 12) | (1 << 3),
+                          (1 << 13) | (1 << 22) | (1 << 23), 1 << 13]
+
+
+def _check_plan(c, nbr, window, perm, pnbr, tmask, tile=128):
+    N = c.shape[0]
+    assert sorted(perm.tolist()) == list(range(N))                        # a permutation
+    assert np.array_equal(pnbr, nbr[perm])
+    masks = ref.neighbour_masks(nbr)[perm]
+    # windows: consecutive stretches of the (batch, Z-order) sequence, each a stretch of
+    # `window` voxels -- checked with the comparator, without a Morton code
+    key = lambda i: (int(c[i, 0]),) + tuple(int(v) for v in c[i, 1:])
+    for w0 in range(0, N, window):
+        seg = perm[w0:w0 + window]
+        if w0 + window < N:   # everything in this window precedes everything after it
+            last = max(seg, key=lambda i: _zkey_rank(c, i))
+            nxt = perm[w0 + window:]
+            first_next = min(nxt, key=lambda i: _zkey_rank(c, i))
+            assert _zless(c, last, first_next), (key(last), key(first_next))
+        ms = masks[w0:w0 + window]
+        assert np.all(ms[1:] >= ms[:-1])                                    # masks ascend
+        for a, b in zip(range(len(seg) - 1), range(1, len(seg))):
+            if ms[a] == ms[b]:
+                assert _zless(c, seg[a], seg[b])                            # Z-order among ties
+    nt = (N + tile - 1) // tile
+    for t in range(nt):
+        want = 0
+        for r in range(t * tile, min(N, (t + 1) * tile)):
+            want |= int(masks[r])
+        assert int(tmask[t]) == want
+
+
+def _zless(c, i, j):
+    p, q = c[i], c[j]
+    if p[0] != q[0]:
+        return p[0] < q[0]
+    return _morton_less(tuple(int(v) for v in p[1:]), tuple(int(v) for v in q[1:]))
+
+
+_zrank_cache = {}
+
+
+def _zkey_rank(c, i):
+    # rank of row i in the comparator's (batch, Z) order, computed once per array
+    key = id(c)
+    if key not in _zrank_cache:
+        import functools
+        idx = list(range(c.shape[0]))
+        idx.sort(key=functools.cmp_to_key(lambda a, b: -1 if _zless(c, a, b) else (1 if _zless(c, b, a) else 0)))
+        _zrank_cache[key] = {v: r for r, v in enumerate(idx)}
+    return _zrank_cache[key][i]
+
+
+@pytest.mark.parametrize("window", [1, 128, 256, 1 << 20])
+def test_tile_plan_properties(window):
+    rng = np.random.default_rng(7 + window % 97)
+    from synth import ellipsoid_shell, union_coords, uniform_rotation
+    parts = [(b, ellipsoid_shell(24, (11.7, 12.2, 12.4), (8.0, 6.5, 9.5), uniform_rotation(rng)))
+             for b in range(2)]
+    c = union_coords(parts, 24)
+    c = c[rng.permutation(c.shape[0])]
+    nbr = ref.kernel_map(c, 24)
+    perm, pnbr, tmask = ref.tile_plan(c, nbr, window)
+    _check_plan(c, nbr, window, perm, pnbr, tmask)
+    _zrank_cache.clear()
+
+
+def test_tile_plan_window_one_is_z_order_and_huge_window_sorts_by_mask():
+    rng = np.random.default_rng(3)
+    c = random_set(rng, 12, 2, 150)
+    nbr = ref.kernel_map(c, 12)
+    perm1 = ref.tile_plan(c, nbr, 1)[0]
+    for a, b in zip(perm1, perm1[1:]):
+        assert _zless(c, a, b)
+    permh = ref.tile_plan(c, nbr, 1 << 30)[0]
+    assert np.all(np.diff(ref.neighbour_masks(nbr)[permh].astype(np.int64)) >= 0)
+
+
+def test_planted_unstable_grouping_is_caught(monkeypatch):
+    rng = np.random.default_rng(5)
+    from synth import ellipsoid_shell, union_coords, uniform_rotation
+    c = union_coords([(0, ellipsoid_shell(20, (9.6, 10.1, 9.8), (7.0, 8.0, 6.0),
+                                          uniform_rotation(rng)))], 20)
+    nbr = ref.kernel_map(c, 20)
+    real = np.lexsort
+
+    def unstable(keys):   # drops the Morton tie-break of the grouping sort
+        keys = tuple(keys)
+        if len(keys) == 3 and keys[0].dtype.kind == "i" and np.array_equal(keys[0], np.arange(len(keys[0]))):
+            return real((keys[0][::-1], keys[1], keys[2]))
+        return real(keys)
+    monkeypatch.setattr(np, "lexsort", unstable)
+    perm, pnbr, tmask = ref.tile_plan(c, nbr, 128)
+    monkeypatch.setattr(np, "lexsort", real)
+    with pytest.raises(AssertionError):
+        _check_plan(c, nbr, 128, perm, pnbr, tmask)
+    _zrank_cache.clear()

@@ -235,7 +235,7 @@ SUBM3D_API int subm3d_forward_grouped(const void* feats, const void* plan, const
  * which may synchronise the device, is not acceptable.
  *
  * Same result and errors as subm3d_build_kmap (coords, N, res, nbr and stream as
- * there), but the scratch space (hash table, sort buffers, status word) is a 9 MiB
+ * there), but the scratch space (hash table, sort buffers, status word) is a 16 MiB
  * array compiled into the library, so N is limited to SUBM3D_NOALLOC_MAX_VOXELS; a
  * larger N returns SUBM3D_ERR_ARG before any device work. Every GPU that loads the
  * library keeps that array until the process exits. The first call on a device looks
@@ -263,9 +263,9 @@ SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32
  *   dtype   SUBM3D_BF16: bf16 inputs, fp32 accumulation (tcgen05 tensor cores,
  *           accumulator in tensor memory), bias added in fp32, output rounded to
  *           bf16 (nearest-even). Needs I % 8 == 0 and O % 8 == 0. I and O in
- *           {16, 32, 48, 64} with feats 32-byte aligned run the narrow kernel (the
- *           gathered rows in tensor memory); other O <= 256 the kernel that stages
- *           them in shared memory; larger O the CUDA-core kernel. All three compute
+ *           {16, 32, 48, 64} run the narrow kernel (the gathered rows in tensor
+ *           memory); other O <= 256 the kernel that stages them in shared memory;
+ *           larger O the CUDA-core kernel. All three compute
  *           the same sums (fp32 accumulation order may differ between them).
  *           SUBM3D_F32: fp32 inputs and accumulation on the CUDA cores.
  *   N, I, O N >= 0 (0 is a no-op), 1 <= I, O <= 4096.

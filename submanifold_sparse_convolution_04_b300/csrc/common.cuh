@@ -135,8 +135,7 @@ int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
                       __nv_bfloat16* out, int64_t N, int I, int O, Epilogue epi,
                       TilePlan plan, cudaStream_t stream);
-// The narrow-layer kernel (A operand in tensor memory, resident weight): I and O in
-// {16, 32, 48, 64} and feats 32-byte aligned.
+// The narrow-layer kernel (A operand in tensor memory): I and O in {16, 32, 48, 64}.
 bool forward_tm_applies(const void* feats, int I, int O);
 int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr,
                       const __nv_bfloat16* weight, const __nv_bfloat16* bias,
@@ -232,6 +231,20 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// 16 bytes global -> shared, cached in L1 as well (rows that neighbouring voxels share
+// are often read again soon).
+__device__ __forceinline__ void cp_async_16_ca(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 // Arrives on `bar` (counted in its expected count) once every cp.async this thread
 // issued so far has landed in shared memory; the thread itself does not wait.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -50,7 +50,7 @@ constexpr int kSortTile = kSortThreads * kSortItems;   // keys per sort block
 constexpr int kMaxPasses = 8;
 constexpr int kMaxProbe = 4096;
 constexpr int kHistParts = 16;   // partial digit histograms (spreads the count kernel's atomics)
-constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 256 * 4;
+constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 2 * 256 * 4;
 
 enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8 };
 
@@ -67,15 +67,24 @@ struct KmapStatus {
   unsigned long long kmin, kmax; // smallest and largest sort key
 };
 
-struct __align__(16) Slot {
+struct __align__(32) Slot {
   unsigned long long key;    // packed block key, kEmptyKey when free
   unsigned long long mask;   // bit (Morton order of the voxel inside the block) per active voxel
+  unsigned long long start;  // first sorted position of the block's voxels
+  unsigned long long pad;    // (one 32-byte load brings the whole slot)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Radix-sort scratch for ntile 2048-key tiles: tile counters (256 bytes), digit starts of
+// every pass, and the published per-tile digit counts.
+__host__ __device__ inline size_t sort_scratch_bytes(int64_t ntile) {
+  return 256 + sizeof(uint32_t) * kMaxPasses * 256 +
+         sizeof(unsigned long long) * size_t(ntile) * 256;
+}
+
 struct Layout {
-  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table, base;
+  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table;
   // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and each
   // sorted position's row of the plan
   size_t k2a, k2b, v2a, v2b, hist2, plan_pos;
@@ -94,9 +103,8 @@ Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   L.mk1 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
   L.ix1 = o;    o = align256(o + sizeof(int32_t) * N);
-  L.cnt = o;    o = align256(o + sizeof(uint32_t) * 256 * L.nblk);
+  L.cnt = o;    o = align256(o + sort_scratch_bytes(L.nblk));
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
-  L.base = o;   o = align256(o + sizeof(int32_t) * cap);
   L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.plan_pos = 0;
   if (grouped) {
     L.k2a = o;      o = align256(o + sizeof(uint64_t) * N);
@@ -110,25 +118,31 @@ Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   return L;
 }
 
-// Interleaves the low `bits` bits of z, y, x: bit t of x -> 3t, of y -> 3t+1, of z -> 3t+2.
-__device__ __forceinline__ unsigned long long morton3(uint32_t z, uint32_t y, uint32_t x, int bits) {
-  unsigned long long m = 0;
-  for (int t = 0; t < bits; ++t) {
-    m |= static_cast<unsigned long long>((x >> t) & 1u) << (3 * t);
-    m |= static_cast<unsigned long long>((y >> t) & 1u) << (3 * t + 1);
-    m |= static_cast<unsigned long long>((z >> t) & 1u) << (3 * t + 2);
-  }
-  return m;
+// Bit t of v (v < 2^21) to bit 3t, and back: the usual shift-and-mask bit interleave,
+// each step moving half of the remaining bit groups apart (or together).
+__host__ __device__ __forceinline__ unsigned long long spread3(uint32_t v) {
+  unsigned long long x = v & 0x1fffffu;
+  x = (x | (x << 32)) & 0x1f00000000ffffull;
+  x = (x | (x << 16)) & 0x1f0000ff0000ffull;
+  x = (x | (x << 8)) & 0x100f00f00f00f00full;
+  x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
+  x = (x | (x << 2)) & 0x1249249249249249ull;
+  return x;
+}
+__host__ __device__ __forceinline__ uint32_t compact3(unsigned long long x) {
+  x &= 0x1249249249249249ull;
+  x = (x | (x >> 2)) & 0x10c30c30c30c30c3ull;
+  x = (x | (x >> 4)) & 0x100f00f00f00f00full;
+  x = (x | (x >> 8)) & 0x1f0000ff0000ffull;
+  x = (x | (x >> 16)) & 0x1f00000000ffffull;
+  x = (x | (x >> 32)) & 0x1fffffull;
+  return static_cast<uint32_t>(x);
+}
+// Morton code of (z, y, x): bit t of x -> 3t, of y -> 3t+1, of z -> 3t+2.
+__device__ __forceinline__ unsigned long long morton3(uint32_t z, uint32_t y, uint32_t x) {
+  return spread3(x) | (spread3(y) << 1) | (spread3(z) << 2);
 }
 
-// b << 42 | (z >> 2) << 28 | (y >> 2) << 14 | (x >> 2): 16 + 3 x 14 bits, never all ones.
-__device__ __forceinline__ unsigned long long block_key(uint32_t b, uint32_t z, uint32_t y,
-                                                        uint32_t x) {
-  return (static_cast<unsigned long long>(b & 0xFFFFu) << 42) |
-         (static_cast<unsigned long long>((z >> 2) & 0x3FFFu) << 28) |
-         (static_cast<unsigned long long>((y >> 2) & 0x3FFFu) << 14) |
-         static_cast<unsigned long long>((x >> 2) & 0x3FFFu);
-}
 
 __device__ __forceinline__ unsigned long long mix64(unsigned long long v) {
   v = (v ^ (v >> 30)) * 0xbf58476d1ce4e5b9ull;
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
       c = make_int4(0, 0, 0, 0);
     }
     const unsigned long long m =
-        (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w, bits);
+        (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w);
     mk[i] = m;
     ix[i] = static_cast<int32_t>(i);
     lo = m < lo ? m : lo;
@@ -188,7 +202,19 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
     lo = l2 < lo ? l2 : lo;
     hi = h2 > hi ? h2 : hi;
   }
+  // one pair of atomics per block (same-address atomics from every warp serialise)
+  __shared__ unsigned long long wlo[8], whi[8];
+  const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
+    wlo[warp] = lo;
+    whi[warp] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) {
+      lo = wlo[w] < lo ? wlo[w] : lo;
+      hi = whi[w] > hi ? whi[w] : hi;
+    }
     atomicMin(&st->kmin, lo);
     atomicMax(&st->kmax, hi);
   }
@@ -212,27 +238,85 @@ __global__ void kmap_plan2(int npass, KmapStatus* st) {
   st->plan2[kMaxPasses] = npass & 1;
 }
 
-// 4a. per-block digit counts, digit-major: cnt[d * nblk + blk] -------------------------
-__global__ void __launch_bounds__(kSortThreads) kmap_sort_count(
-    const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
-    int64_t N, int pass, int64_t nblk, uint32_t* __restrict__ cnt, uint32_t* __restrict__ hist,
-    const int* plans) {
-  const int plan = plans[pass];
-  if (!(plan & 2)) return;
-  const unsigned long long* src = (plan & 1) ? mk1 : mk0;
-  __shared__ uint32_t sh[256];
-  sh[threadIdx.x] = 0;
+// 4. Single-pass LSD radix sort passes (decoupled look-back, after Merrill and Garland's
+// single-pass prefix scan, 2016, as used for radix sorting by Adinets and Merrill's
+// Onesweep, 2022). Before the passes, one read of the keys gives every pass's digit
+// histogram, hence each digit's global start. A pass is then one kernel: a block takes
+// the next 2048-key tile (tile numbers handed out in start order by an atomic counter,
+// so a tile only ever waits for tiles whose blocks are already running), ranks its keys
+// per digit in shared memory, publishes its per-digit counts, and, per digit, walks back
+// over the earlier tiles' published values (a tile's own count, or the count of keys
+// in that tile and all before it) until it has the number of keys of that digit before
+// its own; it publishes that inclusive count in turn and writes each digit's run of its
+// keys contiguously. Every wait is bounded; a wait that runs out flags the build as
+// failed (internal error) and goes on with what it has.
+constexpr int kWarpsPerSort = kSortThreads / 32;
+// A published status word: (pass + 1) << 34 | kind << 32 | count. One array serves every
+// pass of a sort (it is cleared before the sort's first pass); the pass tag tells a
+// word of the current pass from one an earlier pass left.
+constexpr unsigned long long kTileAggregate = 1ull << 32;   // count of this tile only
+constexpr unsigned long long kTileInclusive = 2ull << 32;   // count through this tile
+
+struct SortScratch {          // in the workspace: counters | digit starts | tile status
+  uint32_t* counter;          // [kMaxPasses] next tile number of each pass
+  uint32_t* gofs;             // [kMaxPasses][256] first sorted position of each digit
+  unsigned long long* status; // [ntile][256] published per-digit counts (pass-tagged)
+};
+inline SortScratch sort_scratch(char* base, int64_t ntile) {
+  SortScratch S;
+  S.counter = reinterpret_cast<uint32_t*>(base);
+  S.gofs = reinterpret_cast<uint32_t*>(base + 256);
+  S.status = reinterpret_cast<unsigned long long*>(base + 256 + sizeof(uint32_t) * kMaxPasses * 256);
+  (void)ntile;
+  return S;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 4a. Digit histograms of every pass from one read of the keys (kHistParts partial
+// histograms [part][pass][digit] spread the atomics); also clears the passes' tile
+// counters and published status words.
+__global__ void __launch_bounds__(256) kmap_hist(const unsigned long long* __restrict__ keys,
+                                                 int64_t N, int npass, const int* plans,
+                                                 uint32_t* __restrict__ hist, SortScratch S,
+                                                 int64_t ntile) {
+  __shared__ uint32_t sh[kMaxPasses][256];
+  for (int i = threadIdx.x; i < kMaxPasses * 256; i += 256) sh[i >> 8][i & 255] = 0;
+  const int64_t gtid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  if (gtid < kMaxPasses) S.counter[gtid] = 0;
+  const int64_t nstat = ntile * 256;
+  for (int64_t i = gtid; i < nstat; i += stride) S.status[i] = 0;
+  unsigned active = 0;   // passes that run (a constant digit's pass is skipped)
+  for (int p = 0; p < npass; ++p)
+    if (plans[p] & 2) active |= 1u << p;
   __syncthreads();
-  const int64_t base = blockIdx.x * int64_t(kSortTile);
-  for (int r = 0; r < kSortItems; ++r) {
-    const int64_t e = base + r * kSortThreads + threadIdx.x;
-    if (e < N) atomicAdd(&sh[(src[e] >> (8 * pass)) & 255u], 1u);
+  const int lane = threadIdx.x & 31;
+  // whole warps take part in every round (warp-aggregated counts: keys of nearby rows
+  // share their high digits)
+  for (int64_t w0 = gtid - lane; w0 < N; w0 += stride) {
+    const int64_t i = w0 + lane;
+    const bool valid = i < N;
+    const unsigned long long k = valid ? keys[i] : 0ull;
+    for (int p = 0; p < npass; ++p) {
+      if (!((active >> p) & 1u)) continue;
+      const uint32_t d = valid ? static_cast<uint32_t>((k >> (8 * p)) & 255u) : 256u;
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      if (valid && lane == __ffs(peers) - 1) atomicAdd(&sh[p][d], __popc(peers));
+    }
   }
   __syncthreads();
-  const uint32_t v = sh[threadIdx.x];
-  cnt[threadIdx.x * nblk + blockIdx.x] = v;
-  // the pass's digit totals, in kHistParts partial histograms [part][pass][digit]
-  if (v) atomicAdd(&hist[((blockIdx.x % kHistParts) * kMaxPasses + pass) * 256 + threadIdx.x], v);
+  for (int p = 0; p < npass; ++p) {
+    const uint32_t v = sh[p][threadIdx.x];
+    if (v) atomicAdd(&hist[((blockIdx.x % kHistParts) * kMaxPasses + p) * 256 + threadIdx.x], v);
+  }
 }
 
 // Exclusive prefix sum of one value per thread over a 256-thread block; returns the
@@ -258,58 +342,46 @@ __device__ __forceinline__ uint32_t block_exclusive_scan256(uint32_t x, uint32_t
   return wpre + incl - x;
 }
 
-// 4b. one block per digit: exclusive scan over blocks plus the digit's base --------
-__global__ void __launch_bounds__(256) kmap_sort_scan(const uint32_t* __restrict__ hist, int pass,
-                                                      int64_t nblk, uint32_t* __restrict__ cnt,
-                                                      const int* plans) {
-  if (!(plans[pass] & 2)) return;
-  const int d = blockIdx.x;
+// 4b. One block of 256 threads: each pass's digit starts (exclusive scan of its histogram).
+__global__ void __launch_bounds__(256) kmap_digit_starts(const uint32_t* __restrict__ hist,
+                                                         int npass, SortScratch S) {
   __shared__ uint32_t tmp[8];
-  uint32_t total;
-  // base = sum of the histogram bins below d (over the partial histograms)
-  uint32_t below = 0;
-  if (threadIdx.x < static_cast<unsigned>(d))
-    for (int q = 0; q < kHistParts; ++q) below += hist[(q * kMaxPasses + pass) * 256 + threadIdx.x];
-  block_exclusive_scan256(below, tmp, &total);
-  uint32_t carry = total;
-  uint32_t* row = cnt + d * nblk;
-  for (int64_t b0 = 0; b0 < nblk; b0 += 256) {
-    const int64_t b = b0 + threadIdx.x;
-    const uint32_t x = b < nblk ? row[b] : 0u;
-    uint32_t sum;
-    const uint32_t pre = block_exclusive_scan256(x, tmp, &sum);
-    if (b < nblk) row[b] = carry + pre;
-    carry += sum;
+  for (int p = 0; p < npass; ++p) {
+    uint32_t c = 0;
+    for (int q = 0; q < kHistParts; ++q) c += hist[(q * kMaxPasses + p) * 256 + threadIdx.x];
+    uint32_t total;
+    S.gofs[p * 256 + threadIdx.x] = block_exclusive_scan256(c, tmp, &total);
   }
 }
 
-// 4c. stable scatter. A tile of 2048 keys is ranked (rank = earlier warps + earlier
-// rounds + earlier lanes with the same digit), laid out digit-sorted in shared
-// memory, then written out in that order, so consecutive threads write consecutive
-// addresses of one digit's run.
-__global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
+// 4c. One pass: rank a tile, look back for each digit's count before it, scatter.
+__global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
     unsigned long long* mk0, unsigned long long* mk1, int32_t* ix0, int32_t* ix1, int64_t N,
-    int pass, int64_t nblk, const uint32_t* __restrict__ cnt, const int* plans, KmapStatus* st) {
+    int pass, int64_t ntile, const int* plans, SortScratch S, KmapStatus* st) {
   const int plan = plans[pass];
   if (!(plan & 2)) return;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
   unsigned long long* dst = (plan & 1) ? mk0 : mk1;
   const int32_t* isrc = (plan & 1) ? ix1 : ix0;
   int32_t* idst = (plan & 1) ? ix0 : ix1;
-  constexpr int kWarps = kSortThreads / 32;
-  constexpr int kPerWarp = kSortTile / kWarps;           // 256
-  constexpr int kRounds = kPerWarp / 32;                 // 8
+  constexpr int kPerWarp = kSortTile / kWarpsPerSort;   // 256
+  constexpr int kRounds = kPerWarp / 32;                // 8
   extern __shared__ __align__(16) unsigned char sort_sm[];
   unsigned long long* skey = reinterpret_cast<unsigned long long*>(sort_sm);
   int32_t* srow = reinterpret_cast<int32_t*>(sort_sm + kSortTile * 8);
   uint32_t* wcnt = reinterpret_cast<uint32_t*>(sort_sm + kSortTile * 12);   // [kWarps][257]
-  uint32_t* loff = wcnt + kWarps * 257;                                       // [256]
+  uint32_t* loff = wcnt + kWarpsPerSort * 257;                                // [256]
+  uint32_t* gbase = loff + 256;                                               // [256]
   __shared__ uint32_t tmp[8];
+  __shared__ uint32_t s_tile;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * 257; i += kSortThreads) wcnt[i] = 0;
+  if (threadIdx.x == 0) s_tile = atomicAdd(&S.counter[pass], 1u);
+  for (int i = threadIdx.x; i < kWarpsPerSort * 257; i += kSortThreads) wcnt[i] = 0;
   __syncthreads();
+  const int64_t tile = s_tile;
+  if (tile >= ntile) return;   // more blocks than tiles: nothing to do
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t tile0 = blockIdx.x * int64_t(kSortTile);
+  const int64_t tile0 = tile * kSortTile;
   const int64_t base = tile0 + warp * kPerWarp;
   unsigned long long key[kRounds];
   int32_t row[kRounds];
@@ -320,6 +392,10 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     const bool valid = e < N;
     key[r] = valid ? src[e] : 0ull;
     row[r] = valid ? isrc[e] : 0;
+  }
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const bool valid = base + r * 32 + lane < N;
     const uint32_t d = valid ? static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u) : 256u;
     const unsigned peers = __match_any_sync(0xffffffffu, d);
     const uint32_t before = __popc(peers & lt_mask);
@@ -330,24 +406,54 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
     rank[r] = prior + before;
   }
   __syncthreads();
-  {   // per digit: exclusive over warps, then the digit's start inside the tile
-    const int d = threadIdx.x;
-    uint32_t run = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t c = wcnt[w * 257 + d];
-      wcnt[w * 257 + d] = run;
-      run += c;
-    }
+  const int d = threadIdx.x;   // this thread's digit from here on
+  uint32_t run = 0;            // keys of digit d in this tile
+  for (int w = 0; w < kWarpsPerSort; ++w) {
+    const uint32_t c = wcnt[w * 257 + d];
+    wcnt[w * 257 + d] = run;
+    run += c;
+  }
+  {
     uint32_t total;
     loff[d] = block_exclusive_scan256(run, tmp, &total);
   }
+  // publish this tile's count, then look back for the count before it
+  const unsigned long long tag = static_cast<unsigned long long>(pass + 1) << 34;
+  unsigned long long* my = S.status + tile * 256 + d;
+  uint32_t before_tile = 0;
+  if (tile == 0) {
+    st_relaxed_u64(my, tag | kTileInclusive | run);
+  } else {
+    st_relaxed_u64(my, tag | kTileAggregate | run);
+    int64_t t = tile - 1;
+    const unsigned long long t0 = global_timer_ns();
+    bool late = false;
+    for (uint32_t it = 0; t >= 0; ++it) {
+      const unsigned long long v = ld_relaxed_u64(S.status + t * 256 + d);
+      const unsigned long long flag = (v >> 34) == static_cast<unsigned long long>(pass + 1)
+                                          ? (v & (3ull << 32)) : 0ull;
+      if (flag == 0) {   // not published yet (or an earlier pass's word): wait (bounded)
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+          late = true;
+          break;
+        }
+        continue;
+      }
+      before_tile += static_cast<uint32_t>(v);
+      if (flag == kTileInclusive) break;
+      --t;
+    }
+    if (late) atomicOr(&st->flags, kFlagInternal);
+    st_relaxed_u64(my, tag | kTileInclusive | (before_tile + run));
+  }
+  gbase[d] = S.gofs[pass * 256 + d] + before_tile;
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int64_t e = base + r * 32 + lane;
     if (e < N) {
-      const uint32_t d = static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u);
-      const uint32_t local = loff[d] + wcnt[warp * 257 + d] + rank[r];
+      const uint32_t dd = static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u);
+      const uint32_t local = loff[dd] + wcnt[warp * 257 + dd] + rank[r];
       skey[local] = key[r];
       srow[local] = row[r];
     }
@@ -356,8 +462,8 @@ __global__ void __launch_bounds__(kSortThreads) kmap_sort_scatter(
   const int nvalid = static_cast<int>((N - tile0) < kSortTile ? (N - tile0) : kSortTile);
   for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
     const unsigned long long k = skey[i];
-    const uint32_t d = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
-    const int64_t pos = int64_t(cnt[d * nblk + blockIdx.x]) + (i - static_cast<int>(loff[d]));
+    const uint32_t dd = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
+    const int64_t pos = int64_t(gbase[dd]) + (i - static_cast<int>(loff[dd]));
     if (pos >= 0 && pos < N) {
       dst[pos] = k;
       idst[pos] = srow[i];
@@ -415,6 +521,8 @@ __global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max,
     Slot s;
     s.key = kEmptyKey;
     s.mask = 0;
+    s.start = 0;
+    s.pad = 0;
     table[i] = s;
   }
 }
@@ -423,13 +531,14 @@ __global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max,
 // A warp takes 32 consecutive sorted positions. Each lane's bit (its code's low 6
 // bits) is OR-ed into the first lane of its block's run by a segmented scan over
 // shuffles (runs are contiguous); the run's first lane inserts the block with its key
-// (from the first voxel's coordinates) and first sorted position. A run that goes on
-// past the warp's last lane is finished from memory by its first lane (a run holds at
-// most 64 distinct codes; longer runs are duplicates, reported in step 5).
+// (the sort key without its low 6 bits: the batch and the Morton code of the block's
+// coordinates) and first sorted position. A run that goes on past the warp's last lane
+// is finished from memory by its first lane (a run holds at most 64 distinct codes;
+// longer runs are duplicates, reported in step 5).
 __global__ void __launch_bounds__(256) kmap_blocks_insert(
     const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
     const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
-    const int32_t* __restrict__ ix1, int64_t N, Slot* table, int32_t* __restrict__ base,
+    const int32_t* __restrict__ ix1, int64_t N, Slot* table,
     KmapStatus* st) {
   const bool second = st->plan[kMaxPasses] & 1;
   const unsigned long long* mk = second ? mk1 : mk0;
@@ -455,9 +564,7 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
       if (lane + off < 32 && ob == blk) acc |= o;
     }
     const unsigned long long last_blk = __shfl_sync(0xffffffffu, blk, 31);
-    const int32_t row = start ? ix[s] : -1;
-    // rows outside [0, N) are flagged in step 5
-    if (start && static_cast<uint64_t>(row) < static_cast<uint64_t>(N)) {
+    if (start) {
       unsigned long long mask = acc;
       if (blk == last_blk) {   // the run reaches lane 31: finish it from memory
         for (int64_t j = w0 + 32; j < N && j < s + 128; ++j) {
@@ -466,15 +573,14 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
           mask |= 1ull << (mj & 63u);
         }
       }
-      const int4 c = coords[row];
-      const unsigned long long key = block_key(c.x, c.y, c.z, c.w);
+      const unsigned long long key = blk;
       unsigned long long h = mix64(key) & cmask;
       int probe = 0;
       for (; probe < max_probe; ++probe) {
         const unsigned long long prevk = atomicCAS(&table[h].key, kEmptyKey, key);
         if (prevk == kEmptyKey) {
           table[h].mask = mask;
-          base[h] = static_cast<int32_t>(s);
+          table[h].start = static_cast<unsigned long long>(s);
           break;
         }
         if (prevk == key) {   // two runs of one block: only possible for rejected coordinates
@@ -507,23 +613,28 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 enum ProbeMode { kProbeNbr = 0, kProbeMask = 1, kProbePlan = 2 };
 constexpr int kProbeThreads = 256;
 
+// One hash lookup: the block's occupancy mask and first sorted position (0 and 0 when
+// the block is not in the table). A slot is one 32-byte load.
 __device__ __forceinline__ void block_lookup(const Slot* __restrict__ table,
-                                             const int32_t* __restrict__ base,
                                              unsigned long long key, unsigned long long cmask,
                                              int max_probe, unsigned long long& mask,
                                              int32_t& start, bool& full) {
   unsigned long long h = mix64(key) & cmask;
   mask = 0;
   start = 0;
-  int probe = 0;
-  for (; probe < max_probe; ++probe) {
-    const ulonglong2 s = __ldg(reinterpret_cast<const ulonglong2*>(table + h));
-    if (s.x == key) {
-      mask = s.y;
-      start = __ldg(base + h);
+  for (int probe = 0; probe < max_probe; ++probe) {
+    uint32_t w[8];
+    asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(table + h));
+    const unsigned long long k = (static_cast<unsigned long long>(w[1]) << 32) | w[0];
+    if (k == key) {
+      mask = (static_cast<unsigned long long>(w[3]) << 32) | w[2];
+      start = static_cast<int32_t>(w[4]);
       return;
     }
-    if (s.x == kEmptyKey) return;
+    if (k == kEmptyKey) return;
     h = (h + 1) & cmask;
   }
   full = true;
@@ -537,10 +648,9 @@ __host__ __device__ __forceinline__ int place_in_block(int z, int y, int x) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
-    const int4* __restrict__ coords, const unsigned long long* __restrict__ mk0,
-    const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
-    const int32_t* __restrict__ ix1, int64_t N, int res, const Slot* __restrict__ table,
-    const int32_t* __restrict__ base, int32_t* __restrict__ nbr,
+    const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
+    const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int res,
+    int bits, const Slot* __restrict__ table, int32_t* __restrict__ nbr,
     const int32_t* __restrict__ plan_pos, unsigned long long* __restrict__ key2,
     int32_t* __restrict__ val2, int window_shift, KmapStatus* st) {
   // tbl[p][lane] = (lane holding the block of the neighbour at offset `lane` of a voxel
@@ -564,7 +674,9 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
   const int lane = threadIdx.x & 31;
   const int kk = lane < 27 ? lane : 13;
   const int dz = kk / 9 - 1, dy = (kk / 3) % 3 - 1, dx = kk % 3 - 1;
-  const int bmax = (res - 1) >> 2;   // largest block coordinate along an axis
+  const int bmax = (res - 1) >> 2;          // largest block coordinate along an axis
+  const int bshift = 3 * (bits - 2);        // batch bits of a block key
+  const unsigned long long bmorton = (1ull << bshift) - 1ull;
   constexpr unsigned kAll = 0xffffffffu;
   bool full = false, bad = false;
   const int64_t nwarps = (int64_t(gridDim.x) * kProbeThreads) >> 5;
@@ -579,34 +691,40 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
       const int j0 = __ffs(starts) - 1;
       starts &= starts - 1;
       const int64_t s0 = w * 32 + j0;
-      const unsigned long long blk = __shfl_sync(kAll, m, j0) >> 6;
-      const int32_t v0 = __ldg(ix + s0);
-      if (static_cast<uint64_t>(v0) >= static_cast<uint64_t>(N)) {   // flagged by blocks_count
-        bad = true;
-        continue;
-      }
-      const int4 c = __ldg(coords + v0);   // (b, z, y, x) of the run's first voxel
+      const unsigned long long blk = __shfl_sync(kAll, m, j0) >> 6;   // the run's block key
+      // the run's first 32 positions, loaded before the lookups so that both are in flight
+      int64_t sj = s0 + lane;
+      unsigned long long mj = sj < N ? mk[sj] : ~0ull;
+      int32_t orow = -1;   // lane j: the row voxel s0 + j is written to
+      if (MODE == kProbeNbr && sj < N) orow = __ldg(ix + sj);
+      if (MODE == kProbePlan && sj < N) orow = __ldg(plan_pos + sj);
+      // lane k: the block at offset (dz, dy, dx) around the run's block
       unsigned long long bm = 0;
       int32_t bb = 0;
       if (lane < 27) {
-        const int nz = (c.y >> 2) + dz, ny = (c.z >> 2) + dy, nx = (c.w >> 2) + dx;
+        const unsigned long long bc = blk & bmorton;
+        const int nz = static_cast<int>(compact3(bc >> 2)) + dz;
+        const int ny = static_cast<int>(compact3(bc >> 1)) + dy;
+        const int nx = static_cast<int>(compact3(bc)) + dx;
         if (nz >= 0 && ny >= 0 && nx >= 0 && nz <= bmax && ny <= bmax && nx <= bmax)
-          block_lookup(table, base, block_key(c.x, nz << 2, ny << 2, nx << 2), cmask, max_probe,
-                       bm, bb, full);
+          block_lookup(table, (blk & ~bmorton) | morton3(nz, ny, nx), cmask, max_probe, bm, bb,
+                       full);
       }
       const uint32_t bm_lo = static_cast<uint32_t>(bm), bm_hi = static_cast<uint32_t>(bm >> 32);
       // the run's voxels, 32 sorted positions at a time (a run without duplicates holds
       // at most 64 voxels; duplicates, flagged by blocks_count, only make it longer)
       for (int64_t c0 = s0;; c0 += 32) {
-        const int64_t sj = c0 + lane;
-        const unsigned long long mj = sj < N ? mk[sj] : ~0ull;
+        if (c0 != s0) {
+          sj = c0 + lane;
+          mj = sj < N ? mk[sj] : ~0ull;
+          orow = -1;
+          if (MODE == kProbeNbr && sj < N) orow = __ldg(ix + sj);
+          if (MODE == kProbePlan && sj < N) orow = __ldg(plan_pos + sj);
+        }
         const unsigned inrun = __ballot_sync(kAll, sj < N && (mj >> 6) == blk);
         const int len = inrun == kAll ? 32 : __ffs(~inrun) - 1;
-        int32_t orow = -1;   // lane j: the row voxel c0 + j is written to
-        if (MODE == kProbeNbr && lane < len) orow = __ldg(ix + sj);
-        if (MODE == kProbePlan && lane < len) orow = __ldg(plan_pos + sj);
         uint32_t my_mask = 0;
-#pragma unroll 2
+#pragma unroll 4
         for (int j = 0; j < len; ++j) {
           const uint32_t p = __shfl_sync(kAll, static_cast<uint32_t>(mj), j) & 63u;
           const uint32_t e = tbl[p * 32 + lane];
@@ -735,18 +853,24 @@ thread_local StageTimer g_stage;
 // pairs ping-ponging between (k0, v0) and (k1, v1); plans[p] (device) says whether pass p
 // runs and which buffer it reads, plans[kMaxPasses] which one holds the result.
 int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, int32_t* v1,
-                 int64_t N, int npass, uint32_t* hist, uint32_t* cnt, int64_t nblk,
+                 int64_t N, int npass, uint32_t* hist, char* scratch, int64_t nblk,
                  const int* plans, KmapStatus* st, cudaStream_t stream,
                  const char* stage = "sort pass") {
+  static PerDevice<bool> attr_set;
+  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(kmap_onesweep),
+                                      kScatterSmem, "kmap_onesweep");
+  if (arc != SUBM3D_OK) return arc;
+  const SortScratch S = sort_scratch(scratch, nblk);
+  kmap_hist<<<grid_for(N, 256, 4), 256, 0, stream>>>(k0, N, npass, plans, hist, S, nblk);
+  SUBM3D_LAUNCHED("kmap_hist");
+  kmap_digit_starts<<<1, 256, 0, stream>>>(hist, npass, S);
+  SUBM3D_LAUNCHED("kmap_digit_starts");
+  g_stage.mark("digit histograms", stream);
   const int grid = static_cast<int>(nblk);
   for (int p = 0; p < npass; ++p) {
-    kmap_sort_count<<<grid, kSortThreads, 0, stream>>>(k0, k1, N, p, nblk, cnt, hist, plans);
-    SUBM3D_LAUNCHED("kmap_sort_count");
-    kmap_sort_scan<<<256, 256, 0, stream>>>(hist, p, nblk, cnt, plans);
-    SUBM3D_LAUNCHED("kmap_sort_scan");
-    kmap_sort_scatter<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, p, nblk,
-                                                                    cnt, plans, st);
-    SUBM3D_LAUNCHED("kmap_sort_scatter");
+    kmap_onesweep<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, p, nblk,
+                                                                plans, S, st);
+    SUBM3D_LAUNCHED("kmap_onesweep");
     g_stage.mark(stage, stream);
   }
   return SUBM3D_OK;
@@ -754,17 +878,12 @@ int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, in
 
 int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* ws,
                 cudaStream_t stream) {
-  static PerDevice<bool> attr_set;
-  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(kmap_sort_scatter),
-                                      kScatterSmem, "kmap_sort_scatter");
-  if (arc != SUBM3D_OK) return arc;
   KmapStatus* st = reinterpret_cast<KmapStatus*>(ws + L.status);
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   unsigned long long* mk0 = reinterpret_cast<unsigned long long*>(ws + L.mk0);
   unsigned long long* mk1 = reinterpret_cast<unsigned long long*>(ws + L.mk1);
   int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
   int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   int bits = 2;   // at least one whole 4x4x4 block level below the batch bits
   while ((1 << bits) < res) ++bits;
   const int npass = (3 * bits + 16 + 7) / 8;
@@ -778,7 +897,7 @@ int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* w
   g_stage.mark("pack", stream);
   const int* plans = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
                                                   offsetof(KmapStatus, plan));
-  return launch_radix(mk0, mk1, ix0, ix1, N, npass, hist, cnt, L.nblk, plans, st, stream);
+  return launch_radix(mk0, mk1, ix0, ix1, N, npass, hist, ws + L.cnt, L.nblk, plans, st, stream);
 }
 
 // SparseDownsample(2) / SparseUpsample(2) ------------------------------------------
@@ -1178,7 +1297,8 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
   int32_t* ix0 = reinterpret_cast<int32_t*>(ws + L.ix0);
   int32_t* ix1 = reinterpret_cast<int32_t*>(ws + L.ix1);
   Slot* table = reinterpret_cast<Slot*>(ws + L.table);
-  int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
+  int bits = 2;   // bits per axis of the sort key (as launch_sort chooses them)
+  while ((1 << bits) < res) ++bits;
 
   const int4* c4 = reinterpret_cast<const int4*>(coords);
   g_stage.begin(stream);
@@ -1191,13 +1311,13 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
   kmap_table_init<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, hash_capacity, cap_max, st);
   SUBM3D_LAUNCHED("kmap_table_init");
   kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
-                                                              base, st);
+                                                              st);
   SUBM3D_LAUNCHED("kmap_blocks_insert");
   g_stage.mark("block table", stream);
   const int probe_grid = grid_for((N + 31) / 32 * 32, kProbeThreads, 8);
   if (!grouped) {
     kmap_probe<kProbeNbr><<<probe_grid, kProbeThreads, 0, stream>>>(
-        c4, mk0, mk1, ix0, ix1, N, res, table, base, nbr, nullptr, nullptr, nullptr, 0, st);
+        mk0, mk1, ix0, ix1, N, res, bits, table, nbr, nullptr, nullptr, nullptr, 0, st);
     SUBM3D_LAUNCHED("kmap_probe");
     g_stage.mark("probe", stream);
   } else {
@@ -1211,7 +1331,6 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     int32_t* v2b = reinterpret_cast<int32_t*>(ws + L.v2b);
     int32_t* plan_pos = reinterpret_cast<int32_t*>(ws + L.plan_pos);
     uint32_t* hist2 = reinterpret_cast<uint32_t*>(ws + L.hist2);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
     int wshift = 0;
     while ((int64_t(1) << wshift) < window) ++wshift;
     const int64_t last_window = (N - 1) >> wshift;
@@ -1219,22 +1338,22 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     while ((last_window >> wbits) != 0) ++wbits;
     const int npass2 = (27 + wbits + 7) / 8;
     kmap_probe<kProbeMask><<<probe_grid, kProbeThreads, 0, stream>>>(
-        c4, mk0, mk1, ix0, ix1, N, res, table, base, nullptr, nullptr, k2a, v2a, wshift, st);
+        mk0, mk1, ix0, ix1, N, res, bits, table, nullptr, nullptr, k2a, v2a, wshift, st);
     SUBM3D_LAUNCHED("kmap_probe_mask");
     g_stage.mark("mask probe", stream);
     kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);
     SUBM3D_LAUNCHED("kmap_plan2");
     const int* plans2 = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
                                                      offsetof(KmapStatus, plan2));
-    const int rc = launch_radix(k2a, k2b, v2a, v2b, N, npass2, hist2, cnt, L.nblk, plans2, st,
-                                stream, "grouping sort pass");
+    const int rc = launch_radix(k2a, k2b, v2a, v2b, N, npass2, hist2, ws + L.cnt, L.nblk, plans2,
+                                st, stream, "grouping sort pass");
     if (rc != SUBM3D_OK) return rc;
     kmap_plan_index<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
         k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, plan_pos, perm, tmask, st);
     SUBM3D_LAUNCHED("kmap_plan_index");
     g_stage.mark("plan index", stream);
     kmap_probe<kProbePlan><<<probe_grid, kProbeThreads, 0, stream>>>(
-        c4, mk0, mk1, ix0, ix1, N, res, table, base, pnbr, plan_pos, nullptr, nullptr, 0, st);
+        mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, plan_pos, nullptr, nullptr, 0, st);
     SUBM3D_LAUNCHED("kmap_probe_plan");
     g_stage.mark("plan probe", stream);
   }
@@ -1271,7 +1390,14 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
 
 }  // namespace
 
-void kmap_stage_timing(bool on) { g_stage.on = on; }
+void kmap_stage_timing(bool on) {
+  // the events are made here, not during a build (making one takes far longer than a
+  // small stage runs)
+  if (on)
+    for (int i = 0; i < StageTimer::kMax; ++i)
+      if (!g_stage.ev[i] && cudaEventCreate(&g_stage.ev[i]) != cudaSuccess) break;
+  g_stage.on = on;
+}
 
 int kmap_stage_times(float* ms, const char** names, int max) {
   const int n = g_stage.n;

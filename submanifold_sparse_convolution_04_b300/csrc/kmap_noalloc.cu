@@ -10,7 +10,7 @@
 // g_kmap_scratch, sized for at most kNoAllocMaxVoxels voxels.
 //
 // g_kmap_scratch is a file-scope __device__ array: every GPU that loads the library
-// holds its 9 MiB until the process exits. In host code its name is only a host-side
+// holds its 16 MiB until the process exits. In host code its name is only a host-side
 // stand-in, so its device address is fetched with cudaGetSymbolAddress, once per
 // device, with that device current, by the first call made on that device (make that
 // first call before any stream capture begins). Like subm3d_build_kmap, each call
@@ -26,7 +26,7 @@ namespace subm3d {
 namespace {
 
 constexpr int64_t kNoAllocMaxVoxels = SUBM3D_NOALLOC_MAX_VOXELS;
-constexpr size_t kNoAllocScratchBytes = size_t(9) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_kmap_scratch[kNoAllocScratchBytes];
 

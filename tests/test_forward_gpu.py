@@ -143,8 +143,7 @@ def test_forward_narrow_kernel_shapes(dev, I, O):
 
 
 def test_forward_narrow_shape_with_16_byte_aligned_feats(dev):
-    # the narrow kernel needs 32-byte-aligned rows; a feats pointer that is only 16-byte
-    # aligned takes the shared-memory kernel, and both match the oracle
+    # a feats pointer that is 16-byte but not 32-byte aligned gives the same result
     coords, v = shell_case(77, 40, 64, 64, "bf16", batch=2)
     N = coords.shape[0]
     nbr = subm3d_build_kmap(torch.from_numpy(coords).to(dev), 40)

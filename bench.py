@@ -65,6 +65,10 @@ def parse_args():
                    help="conv: kmap + forward (the default step); the others: SparseDownsample(2), "
                         "its paired SparseUpsample(2), SparseSpatial2Channel(2) and its inverse on "
                         "the workload's voxels and features")
+    p.add_argument("--ds-sort", action="store_true",
+                   help="--op downsample: sort the voxels itself (subm3d_downsample) instead of "
+                        "taking the Morton order of the kernel map on the same voxels "
+                        "(subm3d_downsample_sorted)")
     p.add_argument("--pool", default="mean", choices=["mean", "max"],
                    help="pooling of --op downsample (and of the coarse rows --op upsample uses)")
     p.add_argument("--residual", action="store_true",
@@ -340,13 +344,20 @@ def active_passes(coords, res):
 
 
 def kmap_algorithmic_bytes(N, passes, grouped, window):
-    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N
+    """Algorithmic bytes of one kernel-map build: every pass reads its inputs and writes
+    its outputs once (the L2-resident block table is not counted). pack: coords 16 N in,
+    keys 8 N + rows 4 N out; each active radix pass (constant high digits are skipped):
+    12 N in, 12 N out; block runs and table: keys 8 N, twice; probe: keys 8 N + rows 4 N
+    in, the table 108 N out. The tile plan's probe writes the table in Morton order plus
+    grouping keys and values (12 N); then the grouping sort (24 N per pass) and the plan
+    index (keys, values, rows 16 N in; perm 4 N out; the table's 108 N read and written
+    again in plan order)."""
+    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N + 108 * N
     if not grouped:
-        return base + 108 * N
+        return base
     last_window = (N - 1) // window
-    wbits = last_window.bit_length()
-    passes2 = (27 + wbits + 7) // 8
-    return base + 24 * N + 24 * N * passes2 + 20 * N + 4 * N + 108 * N
+    passes2 = (27 + last_window.bit_length() + 7) // 8
+    return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N
 
 
 def spread(xs):
@@ -651,7 +662,8 @@ def run_resample(args, world, rank, local):
     N C e + 20 N + M + 8 M C e; channel2spatial 2 N C e + 20 N."""
     import numpy as np
     import torch
-    from submanifold_sparse_convolution_04_b300 import (lib, subm3d_channel2spatial,
+    from submanifold_sparse_convolution_04_b300 import (lib, subm3d_build_kmap_ex,
+                                                        subm3d_channel2spatial,
                                                         subm3d_downsample,
                                                         subm3d_forward_status,
                                                         subm3d_kernel_launches,
@@ -673,10 +685,16 @@ def run_resample(args, world, rank, local):
     M = cc.shape[0]
     up = torch.empty((N, C), dtype=f.dtype, device=dev)
     if args.op == "downsample":
+        # the kernel map at this resolution (built anyway by the convolutions that run on
+        # these voxels) already holds their Morton order
+        order = None if args.ds_sort else subm3d_build_kmap_ex(c, res, order=True)[1]
+
         def step():
-            subm3d_downsample(c, res, f, args.pool, workspace=ws)
+            subm3d_downsample(c, res, f, args.pool, workspace=ws, order=order)
         nbytes = 16 * N + N * C * e + 4 * N + M * (16 + 1 + C * e)
-        kernel = "downsample: sort + ds_count/ds_scan/ds_emit + ds_pool"
+        kernel = ("downsample: sort + ds_count/ds_scan/ds_emit + ds_pool" if args.ds_sort else
+                  "downsample on the kernel map's Morton order: ds_keys_in_order + "
+                  "ds_count/ds_scan/ds_emit + ds_pool")
     elif args.op == "upsample":
         def step():
             subm3d_upsample(cf, parent, out=up)

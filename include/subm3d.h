@@ -90,7 +90,7 @@ typedef enum {
 /*
  * Workspace bytes that subm3d_build_kmap needs for N voxels (the default hash table
  * is reserved for its worst case, one occupied block per voxel: the smallest power
- * of two >= 2N slots, at least 64, of 20 bytes each). Host-only, no CUDA
+ * of two >= 2N slots, at least 64, of 32 bytes each). Host-only, no CUDA
  * call. Returns 0 for N < 0.
  */
 SUBM3D_API size_t subm3d_kmap_workspace_bytes(int64_t N);
@@ -339,7 +339,7 @@ SUBM3D_API int subm3d_forward_ex(const void* feats, const int32_t* nbr, const vo
  *                 aligned; other pointers 16-byte aligned.
  *
  * Synchronises `stream` once (to read M and the status word), like subm3d_build_kmap;
- * the pooling kernel is then enqueued after it. Errors: ERR_ARG, ERR_WORKSPACE,
+ * the pooling kernel is enqueued before that wait and reads M on the device. Errors: ERR_ARG, ERR_WORKSPACE,
  * ERR_COORD_RANGE, ERR_DUPLICATE (outputs unspecified), ERR_CUDA, ERR_DEVICE.
  */
 SUBM3D_API size_t subm3d_downsample_workspace_bytes(int64_t N);
@@ -348,6 +348,22 @@ SUBM3D_API int subm3d_downsample(const int32_t* coords, int64_t N, int32_t res, 
                                  int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
                                  uint8_t* child_mask, int64_t* M_out, void* workspace,
                                  size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * subm3d_downsample on coordinates whose Morton order the caller already has: `order`
+ * is what subm3d_build_kmap_ex wrote for the same coords and res (order[s] = input row
+ * at position s of the (batch, Morton code) sort), device int32 [N], 16-byte aligned.
+ * The radix sort is skipped: the sort keys are gathered in that order, and checked (rows
+ * in [0, N), coordinates in the grid, keys ascending; SUBM3D_ERR_ARG otherwise). The
+ * other arguments, the results and the one synchronisation are those of
+ * subm3d_downsample.
+ */
+SUBM3D_API int subm3d_downsample_sorted(const int32_t* coords, int64_t N, int32_t res,
+                                        const int32_t* order, const void* feats, int32_t C,
+                                        subm3d_dtype dtype, subm3d_pool mode,
+                                        int32_t* coarse_coords, void* coarse_feats,
+                                        int32_t* parent, uint8_t* child_mask, int64_t* M_out,
+                                        void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * SparseUpsample(2) with the subdivision a subm3d_downsample stored:

@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.subm3d_downsample.argtypes = [vp, i64, i32, vp, i32, ctypes.c_int, ctypes.c_int, vp, vp,
                                         vp, vp, ctypes.POINTER(ctypes.c_int64), vp, sz, vp]
         L.subm3d_downsample.restype = ctypes.c_int
+        L.subm3d_downsample_sorted.argtypes = [vp, i64, i32, vp, vp, i32, ctypes.c_int,
+                                               ctypes.c_int, vp, vp, vp, vp,
+                                               ctypes.POINTER(ctypes.c_int64), vp, sz, vp]
+        L.subm3d_downsample_sorted.restype = ctypes.c_int
         L.subm3d_upsample.argtypes = [vp, i64, i32, vp, i64, ctypes.c_int, vp, vp]
         L.subm3d_upsample.restype = ctypes.c_int
         L.subm3d_spatial2channel.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_int, vp, vp]
@@ -321,11 +325,14 @@ def subm3d_forward_ex(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tens
 
 
 def subm3d_downsample(coords: torch.Tensor, res: int, feats: torch.Tensor | None = None,
-                      mode: str = "mean", workspace: torch.Tensor | None = None, stream=None):
+                      mode: str = "mean", workspace: torch.Tensor | None = None, stream=None,
+                      order: torch.Tensor | None = None):
     """SparseDownsample(2): (coarse_coords int32 [M, 4], coarse_feats [M, C] or None,
     parent int32 [N], child_mask uint8 [M]) for coords int32 [N, 4] (b, z, y, x) on a
     grid of side res. Coarse voxels come in (batch, Morton) order; parent and
-    child_mask are the subdivision subm3d_upsample takes. Synchronises the stream once."""
+    child_mask are the subdivision subm3d_upsample takes. Synchronises the stream once.
+    order: the Morton order subm3d_build_kmap_ex gave for the same coords (int32 [N]);
+    when given, the radix sort is skipped (subm3d_downsample_sorted)."""
     if mode not in POOL_MODES:
         raise ValueError(f"mode {mode!r} is not one of {sorted(POOL_MODES)}")
     N = coords.shape[0]
@@ -348,9 +355,17 @@ def subm3d_downsample(coords: torch.Tensor, res: int, feats: torch.Tensor | None
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     pw = _dev(workspace, "workspace", torch.uint8)
     M = ctypes.c_int64(0)
-    _check(lib().subm3d_downsample(pc, N, int(res), pf, C, dt, POOL_MODES[mode], _dev(cc, "cc"),
-                                   pcf, _dev(parent, "parent"), _dev(mask, "mask"),
-                                   ctypes.byref(M), pw, workspace.numel(), _stream(stream)))
+    if order is None:
+        _check(lib().subm3d_downsample(pc, N, int(res), pf, C, dt, POOL_MODES[mode],
+                                       _dev(cc, "cc"), pcf, _dev(parent, "parent"),
+                                       _dev(mask, "mask"), ctypes.byref(M), pw, workspace.numel(),
+                                       _stream(stream)))
+    else:
+        po = _dev(order, "order", torch.int32, (N,))
+        _check(lib().subm3d_downsample_sorted(pc, N, int(res), po, pf, C, dt, POOL_MODES[mode],
+                                              _dev(cc, "cc"), pcf, _dev(parent, "parent"),
+                                              _dev(mask, "mask"), ctypes.byref(M), pw,
+                                              workspace.numel(), _stream(stream)))
     m = M.value
     return cc[:m], (None if cf is None else cf[:m]), parent, mask[:m]
 

@@ -247,8 +247,24 @@ int subm3d_downsample(const int32_t* coords, int64_t N, int32_t res, const void*
                       void* coarse_feats, int32_t* parent, uint8_t* child_mask, int64_t* M_out,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
   clear_error();
-  return downsample_build(coords, N, res, feats, C, dtype, static_cast<int>(mode), coarse_coords,
-                          coarse_feats, parent, child_mask, M_out, workspace, ws_bytes, stream);
+  return downsample_build(coords, N, res, nullptr, feats, C, dtype, static_cast<int>(mode),
+                          coarse_coords, coarse_feats, parent, child_mask, M_out, workspace,
+                          ws_bytes, stream);
+}
+
+int subm3d_downsample_sorted(const int32_t* coords, int64_t N, int32_t res, const int32_t* order,
+                             const void* feats, int32_t C, subm3d_dtype dtype, subm3d_pool mode,
+                             int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
+                             uint8_t* child_mask, int64_t* M_out, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream) {
+  clear_error();
+  if (!order && N > 0) {
+    set_error("subm3d_downsample_sorted: order is NULL");
+    return SUBM3D_ERR_ARG;
+  }
+  return downsample_build(coords, N, res, order, feats, C, dtype, static_cast<int>(mode),
+                          coarse_coords, coarse_feats, parent, child_mask, M_out, workspace,
+                          ws_bytes, stream);
 }
 
 int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,

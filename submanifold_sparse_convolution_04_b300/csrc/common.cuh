@@ -156,10 +156,11 @@ int kmap_build_grouped(const int32_t* coords, int64_t N, int32_t res, int64_t wi
                        cudaStream_t stream);
 size_t kmap_workspace_bytes(int64_t N, int64_t hash_capacity);
 size_t downsample_workspace_bytes(int64_t N);
-int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,
-                     subm3d_dtype dtype, int mode, int32_t* coarse_coords, void* coarse_feats,
-                     int32_t* parent, uint8_t* child_mask, int64_t* M_out, void* workspace,
-                     size_t ws_bytes, cudaStream_t stream);
+int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_t* order,
+                     const void* feats, int32_t C, subm3d_dtype dtype, int mode,
+                     int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
+                     uint8_t* child_mask, int64_t* M_out, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream);
 int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
                     int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
 int spatial2channel_launch(const void* feats, const int32_t* coords, const int32_t* parent,
@@ -237,6 +238,10 @@ __device__ __forceinline__ void cp_async_16_ca(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most one of this thread's committed cp.async groups is still pending.
+__device__ __forceinline__ void cp_async_wait_group1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -331,6 +336,17 @@ __device__ __forceinline__ float apply_act(float y, int act) {
   if (act == SUBM3D_ACT_SILU) return y < -80.f ? 0.f : __fdividef(y, 1.f + __expf(-y));
   return y;
 }
+// silu(y) for an output that is rounded to bf16 next: y * sigmoid(y) with
+// sigmoid(y) = (1 + tanh(y / 2)) / 2, tanh from the hardware approximation (relative
+// error about 2^-11, below half a bf16 unit in the last place, 2^-9). One special-
+// function instruction instead of an exponential and a division: the four epilogue
+// warps, not the gathers, set the pace with the exact form.
+__device__ __forceinline__ float silu_for_bf16(float y) {
+  float t;
+  const float h = 0.5f * y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
 // Asks L2 for every 128-byte line of a row of `bytes` (> 0) bytes at p; the addresses
 // must lie inside the allocation. A hint: no data comes back, nothing waits for it.
 __device__ __forceinline__ void prefetch_row_l2(const void* p, int bytes) {
@@ -360,9 +376,12 @@ __device__ __forceinline__ uint4 epilogue8_bf16(const uint32_t (&acc)[8], const 
       y[2 * e + 1] += f.y;
     }
   }
-  if (act != SUBM3D_ACT_NONE) {
+  if (act == SUBM3D_ACT_RELU) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = apply_act(y[e], act);
+    for (int e = 0; e < 8; ++e) y[e] = fmaxf(y[e], 0.f);
+  } else if (act == SUBM3D_ACT_SILU) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = silu_for_bf16(y[e]);
   }
   uint32_t packed[4];
 #pragma unroll

@@ -459,8 +459,9 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
         }
         const int col0 = cc * 8;
         if (row < p.N && col0 < p.O) {
-          *reinterpret_cast<uint4*>(orow + col0) =
-              epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act);
+          // streaming store: the output is not read again here, the gathered rows are
+          __stcs(reinterpret_cast<uint4*>(orow + col0),
+                 epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act));
         }
       }
     }

@@ -25,17 +25,16 @@
 //     into a double-buffered shared-memory ring with one bulk copy, a tile ahead, so
 //     a producer reads its row's index with one conflict-free shared load (27 is
 //     odd) instead of one 32-byte global sector per 4-byte index.
-// Tensor memory (512 columns): two accumulators of 64 columns (double buffer) and six
-// A stages of 64 columns. A stage carries two offsets (2p, 2p + 1; the last of a tile
-// only offset 26), because every stage costs the single MMA-issuing warp a barrier wait
-// and a commit, and that per-stage cost, not the memory system, bounded the kernel with
-// one offset per stage. Stage g of the CTA (tile, pair p) is written by producer group
-// g mod 6 (four warps, warp w writing lanes 32 (w % 4) .. + 31) into slot g mod 6: each
-// warp gathers its rows of the stage's first offset (copies in flight while the slot
-// frees), reads them back, starts the second offset's copies, stores the first rows,
-// then reads back and stores the second; the group leader fetches both weight taps into
-// the stage's weight slot by TMA. The stage is full when its four
-// warps have arrived (after tcgen05.wait::st) and its weight bytes have landed.
+// Tensor memory (512 columns allocated): two accumulators of 64 columns (double buffer)
+// and four A stages of 64 columns. A stage carries two offsets of the tile (consecutive
+// offsets of its mask; the last may have one), because every stage costs the single
+// MMA-issuing warp a barrier wait and a commit. Stage g of the CTA is filled by producer
+// group g mod 4 (four warps, warp w writing lanes 32 (w % 4) .. + 31) into slot g mod 4:
+// each warp starts the copies of its rows of both offsets into its two staging buffers
+// (so both are in flight while the slot frees), then reads back and stores the first,
+// then the second; the group leader fetches both weight taps into the stage's weight
+// slot by TMA. The stage is full when its four warps have arrived (after
+// tcgen05.wait::st) and its weight bytes have landed.
 // One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
 // up to four per offset) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
 // t (tcgen05.ld -> + bias [+ residual row, activation: the fused block epilogue] ->
@@ -52,8 +51,8 @@ namespace subm3d {
 namespace {
 
 constexpr int kBM = 128;              // output rows per tile = tensor-memory lanes
-constexpr int kGroups = 6;            // producer groups of four warps
-constexpr int kStages = 6;            // A stages in tensor memory
+constexpr int kGroups = 4;            // producer groups of four warps
+constexpr int kStages = 4;            // A stages in tensor memory
 constexpr int kOffCols = 32;          // one offset's row: 64 bf16 = 32 columns of 32 bits
 constexpr int kStageCols = 2 * kOffCols;   // a stage holds two offsets (2p, 2p + 1)
 constexpr int kPairs = 14;            // stages per tile: offsets (0,1) .. (24,25), (26)
@@ -61,14 +60,15 @@ constexpr int kAccCols = 64;          // one accumulator (N <= 64)
 constexpr int kAColBase = 2 * kAccCols;
 constexpr int kProducerWarps = 4 * kGroups;
 constexpr int kMmaWarp = kProducerWarps;
-constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 25..28: lane groups 1, 2, 3, 0
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 17..20: lane groups 1, 2, 3, 0
 constexpr int kNbrWarp = kEpiWarp0 + 4;
-constexpr int kThreads = 32 * (kNbrWarp + 1);    // 960
+constexpr int kThreads = 32 * (kNbrWarp + 1);    // 704
 constexpr int kNbrTileBytes = kBM * 27 * 4;      // one tile's rows of nbr
-constexpr int kWarpStaging = 32 * 128;           // a producer warp's 32 gathered rows
+constexpr int kRowsStaging = 32 * 128;           // a producer warp's 32 gathered rows
+constexpr int kWarpStaging = 2 * kRowsStaging;   // one buffer per offset of a stage
 constexpr int kStagingBytes = kProducerWarps * kWarpStaging;
 constexpr int kSmemLimit = 227 * 1024;
-static_assert(kAColBase + kStages * kStageCols == 512, "tensor memory layout");
+static_assert(kAColBase + kStages * kStageCols <= 512, "tensor memory layout");
 static_assert(kStages % kGroups == 0, "slots per group");
 
 template <int NMMA>
@@ -283,26 +283,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nor the row reads below conflict; then every lane reads its own row back. Loading
     // whole rows per instruction costs the L1 data pipe one pass per 128-byte row
     // instead of one per 16 bytes of each lane's own row.
+    // buffer b of the warp holds the rows of the stage's offset b, so that both offsets'
+    // copies are in flight at once
     const uint32_t stage_base = sStage + warp * kWarpStaging;
-    auto gather_issue = [&](int32_t jown) {   // jown: this lane's input row (-1: absent)
+    auto gather_issue = [&](int32_t jown, int b) {   // jown: this lane's input row (-1: absent)
       const int c = lane & 7;
+      const uint32_t buf = stage_base + b * kRowsStaging;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int rr = 4 * i + (lane >> 3);
         const int32_t j = __shfl_sync(0xffffffffu, jown, rr);
         if (j >= 0 && c * 8 < p.I)
-          cp_async_16_ca(stage_base + rr * 128 + ((c ^ (rr & 7)) << 4),
+          cp_async_16_ca(buf + rr * 128 + ((c ^ (rr & 7)) << 4),
                          p.feats + int64_t(j) * p.I + c * 8);
       }
       cp_async_commit();
     };
-    auto gather_finish = [&](int32_t jown, uint32_t (&v)[32]) {
-      cp_async_wait_all();
+    // younger: copy groups issued after this one that may still be in flight (0 or 1)
+    auto gather_finish = [&](int32_t jown, int b, int younger, uint32_t (&v)[32]) {
+      if (younger) cp_async_wait_group1();
+      else cp_async_wait_all();
       __syncwarp();
+      const uint32_t buf = stage_base + b * kRowsStaging;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (jown >= 0 && c * 8 < p.I) q = ld_shared_v4(stage_base + lane * 128 + ((c ^ (lane & 7)) << 4));
+        if (jown >= 0 && c * 8 < p.I) q = ld_shared_v4(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
         v[4 * c] = q.x;
         v[4 * c + 1] = q.y;
         v[4 * c + 2] = q.z;
@@ -349,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t v[32];
       const int32_t j0 = row_index(lt, k0);
-      gather_issue(j0);   // in flight while the slot frees
+      const int32_t j1 = two ? row_index(lt, k1) : -1;
+      gather_issue(j0, 0);   // both offsets' rows in flight while the slot frees
+      if (two) gather_issue(j1, 1);
       const uint32_t s = g % kStages;
       const uint32_t use = g / kStages;
       const bool ok = mbar_wait(aempty0 + 8 * s, (use & 1u) ^ 1u, abort_flag);
@@ -365,16 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       last = g + kGroups;
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + kAColBase + s * kStageCols;
-      gather_finish(j0, v);
-      int32_t j1 = -1;
-      if (two) {   // the second offset's rows travel while the first one's are stored
-        j1 = row_index(lt, k1);
-        gather_issue(j1);
-      }
+      gather_finish(j0, 0, two ? 1 : 0, v);
       tmem_st32(taddr, v);
       if (two) {
         tmem_st_wait();   // v is free again
-        gather_finish(j1, v);
+        gather_finish(j1, 1, 0, v);
         tmem_st32(taddr + kOffCols, v);
       }
       tmem_st_wait();
@@ -520,8 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int col0 = cc * 8;
         if (row < p.N) {
-          *reinterpret_cast<uint4*>(orow + col0) =
-              epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act);
+          // streaming store: the output is not read again here, the gathered rows are
+          __stcs(reinterpret_cast<uint4*>(orow + col0),
+                 epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act));
         }
       }
     }

@@ -52,7 +52,7 @@ constexpr int kMaxProbe = 4096;
 constexpr int kHistParts = 16;   // partial digit histograms (spreads the count kernel's atomics)
 constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 2 * 256 * 4;
 
-enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8 };
+enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8, kFlagOrder = 16 };
 
 struct KmapStatus {
   int flags;
@@ -85,9 +85,9 @@ __host__ __device__ inline size_t sort_scratch_bytes(int64_t ntile) {
 
 struct Layout {
   size_t status, hist, mk0, mk1, ix0, ix1, cnt, table;
-  // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and each
-  // sorted position's row of the plan
-  size_t k2a, k2b, v2a, v2b, hist2, plan_pos;
+  // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and the
+  // neighbour table in sorted (Morton) order
+  size_t k2a, k2b, v2a, v2b, hist2, nbr_sorted;
   size_t total;
   int64_t nblk;
 };
@@ -105,14 +105,14 @@ Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   L.ix1 = o;    o = align256(o + sizeof(int32_t) * N);
   L.cnt = o;    o = align256(o + sort_scratch_bytes(L.nblk));
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
-  L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.plan_pos = 0;
+  L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.nbr_sorted = 0;
   if (grouped) {
     L.k2a = o;      o = align256(o + sizeof(uint64_t) * N);
     L.k2b = o;      o = align256(o + sizeof(uint64_t) * N);
     L.v2a = o;      o = align256(o + sizeof(int32_t) * N);
     L.v2b = o;      o = align256(o + sizeof(int32_t) * N);
     L.hist2 = o;    o = align256(o + hist_bytes);
-    L.plan_pos = o; o = align256(o + sizeof(int32_t) * N);
+    L.nbr_sorted = o; o = align256(o + sizeof(int32_t) * 27 * N);
   }
   L.total = o;
   return L;
@@ -308,8 +308,12 @@ __global__ void __launch_bounds__(256) kmap_hist(const unsigned long long* __res
     for (int p = 0; p < npass; ++p) {
       if (!((active >> p) & 1u)) continue;
       const uint32_t d = valid ? static_cast<uint32_t>((k >> (8 * p)) & 255u) : 256u;
-      const unsigned peers = __match_any_sync(0xffffffffu, d);
-      if (valid && lane == __ffs(peers) - 1) atomicAdd(&sh[p][d], __popc(peers));
+      const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+      if (__all_sync(0xffffffffu, d == d0)) {   // one digit for the whole warp (common)
+        if (lane == 0 && d0 < 256u) atomicAdd(&sh[p][d0], 32u);
+      } else if (valid) {                      // a few lanes per digit: plain atomics
+        atomicAdd(&sh[p][d], 1u);
+      }
     }
   }
   __syncthreads();
@@ -425,23 +429,35 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
     st_relaxed_u64(my, tag | kTileInclusive | run);
   } else {
     st_relaxed_u64(my, tag | kTileAggregate | run);
+    // eight earlier tiles' words are read at once; the walk goes on from the first one
+    // not yet published (waiting for it, bounded) until an inclusive count ends it
     int64_t t = tile - 1;
     const unsigned long long t0 = global_timer_ns();
     bool late = false;
     for (uint32_t it = 0; t >= 0; ++it) {
-      const unsigned long long v = ld_relaxed_u64(S.status + t * 256 + d);
-      const unsigned long long flag = (v >> 34) == static_cast<unsigned long long>(pass + 1)
-                                          ? (v & (3ull << 32)) : 0ull;
-      if (flag == 0) {   // not published yet (or an earlier pass's word): wait (bounded)
-        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
-          late = true;
-          break;
-        }
-        continue;
+      unsigned long long v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = t - q >= 0 ? ld_relaxed_u64(S.status + (t - q) * 256 + d)
+                          : (tag | kTileInclusive);   // before tile 0: nothing
+      int used = 0;
+      bool done = false;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (done || used < q) continue;   // stopped at an unpublished word
+        const unsigned long long flag = (v[q] >> 34) == static_cast<unsigned long long>(pass + 1)
+                                            ? (v[q] & (3ull << 32)) : 0ull;
+        if (flag == 0) continue;          // not published yet (or an earlier pass's word)
+        before_tile += static_cast<uint32_t>(v[q]);
+        ++used;
+        if (flag == kTileInclusive) done = true;
       }
-      before_tile += static_cast<uint32_t>(v);
-      if (flag == kTileInclusive) break;
-      --t;
+      if (done) break;
+      t -= used;
+      if (used < 8 && (it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+        late = true;
+        break;
+      }
     }
     if (late) atomicOr(&st->flags, kFlagInternal);
     st_relaxed_u64(my, tag | kTileInclusive | (before_tile + run));
@@ -502,7 +518,15 @@ __global__ void __launch_bounds__(256) kmap_blocks_count(
     }
   }
   for (int o = 16; o > 0; o >>= 1) starts += __shfl_xor_sync(0xffffffffu, starts, o);
-  if ((threadIdx.x & 31) == 0 && starts) atomicAdd(&st->nblocks, starts);
+  // one atomic per block (same-address atomics from every warp serialise)
+  __shared__ unsigned long long wsum[8];
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = starts;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += wsum[w];
+    if (total) atomicAdd(&st->nblocks, total);
+  }
 }
 
 // 6. ------------------------------------------------------------------------------
@@ -564,15 +588,27 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
       if (lane + off < 32 && ob == blk) acc |= o;
     }
     const unsigned long long last_blk = __shfl_sync(0xffffffffu, blk, 31);
+    // the run that reaches lane 31 may go on: its bits among the next 64 positions (a run
+    // without duplicates holds at most 64 voxels), loaded by the whole warp at once
+    unsigned long long tail = 0;
+    if (w0 + 31 < N) {   // lane 31 holds a voxel (warp-uniform)
+      unsigned long long t_or = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t j = w0 + 32 + 32 * h + lane;
+        const unsigned long long mj = j < N ? mk[j] : ~0ull;
+        // only the stretch that continues the run without a break counts
+        const unsigned brk = __ballot_sync(0xffffffffu, (mj >> 6) != last_blk);
+        const unsigned keep = brk ? ((1u << (__ffs(brk) - 1)) - 1u) : 0xffffffffu;
+        if ((keep >> lane) & 1u) t_or |= 1ull << (mj & 63u);
+        for (int o = 16; o > 0; o >>= 1) t_or |= __shfl_xor_sync(0xffffffffu, t_or, o);
+        if (brk) break;
+      }
+      tail = t_or;
+    }
     if (start) {
       unsigned long long mask = acc;
-      if (blk == last_blk) {   // the run reaches lane 31: finish it from memory
-        for (int64_t j = w0 + 32; j < N && j < s + 128; ++j) {
-          const unsigned long long mj = mk[j];
-          if ((mj >> 6) != blk) break;
-          mask |= 1ull << (mj & 63u);
-        }
-      }
+      if (blk == last_blk) mask |= tail;   // the run reaches lane 31: add what follows
       const unsigned long long key = blk;
       unsigned long long h = mix64(key) & cmask;
       int probe = 0;
@@ -596,22 +632,24 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 
 // 8. ------------------------------------------------------------------------------
 // Warp-cooperative probe over the sorted order. A warp takes 32 consecutive sorted
-// positions and handles every block run that starts among them (a run may go on past
-// them). For a run, lanes 0..26 each look up one of the 27 blocks around the run's
-// block (lane k: block offset (k / 9 - 1, k / 3 % 3 - 1, k % 3 - 1)), so every
-// neighbour of every voxel of the run lies in a block one of the lanes holds. Then,
-// voxel by voxel, lane k resolves the voxel's neighbour at offset k: a table indexed by
-// the voxel's place inside its block (the low 6 bits of its Morton code) gives the
-// lane that holds the neighbour's block and the neighbour's bit there; that lane's
-// mask and first sorted position come over by shuffles; a bit test and a popcount
-// give the neighbour's sorted position, and the input row there is the answer.
-// Depending on the mode the warp then writes
-//   kProbeNbr   the voxel's row of nbr (lanes 0..26: 108 contiguous bytes) at its input row;
-//   kProbeMask  its 27-bit presence mask (a ballot over the lanes) as a grouping key
-//               (window << 27 | mask) with its sorted position as the value;
-//   kProbePlan  its row of nbr at its row of the tile plan.
-enum ProbeMode { kProbeNbr = 0, kProbeMask = 1, kProbePlan = 2 };
-constexpr int kProbeThreads = 256;
+// positions, one voxel per lane. Its voxels fall into a few block runs (a run is one
+// occupied 4x4x4 block); for every run the warp looks up, spread over its lanes, the 27
+// blocks around the run's block, which hold every neighbour of every voxel of the run,
+// and keeps their occupancy masks and first sorted positions in shared memory. Each
+// lane then resolves its voxel's 27 neighbours: a table indexed by the voxel's place
+// inside its block (the low 6 bits of its Morton code) gives, per offset, which of the
+// 27 blocks holds the neighbour and the neighbour's bit there; a bit test and a
+// popcount give the neighbour's sorted position, and the input row there is the answer.
+// The rows are staged in shared memory and written out coalesced. Depending on the mode
+// the warp writes
+//   kProbeNbr     each voxel's row of nbr at its input row;
+//   kProbeSorted  its row at its sorted position (a Morton-ordered copy of the table,
+//                 which the tile plan reorders) and its 27-bit presence mask as a
+//                 grouping key (window << 27 | mask) with its sorted position as the value.
+enum ProbeMode { kProbeNbr = 0, kProbeSorted = 1 };
+constexpr int kProbeThreads = 128;
+constexpr int kProbeWarps = kProbeThreads / 32;
+constexpr int kRunsAtOnce = 8;   // runs of a warp's 32 voxels whose blocks are held at once
 
 // One hash lookup: the block's occupancy mask and first sorted position (0 and 0 when
 // the block is not in the table). A slot is one 32-byte load.
@@ -651,19 +689,37 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
     const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
     const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int res,
     int bits, const Slot* __restrict__ table, int32_t* __restrict__ nbr,
-    const int32_t* __restrict__ plan_pos, unsigned long long* __restrict__ key2,
-    int32_t* __restrict__ val2, int window_shift, KmapStatus* st) {
-  // tbl[p][lane] = (lane holding the block of the neighbour at offset `lane` of a voxel
-  // at place p) << 8 | (that neighbour's place in its block); lanes 27..31 repeat the
-  // centre and write nothing
-  __shared__ uint16_t tbl[64 * 32];
-  for (int e = threadIdx.x; e < 64 * 32; e += kProbeThreads) {
-    const int p = e >> 5, l = e & 31, k = l < 27 ? l : 13;
+    unsigned long long* __restrict__ key2, int32_t* __restrict__ val2, int window_shift,
+    KmapStatus* st) {
+  // tbl[k][p] = (which of the 27 blocks around a voxel's block holds its neighbour at
+  // offset k, for a voxel at place p) << 8 | (that neighbour's place in its block); the
+  // lanes of a warp read one offset's row at their own places, without bank conflicts
+  __shared__ uint16_t tbl[27 * 64];
+  // per warp: the 27 blocks of up to kRunsAtOnce runs {mask low, mask high, first
+  // position, first position of the upper half}, the runs' block keys, and the 32
+  // voxels' rows
+  __shared__ uint4 s_blk[kProbeWarps][kRunsAtOnce][27];
+  __shared__ unsigned long long s_runkey[kProbeWarps][32];
+  __shared__ uint32_t s_need[kProbeWarps][32];   // per run: the blocks its voxels reach
+  __shared__ uint32_t need_tbl[64];              // per place: the blocks a voxel there reaches
+  __shared__ int32_t s_row[kProbeWarps][32 * 27];
+  for (int e = threadIdx.x; e < 27 * 64; e += kProbeThreads) {
+    const int k = e >> 6, p = e & 63;
     const int lz = ((p >> 2) & 1) | ((p >> 4) & 2), ly = ((p >> 1) & 1) | ((p >> 3) & 2),
               lx = (p & 1) | ((p >> 2) & 2);
     const int nz = lz + k / 9 - 1, ny = ly + (k / 3) % 3 - 1, nx = lx + k % 3 - 1;
     const int kb = 9 * ((nz >> 2) + 1) + 3 * ((ny >> 2) + 1) + ((nx >> 2) + 1);
     tbl[e] = static_cast<uint16_t>((kb << 8) | place_in_block(nz & 3, ny & 3, nx & 3));
+  }
+  for (int p = threadIdx.x; p < 64; p += kProbeThreads) {
+    uint32_t need = 0;
+    for (int k = 0; k < 27; ++k) {
+      const int lz = ((p >> 2) & 1) | ((p >> 4) & 2), ly = ((p >> 1) & 1) | ((p >> 3) & 2),
+                lx = (p & 1) | ((p >> 2) & 2);
+      const int nz = lz + k / 9 - 1, ny = ly + (k / 3) % 3 - 1, nx = lx + k % 3 - 1;
+      need |= 1u << (9 * ((nz >> 2) + 1) + 3 * ((ny >> 2) + 1) + ((nx >> 2) + 1));
+    }
+    need_tbl[p] = need;
   }
   __syncthreads();
   const bool second = st->plan[kMaxPasses] & 1;
@@ -672,94 +728,117 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
   const unsigned long long cmask = st->cap - 1;
   const int max_probe = st->cap < kMaxProbe ? static_cast<int>(st->cap) : kMaxProbe;
   const int lane = threadIdx.x & 31;
-  const int kk = lane < 27 ? lane : 13;
-  const int dz = kk / 9 - 1, dy = (kk / 3) % 3 - 1, dx = kk % 3 - 1;
-  const int bmax = (res - 1) >> 2;          // largest block coordinate along an axis
-  const int bshift = 3 * (bits - 2);        // batch bits of a block key
-  const unsigned long long bmorton = (1ull << bshift) - 1ull;
+  const int wid = threadIdx.x >> 5;
+  uint32_t* need_sm = s_need[wid];
+  uint4 (*blk_sm)[27] = s_blk[wid];
+  unsigned long long* runkey = s_runkey[wid];
+  int32_t* row_sm = s_row[wid];
+  // Block keys are (batch | Morton code of the block's coordinates); a neighbour block's
+  // key comes from the run's by a masked increment or decrement of one axis's
+  // interleaved bits, and the bounds test compares those bits, which keep the order of
+  // the coordinate, with the interleaved largest block coordinate.
+  const uint32_t bmax = static_cast<uint32_t>(res - 1) >> 2;
+  const uint32_t ones = (1u << (bits - 2)) - 1u;
+  const unsigned long long ax = spread3(ones), ay = ax << 1, az = ax << 2;
+  const unsigned long long lx = spread3(bmax), ly = lx << 1, lz = lx << 2;
+  const uint32_t n32 = static_cast<uint32_t>(N);
   constexpr unsigned kAll = 0xffffffffu;
   bool full = false, bad = false;
   const int64_t nwarps = (int64_t(gridDim.x) * kProbeThreads) >> 5;
   for (int64_t w = (blockIdx.x * int64_t(kProbeThreads) + threadIdx.x) >> 5; w * 32 < N;
        w += nwarps) {
     const int64_t s = w * 32 + lane;
-    const unsigned long long m = s < N ? mk[s] : ~0ull;
-    unsigned long long prev = __shfl_up_sync(kAll, m, 1);
-    if (lane == 0) prev = s > 0 ? mk[s - 1] : ~0ull;
-    unsigned starts = __ballot_sync(kAll, s < N && (s == 0 || (prev >> 6) != (m >> 6)));
-    while (starts) {
-      const int j0 = __ffs(starts) - 1;
-      starts &= starts - 1;
-      const int64_t s0 = w * 32 + j0;
-      const unsigned long long blk = __shfl_sync(kAll, m, j0) >> 6;   // the run's block key
-      // the run's first 32 positions, loaded before the lookups so that both are in flight
-      int64_t sj = s0 + lane;
-      unsigned long long mj = sj < N ? mk[sj] : ~0ull;
-      int32_t orow = -1;   // lane j: the row voxel s0 + j is written to
-      if (MODE == kProbeNbr && sj < N) orow = __ldg(ix + sj);
-      if (MODE == kProbePlan && sj < N) orow = __ldg(plan_pos + sj);
-      // lane k: the block at offset (dz, dy, dx) around the run's block
-      unsigned long long bm = 0;
-      int32_t bb = 0;
-      if (lane < 27) {
-        const unsigned long long bc = blk & bmorton;
-        const int nz = static_cast<int>(compact3(bc >> 2)) + dz;
-        const int ny = static_cast<int>(compact3(bc >> 1)) + dy;
-        const int nx = static_cast<int>(compact3(bc)) + dx;
-        if (nz >= 0 && ny >= 0 && nx >= 0 && nz <= bmax && ny <= bmax && nx <= bmax)
-          block_lookup(table, (blk & ~bmorton) | morton3(nz, ny, nx), cmask, max_probe, bm, bb,
-                       full);
+    const bool valid = s < N;
+    const int nvalid = (N - w * 32) < 32 ? static_cast<int>(N - w * 32) : 32;
+    const unsigned long long m = valid ? mk[s] : ~0ull;
+    const unsigned long long blk = m >> 6;
+    int32_t orow = -1;   // the row this lane's voxel is written to
+    if (MODE == kProbeNbr && valid) orow = __ldg(ix + s);
+    const unsigned long long prev = __shfl_up_sync(kAll, blk, 1);
+    const unsigned newb = __ballot_sync(kAll, valid && (lane == 0 || prev != blk));
+    const int run = __popc(newb & ((2u << lane) - 1u)) - 1;   // this lane's run, from 0
+    const int nruns = __popc(newb);
+    if ((newb >> lane) & 1u) {
+      runkey[run] = blk;
+      need_sm[run] = 0;
+    }
+    __syncwarp();
+    const uint32_t p = static_cast<uint32_t>(m) & 63u;
+    if (valid) atomicOr(&need_sm[run], need_tbl[p]);
+    __syncwarp();
+    uint32_t present_mask = 0;
+    for (int g0 = 0; g0 < nruns; g0 += kRunsAtOnce) {
+      const int G = nruns - g0 < kRunsAtOnce ? nruns - g0 : kRunsAtOnce;
+      // the blocks these runs' voxels reach (of the 27 around each run's block), one per
+      // lane: lookup q is the (q - first[r])-th needed block of run r
+      int total = 0;
+      for (int r = 0; r < G; ++r) total += __popc(need_sm[g0 + r]);
+      for (int q = lane; q < total; q += 32) {
+        int r = 0, before = 0;
+        for (;; ++r) {
+          const int c = __popc(need_sm[g0 + r]);
+          if (q < before + c) break;
+          before += c;
+        }
+        uint32_t nm = need_sm[g0 + r];
+        for (int i = q - before; i > 0; --i) nm &= nm - 1u;
+        const int kb = __ffs(nm) - 1;
+        const int dz = kb / 9 - 1, dy = (kb / 3) % 3 - 1, dx = kb % 3 - 1;
+        unsigned long long key = runkey[g0 + r];
+        bool inside = true;
+        if (dx > 0) { inside &= (key & ax) < lx; key = (((key | ~ax) + 1) & ax) | (key & ~ax); }
+        if (dx < 0) { inside &= (key & ax) != 0; key = (((key & ax) - 1) & ax) | (key & ~ax); }
+        if (dy > 0) { inside &= (key & ay) < ly; key = (((key | ~ay) + 1) & ay) | (key & ~ay); }
+        if (dy < 0) { inside &= (key & ay) != 0; key = (((key & ay) - 1) & ay) | (key & ~ay); }
+        if (dz > 0) { inside &= (key & az) < lz; key = (((key | ~az) + 1) & az) | (key & ~az); }
+        if (dz < 0) { inside &= (key & az) != 0; key = (((key & az) - 1) & az) | (key & ~az); }
+        unsigned long long bm = 0;
+        int32_t bb = 0;
+        if (inside) block_lookup(table, key, cmask, max_probe, bm, bb, full);
+        const uint32_t lo = static_cast<uint32_t>(bm), hi = static_cast<uint32_t>(bm >> 32);
+        blk_sm[r][kb] = make_uint4(lo, hi, static_cast<uint32_t>(bb),
+                                   static_cast<uint32_t>(bb) + __popc(lo));
       }
-      const uint32_t bm_lo = static_cast<uint32_t>(bm), bm_hi = static_cast<uint32_t>(bm >> 32);
-      // the run's voxels, 32 sorted positions at a time (a run without duplicates holds
-      // at most 64 voxels; duplicates, flagged by blocks_count, only make it longer)
-      for (int64_t c0 = s0;; c0 += 32) {
-        if (c0 != s0) {
-          sj = c0 + lane;
-          mj = sj < N ? mk[sj] : ~0ull;
-          orow = -1;
-          if (MODE == kProbeNbr && sj < N) orow = __ldg(ix + sj);
-          if (MODE == kProbePlan && sj < N) orow = __ldg(plan_pos + sj);
-        }
-        const unsigned inrun = __ballot_sync(kAll, sj < N && (mj >> 6) == blk);
-        const int len = inrun == kAll ? 32 : __ffs(~inrun) - 1;
-        uint32_t my_mask = 0;
-#pragma unroll 4
-        for (int j = 0; j < len; ++j) {
-          const uint32_t p = __shfl_sync(kAll, static_cast<uint32_t>(mj), j) & 63u;
-          const uint32_t e = tbl[p * 32 + lane];
-          const int kb = static_cast<int>(e >> 8);
+      __syncwarp();
+      if (valid && run >= g0 && run < g0 + G) {   // this lane's voxel: its 27 neighbours
+        const uint4* nb = blk_sm[run - g0];
+#pragma unroll
+        for (int k = 0; k < 27; ++k) {
+          const uint32_t e = tbl[k * 64 + p];
+          const uint4 b4 = nb[e >> 8];
           const uint32_t bit = e & 63u;
-          const uint32_t lo = __shfl_sync(kAll, bm_lo, kb);
-          const uint32_t hi = __shfl_sync(kAll, bm_hi, kb);
-          const int32_t bs = __shfl_sync(kAll, bb, kb);
-          const uint32_t word = bit < 32 ? lo : hi;
+          const bool upper = bit >= 32;
+          const uint32_t word = upper ? b4.y : b4.x;
           const uint32_t b5 = bit & 31u;
-          const bool present = lane < 27 && ((word >> b5) & 1u);
-          if (MODE == kProbeMask) {
-            const unsigned pm = __ballot_sync(kAll, present) & 0x7FFFFFFu;
-            if (lane == j) my_mask = pm;
-          } else {
-            int32_t val = -1;
-            if (present) {
-              const uint32_t below =
-                  __popc(word & ((1u << b5) - 1u)) + (bit >= 32 ? __popc(lo) : 0u);
-              const int64_t pos = int64_t(bs) + below;
-              if (pos < N) val = __ldg(ix + pos);
-              else bad = true;
-            }
-            const int32_t r = __shfl_sync(kAll, orow, j);
-            if (lane < 27 && static_cast<uint64_t>(r) < static_cast<uint64_t>(N))
-              nbr[int64_t(r) * 27 + lane] = val;
+          int32_t val = -1;
+          if ((word >> b5) & 1u) {
+            const uint32_t pos = (upper ? b4.w : b4.z) + __popc(word & ((1u << b5) - 1u));
+            present_mask |= 1u << k;
+            if (pos < n32) val = __ldg(ix + pos);
+            else bad = true;
           }
+          row_sm[lane * 27 + k] = val;
         }
-        if (MODE == kProbeMask && lane < len) {
-          key2[sj] = (static_cast<unsigned long long>(sj >> window_shift) << 27) | my_mask;
-          val2[sj] = static_cast<int32_t>(sj);
-        }
-        if (len < 32) break;
+      }
+      __syncwarp();
+    }
+    // the 32 rows, out of shared memory
+    if (MODE == kProbeSorted) {   // contiguous: rows of consecutive sorted positions
+      int32_t* dst = nbr + w * 32 * 27;
+      // (streaming stores: the table is written once and must not push the block table
+      // and the sort arrays, which the probe keeps reading, out of L2)
+      for (int i = lane; i < nvalid * 27; i += 32) __stcs(dst + i, row_sm[i]);
+      if (valid) {
+        key2[s] = (static_cast<unsigned long long>(s >> window_shift) << 27) | present_mask;
+        val2[s] = static_cast<int32_t>(s);
+      }
+    } else {                      // row by row, each to its input row
+      for (int j = 0; j < nvalid; ++j) {
+        const uint32_t r = static_cast<uint32_t>(__shfl_sync(kAll, orow, j));
+        if (lane < 27 && r < n32) __stcs(nbr + static_cast<size_t>(r) * 27u + lane, row_sm[j * 27 + lane]);
       }
     }
+    __syncwarp();
   }
   if (__any_sync(kAll, full) && lane == 0) atomicOr(&st->flags, kFlagFull);
   if (__any_sync(kAll, bad) && lane == 0) atomicOr(&st->flags, kFlagInternal);
@@ -767,39 +846,51 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
 
 // The tile plan from the grouping sort, a block of 128 threads per tile: plan row r is
 // the voxel at sorted position s = v2[r] (grouping key k2[r] = window << 27 | mask);
-// plan_pos[s] = r, perm[r] = its input row, and the tile's offset mask is the OR of its
-// rows' presence masks (the centre offset always included).
+// perm[r] = its input row, its row of the plan's nbr is the Morton-ordered row s
+// (copied: 27 contiguous words read, the tile's 128 rows written as one stretch), and
+// the tile's offset mask is the OR of its rows' presence masks (the centre always
+// included).
 __global__ void __launch_bounds__(128) kmap_plan_index(
     const unsigned long long* __restrict__ k2a, const unsigned long long* __restrict__ k2b,
     const int32_t* __restrict__ v2a, const int32_t* __restrict__ v2b,
     const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int64_t ntiles,
-    int32_t* __restrict__ plan_pos, int32_t* __restrict__ perm, uint32_t* __restrict__ tmask,
-    KmapStatus* st) {
+    const int32_t* __restrict__ nbr_sorted, int32_t* __restrict__ perm,
+    int32_t* __restrict__ pnbr, uint32_t* __restrict__ tmask, KmapStatus* st) {
   const bool sec2 = st->plan2[kMaxPasses] & 1;
   const unsigned long long* k2 = sec2 ? k2b : k2a;
   const int32_t* v2 = sec2 ? v2b : v2a;
   const int32_t* ix = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
   __shared__ uint32_t wm[4];
+  __shared__ int32_t src[128];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   bool bad = false;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int64_t r = t * 128 + threadIdx.x;
     uint32_t m = 0;
+    int32_t sp = -1;
     if (r < N) {
-      const int32_t sp = v2[r];
+      sp = v2[r];
       if (static_cast<uint64_t>(sp) < static_cast<uint64_t>(N)) {
-        plan_pos[sp] = static_cast<int32_t>(r);
         perm[r] = ix[sp];
         m = static_cast<uint32_t>(k2[r]) & 0x7FFFFFFu;
       } else {
         perm[r] = -1;
+        sp = -1;
         bad = true;
       }
     }
+    src[threadIdx.x] = sp;
     for (int o = 16; o > 0; o >>= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
     if (lane == 0) wm[warp] = m;
     __syncthreads();
     if (threadIdx.x == 0) tmask[t] = wm[0] | wm[1] | wm[2] | wm[3] | (1u << 13);
+    const int rows = static_cast<int>((N - t * 128) < 128 ? (N - t * 128) : 128);
+    int32_t* dst = pnbr + t * 128 * 27;
+    for (int w = threadIdx.x; w < rows * 27; w += 128) {
+      const int rr = w / 27, k = w - 27 * rr;
+      const int32_t from = src[rr];
+      dst[w] = from >= 0 ? nbr_sorted[int64_t(from) * 27 + k] : -1;
+    }
     __syncthreads();
   }
   if (bad) atomicOr(&st->flags, kFlagInternal);
@@ -935,6 +1026,50 @@ __device__ __forceinline__ bool parent_starts(const unsigned long long* mk, int6
   return s == 0 || (mk[s - 1] >> 3) != (mk[s] >> 3);
 }
 
+// The sort keys of a voxel set in a Morton order the caller already has (the kernel
+// map's `order` on the same coordinates): mk[s] = key of input row order[s]. Checks what
+// the sort would otherwise guarantee: rows in range, coordinates in range, keys
+// ascending (an order that is not the Morton order is an argument error).
+__global__ void __launch_bounds__(256) ds_keys_in_order(
+    const int4* __restrict__ coords, const int32_t* __restrict__ order, int64_t N, int res,
+    int bits, unsigned long long* __restrict__ mk, int32_t* __restrict__ ix, KmapStatus* st) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  auto key_of = [&](int32_t r, bool& good) -> unsigned long long {
+    const int4 c = coords[r];
+    good = good && static_cast<unsigned>(c.x) <= SUBM3D_MAX_BATCH &&
+           static_cast<unsigned>(c.y) < static_cast<unsigned>(res) &&
+           static_cast<unsigned>(c.z) < static_cast<unsigned>(res) &&
+           static_cast<unsigned>(c.w) < static_cast<unsigned>(res);
+    return (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w);
+  };
+  // whole warps per round: the previous position's key comes from the lane before
+  for (int64_t w0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x - lane; w0 < N; w0 += stride) {
+    const int64_t s = w0 + lane;
+    const bool live = s < N;
+    const int32_t row = live ? order[s] : 0;
+    unsigned long long key = 0;
+    bool ok = live && static_cast<uint64_t>(row) < static_cast<uint64_t>(N);
+    if (ok) key = key_of(row, ok);
+    unsigned long long prev_key = __shfl_up_sync(0xffffffffu, key, 1);
+    bool prev_ok = __shfl_up_sync(0xffffffffu, ok, 1);
+    if (lane == 0 && s > 0 && live) {
+      const int32_t prow = order[s - 1];
+      prev_ok = static_cast<uint64_t>(prow) < static_cast<uint64_t>(N);
+      if (prev_ok) prev_key = key_of(prow, prev_ok);
+    }
+    if (!live) continue;
+    if (ok && s > 0 && prev_ok && prev_key > key) ok = false;
+    if (!ok) {
+      atomicOr(&st->flags, kFlagOrder);
+      atomicMin(&st->bad_row, static_cast<long long>(s));
+      key = 0;
+    }
+    mk[s] = key;
+    ix[s] = ok ? row : 0;
+  }
+}
+
 // Parents per tile; duplicate keys (adjacent equal) and sort indices out of range are
 // flagged in the status word.
 __global__ void __launch_bounds__(kSortThreads) ds_count(
@@ -992,7 +1127,7 @@ __global__ void __launch_bounds__(kSortThreads) ds_emit(
     const unsigned long long* __restrict__ mk1, const int32_t* __restrict__ ix0,
     const int32_t* __restrict__ ix1, int64_t N, const uint32_t* __restrict__ tsum,
     int4* __restrict__ coarse, int32_t* __restrict__ parent, uint8_t* __restrict__ cmask,
-    int32_t* __restrict__ pstart, const KmapStatus* st) {
+    int32_t* __restrict__ pstart, int bits, const KmapStatus* st) {
   if (st->flags & kFlagInternal) return;
   const bool second = st->plan[kMaxPasses] & 1;
   const unsigned long long* mk = second ? mk1 : mk0;
@@ -1015,15 +1150,21 @@ __global__ void __launch_bounds__(kSortThreads) ds_emit(
     const int32_t row = ix[s];
     parent[row] = static_cast<int32_t>(p);
     if (head) {
-      const int4 c = coords[row];   // (b, z, y, x)
-      coarse[p] = make_int4(c.x, c.y >> 1, c.z >> 1, c.w >> 1);
+      // the parent's coordinates and the children's bits from the sort keys (the lowest
+      // Morton triple is (z&1)<<2 | (y&1)<<1 | (x&1), the child bit)
+      const unsigned long long k0 = mk[s];
+      const unsigned long long morton = k0 & ((1ull << (3 * bits)) - 1ull);
+      coarse[p] = make_int4(static_cast<int>(k0 >> (3 * bits)),
+                            static_cast<int>(compact3(morton >> 2) >> 1),
+                            static_cast<int>(compact3(morton >> 1) >> 1),
+                            static_cast<int>(compact3(morton) >> 1));
       pstart[p] = static_cast<int32_t>(s);
-      const unsigned long long key = mk[s] >> 3;
+      const unsigned long long key = k0 >> 3;
       uint32_t mask = 0;
       for (int t = 0; t < 8 && s + t < N; ++t) {
-        if ((mk[s + t] >> 3) != key) break;
-        const int4 d = coords[ix[s + t]];
-        mask |= 1u << (((d.y & 1) << 2) | ((d.z & 1) << 1) | (d.w & 1));
+        const unsigned long long kt = mk[s + t];
+        if ((kt >> 3) != key) break;
+        mask |= 1u << (kt & 7u);
       }
       cmask[p] = static_cast<uint8_t>(mask);
     }
@@ -1081,12 +1222,19 @@ struct Vec<__nv_bfloat16, 8> {
 };
 
 // Pools each parent's children: a thread per (parent, V consecutive channels), fp32
-// accumulation, mean = sum / count, rounded once to the feature dtype.
+// accumulation, mean = sum / count, rounded once to the feature dtype. The number of
+// parents and the sorted order are read on the device (the launch is enqueued before
+// the host learns M).
 template <typename T, int V>
 __global__ void __launch_bounds__(256) ds_pool(const T* __restrict__ feats, int C,
-                                               const int32_t* __restrict__ ix,
-                                               const int32_t* __restrict__ pstart, int64_t M,
-                                               int mode, T* __restrict__ out) {
+                                               const int32_t* __restrict__ ix0,
+                                               const int32_t* __restrict__ ix1,
+                                               const int32_t* __restrict__ pstart,
+                                               const uint32_t* __restrict__ m_dev, int mode,
+                                               T* __restrict__ out, const KmapStatus* st) {
+  if (st->flags) return;   // the structure failed: the call reports it, nothing to pool
+  const int32_t* ix = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
+  const int64_t M = *m_dev;
   const int cv = C / V;
   const int64_t total = M * cv;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -1306,7 +1454,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     const int rc = launch_sort(c4, N, res, L, ws, stream);
     if (rc != SUBM3D_OK) return rc;
   }
-  kmap_blocks_count<<<grid_for(N, 256, 8), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
+  kmap_blocks_count<<<grid_for(N, 256, 4), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
   SUBM3D_LAUNCHED("kmap_blocks_count");
   kmap_table_init<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, hash_capacity, cap_max, st);
   SUBM3D_LAUNCHED("kmap_table_init");
@@ -1314,10 +1462,27 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
                                                               st);
   SUBM3D_LAUNCHED("kmap_blocks_insert");
   g_stage.mark("block table", stream);
-  const int probe_grid = grid_for((N + 31) / 32 * 32, kProbeThreads, 8);
+  // the probe's grid is exactly the blocks that fit on the GPU at once (its shared memory
+  // limits them), so that its grid-stride loop runs in one wave
+  static PerDevice<int> probe_fit[2];
+  int fit = 0;
+  {
+    const int mode = grouped ? 1 : 0;
+    const int rc = probe_fit[mode].get(&fit, [mode](int* v) -> int {
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, mode ? reinterpret_cast<const void*>(kmap_probe<kProbeSorted>)
+                   : reinterpret_cast<const void*>(kmap_probe<kProbeNbr>),
+          kProbeThreads, 0);
+      *v = (e == cudaSuccess && n > 0) ? n : 4;
+      return static_cast<int>(SUBM3D_OK);
+    });
+    if (rc != SUBM3D_OK) return rc;
+  }
+  const int probe_grid = grid_for((N + 31) / 32 * 32, kProbeThreads, fit);
   if (!grouped) {
     kmap_probe<kProbeNbr><<<probe_grid, kProbeThreads, 0, stream>>>(
-        mk0, mk1, ix0, ix1, N, res, bits, table, nbr, nullptr, nullptr, nullptr, 0, st);
+        mk0, mk1, ix0, ix1, N, res, bits, table, nbr, nullptr, nullptr, 0, st);
     SUBM3D_LAUNCHED("kmap_probe");
     g_stage.mark("probe", stream);
   } else {
@@ -1329,7 +1494,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     unsigned long long* k2b = reinterpret_cast<unsigned long long*>(ws + L.k2b);
     int32_t* v2a = reinterpret_cast<int32_t*>(ws + L.v2a);
     int32_t* v2b = reinterpret_cast<int32_t*>(ws + L.v2b);
-    int32_t* plan_pos = reinterpret_cast<int32_t*>(ws + L.plan_pos);
+    int32_t* nbr_sorted = reinterpret_cast<int32_t*>(ws + L.nbr_sorted);
     uint32_t* hist2 = reinterpret_cast<uint32_t*>(ws + L.hist2);
     int wshift = 0;
     while ((int64_t(1) << wshift) < window) ++wshift;
@@ -1337,10 +1502,10 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     int wbits = 0;
     while ((last_window >> wbits) != 0) ++wbits;
     const int npass2 = (27 + wbits + 7) / 8;
-    kmap_probe<kProbeMask><<<probe_grid, kProbeThreads, 0, stream>>>(
-        mk0, mk1, ix0, ix1, N, res, bits, table, nullptr, nullptr, k2a, v2a, wshift, st);
-    SUBM3D_LAUNCHED("kmap_probe_mask");
-    g_stage.mark("mask probe", stream);
+    kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
+        mk0, mk1, ix0, ix1, N, res, bits, table, nbr_sorted, k2a, v2a, wshift, st);
+    SUBM3D_LAUNCHED("kmap_probe_sorted");
+    g_stage.mark("probe (Morton order) + masks", stream);
     kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);
     SUBM3D_LAUNCHED("kmap_plan2");
     const int* plans2 = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
@@ -1349,13 +1514,9 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
                                 st, stream, "grouping sort pass");
     if (rc != SUBM3D_OK) return rc;
     kmap_plan_index<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
-        k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, plan_pos, perm, tmask, st);
+        k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, nbr_sorted, perm, pnbr, tmask, st);
     SUBM3D_LAUNCHED("kmap_plan_index");
-    g_stage.mark("plan index", stream);
-    kmap_probe<kProbePlan><<<probe_grid, kProbeThreads, 0, stream>>>(
-        mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, plan_pos, nullptr, nullptr, 0, st);
-    SUBM3D_LAUNCHED("kmap_probe_plan");
-    g_stage.mark("plan probe", stream);
+    g_stage.mark("plan index + rows", stream);
   }
 
   if (!sync) {
@@ -1447,15 +1608,18 @@ size_t downsample_workspace_bytes(int64_t N) {
 
 namespace {
 template <typename T>
-int launch_pool(const void* feats, int C, const int32_t* ix, const int32_t* pstart, int64_t M,
-                int mode, void* out, cudaStream_t stream) {
+int launch_pool(const void* feats, int C, const int32_t* ix0, const int32_t* ix1,
+                const int32_t* pstart, const uint32_t* m_dev, int64_t M_max, int mode, void* out,
+                const KmapStatus* st, cudaStream_t stream) {
   constexpr int V = 16 / sizeof(T);
   const T* f = static_cast<const T*>(feats);
   T* o = static_cast<T*>(out);
   if (C % V == 0) {
-    ds_pool<T, V><<<grid_for(M * (C / V), 256, 8), 256, 0, stream>>>(f, C, ix, pstart, M, mode, o);
+    ds_pool<T, V><<<grid_for(M_max * (C / V), 256, 8), 256, 0, stream>>>(f, C, ix0, ix1, pstart,
+                                                                         m_dev, mode, o, st);
   } else {
-    ds_pool<T, 1><<<grid_for(M * C, 256, 8), 256, 0, stream>>>(f, C, ix, pstart, M, mode, o);
+    ds_pool<T, 1><<<grid_for(M_max * C, 256, 8), 256, 0, stream>>>(f, C, ix0, ix1, pstart, m_dev,
+                                                                   mode, o, st);
   }
   SUBM3D_LAUNCHED("ds_pool");
   return SUBM3D_OK;
@@ -1478,10 +1642,11 @@ int launch_unpool(const void* coarse, int64_t M, int C, const int32_t* parent, i
 }
 }  // namespace
 
-int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* feats, int32_t C,
-                     subm3d_dtype dtype, int mode, int32_t* coarse_coords, void* coarse_feats,
-                     int32_t* parent, uint8_t* child_mask, int64_t* M_out, void* workspace,
-                     size_t ws_bytes, cudaStream_t stream) {
+int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_t* order,
+                     const void* feats, int32_t C, subm3d_dtype dtype, int mode,
+                     int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
+                     uint8_t* child_mask, int64_t* M_out, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
   if (!M_out) {
     set_error("subm3d_downsample: M_out (host) is NULL");
     return SUBM3D_ERR_ARG;
@@ -1541,7 +1706,18 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* 
   uint32_t* tsum = reinterpret_cast<uint32_t*>(ws + D.tsum);
   int32_t* pstart = reinterpret_cast<int32_t*>(ws + D.pstart);
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-  {
+  if (order) {   // the caller's Morton order: keys gathered in that order, no sort
+    if (reinterpret_cast<uintptr_t>(order) & 15) {
+      set_error("subm3d_downsample_sorted: order=%p must be 16-byte aligned", (const void*)order);
+      return SUBM3D_ERR_ARG;
+    }
+    int bits = 2;
+    while ((1 << bits) < res) ++bits;
+    kmap_init<<<8, 256, 0, stream>>>(st, reinterpret_cast<uint32_t*>(ws + L.hist), nullptr);
+    SUBM3D_LAUNCHED("kmap_init");
+    ds_keys_in_order<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, order, N, res, bits, mk0, ix0, st);
+    SUBM3D_LAUNCHED("ds_keys_in_order");
+  } else {
     const int rc = launch_sort(c4, N, res, L, ws, stream);
     if (rc != SUBM3D_OK) return rc;
   }
@@ -1550,14 +1726,31 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* 
   SUBM3D_LAUNCHED("ds_count");
   ds_scan<<<1, 256, 0, stream>>>(tsum, D.ntile, st);
   SUBM3D_LAUNCHED("ds_scan");
+  int bits = 2;
+  while ((1 << bits) < res) ++bits;
   ds_emit<<<ntile, kSortThreads, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, tsum,
                                               reinterpret_cast<int4*>(coarse_coords), parent,
-                                              child_mask, pstart, st);
+                                              child_mask, pstart, bits, st);
   SUBM3D_LAUNCHED("ds_emit");
+  if (feats) {   // enqueued before the wait: M is read on the device
+    const int prc =
+        dtype == SUBM3D_BF16
+            ? launch_pool<__nv_bfloat16>(feats, C, ix0, ix1, pstart, tsum + D.ntile, N, mode,
+                                         coarse_feats, st, stream)
+            : launch_pool<float>(feats, C, ix0, ix1, pstart, tsum + D.ntile, N, mode,
+                                 coarse_feats, st, stream);
+    if (prc != SUBM3D_OK) return prc;
+  }
 
   KmapStatus host;
   SUBM3D_CUDA_TRY(cudaMemcpyAsync(&host, st, sizeof(host), cudaMemcpyDeviceToHost, stream));
   SUBM3D_CUDA_TRY(cudaStreamSynchronize(stream));
+  if (host.flags & kFlagOrder) {
+    set_error("subm3d_downsample_sorted: order[%lld] does not continue the Morton order of the "
+              "coordinates (a row outside [0, N), a coordinate outside the grid, or a smaller key)",
+              host.bad_row);
+    return SUBM3D_ERR_ARG;
+  }
   if (host.flags & kFlagCoord) {
     set_error("subm3d_downsample: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d",
               host.bad_row, SUBM3D_MAX_BATCH, res);
@@ -1579,11 +1772,7 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const void* 
     return SUBM3D_ERR_DEVICE;
   }
   *M_out = M;
-  if (!feats) return SUBM3D_OK;
-  const int32_t* ix = (host.plan[kMaxPasses] & 1) ? ix1 : ix0;
-  return dtype == SUBM3D_BF16
-             ? launch_pool<__nv_bfloat16>(feats, C, ix, pstart, M, mode, coarse_feats, stream)
-             : launch_pool<float>(feats, C, ix, pstart, M, mode, coarse_feats, stream);
+  return SUBM3D_OK;
 }
 
 int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,

@@ -222,3 +222,45 @@ def test_spatial2channel_full_workload_and_bad_parent(dev):
     assert e.value.code == B.ERR_DEVICE and "parent" in str(e.value)
     assert float(fine[3].float().abs().sum()) == 0.0
     assert torch.equal(fine[4:], f[4:])
+
+
+@pytest.mark.parametrize("seed,res,batch,n,C", [(0, 9, 2, 300, 8), (1, 40, 3, 5000, 64),
+                                                 (2, 1, 2, 1, 16), (4, 129, 1, 7000, 12)])
+def test_downsample_on_the_kernel_maps_order(dev, seed, res, batch, n, C):
+    # the Morton order the kernel map wrote for the same coords: the same result as the
+    # downsample that sorts by itself, bit for bit (structure and pooled rows)
+    from submanifold_sparse_convolution_04_b300 import subm3d_build_kmap_ex
+    rng = np.random.default_rng(seed + 100)
+    c = random_set(rng, res, batch, n)
+    f = values(rng, c.shape[0], C, "bf16")
+    ct, ft = torch.from_numpy(c).to(dev), as_tensor(f, "bf16", dev)
+    _, order = subm3d_build_kmap_ex(ct, res, order=True)
+    for mode in ("mean", "max"):
+        got = subm3d_downsample(ct, res, ft, mode, order=order)
+        plain = subm3d_downsample(ct, res, ft, mode)
+        want = ref.downsample(c, f, res, mode)
+        check_structure(got, want)
+        assert torch.equal(got[1], plain[1])
+        assert_close(got[1].float().cpu().numpy(), want[1], "bf16", f"sorted {mode}")
+
+
+def test_downsample_on_order_full_workload_and_a_wrong_order(dev):
+    from submanifold_sparse_convolution_04_b300 import subm3d_build_kmap_ex
+    case = cached_case(5)
+    c, f, _, _ = to_device(case, dev)
+    _, order = subm3d_build_kmap_ex(c, case["res"], order=True)
+    got = subm3d_downsample(c, case["res"], f, "mean", order=order)
+    plain = subm3d_downsample(c, case["res"], f, "mean")
+    for a, b in zip(got, plain):
+        assert torch.equal(a, b)
+    bad = order.clone()
+    bad[[10, 11]] = bad[[11, 10]]           # two positions swapped: keys no longer ascend
+    with pytest.raises(Subm3dError) as e:
+        subm3d_downsample(c, case["res"], f, "mean", order=bad)
+    assert e.value.code == B.ERR_ARG
+    bad[10] = c.shape[0] + 5                 # a row outside [0, N)
+    with pytest.raises(Subm3dError):
+        subm3d_downsample(c, case["res"], f, "mean", order=bad)
+    # recovery
+    got2 = subm3d_downsample(c, case["res"], f, "mean", order=order)
+    assert torch.equal(got2[1], plain[1])

@@ -11,13 +11,17 @@
 // stage costs 48 KB of shared-memory traffic at O = 64 (16 KB of cp.async writes,
 // most of them zero-fill, the MMA re-reading them, and the weight tile written and
 // read), and the shared-memory port, not HBM, sets the pace. Here:
-//   * a producer warp gathers its 32 rows of an offset with coalesced 16-byte cp.async
-//     copies (eight lanes per 128-byte row) into its own shared-memory staging area, an
-//     absent neighbour costing no copy at all; each lane then reads its own row back
-//     (zeros for an absent one) and writes it with tcgen05.st into a tensor-memory
-//     stage, the row in the lane of its output row, channels 2c and 2c+1 in column c.
-//     Whole-row copies cost the L1 data pipe one pass per row; with each lane loading
-//     its own row, 32 bytes at a time, the pipe took about eight and bounded the kernel;
+//   * the gathered rows reach a tensor-memory stage through registers, the row in the
+//     lane of its output row, channels 2c and 2c+1 in column c, written by tcgen05.st;
+//     an absent neighbour costs no load at all (zeros). Two forms of the gather:
+//     - each lane loads its own row with four 32-byte read-only loads (six producer
+//       groups): few instructions per row, but the L1 data pipe takes about eight passes
+//       per row; the faster form for input-order tiles, which run all 27 offsets;
+//     - a producer warp copies its 32 rows of an offset with coalesced 16-byte cp.async
+//       copies (eight lanes per 128-byte row) into its own shared-memory staging area,
+//       and each lane reads its own row back (four producer groups, a staging buffer
+//       per offset of a stage): one L1 pass per row, more instructions per offset; the
+//       faster form for the tiles of a plan, which run about half the offsets;
 //   * tcgen05.mma reads A from tensor memory and only B, the stage's weight tap
 //     W_k = weight[:, kz, ky, kx, :] ([O x 64] K-major, 128-byte swizzle, fetched by
 //     TMA into the stage's weight slot), from shared memory;
@@ -26,15 +30,15 @@
 //     a producer reads its row's index with one conflict-free shared load (27 is
 //     odd) instead of one 32-byte global sector per 4-byte index.
 // Tensor memory (512 columns allocated): two accumulators of 64 columns (double buffer)
-// and four A stages of 64 columns. A stage carries two offsets of the tile (consecutive
-// offsets of its mask; the last may have one), because every stage costs the single
-// MMA-issuing warp a barrier wait and a commit. Stage g of the CTA is filled by producer
-// group g mod 4 (four warps, warp w writing lanes 32 (w % 4) .. + 31) into slot g mod 4:
-// each warp starts the copies of its rows of both offsets into its two staging buffers
-// (so both are in flight while the slot frees), then reads back and stores the first,
-// then the second; the group leader fetches both weight taps into the stage's weight
-// slot by TMA. The stage is full when its four warps have arrived (after
-// tcgen05.wait::st) and its weight bytes have landed.
+// and one A stage of 64 columns per producer group (six or four). A stage carries two
+// offsets of the tile (consecutive offsets of its mask; the last may have one), because
+// every stage costs the single MMA-issuing warp a barrier wait and a commit. Stage g of
+// the CTA is filled by producer group g mod G (four warps, warp w writing lanes
+// 32 (w % 4) .. + 31) into slot g mod G: each warp starts its rows of the stage's first
+// offset (with staging, of both offsets) while the slot frees, stores the first and then
+// the second; the group leader fetches both weight taps into the stage's weight slot by
+// TMA. The stage is full when its four warps have arrived (after tcgen05.wait::st) and
+// its weight bytes have landed.
 // One elected lane of the MMA warp issues the stage's MMAs (M = 128, N = O, K = 16,
 // up to four per offset) and frees the slot with tcgen05.commit. Four epilogue warps drain tile
 // t (tcgen05.ld -> + bias [+ residual row, activation: the fused block epilogue] ->
@@ -51,32 +55,41 @@ namespace subm3d {
 namespace {
 
 constexpr int kBM = 128;              // output rows per tile = tensor-memory lanes
-constexpr int kGroups = 4;            // producer groups of four warps
-constexpr int kStages = 4;            // A stages in tensor memory
 constexpr int kOffCols = 32;          // one offset's row: 64 bf16 = 32 columns of 32 bits
 constexpr int kStageCols = 2 * kOffCols;   // a stage holds two offsets (2p, 2p + 1)
-constexpr int kPairs = 14;            // stages per tile: offsets (0,1) .. (24,25), (26)
 constexpr int kAccCols = 64;          // one accumulator (N <= 64)
 constexpr int kAColBase = 2 * kAccCols;
-constexpr int kProducerWarps = 4 * kGroups;
-constexpr int kMmaWarp = kProducerWarps;
-constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 17..20: lane groups 1, 2, 3, 0
-constexpr int kNbrWarp = kEpiWarp0 + 4;
-constexpr int kThreads = 32 * (kNbrWarp + 1);    // 704
 constexpr int kNbrTileBytes = kBM * 27 * 4;      // one tile's rows of nbr
 constexpr int kRowsStaging = 32 * 128;           // a producer warp's 32 gathered rows
-constexpr int kWarpStaging = 2 * kRowsStaging;   // one buffer per offset of a stage
-constexpr int kStagingBytes = kProducerWarps * kWarpStaging;
 constexpr int kSmemLimit = 227 * 1024;
-static_assert(kAColBase + kStages * kStageCols <= 512, "tensor memory layout");
-static_assert(kStages % kGroups == 0, "slots per group");
 
-template <int NMMA>
+// Warp roles and pipeline depth of the two gather forms (see the file comment):
+// STAGED, whole rows copied through a per-warp shared-memory staging area, four producer
+// groups with two buffers per warp; otherwise each lane loads its own row into
+// registers, six producer groups (more warps keep more loads in flight).
+template <bool STAGED>
+struct TmRoles {
+  static constexpr int kGroups = STAGED ? 4 : 6;        // producer groups of four warps
+  static constexpr int kStages = kGroups;               // A stages in tensor memory
+  static constexpr int kProducerWarps = 4 * kGroups;
+  static constexpr int kMmaWarp = kProducerWarps;
+  static constexpr int kEpiWarp0 = kMmaWarp + 1;        // four warps: lane groups w % 4
+  static constexpr int kNbrWarp = kEpiWarp0 + 4;
+  static constexpr int kThreads = 32 * (kNbrWarp + 1);  // 704 staged, 960 otherwise
+  static constexpr int kWarpStaging = STAGED ? 2 * kRowsStaging : 0;   // a buffer per offset
+  static constexpr int kStagingBytes = kProducerWarps * kWarpStaging;
+  static_assert(kAColBase + kStages * kStageCols <= 512, "tensor memory layout");
+  static_assert(kStages % kGroups == 0, "slots per group");
+  static_assert(((kEpiWarp0 & 3) + 0) >= 0, "epilogue warps cover the four lane groups");
+};
+
+template <int NMMA, bool STAGED>
 struct TmCfg {
-  static constexpr int kTapBytes = NMMA * 128;            // one [NMMA x 64] weight tile
-  static constexpr int kWBytes = kStages * 2 * kTapBytes;  // two taps per stage
+  using R = TmRoles<STAGED>;
+  static constexpr int kTapBytes = NMMA * 128;               // one [NMMA x 64] weight tile
+  static constexpr int kWBytes = R::kStages * 2 * kTapBytes;  // two taps per stage
   static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 2 * kNbrTileBytes +
-                               512 /*barriers*/ + 256 * 4 /*bias*/ + kStagingBytes;
+                               512 /*barriers*/ + 256 * 4 /*bias*/ + R::kStagingBytes;
   // at least half the SM's shared memory, so that one CTA (which takes all of tensor
   // memory) runs per SM
   static constexpr int kSmemBytes = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
@@ -195,10 +208,26 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 
-template <int NMMA>
-__global__ void __launch_bounds__(kThreads, 1)
+// 32 read-only bytes (8 words) from a 32-byte-aligned global address.
+__device__ __forceinline__ void ld32B(const void* p, uint32_t* w) {
+  asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+template <int NMMA, bool STAGED>
+__global__ void __launch_bounds__(TmRoles<STAGED>::kThreads, 1)
     fwd_tm(const __grid_constant__ CUtensorMap wmap, const TmParams p) {
-  using C = TmCfg<NMMA>;
+  using C = TmCfg<NMMA, STAGED>;
+  using R = TmRoles<STAGED>;
+  constexpr int kGroups = R::kGroups;
+  constexpr int kStages = R::kStages;
+  constexpr int kProducerWarps = R::kProducerWarps;
+  constexpr int kMmaWarp = R::kMmaWarp;
+  constexpr int kEpiWarp0 = R::kEpiWarp0;
+  constexpr int kNbrWarp = R::kNbrWarp;
+  constexpr int kWarpStaging = R::kWarpStaging;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -283,6 +312,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nor the row reads below conflict; then every lane reads its own row back. Loading
     // whole rows per instruction costs the L1 data pipe one pass per 128-byte row
     // instead of one per 16 bytes of each lane's own row.
+    // each lane's own row into registers: four 32-byte read-only loads (the form without
+    // staging, for the dense offsets of input-order tiles)
+    auto load_row = [&](int32_t j, uint32_t (&v)[32]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // 16 channels (32 bytes) per load
+        if (j >= 0 && q * 16 < p.I) {
+          ld32B(p.feats + int64_t(j) * p.I + q * 16, v + 8 * q);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * q + e] = 0u;
+        }
+      }
+    };
     // buffer b of the warp holds the rows of the stage's offset b, so that both offsets'
     // copies are in flight at once
     const uint32_t stage_base = sStage + warp * kWarpStaging;
@@ -356,8 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t v[32];
       const int32_t j0 = row_index(lt, k0);
       const int32_t j1 = two ? row_index(lt, k1) : -1;
-      gather_issue(j0, 0);   // both offsets' rows in flight while the slot frees
-      if (two) gather_issue(j1, 1);
+      if constexpr (STAGED) {
+        gather_issue(j0, 0);   // both offsets' rows in flight while the slot frees
+        if (two) gather_issue(j1, 1);
+      } else {
+        load_row(j0, v);       // in flight while the slot frees
+      }
       const uint32_t s = g % kStages;
       const uint32_t use = g / kStages;
       const bool ok = mbar_wait(aempty0 + 8 * s, (use & 1u) ^ 1u, abort_flag);
@@ -373,11 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       last = g + kGroups;
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + kAColBase + s * kStageCols;
-      gather_finish(j0, 0, two ? 1 : 0, v);
+      if constexpr (STAGED) gather_finish(j0, 0, two ? 1 : 0, v);
       tmem_st32(taddr, v);
       if (two) {
         tmem_st_wait();   // v is free again
-        gather_finish(j1, 1, 0, v);
+        if constexpr (STAGED) gather_finish(j1, 1, 0, v);
+        else load_row(j1, v);
         tmem_st32(taddr + kOffCols, v);
       }
       tmem_st_wait();
@@ -556,11 +603,12 @@ TmEncodeTiledFn tm_get_encode() {
   return fn;
 }
 
-template <int NMMA>
+template <int NMMA, bool STAGED>
 int tm_launch(const TmParams& prm, const __nv_bfloat16* weight, cudaStream_t stream) {
-  using C = TmCfg<NMMA>;
+  using C = TmCfg<NMMA, STAGED>;
   static PerDevice<bool> attr_set;
-  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(fwd_tm<NMMA>),
+  const int arc = set_smem_limit_once(attr_set,
+                                      reinterpret_cast<const void*>(fwd_tm<NMMA, STAGED>),
                                       C::kSmemBytes, "fwd_tm");
   if (arc != SUBM3D_OK) return arc;
   TmEncodeTiledFn encode = tm_get_encode();
@@ -585,7 +633,7 @@ int tm_launch(const TmParams& prm, const __nv_bfloat16* weight, cudaStream_t str
     return SUBM3D_ERR_CUDA;
   }
   const int grid = prm.ntiles < num_sms() ? prm.ntiles : num_sms();
-  fwd_tm<NMMA><<<grid, kThreads, C::kSmemBytes, stream>>>(wmap, prm);
+  fwd_tm<NMMA, STAGED><<<grid, TmRoles<STAGED>::kThreads, C::kSmemBytes, stream>>>(wmap, prm);
   SUBM3D_LAUNCHED("fwd_tm");
   return SUBM3D_OK;
 }
@@ -609,11 +657,20 @@ int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
   if (!err) return SUBM3D_ERR_CUDA;
   TmParams prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual),
                epi.act, N, I, O, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
+  // Tiles of a plan run about half the offsets, so their fewer stages can afford whole-
+  // row copies through shared memory (which spare the L1 data pipe); dense input-order
+  // tiles run every offset and go faster with each lane loading its own row, which
+  // needs 32-byte-aligned rows.
+  const bool staged = plan.tmask != nullptr || (reinterpret_cast<uintptr_t>(feats) & 31) != 0;
   switch (O) {
-    case 16: return tm_launch<16>(prm, weight, stream);
-    case 32: return tm_launch<32>(prm, weight, stream);
-    case 48: return tm_launch<48>(prm, weight, stream);
-    case 64: return tm_launch<64>(prm, weight, stream);
+    case 16: return staged ? tm_launch<16, true>(prm, weight, stream)
+                           : tm_launch<16, false>(prm, weight, stream);
+    case 32: return staged ? tm_launch<32, true>(prm, weight, stream)
+                           : tm_launch<32, false>(prm, weight, stream);
+    case 48: return staged ? tm_launch<48, true>(prm, weight, stream)
+                           : tm_launch<48, false>(prm, weight, stream);
+    case 64: return staged ? tm_launch<64, true>(prm, weight, stream)
+                           : tm_launch<64, false>(prm, weight, stream);
     default:
       set_error("subm3d_forward: O=%d outside the narrow tensor-core kernel's range", O);
       return SUBM3D_ERR_UNSUPPORTED;

@@ -345,16 +345,19 @@ def active_passes(coords, res):
 
 def kmap_algorithmic_bytes(N, passes, grouped, window):
     """Algorithmic bytes of one kernel-map build: every pass reads its inputs and writes
-    its outputs once (the L2-resident block table is not counted). pack: coords 16 N in,
+    its outputs once (the L2-resident block table is not counted). A build of nbr alone
+    takes the hashed front end (passes = 0): insert, coords 16 N in, keys 8 N + slot
+    indices 4 N out; scatter, those 12 N in, block-grouped keys and rows 12 N out; probe,
+    keys and rows 12 N in, the table 108 N out. The sorted front end: pack: coords 16 N in,
     keys 8 N + rows 4 N out; each active radix pass (constant high digits are skipped):
     12 N in, 12 N out; block runs and table: keys 8 N, twice; probe: keys 8 N + rows 4 N
     in, the table 108 N out. The tile plan's probe writes the table in Morton order plus
     grouping keys and values (12 N); then the grouping sort (24 N per pass) and the plan
     index (keys, values, rows 16 N in; perm 4 N out; the table's 108 N read and written
     again in plan order)."""
-    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N + 108 * N
     if not grouped:
-        return base
+        return 16 * N + 12 * N + 12 * N + 12 * N + 12 * N + 108 * N
+    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N + 108 * N
     last_window = (N - 1) // window
     passes2 = (27 + last_window.bit_length() + 7) // 8
     return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N
@@ -606,12 +609,13 @@ def run_ours(args, world, rank, local):
                     case["name"] + ("_grouped" if grouped else "") +
                     ("" if not fused else "_" + epi.replace("+", "_")),
                     e=2 if bf16 else 4, residual=args.residual)
-    passes = active_passes(case["coords"], res)
+    passes = active_passes(case["coords"], res) if grouped else 0   # nbr alone: no sort
     kbytes = kmap_algorithmic_bytes(N, passes, grouped, window)
     hbm = float(peaks["hbm_gbs"])
     kmap_roof = {"bound": "hbm", "achieved": kbytes / (kmap_ms / 1e3) / 1e9, "peak": hbm,
                  "unit": "GB/s", "frac": kbytes / (kmap_ms / 1e3) / 1e9 / hbm,
                  "algorithmic_bytes": kbytes, "radix_passes": passes,
+                 "front_end": "Morton radix sort" if grouped else "hashed blocks (no sort)",
                  "peak_source": f"hbm_gbs, {peak_kind}",
                  "stages_ms": [[n, round(t, 4)] for n, t in stages]}
     line = {

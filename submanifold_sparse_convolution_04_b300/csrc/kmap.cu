@@ -52,7 +52,10 @@ constexpr int kMaxProbe = 4096;
 constexpr int kHistParts = 16;   // partial digit histograms (spreads the count kernel's atomics)
 constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 2 * 256 * 4;
 
-enum : int { kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8, kFlagOrder = 16 };
+enum : int {
+  kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8, kFlagOrder = 16,
+  kFlagGrow = 32,   // hashed front end: the first table was too small, rebuilt at full size
+};
 
 struct KmapStatus {
   int flags;
@@ -65,6 +68,7 @@ struct KmapStatus {
   unsigned long long nblocks;    // occupied 4x4x4 blocks
   unsigned long long cap;        // hash capacity in use (a power of two)
   unsigned long long kmin, kmax; // smallest and largest sort key
+  unsigned long long npos;       // positions of the block-grouped order the probe walks
 };
 
 struct __align__(32) Slot {
@@ -164,6 +168,7 @@ __global__ void kmap_init(KmapStatus* st, uint32_t* hist, uint32_t* hist2) {
     st->cap = 0;
     st->kmin = ~0ull;
     st->kmax = 0;
+    st->npos = 0;
   }
   for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) {
     hist[i] = 0;
@@ -221,7 +226,8 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
 }
 
 // 3. ------------------------------------------------------------------------------
-__global__ void kmap_plan(int npass, KmapStatus* st) {
+__global__ void kmap_plan(int npass, int64_t N, KmapStatus* st) {
+  st->npos = static_cast<unsigned long long>(N);   // the sorted order holds every voxel
   const unsigned long long diff = st->kmax ^ st->kmin;
   int buf = 0;
   for (int p = 0; p < kMaxPasses; ++p) {
@@ -630,6 +636,167 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
   }
 }
 
+// 7h. -----------------------------------------------------------------------------
+// Hashed front end (builds that only want nbr). The probe needs an order of the
+// voxels in which every occupied 4x4x4 block is one contiguous run, with each block's
+// slot giving its occupancy mask and first position; nbr's values are input rows, so
+// which order the blocks come in does not matter. The Morton sort gives such an order,
+// but so do three passes without one:
+//   insert : each voxel finds or claims its block's slot (the lanes of a warp that
+//            share a block send one lookup) and ORs its bit into the slot's mask; a bit
+//            that was already set is a duplicate coordinate;
+//   alloc  : a pass over the slots gives each occupied one a range of positions as
+//            long as its mask's popcount (block-wide scan, one atomic add per block);
+//   scatter: each voxel's position is its block's first position plus the rank of its
+//            bit in the mask; its sort key and input row go there.
+// The table is first sized for N/4 blocks (shells hold about ten voxels per block); a
+// voxel whose block needs more than kGrowProbe probes there marks the build, and the
+// table is cleared and filled again at the workspace's full capacity (>= 2N slots).
+constexpr int kGrowProbe = 32;
+
+// Status word for a hashed build, and the first table cleared.
+__global__ void kmap_h_init(Slot* table, unsigned long long cap, KmapStatus* st) {
+  const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (tid == 0) {
+    st->flags = 0;
+    st->pad = 0;
+    st->bad_row = 0x7FFFFFFFFFFFFFFFll;
+    for (int p = 0; p <= kMaxPasses; ++p) st->plan[p] = st->plan2[p] = 0;
+    st->pad2 = st->pad3 = 0;
+    st->nblocks = 0;
+    st->cap = cap;
+    st->kmin = ~0ull;
+    st->kmax = 0;
+    st->npos = 0;
+  }
+  const Slot empty{kEmptyKey, 0ull, 0ull, 0ull};
+  for (int64_t i = tid; i < static_cast<int64_t>(cap); i += int64_t(gridDim.x) * blockDim.x)
+    table[i] = empty;
+}
+
+// The full-capacity table, only when the first one was too small.
+__global__ void kmap_h_grow(Slot* table, unsigned long long cap, KmapStatus* st) {
+  if (!(st->flags & kFlagGrow)) return;
+  const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (tid == 0) st->cap = cap;
+  const Slot empty{kEmptyKey, 0ull, 0ull, 0ull};
+  for (int64_t i = tid; i < static_cast<int64_t>(cap); i += int64_t(gridDim.x) * blockDim.x)
+    table[i] = empty;
+}
+
+// kSkip: the voxel takes no position (a coordinate out of range, a duplicate, or a
+// block that did not fit).
+constexpr uint32_t kSkip = 0xFFFFFFFFu;
+
+// refill: the second launch, which runs only when the first table was too small.
+// can_grow: a block needing more than kGrowProbe probes marks the build for the
+// full-size table instead of failing.
+__global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
+                                                     int res, int bits, Slot* table,
+                                                     unsigned long long* __restrict__ key_in,
+                                                     uint32_t* __restrict__ slot_of, bool refill,
+                                                     bool can_grow, KmapStatus* st) {
+  if (refill && !(st->flags & kFlagGrow)) return;
+  const unsigned long long cap = st->cap;
+  const unsigned long long cmask = cap - 1;
+  const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
+  const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t w0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x - lane; w0 < N; w0 += stride) {
+    const int64_t i = w0 + lane;
+    const bool live = i < N;
+    int4 c = live ? coords[i] : make_int4(0, 0, 0, 0);   // (b, z, y, x)
+    const bool ok = live && static_cast<unsigned>(c.x) <= SUBM3D_MAX_BATCH &&
+                    static_cast<unsigned>(c.y) < static_cast<unsigned>(res) &&
+                    static_cast<unsigned>(c.z) < static_cast<unsigned>(res) &&
+                    static_cast<unsigned>(c.w) < static_cast<unsigned>(res);
+    if (live && !ok) {
+      atomicOr(&st->flags, kFlagCoord);
+      atomicMin(&st->bad_row, static_cast<long long>(i));
+    }
+    const unsigned long long key =
+        ok ? (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w)
+           : ~0ull;
+    const unsigned long long blk = key >> 6;   // ~0 >> 6 is no block key of a valid voxel
+    const unsigned peers = __match_any_sync(0xffffffffu, blk);
+    const int leader = __ffs(peers) - 1;
+    long long h = -1;
+    if (ok && lane == leader) {
+      unsigned long long hh = mix64(blk) & cmask;
+      for (int probe = 0; probe < limit; ++probe) {
+        unsigned long long k = __ldcg(&table[hh].key);
+        if (k == kEmptyKey) k = atomicCAS(&table[hh].key, kEmptyKey, blk);
+        if (k == kEmptyKey || k == blk) {
+          h = static_cast<long long>(hh);
+          break;
+        }
+        hh = (hh + 1) & cmask;
+      }
+      if (h < 0) atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+    }
+    h = __shfl_sync(0xffffffffu, h, leader);
+    uint32_t sidx = kSkip;
+    if (ok && h >= 0) {
+      const unsigned long long bit = 1ull << (key & 63u);
+      const unsigned long long old = atomicOr(&table[h].mask, bit);
+      if (old & bit) atomicOr(&st->flags, kFlagDup);
+      else sidx = static_cast<uint32_t>(h);
+    }
+    if (live) {
+      key_in[i] = key;
+      slot_of[i] = sidx;
+    }
+  }
+}
+
+// Positions for the occupied slots, 256 slots per block and round.
+__global__ void __launch_bounds__(256) kmap_h_alloc(Slot* table, KmapStatus* st) {
+  __shared__ uint32_t tmp[8];
+  __shared__ unsigned long long s_base;
+  const unsigned long long cap = st->cap;
+  for (unsigned long long b0 = blockIdx.x * 256ull; b0 < cap; b0 += gridDim.x * 256ull) {
+    const unsigned long long i = b0 + threadIdx.x;
+    uint32_t cnt = 0;
+    if (i < cap && __ldcg(&table[i].key) != kEmptyKey)
+      cnt = static_cast<uint32_t>(__popcll(__ldcg(&table[i].mask)));
+    uint32_t total;
+    const uint32_t before = block_exclusive_scan256(cnt, tmp, &total);
+    const int occupied = __syncthreads_count(cnt != 0);
+    if (threadIdx.x == 0) {
+      s_base = total ? atomicAdd(&st->npos, static_cast<unsigned long long>(total)) : 0ull;
+      if (occupied) atomicAdd(&st->nblocks, static_cast<unsigned long long>(occupied));
+    }
+    __syncthreads();
+    if (cnt) table[i].start = s_base + before;
+    __syncthreads();
+  }
+}
+
+// Each voxel to its position: sort key to mk, input row to ix.
+__global__ void __launch_bounds__(256) kmap_h_scatter(
+    const unsigned long long* __restrict__ key_in, const uint32_t* __restrict__ slot_of,
+    int64_t N, const Slot* __restrict__ table, unsigned long long* __restrict__ mk,
+    int32_t* __restrict__ ix, KmapStatus* st) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
+    const uint32_t h = slot_of[i];
+    if (h == kSkip) continue;
+    const unsigned long long key = key_in[i];
+    const unsigned long long mask = table[h].mask;
+    const unsigned long long pos =
+        table[h].start + __popcll(mask & ((1ull << (key & 63u)) - 1ull));
+    if (pos < static_cast<unsigned long long>(N)) {
+      mk[pos] = key;
+      ix[pos] = static_cast<int32_t>(i);
+    } else {
+      bad = true;
+    }
+  }
+  if (bad) atomicOr(&st->flags, kFlagInternal);
+}
+
 // 8. ------------------------------------------------------------------------------
 // Warp-cooperative probe over the sorted order. A warp takes 32 consecutive sorted
 // positions, one voxel per lane. Its voxels fall into a few block runs (a run is one
@@ -725,6 +892,9 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
   const bool second = st->plan[kMaxPasses] & 1;
   const unsigned long long* mk = second ? mk1 : mk0;
   const int32_t* ix = second ? ix1 : ix0;
+  // the positions of the order (fewer than N only when the hashed front end skipped a
+  // voxel: the build then fails, and nbr is unspecified)
+  if (static_cast<unsigned long long>(N) > st->npos) N = static_cast<int64_t>(st->npos);
   const unsigned long long cmask = st->cap - 1;
   const int max_probe = st->cap < kMaxProbe ? static_cast<int>(st->cap) : kMaxProbe;
   const int lane = threadIdx.x & 31;
@@ -983,7 +1153,7 @@ int launch_sort(const int4* c4, int64_t N, int32_t res, const Layout& L, char* w
   SUBM3D_LAUNCHED("kmap_init");
   kmap_pack<<<grid_for(N, 256, 4), 256, 0, stream>>>(c4, N, res, bits, mk0, ix0, st);
   SUBM3D_LAUNCHED("kmap_pack");
-  kmap_plan<<<1, 1, 0, stream>>>(npass, st);
+  kmap_plan<<<1, 1, 0, stream>>>(npass, N, st);
   SUBM3D_LAUNCHED("kmap_plan");
   g_stage.mark("pack", stream);
   const int* plans = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
@@ -1384,7 +1554,7 @@ namespace {
 int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
              int32_t* order, int64_t hash_capacity, int64_t window, void* plan,
              size_t plan_bytes, void* workspace, size_t ws_bytes, bool sync,
-             cudaStream_t stream) {
+             cudaStream_t stream, bool force_sorted = false) {
   const bool grouped = plan != nullptr;
   if (N < 0 || N > 0x7FFFFFFFll) {
     set_error("%s: N=%lld outside [0, 2^31)", fn, (long long)N);
@@ -1449,19 +1619,50 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
   while ((1 << bits) < res) ++bits;
 
   const int4* c4 = reinterpret_cast<const int4*>(coords);
+  // nbr alone needs no Morton order: the hashed front end (slot indices kept as 32-bit
+  // words, so only while the full-size table has at most 2^31 slots)
+  const bool hashed = !grouped && !order && !force_sorted && cap_max <= (int64_t(1) << 31);
   g_stage.begin(stream);
-  {
+  if (hashed) {
+    int64_t cap0 = hash_capacity;
+    if (cap0 == 0) {
+      cap0 = 64;
+      while (cap0 < N / 4 && cap0 < cap_max) cap0 <<= 1;
+    }
+    const bool can_grow = hash_capacity == 0 && cap0 < cap_max;
+    unsigned long long* key_in = mk1;                      // input order
+    uint32_t* slot_of = reinterpret_cast<uint32_t*>(ix1);  // input order
+    kmap_h_init<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, cap0, st);
+    SUBM3D_LAUNCHED("kmap_h_init");
+    kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, key_in,
+                                                           slot_of, false, can_grow, st);
+    SUBM3D_LAUNCHED("kmap_h_insert");
+    if (can_grow) {   // both return at once unless the first table was too small
+      kmap_h_grow<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, cap_max, st);
+      SUBM3D_LAUNCHED("kmap_h_grow");
+      kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, key_in,
+                                                             slot_of, true, false, st);
+      SUBM3D_LAUNCHED("kmap_h_insert");
+    }
+    kmap_h_alloc<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, st);
+    SUBM3D_LAUNCHED("kmap_h_alloc");
+    kmap_h_scatter<<<grid_for(N, 256, 8), 256, 0, stream>>>(key_in, slot_of, N, table, mk0, ix0,
+                                                            st);
+    SUBM3D_LAUNCHED("kmap_h_scatter");
+    g_stage.mark("block table (hashed, no sort)", stream);
+  } else {
     const int rc = launch_sort(c4, N, res, L, ws, stream);
     if (rc != SUBM3D_OK) return rc;
+    kmap_blocks_count<<<grid_for(N, 256, 4), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
+    SUBM3D_LAUNCHED("kmap_blocks_count");
+    kmap_table_init<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, hash_capacity, cap_max,
+                                                                  st);
+    SUBM3D_LAUNCHED("kmap_table_init");
+    kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
+                                                                st);
+    SUBM3D_LAUNCHED("kmap_blocks_insert");
+    g_stage.mark("block table", stream);
   }
-  kmap_blocks_count<<<grid_for(N, 256, 4), 256, 0, stream>>>(mk0, mk1, ix0, ix1, N, order, st);
-  SUBM3D_LAUNCHED("kmap_blocks_count");
-  kmap_table_init<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, hash_capacity, cap_max, st);
-  SUBM3D_LAUNCHED("kmap_table_init");
-  kmap_blocks_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, mk0, mk1, ix0, ix1, N, table,
-                                                              st);
-  SUBM3D_LAUNCHED("kmap_blocks_insert");
-  g_stage.mark("block table", stream);
   // the probe's grid is exactly the blocks that fit on the GPU at once (its shared memory
   // limits them), so that its grid-stride loop runs in one wave
   static PerDevice<int> probe_fit[2];
@@ -1531,6 +1732,12 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     set_error("%s: coordinate row %lld outside 0<=b<=%d, 0<=z,y,x<%d", fn, host.bad_row,
               SUBM3D_MAX_BATCH, res);
     return SUBM3D_ERR_COORD_RANGE;
+  }
+  if (hashed && (host.flags & kFlagDup)) {
+    // the hashed front end knows that two rows share a coordinate, not which row is the
+    // first repeat (that depends on the order of its atomics): the sorted build says so
+    return kmap_run(fn, coords, N, res, nbr, order, hash_capacity, window, plan, plan_bytes,
+                    workspace, ws_bytes, sync, stream, true);
   }
   if (host.flags & kFlagInternal) {
     set_error("%s: internal error (sort or block table produced an index outside [0, N))", fn);

@@ -153,3 +153,40 @@ def test_kmap_reuses_dirty_workspace(dev):
     with pytest.raises(Subm3dError) as e:
         subm3d_build_kmap(c, case["res"], workspace=ws[:1024])
     assert e.value.code == B.ERR_WORKSPACE
+
+
+def sparse_pairs(rng, res, batch, n):
+    """Isolated voxels, about half with a +x neighbour (often across a 4x4x4 block's
+    face): roughly one voxel per occupied block."""
+    rows = []
+    for b in range(batch):
+        flat = rng.choice((res // 8) ** 3, size=n, replace=False)
+        z, rem = np.divmod(flat, (res // 8) ** 2)
+        y, x = np.divmod(rem, res // 8)
+        p = np.stack([np.full(n, b), 8 * z + 3, 8 * y + rng.integers(0, 8, n), 8 * x + 3], 1)
+        q = p[rng.random(n) < 0.5].copy()
+        q[:, 3] += 1
+        rows += [p, q]
+    c = np.concatenate(rows).astype(np.int32)
+    return c[rng.permutation(c.shape[0])]
+
+
+def test_kmap_hashed_table_grows(dev):
+    # the nbr-only build first sizes its block table for N/4 blocks; here there are about
+    # N of them, so it rebuilds the table at full size, with the same answer
+    rng = np.random.default_rng(11)
+    c = sparse_pairs(rng, 1024, 2, 20000)
+    got = gpu_nbr(c, 1024, dev)
+    np.testing.assert_array_equal(got, ref.kernel_map(c, 1024))
+    assert (got[:, 12] >= 0).sum() + (got[:, 14] >= 0).sum() > 0   # some pairs
+
+
+@pytest.mark.parametrize("cfg_id", [3, 5])
+def test_kmap_front_ends_agree(dev, cfg_id):
+    # nbr alone (hashed blocks, no sort) and with the Morton order (radix-sort front end)
+    case = cached_case(cfg_id)
+    c = torch.from_numpy(case["coords"]).to(dev)
+    hashed = subm3d_build_kmap(c, case["res"]).cpu().numpy()
+    sorted_nbr, _ = subm3d_build_kmap_ex(c, case["res"], order=True)
+    np.testing.assert_array_equal(hashed, sorted_nbr.cpu().numpy())
+    np.testing.assert_array_equal(hashed, cpu.kernel_map(case["coords"], case["res"]))

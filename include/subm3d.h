@@ -116,15 +116,16 @@ SUBM3D_API size_t subm3d_kmap_workspace_bytes_ex(int64_t N, int64_t hash_capacit
  *   workspace device scratch of at least subm3d_kmap_workspace_bytes(N) bytes,
  *             256-byte aligned; its contents on entry do not matter.
  *
- * Steps (all CUDA kernels on `stream`): validate each coordinate and pack it into a
- * 64-bit sort key (b above the interleaved z/y/x bits: its Morton code); Morton-order
- * the voxels (LSD radix sort). In that order every aligned 4x4x4 block is one run
- * (the low 6 bits of the code are the place inside the block), so duplicates are
- * adjacent equal codes; each occupied block is inserted into an open-addressing hash
- * table (key b<<42 | (z>>2)<<28 | (y>>2)<<14 | (x>>2), a 64-bit occupancy mask, the
- * block's first sorted position; bounded linear probing). The 27 offsets of each
- * voxel are probed by warps that take 32 voxels of the sorted order and write each
- * voxel's row of nbr contiguously.
+ * Steps (all CUDA kernels on `stream`). A voxel's sort key is b above the interleaved
+ * z/y/x bits (its Morton code); the low 6 bits of the code are its place inside its
+ * aligned 4x4x4 block, the bits above name the block. Each voxel finds or claims its
+ * block's slot in an open-addressing hash table (64-bit block key, 64-bit occupancy
+ * mask, the block's first position; bounded linear probing) and sets its bit in the
+ * mask (a bit already set is a duplicate coordinate). Only the occupied blocks' keys
+ * are radix-sorted; a scan of their popcounts gives each block its first position, and
+ * each voxel's position (first position + rank of its bit) puts the voxels in Morton
+ * order. The 27 offsets of each voxel are probed by warps that take 32 consecutive
+ * positions of that order and write each voxel's row of nbr contiguously.
  *
  * Synchronisation: the call waits for `stream` once, at its end, to read the
  * device status word, so it is not capturable into a CUDA graph. Errors found on
@@ -139,11 +140,12 @@ SUBM3D_API int subm3d_build_kmap(const int32_t* coords, int64_t N, int32_t res, 
  *   order          device int32 [N] or NULL. If given, receives the Morton order:
  *                  order[s] = the input row at position s of the (b, Morton code)
  *                  ascending sort (stable, so ties keep input order).
- *   hash_capacity  0 for the default (the smallest power of two >= 2 x the number of
- *                  occupied 4x4x4 blocks, chosen on the device; the workspace is sized
- *                  for the worst case of one block per voxel), else a fixed power of
- *                  two >= 8 (slots, one per occupied block). A capacity below the
- *                  number of occupied blocks makes the call fail with
+ *   hash_capacity  0 for the default: a table of the smallest power of two >= N/4
+ *                  slots (at least 64), rebuilt on the device at the workspace's full
+ *                  size (the smallest power of two >= 2N, the worst case of one block
+ *                  per voxel) when a block needs more than 32 probes; else a fixed
+ *                  power of two >= 8 (slots, one per occupied block). A capacity below
+ *                  the number of occupied blocks makes the call fail with
  *                  SUBM3D_ERR_HASH_FULL.
  */
 SUBM3D_API int subm3d_build_kmap_ex(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
@@ -427,9 +429,10 @@ SUBM3D_API int subm3d_forward_status(cudaStream_t stream);
 /*
  * Stage timing of the kernel-map builds, for measurement. While enabled (per host
  * thread; off by default), every kernel-map build made by this thread records a CUDA
- * event on its stream before its first stage and after each stage (pack, each radix
- * pass, block table, probe; for the tile plan also the mask probe, each grouping-sort
- * pass, the plan index and the plan probe). No extra synchronisation is added.
+ * event on its stream before its first stage and after each stage (block insert,
+ * block compact, each block-sort pass, block starts, voxel scatter, probe; for the tile
+ * plan the probe in Morton order with the masks, each grouping-sort pass and the plan
+ * index). No extra synchronisation is added.
  * subm3d_kmap_stage_times waits for the last build's events and writes, for up to `max`
  * stages in order, the GPU milliseconds of each (ms[i]) and its name (names[i], a
  * static string); it returns the number of stages written, or a negative status.

@@ -6,35 +6,35 @@
 // needs exactly this table; the pages' "spatial cache" (README scope table) is what
 // lets one table serve several convolutions on one voxel set.
 //
-// Pipeline (one stream, one host sync at the end to read the status word):
-//   1. init    : status word and digit histograms cleared
-//   2. pack    : validate (b, z, y, x); sort key (b << 3*bits) | Morton(z, y, x) with
-//                bits >= 2; smallest and largest key
-//   3. plan    : passes whose digit lies above the highest bit in which the smallest
-//                and largest key differ are constant and skipped
-//   4. passes  : LSD radix sort of (sort key, row) -- count / scan / stable scatter;
-//                the scatter ranks a 2048-key tile in shared memory and writes each
-//                digit's run contiguously
-//   5. blocks  : the low 6 bits of a Morton code are the voxel's place inside its
-//                aligned 4x4x4 block and the bits above name the block, so in sorted
-//                order every block is one contiguous run. Adjacent equal codes are
-//                duplicate coordinates; the run starts are counted
-//   6. table   : hash capacity = the smallest power of two >= 2 x blocks (unless the
-//                caller fixed it), chosen and cleared on the device
-//   7. insert  : one slot per block, {packed block key b<<42|bz<<28|by<<14|bx,
-//                64-bit occupancy mask}, plus the block's first sorted position;
-//                open addressing, atomicCAS, bounded linear probing
-//   8. probe   : a thread per voxel (input order) looks up the at most 2 x 2 x 2
-//                blocks its 27 neighbours fall in; a neighbour is then a bit test,
-//                and the bit's rank inside the mask turns into a sorted position,
-//                whose input row is the answer. A block's 128 rows of results are
-//                staged in shared memory and written as one contiguous stretch.
-//
+// Pipeline (one stream; a synchronous build waits once, at the end, for the status
+// word). Sort key of a voxel: (b << 3*bits) | Morton(z, y, x), bits >= 2 per axis. The
+// low 6 bits of a Morton code are the voxel's place inside its aligned 4x4x4 block and
+// the bits above name the block, so the Morton order is the order of the occupied
+// blocks by key, each block's voxels by place.
+//   1. insert  : validate each coordinate; find or claim its block's slot in an
+//                open-addressing hash table (splitmix64 of the block key, bounded linear
+//                probing, atomicCAS) and OR its bit into the slot's 64-bit occupancy
+//                mask (a bit already set is a duplicate coordinate)
+//   2. compact : the occupied slots (block key, slot index)
+//   3. sort    : LSD radix sort of the block keys only (single-pass passes with
+//                decoupled look-back; passes whose digit is constant are skipped)
+//   4. starts  : exclusive scan of the sorted blocks' popcounts: each block's first
+//                position, stored in its slot
+//   5. scatter : a voxel's position = its block's first position + the rank of its
+//                bit; (sort key, input row) stored there: the Morton order
+//   6. probe   : warps take 32 consecutive positions; per run of one block they look
+//                up the (at most 27) neighbour blocks the run's voxels reach, then each
+//                lane resolves its voxel's 27 neighbours by a bit test and a popcount
+//                (position = neighbour block's first position + rank), whose input row
+//                is the answer; rows are staged in shared memory and written out whole.
+// The radix sort of all N voxels' keys (pack, histograms, passes, block runs, table)
+// is kept for the downsample's own sort, for builds whose table would exceed 2^31
+// slots, and to name the first repeated row when a build finds a duplicate.
 // The blocks of a shell hold ~10 voxels each, so the table is about a tenth of a
 // per-voxel table and stays in L2.
 // Hash of a block key: the splitmix64 finaliser (Steele, Lea and Flood, 2014).
 //
-// The structure ops that share steps 1-4 live here too (their section is below the
+// The structure ops that share the radix sort live here too (their section is below the
 // probe): SparseDownsample(2), which numbers the parents of the sorted voxels and pools
 // their features; SparseUpsample(2), its cache-paired inverse; SparseSpatial2Channel(2)
 // and its inverse, the sparse pixel-(un)shuffle on the same subdivision.
@@ -88,7 +88,9 @@ __host__ __device__ inline size_t sort_scratch_bytes(int64_t ntile) {
 }
 
 struct Layout {
-  size_t status, hist, mk0, mk1, ix0, ix1, cnt, table;
+  // bv1: the second value buffer of the hashed front end's block sort (ix1 holds each
+  // voxel's slot meanwhile)
+  size_t status, hist, mk0, mk1, ix0, ix1, bv1, cnt, table;
   // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and the
   // neighbour table in sorted (Morton) order
   size_t k2a, k2b, v2a, v2b, hist2, nbr_sorted;
@@ -107,6 +109,7 @@ Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   L.mk1 = o;    o = align256(o + sizeof(uint64_t) * N);
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
   L.ix1 = o;    o = align256(o + sizeof(int32_t) * N);
+  L.bv1 = o;    o = align256(o + sizeof(int32_t) * N);
   L.cnt = o;    o = align256(o + sort_scratch_bytes(L.nblk));
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
   L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.nbr_sorted = 0;
@@ -226,8 +229,9 @@ __global__ void __launch_bounds__(256) kmap_pack(const int4* __restrict__ coords
 }
 
 // 3. ------------------------------------------------------------------------------
+// N >= 0: the sort is of all N voxels, and the order the probe walks holds every one.
 __global__ void kmap_plan(int npass, int64_t N, KmapStatus* st) {
-  st->npos = static_cast<unsigned long long>(N);   // the sorted order holds every voxel
+  if (N >= 0) st->npos = static_cast<unsigned long long>(N);
   const unsigned long long diff = st->kmax ^ st->kmin;
   int buf = 0;
   for (int p = 0; p < kMaxPasses; ++p) {
@@ -290,9 +294,11 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 // histograms [part][pass][digit] spread the atomics); also clears the passes' tile
 // counters and published status words.
 __global__ void __launch_bounds__(256) kmap_hist(const unsigned long long* __restrict__ keys,
-                                                 int64_t N, int npass, const int* plans,
+                                                 int64_t N, const unsigned long long* count,
+                                                 int npass, const int* plans,
                                                  uint32_t* __restrict__ hist, SortScratch S,
                                                  int64_t ntile) {
+  if (count && *count < static_cast<unsigned long long>(N)) N = static_cast<int64_t>(*count);
   __shared__ uint32_t sh[kMaxPasses][256];
   for (int i = threadIdx.x; i < kMaxPasses * 256; i += 256) sh[i >> 8][i & 255] = 0;
   const int64_t gtid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
@@ -367,9 +373,13 @@ __global__ void __launch_bounds__(256) kmap_digit_starts(const uint32_t* __restr
 // 4c. One pass: rank a tile, look back for each digit's count before it, scatter.
 __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
     unsigned long long* mk0, unsigned long long* mk1, int32_t* ix0, int32_t* ix1, int64_t N,
-    int pass, int64_t ntile, const int* plans, SortScratch S, KmapStatus* st) {
+    const unsigned long long* count, int pass, int64_t ntile, const int* plans, SortScratch S,
+    KmapStatus* st) {
   const int plan = plans[pass];
   if (!(plan & 2)) return;
+  // a count on the device: N is then only the bound the grid was sized for
+  if (count && *count < static_cast<unsigned long long>(N)) N = static_cast<int64_t>(*count);
+  (void)ntile;
   const unsigned long long* src = (plan & 1) ? mk1 : mk0;
   unsigned long long* dst = (plan & 1) ? mk0 : mk1;
   const int32_t* isrc = (plan & 1) ? ix1 : ix0;
@@ -389,7 +399,9 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
   for (int i = threadIdx.x; i < kWarpsPerSort * 257; i += kSortThreads) wcnt[i] = 0;
   __syncthreads();
   const int64_t tile = s_tile;
-  if (tile >= ntile) return;   // more blocks than tiles: nothing to do
+  // more blocks than tiles: nothing to do (tiles are handed out in order, so no tile that
+  // holds keys waits for one past the end)
+  if (tile * kSortTile >= N) return;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int64_t tile0 = tile * kSortTile;
   const int64_t base = tile0 + warp * kPerWarp;
@@ -572,7 +584,8 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
     KmapStatus* st) {
   const bool second = st->plan[kMaxPasses] & 1;
   const unsigned long long* mk = second ? mk1 : mk0;
-  const int32_t* ix = second ? ix1 : ix0;
+  (void)ix0;
+  (void)ix1;
   const unsigned long long cap = st->cap;
   const unsigned long long cmask = cap - 1;
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
@@ -637,26 +650,34 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 }
 
 // 7h. -----------------------------------------------------------------------------
-// Hashed front end (builds that only want nbr). The probe needs an order of the
-// voxels in which every occupied 4x4x4 block is one contiguous run, with each block's
-// slot giving its occupancy mask and first position; nbr's values are input rows, so
-// which order the blocks come in does not matter. The Morton sort gives such an order,
-// but so do three passes without one:
+// Hashed front end. The probe needs an order of the voxels in which every occupied
+// 4x4x4 block is one contiguous run, with each block's slot giving its occupancy mask
+// and first position. The Morton order is such an order, and it is also the order of
+// the occupied blocks by their keys, each block's voxels by their place in it (the low
+// 6 bits of the code). So instead of sorting the N voxels' codes, the blocks are found
+// first and only their keys are sorted (about a tenth as many on surfaces):
 //   insert : each voxel finds or claims its block's slot (the lanes of a warp that
-//            share a block send one lookup) and ORs its bit into the slot's mask; a bit
-//            that was already set is a duplicate coordinate;
-//   alloc  : a pass over the slots gives each occupied one a range of positions as
-//            long as its mask's popcount (block-wide scan, one atomic add per block);
+//            share a block send one lookup and one OR of their bits into the slot's
+//            mask); a bit that was already set is a duplicate coordinate;
+//   compact: the occupied slots' keys and indices, with the smallest and largest key;
+//   sort   : the LSD radix sort of (block key, slot) (count read on the device);
+//   starts : an exclusive scan of the sorted blocks' popcounts (per-tile sums, a scan
+//            of those, then each block's first position into its slot);
 //   scatter: each voxel's position is its block's first position plus the rank of its
-//            bit in the mask; its sort key and input row go there.
-// The table is first sized for N/4 blocks (shells hold about ten voxels per block); a
-// voxel whose block needs more than kGrowProbe probes there marks the build, and the
-// table is cleared and filled again at the workspace's full capacity (>= 2N slots).
+//            bit in the mask; its sort key and input row (and the order, if asked for)
+//            go there.
+// The result is the Morton order the radix sort of all voxels gives (positions of
+// distinct codes; ties exist only with duplicates, which fail the build). The table is
+// first sized for N/4 blocks (shells hold about ten voxels per block); a block needing
+// more than kGrowProbe probes there marks the build, and the table is cleared and
+// filled again at the workspace's full capacity (>= 2N slots).
 constexpr int kGrowProbe = 32;
 
-// Status word for a hashed build, and the first table cleared.
-__global__ void kmap_h_init(Slot* table, unsigned long long cap, KmapStatus* st) {
+// Status word for a hashed build, the digit histograms, and the first table cleared.
+__global__ void kmap_h_init(Slot* table, unsigned long long cap, uint32_t* hist,
+                            uint32_t* hist2, KmapStatus* st) {
   const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   if (tid == 0) {
     st->flags = 0;
     st->pad = 0;
@@ -669,9 +690,12 @@ __global__ void kmap_h_init(Slot* table, unsigned long long cap, KmapStatus* st)
     st->kmax = 0;
     st->npos = 0;
   }
+  for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) {
+    hist[i] = 0;
+    if (hist2) hist2[i] = 0;
+  }
   const Slot empty{kEmptyKey, 0ull, 0ull, 0ull};
-  for (int64_t i = tid; i < static_cast<int64_t>(cap); i += int64_t(gridDim.x) * blockDim.x)
-    table[i] = empty;
+  for (int64_t i = tid; i < static_cast<int64_t>(cap); i += stride) table[i] = empty;
 }
 
 // The full-capacity table, only when the first one was too small.
@@ -684,16 +708,25 @@ __global__ void kmap_h_grow(Slot* table, unsigned long long cap, KmapStatus* st)
     table[i] = empty;
 }
 
-// kSkip: the voxel takes no position (a coordinate out of range, a duplicate, or a
-// block that did not fit).
+// kSkip: the voxel takes no position (a coordinate out of range, a repeat of an earlier
+// coordinate, or a block that did not fit).
 constexpr uint32_t kSkip = 0xFFFFFFFFu;
+
+__device__ __forceinline__ bool coord_ok(int4 c, int res) {   // (b, z, y, x)
+  return static_cast<unsigned>(c.x) <= SUBM3D_MAX_BATCH &&
+         static_cast<unsigned>(c.y) < static_cast<unsigned>(res) &&
+         static_cast<unsigned>(c.z) < static_cast<unsigned>(res) &&
+         static_cast<unsigned>(c.w) < static_cast<unsigned>(res);
+}
+__device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
+  return (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w);
+}
 
 // refill: the second launch, which runs only when the first table was too small.
 // can_grow: a block needing more than kGrowProbe probes marks the build for the
 // full-size table instead of failing.
 __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
                                                      int res, int bits, Slot* table,
-                                                     unsigned long long* __restrict__ key_in,
                                                      uint32_t* __restrict__ slot_of, bool refill,
                                                      bool can_grow, KmapStatus* st) {
   if (refill && !(st->flags & kFlagGrow)) return;
@@ -703,25 +736,29 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
   const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
   const int lane = threadIdx.x & 31;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  constexpr unsigned kAll = 0xffffffffu;
   for (int64_t w0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x - lane; w0 < N; w0 += stride) {
     const int64_t i = w0 + lane;
     const bool live = i < N;
-    int4 c = live ? coords[i] : make_int4(0, 0, 0, 0);   // (b, z, y, x)
-    const bool ok = live && static_cast<unsigned>(c.x) <= SUBM3D_MAX_BATCH &&
-                    static_cast<unsigned>(c.y) < static_cast<unsigned>(res) &&
-                    static_cast<unsigned>(c.z) < static_cast<unsigned>(res) &&
-                    static_cast<unsigned>(c.w) < static_cast<unsigned>(res);
+    const int4 c = live ? coords[i] : make_int4(0, 0, 0, 0);
+    const bool ok = live && coord_ok(c, res);
     if (live && !ok) {
       atomicOr(&st->flags, kFlagCoord);
       atomicMin(&st->bad_row, static_cast<long long>(i));
     }
-    const unsigned long long key =
-        ok ? (static_cast<unsigned long long>(c.x) << (3 * bits)) | morton3(c.y, c.z, c.w)
-           : ~0ull;
-    const unsigned long long blk = key >> 6;   // ~0 >> 6 is no block key of a valid voxel
-    const unsigned peers = __match_any_sync(0xffffffffu, blk);
+    const unsigned long long key = ok ? sort_key(c, bits) : ~0ull;
+    const unsigned long long blk = key >> 6;   // ~0 >> 6 is no valid voxel's block key
+    const unsigned long long bit = ok ? 1ull << (key & 63u) : 0ull;
+    const unsigned peers = __match_any_sync(kAll, blk);
+    const unsigned same = __match_any_sync(kAll, key);
     const int leader = __ffs(peers) - 1;
+    // the group's bits (one OR into the slot for the whole group)
+    const unsigned long long gbits =
+        (static_cast<unsigned long long>(__reduce_or_sync(peers, static_cast<uint32_t>(bit >> 32)))
+         << 32) |
+        __reduce_or_sync(peers, static_cast<uint32_t>(bit));
     long long h = -1;
+    unsigned long long old = 0;
     if (ok && lane == leader) {
       unsigned long long hh = mix64(blk) & cmask;
       for (int probe = 0; probe < limit; ++probe) {
@@ -734,62 +771,169 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
         hh = (hh + 1) & cmask;
       }
       if (h < 0) atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+      else old = atomicOr(&table[h].mask, gbits);
     }
-    h = __shfl_sync(0xffffffffu, h, leader);
+    h = __shfl_sync(kAll, h, leader);
+    old = __shfl_sync(kAll, old, leader);
     uint32_t sidx = kSkip;
     if (ok && h >= 0) {
-      const unsigned long long bit = 1ull << (key & 63u);
-      const unsigned long long old = atomicOr(&table[h].mask, bit);
-      if (old & bit) atomicOr(&st->flags, kFlagDup);
+      // a repeat: an earlier lane of this warp, or another warp, holds the same code
+      if ((__ffs(same) - 1) != lane || (old & bit)) atomicOr(&st->flags, kFlagDup);
       else sidx = static_cast<uint32_t>(h);
     }
-    if (live) {
-      key_in[i] = key;
-      slot_of[i] = sidx;
-    }
+    if (live) slot_of[i] = sidx;
   }
 }
 
-// Positions for the occupied slots, 256 slots per block and round.
-__global__ void __launch_bounds__(256) kmap_h_alloc(Slot* table, KmapStatus* st) {
+// The occupied slots (key, index), 256 slots per block and round, and the smallest and
+// largest key (for the sort's constant digits).
+__global__ void __launch_bounds__(256) kmap_h_compact(const Slot* __restrict__ table,
+                                                      unsigned long long* __restrict__ bkey,
+                                                      int32_t* __restrict__ bslot,
+                                                      KmapStatus* st) {
   __shared__ uint32_t tmp[8];
-  __shared__ unsigned long long s_base;
+  __shared__ unsigned long long s_base, wlo[8], whi[8];
   const unsigned long long cap = st->cap;
+  unsigned long long lo = ~0ull, hi = 0;
   for (unsigned long long b0 = blockIdx.x * 256ull; b0 < cap; b0 += gridDim.x * 256ull) {
     const unsigned long long i = b0 + threadIdx.x;
-    uint32_t cnt = 0;
-    if (i < cap && __ldcg(&table[i].key) != kEmptyKey)
-      cnt = static_cast<uint32_t>(__popcll(__ldcg(&table[i].mask)));
+    const unsigned long long k = i < cap ? __ldcg(&table[i].key) : kEmptyKey;
+    const uint32_t occ = k != kEmptyKey;
     uint32_t total;
-    const uint32_t before = block_exclusive_scan256(cnt, tmp, &total);
-    const int occupied = __syncthreads_count(cnt != 0);
-    if (threadIdx.x == 0) {
-      s_base = total ? atomicAdd(&st->npos, static_cast<unsigned long long>(total)) : 0ull;
-      if (occupied) atomicAdd(&st->nblocks, static_cast<unsigned long long>(occupied));
+    const uint32_t before = block_exclusive_scan256(occ, tmp, &total);
+    if (threadIdx.x == 0)
+      s_base = total ? atomicAdd(&st->nblocks, static_cast<unsigned long long>(total)) : 0ull;
+    __syncthreads();
+    if (occ) {
+      bkey[s_base + before] = k;
+      bslot[s_base + before] = static_cast<int32_t>(i);
+      lo = k < lo ? k : lo;
+      hi = k > hi ? k : hi;
     }
     __syncthreads();
-    if (cnt) table[i].start = s_base + before;
-    __syncthreads();
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    const unsigned long long h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    wlo[threadIdx.x >> 5] = lo;
+    whi[threadIdx.x >> 5] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) {
+      lo = wlo[w] < lo ? wlo[w] : lo;
+      hi = whi[w] > hi ? whi[w] : hi;
+    }
+    if (lo <= hi) {
+      atomicMin(&st->kmin, lo);
+      atomicMax(&st->kmax, hi);
+    }
   }
 }
 
-// Each voxel to its position: sort key to mk, input row to ix.
+// Voxels of the sorted blocks [t * 2048, (t + 1) * 2048) per block of 256 threads, eight
+// consecutive blocks per thread.
+constexpr int kStartTile = 2048;
+
+__device__ __forceinline__ const int32_t* sorted_slots(const int32_t* b0, const int32_t* b1,
+                                                       const KmapStatus* st) {
+  return (st->plan[kMaxPasses] & 1) ? b1 : b0;
+}
+
+__global__ void __launch_bounds__(256) kmap_h_tsum(const int32_t* __restrict__ b0,
+                                                   const int32_t* __restrict__ b1,
+                                                   const Slot* __restrict__ table,
+                                                   uint32_t* __restrict__ tsum,
+                                                   const KmapStatus* st) {
+  const unsigned long long nb = st->nblocks;
+  const unsigned long long t0 = blockIdx.x * static_cast<unsigned long long>(kStartTile);
+  if (t0 >= nb) return;
+  const int32_t* bs = sorted_slots(b0, b1, st);
+  uint32_t c = 0;
+  for (int q = 0; q < kStartTile / 256; ++q) {
+    const unsigned long long e = t0 + q * 256 + threadIdx.x;
+    if (e < nb) c += __popcll(table[bs[e]].mask);
+  }
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  __shared__ uint32_t w[8];
+  if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int k = 0; k < 8; ++k) t += w[k];
+    tsum[blockIdx.x] = t;
+  }
+}
+
+// One block: the per-tile sums to exclusive prefixes, in place; the total is the number
+// of positions.
+__global__ void __launch_bounds__(256) kmap_h_tscan(uint32_t* __restrict__ tsum, KmapStatus* st) {
+  __shared__ uint32_t tmp[8];
+  const unsigned long long nb = st->nblocks;
+  const int64_t ntile = static_cast<int64_t>((nb + kStartTile - 1) / kStartTile);
+  unsigned long long carry = 0;
+  for (int64_t b = 0; b < ntile; b += 256) {
+    const int64_t t = b + threadIdx.x;
+    const uint32_t v = t < ntile ? tsum[t] : 0u;
+    uint32_t total;
+    const uint32_t before = block_exclusive_scan256(v, tmp, &total);
+    if (t < ntile) tsum[t] = static_cast<uint32_t>(carry + before);
+    carry += total;
+  }
+  if (threadIdx.x == 0) st->npos = carry;
+}
+
+__global__ void __launch_bounds__(256) kmap_h_apply(const int32_t* __restrict__ b0,
+                                                    const int32_t* __restrict__ b1, Slot* table,
+                                                    const uint32_t* __restrict__ tsum,
+                                                    const KmapStatus* st) {
+  __shared__ uint32_t tmp[8];
+  const unsigned long long nb = st->nblocks;
+  const unsigned long long t0 = blockIdx.x * static_cast<unsigned long long>(kStartTile);
+  if (t0 >= nb) return;
+  const int32_t* bs = sorted_slots(b0, b1, st);
+  constexpr int kPer = kStartTile / 256;
+  const unsigned long long e0 = t0 + threadIdx.x * kPer;
+  int32_t slot[kPer];
+  uint32_t cnt[kPer], mine = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    slot[q] = e0 + q < nb ? bs[e0 + q] : -1;
+    cnt[q] = slot[q] >= 0 ? static_cast<uint32_t>(__popcll(table[slot[q]].mask)) : 0u;
+    mine += cnt[q];
+  }
+  uint32_t total;
+  unsigned long long at = tsum[blockIdx.x] + block_exclusive_scan256(mine, tmp, &total);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    if (slot[q] >= 0) table[slot[q]].start = at;
+    at += cnt[q];
+  }
+}
+
+// Each voxel to its position: sort key to mk, input row to ix (and to order).
 __global__ void __launch_bounds__(256) kmap_h_scatter(
-    const unsigned long long* __restrict__ key_in, const uint32_t* __restrict__ slot_of,
-    int64_t N, const Slot* __restrict__ table, unsigned long long* __restrict__ mk,
-    int32_t* __restrict__ ix, KmapStatus* st) {
+    const int4* __restrict__ coords, const uint32_t* __restrict__ slot_of, int64_t N, int bits,
+    const Slot* __restrict__ table, unsigned long long* __restrict__ mk, int32_t* __restrict__ ix,
+    int32_t* __restrict__ order, KmapStatus* st) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) st->plan[kMaxPasses] = 0;   // the probe reads mk, ix
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   bool bad = false;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
     const uint32_t h = slot_of[i];
     if (h == kSkip) continue;
-    const unsigned long long key = key_in[i];
+    const unsigned long long key = sort_key(coords[i], bits);
     const unsigned long long mask = table[h].mask;
     const unsigned long long pos =
         table[h].start + __popcll(mask & ((1ull << (key & 63u)) - 1ull));
     if (pos < static_cast<unsigned long long>(N)) {
       mk[pos] = key;
       ix[pos] = static_cast<int32_t>(i);
+      if (order) order[pos] = static_cast<int32_t>(i);
     } else {
       bad = true;
     }
@@ -1113,24 +1257,25 @@ thread_local StageTimer g_stage;
 // The count / scan / scatter passes of a stable LSD radix sort of (u64 key, i32 value)
 // pairs ping-ponging between (k0, v0) and (k1, v1); plans[p] (device) says whether pass p
 // runs and which buffer it reads, plans[kMaxPasses] which one holds the result.
+// count: when not NULL, the number of pairs is read on the device (at most N).
 int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, int32_t* v1,
                  int64_t N, int npass, uint32_t* hist, char* scratch, int64_t nblk,
                  const int* plans, KmapStatus* st, cudaStream_t stream,
-                 const char* stage = "sort pass") {
+                 const char* stage = "sort pass", const unsigned long long* count = nullptr) {
   static PerDevice<bool> attr_set;
   const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(kmap_onesweep),
                                       kScatterSmem, "kmap_onesweep");
   if (arc != SUBM3D_OK) return arc;
   const SortScratch S = sort_scratch(scratch, nblk);
-  kmap_hist<<<grid_for(N, 256, 4), 256, 0, stream>>>(k0, N, npass, plans, hist, S, nblk);
+  kmap_hist<<<grid_for(N, 256, 4), 256, 0, stream>>>(k0, N, count, npass, plans, hist, S, nblk);
   SUBM3D_LAUNCHED("kmap_hist");
   kmap_digit_starts<<<1, 256, 0, stream>>>(hist, npass, S);
   SUBM3D_LAUNCHED("kmap_digit_starts");
   g_stage.mark("digit histograms", stream);
   const int grid = static_cast<int>(nblk);
   for (int p = 0; p < npass; ++p) {
-    kmap_onesweep<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, p, nblk,
-                                                                plans, S, st);
+    kmap_onesweep<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, count, p,
+                                                                nblk, plans, S, st);
     SUBM3D_LAUNCHED("kmap_onesweep");
     g_stage.mark(stage, stream);
   }
@@ -1619,9 +1764,10 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
   while ((1 << bits) < res) ++bits;
 
   const int4* c4 = reinterpret_cast<const int4*>(coords);
-  // nbr alone needs no Morton order: the hashed front end (slot indices kept as 32-bit
-  // words, so only while the full-size table has at most 2^31 slots)
-  const bool hashed = !grouped && !order && !force_sorted && cap_max <= (int64_t(1) << 31);
+  // the hashed front end (slot indices are kept as 32-bit words, so only while the
+  // full-size table has at most 2^31 slots); the radix sort of all voxels otherwise, and
+  // to name the first repeated row of a build that found a duplicate
+  const bool hashed = !force_sorted && cap_max <= (int64_t(1) << 31);
   g_stage.begin(stream);
   if (hashed) {
     int64_t cap0 = hash_capacity;
@@ -1630,26 +1776,48 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
       while (cap0 < N / 4 && cap0 < cap_max) cap0 <<= 1;
     }
     const bool can_grow = hash_capacity == 0 && cap0 < cap_max;
-    unsigned long long* key_in = mk1;                      // input order
-    uint32_t* slot_of = reinterpret_cast<uint32_t*>(ix1);  // input order
-    kmap_h_init<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, cap0, st);
+    uint32_t* slot_of = reinterpret_cast<uint32_t*>(ix1);   // per voxel, input order
+    int32_t* bv1 = reinterpret_cast<int32_t*>(ws + L.bv1);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+    uint32_t* hist2 = L.hist2 ? reinterpret_cast<uint32_t*>(ws + L.hist2) : nullptr;
+    kmap_h_init<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, cap0, hist, hist2, st);
     SUBM3D_LAUNCHED("kmap_h_init");
-    kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, key_in,
-                                                           slot_of, false, can_grow, st);
+    kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, slot_of,
+                                                           false, can_grow, st);
     SUBM3D_LAUNCHED("kmap_h_insert");
     if (can_grow) {   // both return at once unless the first table was too small
       kmap_h_grow<<<grid_for(cap_max, 256, 8), 256, 0, stream>>>(table, cap_max, st);
       SUBM3D_LAUNCHED("kmap_h_grow");
-      kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, key_in,
-                                                             slot_of, true, false, st);
+      kmap_h_insert<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, N, res, bits, table, slot_of,
+                                                             true, false, st);
       SUBM3D_LAUNCHED("kmap_h_insert");
     }
-    kmap_h_alloc<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, st);
-    SUBM3D_LAUNCHED("kmap_h_alloc");
-    kmap_h_scatter<<<grid_for(N, 256, 8), 256, 0, stream>>>(key_in, slot_of, N, table, mk0, ix0,
-                                                            st);
+    g_stage.mark("block insert", stream);
+    // the occupied blocks (key, slot) into (mk0, ix0), sorted by key through (mk1, bv1)
+    kmap_h_compact<<<grid_for(cap0, 256, 8), 256, 0, stream>>>(table, mk0, ix0, st);
+    SUBM3D_LAUNCHED("kmap_h_compact");
+    const int npass_b = (3 * bits - 6 + 16 + 7) / 8;
+    kmap_plan<<<1, 1, 0, stream>>>(npass_b, -1, st);
+    SUBM3D_LAUNCHED("kmap_plan");
+    g_stage.mark("block compact", stream);
+    const int* plans = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
+                                                    offsetof(KmapStatus, plan));
+    const int rc = launch_radix(mk0, mk1, ix0, bv1, N, npass_b, hist, ws + L.cnt, L.nblk, plans,
+                                st, stream, "block sort pass", &st->nblocks);
+    if (rc != SUBM3D_OK) return rc;
+    uint32_t* tsum = reinterpret_cast<uint32_t*>(sort_scratch(ws + L.cnt, L.nblk).status);
+    const int tiles = static_cast<int>((N + kStartTile - 1) / kStartTile);
+    kmap_h_tsum<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
+    SUBM3D_LAUNCHED("kmap_h_tsum");
+    kmap_h_tscan<<<1, 256, 0, stream>>>(tsum, st);
+    SUBM3D_LAUNCHED("kmap_h_tscan");
+    kmap_h_apply<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
+    SUBM3D_LAUNCHED("kmap_h_apply");
+    g_stage.mark("block starts", stream);
+    kmap_h_scatter<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, slot_of, N, bits, table, mk0, ix0,
+                                                            order, st);
     SUBM3D_LAUNCHED("kmap_h_scatter");
-    g_stage.mark("block table (hashed, no sort)", stream);
+    g_stage.mark("voxel scatter", stream);
   } else {
     const int rc = launch_sort(c4, N, res, L, ws, stream);
     if (rc != SUBM3D_OK) return rc;

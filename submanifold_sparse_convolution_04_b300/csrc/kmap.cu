@@ -13,9 +13,10 @@
 // blocks by key, each block's voxels by place.
 //   1. insert  : validate each coordinate; find or claim its block's slot in an
 //                open-addressing hash table (splitmix64 of the block key, bounded linear
-//                probing, atomicCAS) and OR its bit into the slot's 64-bit occupancy
-//                mask (a bit already set is a duplicate coordinate)
-//   2. compact : the occupied slots (block key, slot index)
+//                probing, atomicCAS), OR its bit into the slot's 64-bit occupancy mask
+//                and count itself in the slot
+//   2. compact : the occupied slots (block key, slot index); a count above the mask's
+//                popcount is a duplicate coordinate
 //   3. sort    : LSD radix sort of the block keys only (single-pass passes with
 //                decoupled look-back; passes whose digit is constant are skipped)
 //   4. starts  : exclusive scan of the sorted blocks' popcounts: each block's first
@@ -72,10 +73,12 @@ struct KmapStatus {
 };
 
 struct __align__(32) Slot {
-  unsigned long long key;    // packed block key, kEmptyKey when free
+  unsigned long long key;    // block key, kEmptyKey when free
   unsigned long long mask;   // bit (Morton order of the voxel inside the block) per active voxel
   unsigned long long start;  // first sorted position of the block's voxels
-  unsigned long long pad;    // (one 32-byte load brings the whole slot)
+  unsigned long long count;  // hashed front end: voxels that set a bit (more than the mask's
+                             // popcount means a duplicate coordinate); one 32-byte load
+                             // brings the whole slot
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -564,7 +567,7 @@ __global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max,
     s.key = kEmptyKey;
     s.mask = 0;
     s.start = 0;
-    s.pad = 0;
+    s.count = 0;
     table[i] = s;
   }
 }
@@ -656,10 +659,10 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 // the occupied blocks by their keys, each block's voxels by their place in it (the low
 // 6 bits of the code). So instead of sorting the N voxels' codes, the blocks are found
 // first and only their keys are sorted (about a tenth as many on surfaces):
-//   insert : each voxel finds or claims its block's slot (the lanes of a warp that
-//            share a block send one lookup and one OR of their bits into the slot's
-//            mask); a bit that was already set is a duplicate coordinate;
-//   compact: the occupied slots' keys and indices, with the smallest and largest key;
+//   insert : each voxel finds or claims its block's slot, ORs its bit into the slot's
+//            mask and adds one to the slot's count;
+//   compact: the occupied slots' keys and indices, with the smallest and largest key
+//            (a count above the mask's popcount is a duplicate coordinate);
 //   sort   : the LSD radix sort of (block key, slot) (count read on the device);
 //   starts : an exclusive scan of the sorted blocks' popcounts (per-tile sums, a scan
 //            of those, then each block's first position into its slot);
@@ -708,8 +711,8 @@ __global__ void kmap_h_grow(Slot* table, unsigned long long cap, KmapStatus* st)
     table[i] = empty;
 }
 
-// kSkip: the voxel takes no position (a coordinate out of range, a repeat of an earlier
-// coordinate, or a block that did not fit).
+// kSkip: the voxel takes no position (a coordinate out of range, or a block that did not
+// fit).
 constexpr uint32_t kSkip = 0xFFFFFFFFu;
 
 __device__ __forceinline__ bool coord_ok(int4 c, int res) {   // (b, z, y, x)
@@ -724,7 +727,11 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 
 // refill: the second launch, which runs only when the first table was too small.
 // can_grow: a block needing more than kGrowProbe probes marks the build for the
-// full-size table instead of failing.
+// full-size table instead of failing. Each voxel looks its block up on its own (a read
+// first, atomicCAS only on an empty slot), then ORs its bit into the mask and counts
+// itself, both as reductions that return nothing (the compaction compares the count
+// with the mask's popcount to find duplicates). (Grouping a warp's lanes by block with
+// match/reduce intrinsics, or reading back the old mask, cost more than they saved.)
 __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
                                                      int res, int bits, Slot* table,
                                                      uint32_t* __restrict__ slot_of, bool refill,
@@ -734,33 +741,18 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
   const unsigned long long cmask = cap - 1;
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
-  const int lane = threadIdx.x & 31;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  constexpr unsigned kAll = 0xffffffffu;
-  for (int64_t w0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x - lane; w0 < N; w0 += stride) {
-    const int64_t i = w0 + lane;
-    const bool live = i < N;
-    const int4 c = live ? coords[i] : make_int4(0, 0, 0, 0);
-    const bool ok = live && coord_ok(c, res);
-    if (live && !ok) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
+    const int4 c = coords[i];
+    uint32_t sidx = kSkip;
+    if (!coord_ok(c, res)) {
       atomicOr(&st->flags, kFlagCoord);
       atomicMin(&st->bad_row, static_cast<long long>(i));
-    }
-    const unsigned long long key = ok ? sort_key(c, bits) : ~0ull;
-    const unsigned long long blk = key >> 6;   // ~0 >> 6 is no valid voxel's block key
-    const unsigned long long bit = ok ? 1ull << (key & 63u) : 0ull;
-    const unsigned peers = __match_any_sync(kAll, blk);
-    const unsigned same = __match_any_sync(kAll, key);
-    const int leader = __ffs(peers) - 1;
-    // the group's bits (one OR into the slot for the whole group)
-    const unsigned long long gbits =
-        (static_cast<unsigned long long>(__reduce_or_sync(peers, static_cast<uint32_t>(bit >> 32)))
-         << 32) |
-        __reduce_or_sync(peers, static_cast<uint32_t>(bit));
-    long long h = -1;
-    unsigned long long old = 0;
-    if (ok && lane == leader) {
+    } else {
+      const unsigned long long key = sort_key(c, bits);
+      const unsigned long long blk = key >> 6;
       unsigned long long hh = mix64(blk) & cmask;
+      long long h = -1;
       for (int probe = 0; probe < limit; ++probe) {
         unsigned long long k = __ldcg(&table[hh].key);
         if (k == kEmptyKey) k = atomicCAS(&table[hh].key, kEmptyKey, blk);
@@ -770,18 +762,15 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
         }
         hh = (hh + 1) & cmask;
       }
-      if (h < 0) atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
-      else old = atomicOr(&table[h].mask, gbits);
+      if (h < 0) {
+        atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+      } else {
+        atomicOr(&table[h].mask, 1ull << (key & 63u));
+        atomicAdd(&table[h].count, 1ull);
+        sidx = static_cast<uint32_t>(h);
+      }
     }
-    h = __shfl_sync(kAll, h, leader);
-    old = __shfl_sync(kAll, old, leader);
-    uint32_t sidx = kSkip;
-    if (ok && h >= 0) {
-      // a repeat: an earlier lane of this warp, or another warp, holds the same code
-      if ((__ffs(same) - 1) != lane || (old & bit)) atomicOr(&st->flags, kFlagDup);
-      else sidx = static_cast<uint32_t>(h);
-    }
-    if (live) slot_of[i] = sidx;
+    slot_of[i] = sidx;
   }
 }
 
@@ -799,6 +788,9 @@ __global__ void __launch_bounds__(256) kmap_h_compact(const Slot* __restrict__ t
     const unsigned long long i = b0 + threadIdx.x;
     const unsigned long long k = i < cap ? __ldcg(&table[i].key) : kEmptyKey;
     const uint32_t occ = k != kEmptyKey;
+    if (occ && static_cast<unsigned long long>(__popcll(__ldcg(&table[i].mask))) !=
+                   __ldcg(&table[i].count))
+      atomicOr(&st->flags, kFlagDup);   // two voxels set one bit
     uint32_t total;
     const uint32_t before = block_exclusive_scan256(occ, tmp, &total);
     if (threadIdx.x == 0)
@@ -915,7 +907,9 @@ __global__ void __launch_bounds__(256) kmap_h_apply(const int32_t* __restrict__ 
   }
 }
 
-// Each voxel to its position: sort key to mk, input row to ix (and to order).
+// Each voxel to its position: sort key to mk, input row to ix (and to order). Repeats of
+// one coordinate share a position (one of them lands there; the build then fails), so
+// the positions [0, npos) are all written.
 __global__ void __launch_bounds__(256) kmap_h_scatter(
     const int4* __restrict__ coords, const uint32_t* __restrict__ slot_of, int64_t N, int bits,
     const Slot* __restrict__ table, unsigned long long* __restrict__ mk, int32_t* __restrict__ ix,
@@ -960,7 +954,7 @@ __global__ void __launch_bounds__(256) kmap_h_scatter(
 enum ProbeMode { kProbeNbr = 0, kProbeSorted = 1 };
 constexpr int kProbeThreads = 128;
 constexpr int kProbeWarps = kProbeThreads / 32;
-constexpr int kRunsAtOnce = 8;   // runs of a warp's 32 voxels whose blocks are held at once
+constexpr int kRunsAtOnce = 6;   // runs of a warp's 32 voxels whose blocks are held at once
 
 // One hash lookup: the block's occupancy mask and first sorted position (0 and 0 when
 // the block is not in the table). A slot is one 32-byte load.
@@ -996,7 +990,7 @@ __host__ __device__ __forceinline__ int place_in_block(int z, int y, int x) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kProbeThreads) kmap_probe(
+__global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     const unsigned long long* __restrict__ mk0, const unsigned long long* __restrict__ mk1,
     const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int res,
     int bits, const Slot* __restrict__ table, int32_t* __restrict__ nbr,
@@ -1012,6 +1006,8 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
   __shared__ uint4 s_blk[kProbeWarps][kRunsAtOnce][27];
   __shared__ unsigned long long s_runkey[kProbeWarps][32];
   __shared__ uint32_t s_need[kProbeWarps][32];   // per run: the blocks its voxels reach
+  // per warp: the lookups of the runs held at once, run << 5 | block (0..26), in order
+  __shared__ uint8_t s_list[kProbeWarps][kRunsAtOnce * 27];
   __shared__ uint32_t need_tbl[64];              // per place: the blocks a voxel there reaches
   __shared__ int32_t s_row[kProbeWarps][32 * 27];
   for (int e = threadIdx.x; e < 27 * 64; e += kProbeThreads) {
@@ -1083,20 +1079,21 @@ __global__ void __launch_bounds__(kProbeThreads) kmap_probe(
     uint32_t present_mask = 0;
     for (int g0 = 0; g0 < nruns; g0 += kRunsAtOnce) {
       const int G = nruns - g0 < kRunsAtOnce ? nruns - g0 : kRunsAtOnce;
-      // the blocks these runs' voxels reach (of the 27 around each run's block), one per
-      // lane: lookup q is the (q - first[r])-th needed block of run r
+      // the blocks these runs' voxels reach (of the 27 around each run's block), listed
+      // run by run (lane kb < 27 places block kb of run r at its rank), then looked up
+      // one per lane
+      uint8_t* list = s_list[wid];
       int total = 0;
-      for (int r = 0; r < G; ++r) total += __popc(need_sm[g0 + r]);
+      for (int r = 0; r < G; ++r) {
+        const uint32_t nm = need_sm[g0 + r];
+        if (lane < 27 && ((nm >> lane) & 1u))
+          list[total + __popc(nm & ((1u << lane) - 1u))] = static_cast<uint8_t>((r << 5) | lane);
+        total += __popc(nm);
+      }
+      __syncwarp();
       for (int q = lane; q < total; q += 32) {
-        int r = 0, before = 0;
-        for (;; ++r) {
-          const int c = __popc(need_sm[g0 + r]);
-          if (q < before + c) break;
-          before += c;
-        }
-        uint32_t nm = need_sm[g0 + r];
-        for (int i = q - before; i > 0; --i) nm &= nm - 1u;
-        const int kb = __ffs(nm) - 1;
+        const int e = list[q];
+        const int r = e >> 5, kb = e & 31;
         const int dz = kb / 9 - 1, dy = (kb / 3) % 3 - 1, dx = kb % 3 - 1;
         unsigned long long key = runkey[g0 + r];
         bool inside = true;

@@ -326,38 +326,18 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def active_passes(coords, res):
-    """Radix passes the kernel map runs on these coords (constant high digits skipped)."""
-    import numpy as np
-    bits = 2
-    while (1 << bits) < res:
-        bits += 1
-    c = coords.astype(np.uint64)
-    key = c[:, 0] << np.uint64(3 * bits)
-    for t in range(bits):
-        key |= ((c[:, 3] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t)
-        key |= ((c[:, 2] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t + 1)
-        key |= ((c[:, 1] >> np.uint64(t)) & np.uint64(1)) << np.uint64(3 * t + 2)
-    diff = int(key.min()) ^ int(key.max())
-    npass = (3 * bits + 16 + 7) // 8
-    return sum(1 for p in range(npass) if (diff >> (8 * p)) != 0)
-
-
-def kmap_algorithmic_bytes(N, passes, grouped, window):
-    """Algorithmic bytes of one kernel-map build: every pass reads its inputs and writes
-    its outputs once (the L2-resident block table is not counted). A build of nbr alone
-    takes the hashed front end (passes = 0): insert, coords 16 N in, keys 8 N + slot
-    indices 4 N out; scatter, those 12 N in, block-grouped keys and rows 12 N out; probe,
-    keys and rows 12 N in, the table 108 N out. The sorted front end: pack: coords 16 N in,
-    keys 8 N + rows 4 N out; each active radix pass (constant high digits are skipped):
-    12 N in, 12 N out; block runs and table: keys 8 N, twice; probe: keys 8 N + rows 4 N
-    in, the table 108 N out. The tile plan's probe writes the table in Morton order plus
-    grouping keys and values (12 N); then the grouping sort (24 N per pass) and the plan
-    index (keys, values, rows 16 N in; perm 4 N out; the table's 108 N read and written
-    again in plan order)."""
+def kmap_algorithmic_bytes(N, grouped, window):
+    """Algorithmic bytes of one kernel-map build: every kernel reads its inputs and writes
+    its outputs once (the L2-resident block table is not counted). Insert: coords 16 N in,
+    a slot index 4 N out; scatter: coords and slot 20 N in, block-grouped keys and rows
+    12 N out; probe: keys and rows 12 N in, the table 108 N out (the radix sort of the
+    occupied blocks moves 12 bytes per block per pass, about a twelfth of N blocks, and
+    is left out). The tile plan's probe also writes grouping keys and values (12 N);
+    then the grouping sort (24 N per pass) and the plan index (keys, values, rows 16 N
+    in; perm 4 N out; the table's 108 N read and written again in plan order)."""
+    base = 16 * N + 4 * N + 20 * N + 12 * N + 12 * N + 108 * N
     if not grouped:
-        return 16 * N + 12 * N + 12 * N + 12 * N + 12 * N + 108 * N
-    base = 16 * N + 12 * N + 24 * N * passes + 16 * N + 12 * N + 108 * N
+        return base
     last_window = (N - 1) // window
     passes2 = (27 + last_window.bit_length() + 7) // 8
     return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N
@@ -609,13 +589,12 @@ def run_ours(args, world, rank, local):
                     case["name"] + ("_grouped" if grouped else "") +
                     ("" if not fused else "_" + epi.replace("+", "_")),
                     e=2 if bf16 else 4, residual=args.residual)
-    passes = active_passes(case["coords"], res) if grouped else 0   # nbr alone: no sort
-    kbytes = kmap_algorithmic_bytes(N, passes, grouped, window)
+    kbytes = kmap_algorithmic_bytes(N, grouped, window)
     hbm = float(peaks["hbm_gbs"])
     kmap_roof = {"bound": "hbm", "achieved": kbytes / (kmap_ms / 1e3) / 1e9, "peak": hbm,
                  "unit": "GB/s", "frac": kbytes / (kmap_ms / 1e3) / 1e9 / hbm,
-                 "algorithmic_bytes": kbytes, "radix_passes": passes,
-                 "front_end": "Morton radix sort" if grouped else "hashed blocks (no sort)",
+                 "algorithmic_bytes": kbytes,
+                 "front_end": "hashed blocks, radix sort of the block keys",
                  "peak_source": f"hbm_gbs, {peak_kind}",
                  "stages_ms": [[n, round(t, 4)] for n, t in stages]}
     line = {

@@ -51,7 +51,12 @@ constexpr int kSortTile = kSortThreads * kSortItems;   // keys per sort block
 constexpr int kMaxPasses = 8;
 constexpr int kMaxProbe = 4096;
 constexpr int kHistParts = 16;   // partial digit histograms (spreads the count kernel's atomics)
-constexpr int kScatterSmem = kSortTile * 12 + (kSortThreads / 32) * 257 * 4 + 2 * 256 * 4;
+// shared memory of a sort pass over tiles of `tile` keys
+constexpr int scatter_smem(int tile) { return tile * 12 + (kSortThreads / 32) * 257 * 4 + 2 * 256 * 4; }
+// The block-key sort runs on a twelfth as many keys: quarter-size tiles give it four
+// times as many blocks in flight (its passes are latency-bound at that size).
+constexpr int kBlockSortItems = 2;
+constexpr int kSmallTileRatio = kSortItems / kBlockSortItems;
 
 enum : int {
   kFlagCoord = 1, kFlagDup = 2, kFlagFull = 4, kFlagInternal = 8, kFlagOrder = 16,
@@ -97,6 +102,7 @@ struct Layout {
   // tile plan only: grouping-sort keys and values (ping-pong), its histograms, and the
   // neighbour table in sorted (Morton) order
   size_t k2a, k2b, v2a, v2b, hist2, nbr_sorted;
+
   size_t total;
   int64_t nblk;
 };
@@ -113,7 +119,7 @@ Layout make_layout(int64_t N, int64_t cap, bool grouped = false) {
   L.ix0 = o;    o = align256(o + sizeof(int32_t) * N);
   L.ix1 = o;    o = align256(o + sizeof(int32_t) * N);
   L.bv1 = o;    o = align256(o + sizeof(int32_t) * N);
-  L.cnt = o;    o = align256(o + sort_scratch_bytes(L.nblk));
+  L.cnt = o;    o = align256(o + sort_scratch_bytes(L.nblk * kSmallTileRatio));
   L.table = o;  o = align256(o + sizeof(Slot) * cap);
   L.k2a = L.k2b = L.v2a = L.v2b = L.hist2 = L.nbr_sorted = 0;
   if (grouped) {
@@ -300,14 +306,16 @@ __global__ void __launch_bounds__(256) kmap_hist(const unsigned long long* __res
                                                  int64_t N, const unsigned long long* count,
                                                  int npass, const int* plans,
                                                  uint32_t* __restrict__ hist, SortScratch S,
-                                                 int64_t ntile) {
+                                                 int64_t ntile, int tile_keys) {
   if (count && *count < static_cast<unsigned long long>(N)) N = static_cast<int64_t>(*count);
   __shared__ uint32_t sh[kMaxPasses][256];
   for (int i = threadIdx.x; i < kMaxPasses * 256; i += 256) sh[i >> 8][i & 255] = 0;
   const int64_t gtid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   if (gtid < kMaxPasses) S.counter[gtid] = 0;
-  const int64_t nstat = ntile * 256;
+  // the status words of the tiles that hold keys (the passes' other blocks return at once)
+  const int64_t used = (N + tile_keys - 1) / tile_keys;
+  const int64_t nstat = (used < ntile ? used : ntile) * 256;
   for (int64_t i = gtid; i < nstat; i += stride) S.status[i] = 0;
   unsigned active = 0;   // passes that run (a constant digit's pass is skipped)
   for (int p = 0; p < npass; ++p)
@@ -374,6 +382,7 @@ __global__ void __launch_bounds__(256) kmap_digit_starts(const uint32_t* __restr
 }
 
 // 4c. One pass: rank a tile, look back for each digit's count before it, scatter.
+template <int ITEMS>
 __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
     unsigned long long* mk0, unsigned long long* mk1, int32_t* ix0, int32_t* ix1, int64_t N,
     const unsigned long long* count, int pass, int64_t ntile, const int* plans, SortScratch S,
@@ -387,12 +396,13 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
   unsigned long long* dst = (plan & 1) ? mk0 : mk1;
   const int32_t* isrc = (plan & 1) ? ix1 : ix0;
   int32_t* idst = (plan & 1) ? ix0 : ix1;
-  constexpr int kPerWarp = kSortTile / kWarpsPerSort;   // 256
-  constexpr int kRounds = kPerWarp / 32;                // 8
+  constexpr int kTile = kSortThreads * ITEMS;           // keys per tile
+  constexpr int kPerWarp = kTile / kWarpsPerSort;
+  constexpr int kRounds = kPerWarp / 32;                // = ITEMS
   extern __shared__ __align__(16) unsigned char sort_sm[];
   unsigned long long* skey = reinterpret_cast<unsigned long long*>(sort_sm);
-  int32_t* srow = reinterpret_cast<int32_t*>(sort_sm + kSortTile * 8);
-  uint32_t* wcnt = reinterpret_cast<uint32_t*>(sort_sm + kSortTile * 12);   // [kWarps][257]
+  int32_t* srow = reinterpret_cast<int32_t*>(sort_sm + kTile * 8);
+  uint32_t* wcnt = reinterpret_cast<uint32_t*>(sort_sm + kTile * 12);   // [kWarps][257]
   uint32_t* loff = wcnt + kWarpsPerSort * 257;                                // [256]
   uint32_t* gbase = loff + 256;                                               // [256]
   __shared__ uint32_t tmp[8];
@@ -404,9 +414,9 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
   const int64_t tile = s_tile;
   // more blocks than tiles: nothing to do (tiles are handed out in order, so no tile that
   // holds keys waits for one past the end)
-  if (tile * kSortTile >= N) return;
+  if (tile * kTile >= N) return;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t tile0 = tile * kSortTile;
+  const int64_t tile0 = tile * kTile;
   const int64_t base = tile0 + warp * kPerWarp;
   unsigned long long key[kRounds];
   int32_t row[kRounds];
@@ -496,7 +506,7 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
     }
   }
   __syncthreads();
-  const int nvalid = static_cast<int>((N - tile0) < kSortTile ? (N - tile0) : kSortTile);
+  const int nvalid = static_cast<int>((N - tile0) < kTile ? (N - tile0) : kTile);
   for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
     const unsigned long long k = skey[i];
     const uint32_t dd = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
@@ -732,6 +742,10 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 // itself, both as reductions that return nothing (the compaction compares the count
 // with the mask's popcount to find duplicates). (Grouping a warp's lanes by block with
 // match/reduce intrinsics, or reading back the old mask, cost more than they saved.)
+// Voxels per thread and round of the insert and the scatter: their loads are independent,
+// so issuing them together overlaps their latencies.
+constexpr int kHashUnroll = 4;
+
 __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
                                                      int res, int bits, Slot* table,
                                                      uint32_t* __restrict__ slot_of, bool refill,
@@ -742,35 +756,56 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
-    const int4 c = coords[i];
-    uint32_t sidx = kSkip;
-    if (!coord_ok(c, res)) {
-      atomicOr(&st->flags, kFlagCoord);
-      atomicMin(&st->bad_row, static_cast<long long>(i));
-    } else {
-      const unsigned long long key = sort_key(c, bits);
-      const unsigned long long blk = key >> 6;
-      unsigned long long hh = mix64(blk) & cmask;
-      long long h = -1;
-      for (int probe = 0; probe < limit; ++probe) {
-        unsigned long long k = __ldcg(&table[hh].key);
-        if (k == kEmptyKey) k = atomicCAS(&table[hh].key, kEmptyKey, blk);
-        if (k == kEmptyKey || k == blk) {
-          h = static_cast<long long>(hh);
-          break;
-        }
-        hh = (hh + 1) & cmask;
-      }
-      if (h < 0) {
-        atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
-      } else {
-        atomicOr(&table[h].mask, 1ull << (key & 63u));
-        atomicAdd(&table[h].count, 1ull);
-        sidx = static_cast<uint32_t>(h);
-      }
+  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < N;
+       i0 += stride * kHashUnroll) {
+    int4 c[kHashUnroll];
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      c[u] = i < N ? coords[i] : make_int4(-1, 0, 0, 0);
     }
-    slot_of[i] = sidx;
+    unsigned long long key[kHashUnroll], hh[kHashUnroll], k0[kHashUnroll];
+    bool ok[kHashUnroll];
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {   // every voxel's first probe in flight at once
+      const int64_t i = i0 + u * stride;
+      ok[u] = i < N && coord_ok(c[u], res);
+      if (i < N && !ok[u]) {
+        atomicOr(&st->flags, kFlagCoord);
+        atomicMin(&st->bad_row, static_cast<long long>(i));
+      }
+      key[u] = ok[u] ? sort_key(c[u], bits) : 0ull;
+      hh[u] = mix64(key[u] >> 6) & cmask;
+      k0[u] = ok[u] ? __ldcg(&table[hh[u]].key) : 0ull;
+    }
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= N) break;
+      uint32_t sidx = kSkip;
+      if (ok[u]) {
+        const unsigned long long blk = key[u] >> 6;
+        unsigned long long h = hh[u], k = k0[u];
+        long long found = -1;
+        for (int probe = 0; probe < limit; ++probe) {
+          if (probe > 0) k = __ldcg(&table[h].key);
+          if (k == kEmptyKey) k = atomicCAS(&table[h].key, kEmptyKey, blk);
+          if (k == kEmptyKey || k == blk) {
+            found = static_cast<long long>(h);
+            break;
+          }
+          h = (h + 1) & cmask;
+        }
+        if (found < 0) {
+          atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+        } else {
+          atomicOr(&table[found].mask, 1ull << (key[u] & 63u));
+          atomicAdd(&table[found].count, 1ull);
+          sidx = static_cast<uint32_t>(found);
+        }
+      }
+      slot_of[i] = sidx;
+    }
   }
 }
 
@@ -917,19 +952,38 @@ __global__ void __launch_bounds__(256) kmap_h_scatter(
   if (blockIdx.x == 0 && threadIdx.x == 0) st->plan[kMaxPasses] = 0;   // the probe reads mk, ix
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   bool bad = false;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
-    const uint32_t h = slot_of[i];
-    if (h == kSkip) continue;
-    const unsigned long long key = sort_key(coords[i], bits);
-    const unsigned long long mask = table[h].mask;
-    const unsigned long long pos =
-        table[h].start + __popcll(mask & ((1ull << (key & 63u)) - 1ull));
-    if (pos < static_cast<unsigned long long>(N)) {
-      mk[pos] = key;
-      ix[pos] = static_cast<int32_t>(i);
-      if (order) order[pos] = static_cast<int32_t>(i);
-    } else {
-      bad = true;
+  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < N;
+       i0 += stride * kHashUnroll) {
+    uint32_t h[kHashUnroll];
+    unsigned long long mask[kHashUnroll], start[kHashUnroll], key[kHashUnroll];
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      h[u] = i < N ? slot_of[i] : kSkip;
+    }
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {   // the voxels' slots and keys in flight at once
+      const int64_t i = i0 + u * stride;
+      mask[u] = start[u] = key[u] = 0ull;
+      if (h[u] != kSkip) {
+        mask[u] = table[h[u]].mask;
+        start[u] = table[h[u]].start;
+        key[u] = sort_key(coords[i], bits);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kHashUnroll; ++u) {
+      if (h[u] == kSkip) continue;
+      const int64_t i = i0 + u * stride;
+      const unsigned long long pos =
+          start[u] + __popcll(mask[u] & ((1ull << (key[u] & 63u)) - 1ull));
+      if (pos < static_cast<unsigned long long>(N)) {
+        mk[pos] = key[u];
+        ix[pos] = static_cast<int32_t>(i);
+        if (order) order[pos] = static_cast<int32_t>(i);
+      } else {
+        bad = true;
+      }
     }
   }
   if (bad) atomicOr(&st->flags, kFlagInternal);
@@ -1255,24 +1309,39 @@ thread_local StageTimer g_stage;
 // pairs ping-ponging between (k0, v0) and (k1, v1); plans[p] (device) says whether pass p
 // runs and which buffer it reads, plans[kMaxPasses] which one holds the result.
 // count: when not NULL, the number of pairs is read on the device (at most N).
+// small_tiles: 512-key tiles (the scratch holds status words for that many tiles).
 int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, int32_t* v1,
                  int64_t N, int npass, uint32_t* hist, char* scratch, int64_t nblk,
                  const int* plans, KmapStatus* st, cudaStream_t stream,
-                 const char* stage = "sort pass", const unsigned long long* count = nullptr) {
-  static PerDevice<bool> attr_set;
-  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(kmap_onesweep),
-                                      kScatterSmem, "kmap_onesweep");
-  if (arc != SUBM3D_OK) return arc;
-  const SortScratch S = sort_scratch(scratch, nblk);
-  kmap_hist<<<grid_for(N, 256, 4), 256, 0, stream>>>(k0, N, count, npass, plans, hist, S, nblk);
+                 const char* stage = "sort pass", const unsigned long long* count = nullptr,
+                 bool small_tiles = false) {
+  static PerDevice<bool> attr_set[2];
+  const int arc0 = set_smem_limit_once(attr_set[0],
+                                       reinterpret_cast<const void*>(kmap_onesweep<kSortItems>),
+                                       scatter_smem(kSortTile), "kmap_onesweep");
+  if (arc0 != SUBM3D_OK) return arc0;
+  const int arc1 = set_smem_limit_once(
+      attr_set[1], reinterpret_cast<const void*>(kmap_onesweep<kBlockSortItems>),
+      scatter_smem(kSortThreads * kBlockSortItems), "kmap_onesweep");
+  if (arc1 != SUBM3D_OK) return arc1;
+  const int64_t ntile = small_tiles ? nblk * kSmallTileRatio : nblk;
+  const SortScratch S = sort_scratch(scratch, ntile);
+  kmap_hist<<<grid_for(N, 256, 4), 256, 0, stream>>>(
+      k0, N, count, npass, plans, hist, S, ntile,
+      small_tiles ? kSortThreads * kBlockSortItems : kSortTile);
   SUBM3D_LAUNCHED("kmap_hist");
   kmap_digit_starts<<<1, 256, 0, stream>>>(hist, npass, S);
   SUBM3D_LAUNCHED("kmap_digit_starts");
   g_stage.mark("digit histograms", stream);
-  const int grid = static_cast<int>(nblk);
+  const int grid = static_cast<int>(ntile);
   for (int p = 0; p < npass; ++p) {
-    kmap_onesweep<<<grid, kSortThreads, kScatterSmem, stream>>>(k0, k1, v0, v1, N, count, p,
-                                                                nblk, plans, S, st);
+    if (small_tiles)
+      kmap_onesweep<kBlockSortItems>
+          <<<grid, kSortThreads, scatter_smem(kSortThreads * kBlockSortItems), stream>>>(
+              k0, k1, v0, v1, N, count, p, ntile, plans, S, st);
+    else
+      kmap_onesweep<kSortItems><<<grid, kSortThreads, scatter_smem(kSortTile), stream>>>(
+          k0, k1, v0, v1, N, count, p, ntile, plans, S, st);
     SUBM3D_LAUNCHED("kmap_onesweep");
     g_stage.mark(stage, stream);
   }
@@ -1800,7 +1869,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     const int* plans = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
                                                     offsetof(KmapStatus, plan));
     const int rc = launch_radix(mk0, mk1, ix0, bv1, N, npass_b, hist, ws + L.cnt, L.nblk, plans,
-                                st, stream, "block sort pass", &st->nblocks);
+                                st, stream, "block sort pass", &st->nblocks, true);
     if (rc != SUBM3D_OK) return rc;
     uint32_t* tsum = reinterpret_cast<uint32_t*>(sort_scratch(ws + L.cnt, L.nblk).status);
     const int tiles = static_cast<int>((N + kStartTile - 1) / kStartTile);

@@ -45,9 +45,11 @@ def test_workspace_bytes_host_only(L):
     w1 = L.subm3d_kmap_workspace_bytes(1000)
     w2 = L.subm3d_kmap_workspace_bytes(3_000_000)
     assert 0 < w0 < w1 < w2
-    # two sort-key and two index buffers (24 B per voxel) + the block table reserved
-    # for its worst case (8 M slots of 32 B) dominate at 3 M voxels
-    assert 3_000_000 * 24 + 32 * (1 << 23) <= w2 < 1.05 * (3_000_000 * 24 + 32 * (1 << 23)) + (1 << 22)
+    # two sort-key and three index buffers (28 B per voxel), the sort passes' status
+    # words (8 B x 256 digits per 512-key tile: 4 B per voxel) and the block table
+    # reserved for its worst case (8 M slots of 32 B) dominate at 3 M voxels
+    lower = 3_000_000 * 32 + 32 * (1 << 23)
+    assert lower <= w2 < 1.05 * lower + (1 << 22)
     assert L.subm3d_kmap_workspace_bytes_ex(1000, 64) < w1
     assert L.subm3d_kmap_workspace_bytes_ex(1000, 0) == w1
 

@@ -69,6 +69,9 @@ def parse_args():
                    help="--op downsample: sort the voxels itself (subm3d_downsample) instead of "
                         "taking the Morton order of the kernel map on the same voxels "
                         "(subm3d_downsample_sorted)")
+    p.add_argument("--ds-wait", action="store_true",
+                   help="--op downsample: the call that reads M back to the host every time "
+                        "(one stream wait per call) instead of subm3d_downsample_async")
     p.add_argument("--pool", default="mean", choices=["mean", "max"],
                    help="pooling of --op downsample (and of the coarse rows --op upsample uses)")
     p.add_argument("--residual", action="store_true",
@@ -77,9 +80,10 @@ def parse_args():
                    help="fused block epilogue: activation after bias (+ residual)")
     p.add_argument("--max-voxels", type=int, default=0,
                    help="keep only the first M voxels (raster order): a slab of the workload")
-    p.add_argument("--path", default="grouped", choices=["grouped", "plain"],
-                   help="grouped: the kernel map as a tile plan and the forward on occupancy-"
-                        "grouped tiles; plain: the input-order nbr and the dense-offset tiles")
+    p.add_argument("--path", default="morton", choices=["morton", "grouped", "plain"],
+                   help="morton: the kernel map as a tile plan of the Morton order (window 1) "
+                        "and the forward on its tiles; grouped: a tile plan of mask-grouped "
+                        "windows (--window); plain: the input-order nbr and its tiles")
     p.add_argument("--window", type=int, default=0,
                    help="grouping window of the tile plan (0: the library default)")
     p.add_argument("--graph", action="store_true",
@@ -332,12 +336,16 @@ def kmap_algorithmic_bytes(N, grouped, window):
     a slot index 4 N out; scatter: coords and slot 20 N in, block-grouped keys and rows
     12 N out; probe: keys and rows 12 N in, the table 108 N out (the radix sort of the
     occupied blocks moves 12 bytes per block per pass, about a twelfth of N blocks, and
-    is left out). The tile plan's probe also writes grouping keys and values (12 N);
-    then the grouping sort (24 N per pass) and the plan index (keys, values, rows 16 N
-    in; perm 4 N out; the table's 108 N read and written again in plan order)."""
+    is left out). The tile plan's probe also writes grouping keys and values (12 N).
+    Window 1 (the Morton order): the probe's rows are the plan's, and the plan index
+    reads keys and rows (12 N) and writes perm (4 N). Larger windows: the grouping sort
+    (24 N per pass) and the plan index (keys, values, rows 16 N in; perm 4 N out; the
+    table's 108 N read and written again in plan order)."""
     base = 16 * N + 4 * N + 20 * N + 12 * N + 12 * N + 108 * N
     if not grouped:
         return base
+    if window == 1:
+        return base + 12 * N + 12 * N + 4 * N
     last_window = (N - 1) // window
     passes2 = (27 + last_window.bit_length() + 7) // 8
     return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N
@@ -369,8 +377,8 @@ def run_ours(args, world, rank, local):
     case = load_case(args)
     N, I, O, res = case["coords"].shape[0], case["I"], case["O"], case["res"]
     bf16 = case["dtype"] == "bf16"
-    grouped = args.path == "grouped"
-    window = args.window or GROUP_WINDOW
+    grouped = args.path in ("grouped", "morton")
+    window = 1 if args.path == "morton" else (args.window or GROUP_WINDOW)
     if args.graph:
         args.sync_kmap = False
 
@@ -586,7 +594,7 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = load_peaks()
     epi = "none" if not fused else ("residual+" if args.residual else "") + args.act
     roof = roofline(N, P, I, O, fwd_ms / 1e3, peaks, peak_kind,
-                    case["name"] + ("_grouped" if grouped else "") +
+                    case["name"] + ("_" + args.path if grouped else "") +
                     ("" if not fused else "_" + epi.replace("+", "_")),
                     e=2 if bf16 else 4, residual=args.residual)
     kbytes = kmap_algorithmic_bytes(N, grouped, window)
@@ -672,12 +680,22 @@ def run_resample(args, world, rank, local):
         # these voxels) already holds their Morton order
         order = None if args.ds_sort else subm3d_build_kmap_ex(c, res, order=True)[1]
 
-        def step():
-            subm3d_downsample(c, res, f, args.pool, workspace=ws, order=order)
+        if args.ds_wait:    # the call that returns M to the host (one wait per call)
+            def step():
+                subm3d_downsample(c, res, f, args.pool, workspace=ws, order=order)
+        else:               # M stays on the device: no wait inside the timed steps
+            outs = subm3d_downsample(c, res, f, args.pool, workspace=ws, order=order,
+                                     async_=True)
+
+            def step():
+                subm3d_downsample(c, res, f, args.pool, workspace=ws, order=order,
+                                  async_=True, out=outs)
         nbytes = 16 * N + N * C * e + 4 * N + M * (16 + 1 + C * e)
         kernel = ("downsample: sort + ds_count/ds_scan/ds_emit + ds_pool" if args.ds_sort else
                   "downsample on the kernel map's Morton order: ds_keys_in_order + "
-                  "ds_count/ds_scan/ds_emit + ds_pool")
+                  "ds_count/ds_scan/ds_emit + ds_pool") + (
+                  ", M read by the host every call" if args.ds_wait else
+                  ", M on the device (subm3d_downsample_async)")
     elif args.op == "upsample":
         def step():
             subm3d_upsample(cf, parent, out=up)

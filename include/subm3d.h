@@ -190,9 +190,16 @@ SUBM3D_API int subm3d_build_kmap_async(const int32_t* coords, int64_t N, int32_t
  *                                  [128 t, 128 t + 128) has a neighbour at offset k
  * The window (voxels of the Morton order grouped together) trades the share of offsets
  * skipped against the spread of the rows a tile gathers; SUBM3D_GROUP_WINDOW is the
- * default.
+ * default. Window 1 is the Morton order itself (SUBM3D_GROUP_MORTON): its build needs
+ * neither the grouping sort nor a second pass over the rows (the probe writes them in
+ * plan order), its tiles skip the offsets none of their 128 spatially close voxels has
+ * (about a sixth of them on shells), and it is the fastest plan end to end on the shell
+ * workloads. The forward loads rows per thread on plans of windows below 4096 (whose
+ * tiles keep most offsets) and copies whole rows through shared memory on sparser ones;
+ * the choice is noted per plan buffer when it is built and changes no result.
  */
 #define SUBM3D_GROUP_WINDOW 262144
+#define SUBM3D_GROUP_MORTON 1   /* window 1: tiles of the Morton order */
 #define SUBM3D_KMAP_ASYNC 1u   /* flags: return without waiting (see subm3d_build_kmap_async) */
 SUBM3D_API size_t subm3d_plan_bytes(int64_t N);
 /* Workspace bytes subm3d_build_kmap_grouped needs for N voxels (0 for N outside [0, 2^31)). */
@@ -204,7 +211,7 @@ SUBM3D_API size_t subm3d_kmap_grouped_workspace_bytes(int64_t N);
  * radix sort of the sorted positions by (window, mask), the plan's perm and tile masks,
  * and the neighbour rows written in plan order.
  *   coords, N, res  as subm3d_build_kmap.
- *   window          0 for SUBM3D_GROUP_WINDOW, else a power of two in [128, 2^30].
+ *   window          0 for SUBM3D_GROUP_WINDOW, else a power of two in [1, 2^30].
  *   plan            device buffer of at least subm3d_plan_bytes(N) bytes, written.
  *   workspace       device scratch of subm3d_kmap_grouped_workspace_bytes(N) bytes,
  *                   256-byte aligned.
@@ -367,6 +374,24 @@ SUBM3D_API int subm3d_downsample_sorted(const int32_t* coords, int64_t N, int32_
                                         int32_t* coarse_coords, void* coarse_feats,
                                         int32_t* parent, uint8_t* child_mask, int64_t* M_out,
                                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * subm3d_downsample (order NULL) or subm3d_downsample_sorted (order given) without the
+ * wait: every step is enqueued on `stream`, and M is written to the device word `M`
+ * (int64, 8-byte aligned) instead of returned, so the call can be captured into a CUDA
+ * graph and runs back to back with what follows. The outputs are sized for the worst
+ * case M = N by the caller (coarse_coords [N, 4], coarse_feats [N, C], child_mask [N]);
+ * rows [M, N) are left as they were. Errors found on the device (a coordinate outside the
+ * grid, a duplicate, an order that is not the coordinates' Morton order) set *M to 0 and
+ * are reported by the next subm3d_forward_status (SUBM3D_ERR_COORD_RANGE,
+ * SUBM3D_ERR_DUPLICATE, SUBM3D_ERR_ARG). Host-side argument errors are returned here.
+ */
+SUBM3D_API int subm3d_downsample_async(const int32_t* coords, int64_t N, int32_t res,
+                                       const int32_t* order, const void* feats, int32_t C,
+                                       subm3d_dtype dtype, subm3d_pool mode,
+                                       int32_t* coarse_coords, void* coarse_feats,
+                                       int32_t* parent, uint8_t* child_mask, int64_t* M,
+                                       void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * SparseUpsample(2) with the subdivision a subm3d_downsample stored:

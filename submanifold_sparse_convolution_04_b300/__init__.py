@@ -21,7 +21,7 @@ so that each 128-row tile's rows share their neighbour offsets, and
 subm3d_forward_grouped(feats, plan, weight, bias) runs only the offsets each tile has;
 out stays in input order.
 """
-from ._binding import (ACTIVATIONS, BF16, F32, GROUP_WINDOW, LIB_PATH, POOL_MODES, Subm3dError,
+from ._binding import (ACTIVATIONS, BF16, F32, GROUP_MORTON, GROUP_WINDOW, LIB_PATH, POOL_MODES, Subm3dError,
                        lib, plan_views, subm3d_build_kmap, subm3d_build_kmap_async,
                        subm3d_build_kmap_ex, subm3d_build_kmap_grouped, subm3d_build_kmap_noalloc,
                        subm3d_forward_grouped, subm3d_kmap_grouped_workspace_bytes,
@@ -30,7 +30,7 @@ from ._binding import (ACTIVATIONS, BF16, F32, GROUP_WINDOW, LIB_PATH, POOL_MODE
                        subm3d_kernel_launches, subm3d_kmap_workspace_bytes, subm3d_last_error,
                        subm3d_upsample, subm3d_spatial2channel, subm3d_channel2spatial)
 
-__all__ = ["ACTIVATIONS", "BF16", "F32", "GROUP_WINDOW", "LIB_PATH", "POOL_MODES", "Subm3dError",
+__all__ = ["ACTIVATIONS", "BF16", "F32", "GROUP_MORTON", "GROUP_WINDOW", "LIB_PATH", "POOL_MODES", "Subm3dError",
            "lib", "plan_views", "subm3d_build_kmap", "subm3d_build_kmap_async",
            "subm3d_build_kmap_ex", "subm3d_build_kmap_grouped", "subm3d_build_kmap_noalloc",
            "subm3d_forward_grouped", "subm3d_kmap_grouped_workspace_bytes", "subm3d_plan_bytes",

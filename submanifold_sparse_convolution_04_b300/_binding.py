@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_int, vp, vp, vp, vp,
                                                ctypes.POINTER(ctypes.c_int64), vp, sz, vp]
         L.subm3d_downsample_sorted.restype = ctypes.c_int
+        L.subm3d_downsample_async.argtypes = [vp, i64, i32, vp, vp, i32, ctypes.c_int,
+                                              ctypes.c_int, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.subm3d_downsample_async.restype = ctypes.c_int
         L.subm3d_upsample.argtypes = [vp, i64, i32, vp, i64, ctypes.c_int, vp, vp]
         L.subm3d_upsample.restype = ctypes.c_int
         L.subm3d_spatial2channel.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_int, vp, vp]
@@ -203,6 +206,7 @@ def subm3d_build_kmap_async(coords: torch.Tensor, res: int, nbr: torch.Tensor | 
 
 KMAP_ASYNC = 1
 GROUP_WINDOW = 262144
+GROUP_MORTON = 1   # window 1: tiles of the Morton order (no grouping sort)
 
 
 def subm3d_plan_bytes(N: int) -> int:
@@ -233,7 +237,7 @@ def subm3d_build_kmap_grouped(coords: torch.Tensor, res: int, window: int = 0,
                               workspace: torch.Tensor | None = None, async_: bool = False,
                               stream=None) -> torch.Tensor:
     """The kernel map as a tile plan (uint8 device buffer; see plan_views). window 0 is
-    the default grouping window."""
+    the default grouping window; GROUP_MORTON (1) gives tiles of the Morton order."""
     N = coords.shape[0]
     dev = coords.device
     pc = _dev(coords, "coords", torch.int32, (N, 4))
@@ -326,13 +330,17 @@ def subm3d_forward_ex(feats: torch.Tensor, nbr: torch.Tensor, weight: torch.Tens
 
 def subm3d_downsample(coords: torch.Tensor, res: int, feats: torch.Tensor | None = None,
                       mode: str = "mean", workspace: torch.Tensor | None = None, stream=None,
-                      order: torch.Tensor | None = None):
+                      order: torch.Tensor | None = None, async_: bool = False, out=None):
     """SparseDownsample(2): (coarse_coords int32 [M, 4], coarse_feats [M, C] or None,
     parent int32 [N], child_mask uint8 [M]) for coords int32 [N, 4] (b, z, y, x) on a
     grid of side res. Coarse voxels come in (batch, Morton) order; parent and
     child_mask are the subdivision subm3d_upsample takes. Synchronises the stream once.
     order: the Morton order subm3d_build_kmap_ex gave for the same coords (int32 [N]);
-    when given, the radix sort is skipped (subm3d_downsample_sorted)."""
+    when given, the radix sort is skipped (subm3d_downsample_sorted).
+    async_: subm3d_downsample_async -- no wait; returns (coarse_coords [N, 4],
+    coarse_feats [N, C] or None, parent [N], child_mask [N], M) with M an int64 device
+    tensor of one element and only the first M rows of the coarse outputs written.
+    out: that tuple from an earlier call of the same N and C, to write into again."""
     if mode not in POOL_MODES:
         raise ValueError(f"mode {mode!r} is not one of {sorted(POOL_MODES)}")
     N = coords.shape[0]
@@ -345,15 +353,29 @@ def subm3d_downsample(coords: torch.Tensor, res: int, feats: torch.Tensor | None
         C = feats.shape[1]
         dt = _DTYPES[feats.dtype]
         pf = _dev(feats, "feats", feats.dtype, (N, C))
-        cf = torch.empty((N, C), dtype=feats.dtype, device=dev)
-        pcf = _dev(cf, "coarse_feats")
-    cc = torch.empty((N, 4), dtype=torch.int32, device=dev)
-    parent = torch.empty(N, dtype=torch.int32, device=dev)
-    mask = torch.empty(N, dtype=torch.uint8, device=dev)
+    if out is not None:
+        cc, cf, parent, mask, m_dev = out
+    else:
+        cf = None if feats is None else torch.empty((N, C), dtype=feats.dtype, device=dev)
+        cc = torch.empty((N, 4), dtype=torch.int32, device=dev)
+        parent = torch.empty(N, dtype=torch.int32, device=dev)
+        mask = torch.empty(N, dtype=torch.uint8, device=dev)
+        m_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    if cf is not None:
+        pcf = _dev(cf, "coarse_feats", feats.dtype, (N, C))
     need = lib().subm3d_downsample_workspace_bytes(N)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     pw = _dev(workspace, "workspace", torch.uint8)
+    if async_:
+        po = None if order is None else _dev(order, "order", torch.int32, (N,))
+        _check(lib().subm3d_downsample_async(pc, N, int(res), po, pf, C, dt, POOL_MODES[mode],
+                                             _dev(cc, "cc", torch.int32, (N, 4)), pcf,
+                                             _dev(parent, "parent", torch.int32, (N,)),
+                                             _dev(mask, "mask", torch.uint8, (N,)),
+                                             _dev(m_dev, "M", torch.int64, (1,)), pw,
+                                             workspace.numel(), _stream(stream)))
+        return cc, cf, parent, mask, m_dev
     M = ctypes.c_int64(0)
     if order is None:
         _check(lib().subm3d_downsample(pc, N, int(res), pf, C, dt, POOL_MODES[mode],

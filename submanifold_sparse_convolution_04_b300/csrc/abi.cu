@@ -2,6 +2,9 @@
 // argument checks, the thread-local error message, the launch counter, and
 // dispatch to the kernel-map and forward launchers.
 #include <cstdarg>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -185,6 +188,31 @@ int subm3d_forward_ex(const void* feats, const int32_t* nbr, const void* weight,
                           dtype, TilePlan{nullptr, nullptr}, stream);
 }
 
+namespace {
+// The gather form subm3d_forward_grouped uses on a plan, noted per (device, buffer) when
+// the plan is built: plans of windows below 4096 voxels keep most offsets per tile and
+// run faster with per-thread row loads, sparser ones with staged whole-row copies. Only a
+// performance choice: a buffer not noted here (a copied plan, say) gets the staged form.
+constexpr int64_t kDenseWindowBelow = 4096;
+std::mutex g_plan_mu;
+std::map<std::pair<int, const void*>, bool> g_plan_dense;
+
+void note_plan(const void* plan, bool dense) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (g_plan_dense.size() > 4096) g_plan_dense.clear();   // bounded: notes are only hints
+  g_plan_dense[{dev, plan}] = dense;
+}
+bool plan_is_dense(const void* plan) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  const auto it = g_plan_dense.find({dev, plan});
+  return it != g_plan_dense.end() && it->second;
+}
+}  // namespace
+
 size_t subm3d_plan_bytes(int64_t N) {
   if (N < 0 || N > 0x7FFFFFFFll) return 0;
   return plan_layout(N).total;
@@ -200,8 +228,11 @@ int subm3d_build_kmap_grouped(const int32_t* coords, int64_t N, int32_t res, int
     set_error("subm3d_build_kmap_grouped: unknown flags 0x%x", flags);
     return SUBM3D_ERR_ARG;
   }
-  return kmap_build_grouped(coords, N, res, window, plan, plan_bytes, workspace, ws_bytes,
-                            !(flags & SUBM3D_KMAP_ASYNC), stream);
+  const int rc = kmap_build_grouped(coords, N, res, window, plan, plan_bytes, workspace, ws_bytes,
+                                   !(flags & SUBM3D_KMAP_ASYNC), stream);
+  if (rc == SUBM3D_OK && plan)
+    note_plan(plan, (window ? window : SUBM3D_GROUP_WINDOW) < kDenseWindowBelow);
+  return rc;
 }
 
 int subm3d_build_kmap_async(const int32_t* coords, int64_t N, int32_t res, int32_t* nbr,
@@ -226,7 +257,8 @@ int subm3d_forward_grouped(const void* feats, const void* plan, const void* weig
   const PlanLayout PL = plan_layout(N);
   const char* pl = static_cast<const char*>(plan);
   const TilePlan tp{N > 0 ? reinterpret_cast<const int32_t*>(pl + PL.perm) : nullptr,
-                    N > 0 ? reinterpret_cast<const uint32_t*>(pl + PL.tmask) : nullptr};
+                    N > 0 ? reinterpret_cast<const uint32_t*>(pl + PL.tmask) : nullptr,
+                    N > 0 && plan_is_dense(plan)};
   return forward_dispatch("subm3d_forward_grouped", feats,
                           N > 0 ? reinterpret_cast<const int32_t*>(pl + PL.nbr) : nullptr, weight,
                           bias, residual, act, out, N, I, O, dtype, tp, stream);
@@ -267,6 +299,21 @@ int subm3d_downsample_sorted(const int32_t* coords, int64_t N, int32_t res, cons
                           ws_bytes, stream);
 }
 
+int subm3d_downsample_async(const int32_t* coords, int64_t N, int32_t res, const int32_t* order,
+                            const void* feats, int32_t C, subm3d_dtype dtype, subm3d_pool mode,
+                            int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
+                            uint8_t* child_mask, int64_t* M, void* workspace, size_t ws_bytes,
+                            cudaStream_t stream) {
+  clear_error();
+  if (!M) {
+    set_error("subm3d_downsample_async: M (device) is NULL");
+    return SUBM3D_ERR_ARG;
+  }
+  return downsample_build(coords, N, res, order, feats, C, dtype, static_cast<int>(mode),
+                          coarse_coords, coarse_feats, parent, child_mask, nullptr, workspace,
+                          ws_bytes, stream, M);
+}
+
 int subm3d_upsample(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
                     int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream) {
   clear_error();
@@ -297,7 +344,8 @@ int subm3d_forward_status(cudaStream_t stream) {
   SUBM3D_CUDA_TRY(cudaMemcpy(&host, word, sizeof(int), cudaMemcpyDeviceToHost));
   SUBM3D_CUDA_TRY(cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice));
   if (host == 0) return SUBM3D_OK;
-  set_error("subm3d_forward_status: device reported%s%s%s%s%s%s%s%s",
+  set_error("subm3d_forward_status: device reported%s%s%s%s%s%s%s%s%s",
+            (host & kDevErrBadOrder) ? " [downsample] an order that is not the Morton order" : "",
             (host & kDevErrBadNbr) ? " an nbr entry outside [-1, N)" : "",
             (host & kDevErrTimeout) ? " a pipeline wait that ran out (kernel stopped early)" : "",
             (host & kDevErrBadParent) ? " a parent entry outside [0, M)" : "",
@@ -311,6 +359,7 @@ int subm3d_forward_status(cudaStream_t stream) {
     if (host & kDevErrKmapDup) return SUBM3D_ERR_DUPLICATE;
     if (host & kDevErrKmapFull) return SUBM3D_ERR_HASH_FULL;
   }
+  if (host & kDevErrBadOrder) return SUBM3D_ERR_ARG;
   return SUBM3D_ERR_DEVICE;
 }
 

@@ -92,7 +92,8 @@ int set_smem_limit_once(PerDevice<bool>& done, const void* kernel, int bytes, co
 // asynchronous kernel-map builds (bit flags below).
 enum : int {
   kDevErrBadNbr = 1, kDevErrTimeout = 2, kDevErrBadParent = 4, kDevErrKmapCoord = 8,
-  kDevErrKmapDup = 16, kDevErrKmapFull = 32, kDevErrKmapInternal = 64, kDevErrBadPlan = 128
+  kDevErrKmapDup = 16, kDevErrKmapFull = 32, kDevErrKmapInternal = 64, kDevErrBadPlan = 128,
+  kDevErrBadOrder = 256   // an asynchronous downsample given an order that is not Morton order
 };
 
 // Tile plan (subm3d_build_kmap_grouped): the caller's buffer holds, 256-byte aligned,
@@ -121,6 +122,9 @@ inline PlanLayout plan_layout(int64_t N) {
 struct TilePlan {
   const int32_t* perm;
   const uint32_t* tmask;
+  // a plan whose tiles keep most of their offsets (windows below 4096 voxels, the Morton
+  // order at window 1): the narrow kernel then loads rows per thread, as without a plan
+  bool dense = false;
 };
 // Device address of the word on the current device, or NULL (message set) when it
 // cannot be had; a launcher then returns SUBM3D_ERR_CUDA without launching.
@@ -160,7 +164,7 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_
                      const void* feats, int32_t C, subm3d_dtype dtype, int mode,
                      int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
                      uint8_t* child_mask, int64_t* M_out, void* workspace, size_t ws_bytes,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int64_t* M_dev = nullptr);
 int upsample_launch(const void* coarse_feats, int64_t M, int32_t C, const int32_t* parent,
                     int64_t N, subm3d_dtype dtype, void* fine_feats, cudaStream_t stream);
 int spatial2channel_launch(const void* feats, const int32_t* coords, const int32_t* parent,

@@ -657,11 +657,13 @@ int forward_launch_tm(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
   if (!err) return SUBM3D_ERR_CUDA;
   TmParams prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual),
                epi.act, N, I, O, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
-  // Tiles of a plan run about half the offsets, so their fewer stages can afford whole-
-  // row copies through shared memory (which spare the L1 data pipe); dense input-order
-  // tiles run every offset and go faster with each lane loading its own row, which
-  // needs 32-byte-aligned rows.
-  const bool staged = plan.tmask != nullptr || (reinterpret_cast<uintptr_t>(feats) & 31) != 0;
+  // Tiles of a mask-grouped plan run about half the offsets, so their fewer stages can
+  // afford whole-row copies through shared memory (which spare the L1 data pipe); dense
+  // tiles (input order, or a plan of small windows such as the Morton order) run most
+  // offsets and go faster with each lane loading its own row, which needs 32-byte-
+  // aligned rows.
+  const bool staged = (plan.tmask != nullptr && !plan.dense) ||
+                      (reinterpret_cast<uintptr_t>(feats) & 31) != 0;
   switch (O) {
     case 16: return staged ? tm_launch<16, true>(prm, weight, stream)
                            : tm_launch<16, false>(prm, weight, stream);

@@ -1261,6 +1261,33 @@ __global__ void __launch_bounds__(128) kmap_plan_index(
   if (bad) atomicOr(&st->flags, kFlagInternal);
 }
 
+// The plan of one-voxel windows (the Morton order itself), a block of 128 threads per
+// tile: perm[r] = the input row at Morton position r, the tile's offset mask the OR of
+// its rows' masks (the grouping keys the probe wrote, window bits zero) with the centre.
+__global__ void __launch_bounds__(128) kmap_morton_plan(
+    const unsigned long long* __restrict__ k2, const int32_t* __restrict__ ix0,
+    const int32_t* __restrict__ ix1, int64_t N, int64_t ntiles, int32_t* __restrict__ perm,
+    uint32_t* __restrict__ tmask, const KmapStatus* st) {
+  const int32_t* ix = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
+  // positions past npos exist only when the build failed (a skipped voxel)
+  const int64_t npos = static_cast<int64_t>(st->npos) < N ? static_cast<int64_t>(st->npos) : N;
+  __shared__ uint32_t wm[4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r = t * 128 + threadIdx.x;
+    uint32_t m = 0;
+    if (r < N) {
+      perm[r] = r < npos ? ix[r] : -1;
+      if (r < npos) m = static_cast<uint32_t>(k2[r]) & 0x7FFFFFFu;
+    }
+    for (int o = 16; o > 0; o >>= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
+    if (lane == 0) wm[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) tmask[t] = wm[0] | wm[1] | wm[2] | wm[3] | (1u << 13);
+    __syncthreads();
+  }
+}
+
 // Folds the build's status into the device error word (asynchronous builds).
 __global__ void kmap_report(const KmapStatus* st, int* err) {
   const int f = st->flags;
@@ -1781,8 +1808,8 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
               (long long)hash_capacity);
     return SUBM3D_ERR_ARG;
   }
-  if (grouped && (window < 128 || window > (int64_t(1) << 30) || (window & (window - 1)))) {
-    set_error("%s: window=%lld is not a power of two in [128, 2^30]", fn, (long long)window);
+  if (grouped && (window < 1 || window > (int64_t(1) << 30) || (window & (window - 1)))) {
+    set_error("%s: window=%lld is not a power of two in [1, 2^30]", fn, (long long)window);
     return SUBM3D_ERR_ARG;
   }
   if (N == 0) return SUBM3D_OK;
@@ -1937,21 +1964,35 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     int wbits = 0;
     while ((last_window >> wbits) != 0) ++wbits;
     const int npass2 = (27 + wbits + 7) / 8;
-    kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
-        mk0, mk1, ix0, ix1, N, res, bits, table, nbr_sorted, k2a, v2a, wshift, st);
-    SUBM3D_LAUNCHED("kmap_probe_sorted");
-    g_stage.mark("probe (Morton order) + masks", stream);
-    kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);
-    SUBM3D_LAUNCHED("kmap_plan2");
-    const int* plans2 = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
-                                                     offsetof(KmapStatus, plan2));
-    const int rc = launch_radix(k2a, k2b, v2a, v2b, N, npass2, hist2, ws + L.cnt, L.nblk, plans2,
-                                st, stream, "grouping sort pass");
-    if (rc != SUBM3D_OK) return rc;
-    kmap_plan_index<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
-        k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, nbr_sorted, perm, pnbr, tmask, st);
-    SUBM3D_LAUNCHED("kmap_plan_index");
-    g_stage.mark("plan index + rows", stream);
+    if (window == 1) {
+      // Windows of one voxel: the stable sort by (position, mask) is the identity, so the
+      // plan is the Morton order itself: the probe writes its rows straight into the
+      // plan, and perm and the tile masks follow from the probe's outputs.
+      kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
+          mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, k2a, v2a, 0, st);
+      SUBM3D_LAUNCHED("kmap_probe_sorted");
+      g_stage.mark("probe (Morton order) + masks", stream);
+      kmap_morton_plan<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
+          k2a, ix0, ix1, N, PL.ntiles, perm, tmask, st);
+      SUBM3D_LAUNCHED("kmap_morton_plan");
+      g_stage.mark("plan index (Morton order)", stream);
+    } else {
+      kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
+          mk0, mk1, ix0, ix1, N, res, bits, table, nbr_sorted, k2a, v2a, wshift, st);
+      SUBM3D_LAUNCHED("kmap_probe_sorted");
+      g_stage.mark("probe (Morton order) + masks", stream);
+      kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);
+      SUBM3D_LAUNCHED("kmap_plan2");
+      const int* plans2 = reinterpret_cast<const int*>(reinterpret_cast<const char*>(st) +
+                                                       offsetof(KmapStatus, plan2));
+      const int rc = launch_radix(k2a, k2b, v2a, v2b, N, npass2, hist2, ws + L.cnt, L.nblk,
+                                  plans2, st, stream, "grouping sort pass");
+      if (rc != SUBM3D_OK) return rc;
+      kmap_plan_index<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
+          k2a, k2b, v2a, v2b, ix0, ix1, N, PL.ntiles, nbr_sorted, perm, pnbr, tmask, st);
+      SUBM3D_LAUNCHED("kmap_plan_index");
+      g_stage.mark("plan index + rows", stream);
+    }
   }
 
   if (!sync) {
@@ -2083,16 +2124,35 @@ int launch_unpool(const void* coarse, int64_t M, int C, const int32_t* parent, i
 }
 }  // namespace
 
+// Asynchronous downsample: M (0 after an error) into the caller's device word, the
+// status folded into the device error word.
+__global__ void ds_report(const KmapStatus* st, int64_t N, int64_t* M_dev, int* err) {
+  const int f = st->flags;
+  int bits = 0;
+  if (f & kFlagOrder) bits |= kDevErrBadOrder;
+  if (f & kFlagCoord) bits |= kDevErrKmapCoord;
+  if (f & kFlagDup) bits |= kDevErrKmapDup;
+  if (f & kFlagInternal) bits |= kDevErrKmapInternal;
+  const long long M = static_cast<long long>(st->nblocks);
+  if (!bits && (M < 1 || M > N)) bits |= kDevErrKmapInternal;
+  *M_dev = bits ? 0 : M;
+  if (bits) atomicOr(err, bits);
+}
+
 int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_t* order,
                      const void* feats, int32_t C, subm3d_dtype dtype, int mode,
                      int32_t* coarse_coords, void* coarse_feats, int32_t* parent,
                      uint8_t* child_mask, int64_t* M_out, void* workspace, size_t ws_bytes,
-                     cudaStream_t stream) {
-  if (!M_out) {
+                     cudaStream_t stream, int64_t* M_dev) {
+  if (!M_out && !M_dev) {
     set_error("subm3d_downsample: M_out (host) is NULL");
     return SUBM3D_ERR_ARG;
   }
-  *M_out = 0;
+  if (M_out) *M_out = 0;
+  if (M_dev && (reinterpret_cast<uintptr_t>(M_dev) & 7)) {
+    set_error("subm3d_downsample_async: M=%p must be 8-byte aligned", (void*)M_dev);
+    return SUBM3D_ERR_ARG;
+  }
   if (N < 0 || N > 0x7FFFFFFFll) {
     set_error("subm3d_downsample: N=%lld outside [0, 2^31)", (long long)N);
     return SUBM3D_ERR_ARG;
@@ -2110,7 +2170,10 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_
               static_cast<int>(dtype));
     return SUBM3D_ERR_ARG;
   }
-  if (N == 0) return SUBM3D_OK;
+  if (N == 0) {
+    if (M_dev) SUBM3D_CUDA_TRY(cudaMemsetAsync(M_dev, 0, sizeof(int64_t), stream));
+    return SUBM3D_OK;
+  }
   if (!coords || !coarse_coords || !parent || !child_mask || !workspace || (feats && !coarse_feats)) {
     set_error("subm3d_downsample: NULL pointer (coords=%p coarse_coords=%p parent=%p "
               "child_mask=%p workspace=%p feats=%p coarse_feats=%p)",
@@ -2181,6 +2244,13 @@ int downsample_build(const int32_t* coords, int64_t N, int32_t res, const int32_
             : launch_pool<float>(feats, C, ix0, ix1, pstart, tsum + D.ntile, N, mode,
                                  coarse_feats, st, stream);
     if (prc != SUBM3D_OK) return prc;
+  }
+  if (M_dev) {   // no wait: M and the status stay on the device
+    int* err = forward_error_word();
+    if (!err) return SUBM3D_ERR_CUDA;
+    ds_report<<<1, 1, 0, stream>>>(st, N, M_dev, err);
+    SUBM3D_LAUNCHED("ds_report");
+    return SUBM3D_OK;
   }
 
   KmapStatus host;

@@ -53,7 +53,7 @@ def test_plan_bit_exact_on_workloads(dev, cfg_id):
 
 
 @pytest.mark.parametrize("cfg_id,window", [(3, 128), (3, 4096), (4, 1 << 30), (5, 1 << 16),
-                                           (2, 256)])
+                                           (2, 256), (5, 1), (3, 1), (4, 2), (1, 1)])
 def test_plan_bit_exact_other_windows(dev, cfg_id, window):
     case = cached_case(cfg_id)
     plan = gpu_plan(case["coords"], case["res"], dev, window=window)
@@ -66,15 +66,16 @@ def test_plan_bit_exact_shuffled_and_random_sets(dev):
     for seed, res, batch, n in [(0, 4, 1, 1), (2, 5, 3, 70), (3, 8, 2, 500), (6, 1, 5, 1),
                                 (7, 17, 7, 333), (5, 31, 1, 4000)]:
         c = random_set(np.random.default_rng(seed), res, batch, n)
-        check_plan(gpu_plan(c, res, dev, window=128), c, res, 128, ref.kernel_map(c, res))
+        for window in (128, 1):
+            check_plan(gpu_plan(c, res, dev, window=window), c, res, window, ref.kernel_map(c, res))
 
 
-def run_both(coords, res, v, dtype, dev, residual=None, act="none"):
+def run_both(coords, res, v, dtype, dev, residual=None, act="none", window=0):
     mk = (lambda a: bf16_tensor(a, dev)) if dtype == "bf16" else (lambda a: torch.from_numpy(a).to(dev))
     c = torch.from_numpy(coords).to(dev)
     f, w, b = mk(v["feats"]), mk(v["weight"]), mk(v["bias"])
     r = None if residual is None else mk(residual)
-    plan = subm3d_build_kmap_grouped(c, res)
+    plan = subm3d_build_kmap_grouped(c, res, window=window)
     out_g = subm3d_forward_grouped(f, plan, w, b, residual=r, act=act)
     nbr = subm3d_build_kmap(c, res)
     out_p = subm3d_forward_ex(f, nbr, w, b, residual=r, act=act)
@@ -82,10 +83,13 @@ def run_both(coords, res, v, dtype, dev, residual=None, act="none"):
     return out_g, out_p
 
 
-@pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
-def test_grouped_forward_every_row(dev, cfg_id):
+@pytest.mark.parametrize("cfg_id,window", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (2, 1),
+                                           (3, 1), (5, 1)])
+def test_grouped_forward_every_row(dev, cfg_id, window):
+    # window 0: mask-grouped tiles (staged row copies in the narrow kernel); window 1: the
+    # Morton order (per-thread row loads)
     case = cached_case(cfg_id)
-    out_g, out_p = run_both(case["coords"], case["res"], case, case["dtype"], dev)
+    out_g, out_p = run_both(case["coords"], case["res"], case, case["dtype"], dev, window=window)
     # the same present offsets, in the same order: equal values (signed zeros aside)
     assert bool((out_g == out_p).all())
     want = cpu.forward_rows(case["coords"], case["feats"], case["weight"], case["bias"],
@@ -98,10 +102,11 @@ def test_grouped_forward_every_row(dev, cfg_id):
                                        (32, 32, "f32")])
 def test_grouped_forward_several_tiles_per_cta(dev, I, O, dtype):
     coords, v = multi_tile_case(I * 3 + O + 1, I, O, dtype)
-    out_g, out_p = run_both(coords, 256, v, dtype, dev)
-    assert bool((out_g == out_p).all())
     want = cpu.forward_rows(coords, v["feats"], v["weight"], v["bias"], 256)
-    assert_close(out_g.float().cpu().numpy(), want, dtype, f"grouped I={I} O={O}")
+    for window in (0, 1):
+        out_g, out_p = run_both(coords, 256, v, dtype, dev, window=window)
+        assert bool((out_g == out_p).all())
+        assert_close(out_g.float().cpu().numpy(), want, dtype, f"window {window} I={I} O={O}")
 
 
 @pytest.mark.parametrize("I,O,act", [(64, 64, "relu"), (128, 128, "silu"), (32, 32, "none")])
@@ -179,6 +184,8 @@ def test_grouped_sync_errors(dev):
     c = torch.from_numpy(case["coords"]).to(dev)
     with pytest.raises(Subm3dError):
         subm3d_build_kmap_grouped(c, case["res"], window=100)          # not a power of two
+    with pytest.raises(Subm3dError):
+        subm3d_build_kmap_grouped(c, case["res"], window=-4)
     small = torch.empty(16, dtype=torch.uint8, device=dev)
     with pytest.raises(Subm3dError):
         subm3d_build_kmap_grouped(c, case["res"], plan=small)

@@ -264,3 +264,36 @@ def test_downsample_on_order_full_workload_and_a_wrong_order(dev):
     # recovery
     got2 = subm3d_downsample(c, case["res"], f, "mean", order=order)
     assert torch.equal(got2[1], plain[1])
+
+
+def test_downsample_async_matches_and_reports_errors(dev):
+    # the asynchronous downsample (M on the device, no wait): the same first M rows as the
+    # synchronous call, with and without the kernel map's order; twice into one set of
+    # outputs; device-side errors at the next status call, with M set to 0
+    from submanifold_sparse_convolution_04_b300 import subm3d_build_kmap_ex
+    case = cached_case(4)
+    c, f, _, _ = to_device(case, dev)
+    res = case["res"]
+    want = subm3d_downsample(c, res, f, "mean")
+    M = want[0].shape[0]
+    _, order = subm3d_build_kmap_ex(c, res, order=True)
+    out = None
+    for o in (None, order, order):
+        out = subm3d_downsample(c, res, f, "mean", order=o, async_=True, out=out)
+        subm3d_forward_status()
+        assert int(out[4].item()) == M
+        for a, b in zip((out[0][:M], out[1][:M], out[2], out[3][:M]), want):
+            assert torch.equal(a, b)
+    dup = torch.cat([c[:3000], c[7:8]])
+    d = subm3d_downsample(dup, res, async_=True)
+    with pytest.raises(Subm3dError) as e:
+        subm3d_forward_status()
+    assert e.value.code == B.ERR_DUPLICATE
+    assert int(d[4].item()) == 0
+    bad = order.clone()
+    bad[[10, 11]] = bad[[11, 10]]
+    subm3d_downsample(c, res, f, "mean", order=bad, async_=True)
+    with pytest.raises(Subm3dError) as e:
+        subm3d_forward_status()
+    assert e.value.code == B.ERR_ARG
+    subm3d_forward_status()

@@ -741,11 +741,8 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 // first, atomicCAS only on an empty slot), then ORs its bit into the mask and counts
 // itself, both as reductions that return nothing (the compaction compares the count
 // with the mask's popcount to find duplicates). (Grouping a warp's lanes by block with
-// match/reduce intrinsics, or reading back the old mask, cost more than they saved.)
-// Voxels per thread and round of the insert and the scatter: their loads are independent,
-// so issuing them together overlaps their latencies.
-constexpr int kHashUnroll = 4;
-
+// match/reduce intrinsics, reading back the old mask, or taking four voxels per thread
+// to overlap their lookups -- fewer warps then fit -- each measured slower.)
 __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
                                                      int res, int bits, Slot* table,
                                                      uint32_t* __restrict__ slot_of, bool refill,
@@ -756,56 +753,35 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < N;
-       i0 += stride * kHashUnroll) {
-    int4 c[kHashUnroll];
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {
-      const int64_t i = i0 + u * stride;
-      c[u] = i < N ? coords[i] : make_int4(-1, 0, 0, 0);
-    }
-    unsigned long long key[kHashUnroll], hh[kHashUnroll], k0[kHashUnroll];
-    bool ok[kHashUnroll];
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {   // every voxel's first probe in flight at once
-      const int64_t i = i0 + u * stride;
-      ok[u] = i < N && coord_ok(c[u], res);
-      if (i < N && !ok[u]) {
-        atomicOr(&st->flags, kFlagCoord);
-        atomicMin(&st->bad_row, static_cast<long long>(i));
-      }
-      key[u] = ok[u] ? sort_key(c[u], bits) : 0ull;
-      hh[u] = mix64(key[u] >> 6) & cmask;
-      k0[u] = ok[u] ? __ldcg(&table[hh[u]].key) : 0ull;
-    }
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {
-      const int64_t i = i0 + u * stride;
-      if (i >= N) break;
-      uint32_t sidx = kSkip;
-      if (ok[u]) {
-        const unsigned long long blk = key[u] >> 6;
-        unsigned long long h = hh[u], k = k0[u];
-        long long found = -1;
-        for (int probe = 0; probe < limit; ++probe) {
-          if (probe > 0) k = __ldcg(&table[h].key);
-          if (k == kEmptyKey) k = atomicCAS(&table[h].key, kEmptyKey, blk);
-          if (k == kEmptyKey || k == blk) {
-            found = static_cast<long long>(h);
-            break;
-          }
-          h = (h + 1) & cmask;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
+    const int4 c = coords[i];
+    uint32_t sidx = kSkip;
+    if (!coord_ok(c, res)) {
+      atomicOr(&st->flags, kFlagCoord);
+      atomicMin(&st->bad_row, static_cast<long long>(i));
+    } else {
+      const unsigned long long key = sort_key(c, bits);
+      const unsigned long long blk = key >> 6;
+      unsigned long long hh = mix64(blk) & cmask;
+      long long h = -1;
+      for (int probe = 0; probe < limit; ++probe) {
+        unsigned long long k = __ldcg(&table[hh].key);
+        if (k == kEmptyKey) k = atomicCAS(&table[hh].key, kEmptyKey, blk);
+        if (k == kEmptyKey || k == blk) {
+          h = static_cast<long long>(hh);
+          break;
         }
-        if (found < 0) {
-          atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
-        } else {
-          atomicOr(&table[found].mask, 1ull << (key[u] & 63u));
-          atomicAdd(&table[found].count, 1ull);
-          sidx = static_cast<uint32_t>(found);
-        }
+        hh = (hh + 1) & cmask;
       }
-      slot_of[i] = sidx;
+      if (h < 0) {
+        atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+      } else {
+        atomicOr(&table[h].mask, 1ull << (key & 63u));
+        atomicAdd(&table[h].count, 1ull);
+        sidx = static_cast<uint32_t>(h);
+      }
     }
+    slot_of[i] = sidx;
   }
 }
 
@@ -952,38 +928,19 @@ __global__ void __launch_bounds__(256) kmap_h_scatter(
   if (blockIdx.x == 0 && threadIdx.x == 0) st->plan[kMaxPasses] = 0;   // the probe reads mk, ix
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   bool bad = false;
-  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < N;
-       i0 += stride * kHashUnroll) {
-    uint32_t h[kHashUnroll];
-    unsigned long long mask[kHashUnroll], start[kHashUnroll], key[kHashUnroll];
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {
-      const int64_t i = i0 + u * stride;
-      h[u] = i < N ? slot_of[i] : kSkip;
-    }
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {   // the voxels' slots and keys in flight at once
-      const int64_t i = i0 + u * stride;
-      mask[u] = start[u] = key[u] = 0ull;
-      if (h[u] != kSkip) {
-        mask[u] = table[h[u]].mask;
-        start[u] = table[h[u]].start;
-        key[u] = sort_key(coords[i], bits);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kHashUnroll; ++u) {
-      if (h[u] == kSkip) continue;
-      const int64_t i = i0 + u * stride;
-      const unsigned long long pos =
-          start[u] + __popcll(mask[u] & ((1ull << (key[u] & 63u)) - 1ull));
-      if (pos < static_cast<unsigned long long>(N)) {
-        mk[pos] = key[u];
-        ix[pos] = static_cast<int32_t>(i);
-        if (order) order[pos] = static_cast<int32_t>(i);
-      } else {
-        bad = true;
-      }
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
+    const uint32_t h = slot_of[i];
+    if (h == kSkip) continue;
+    const unsigned long long key = sort_key(coords[i], bits);
+    const unsigned long long mask = table[h].mask;
+    const unsigned long long pos =
+        table[h].start + __popcll(mask & ((1ull << (key & 63u)) - 1ull));
+    if (pos < static_cast<unsigned long long>(N)) {
+      mk[pos] = key;
+      ix[pos] = static_cast<int32_t>(i);
+      if (order) order[pos] = static_cast<int32_t>(i);
+    } else {
+      bad = true;
     }
   }
   if (bad) atomicOr(&st->flags, kFlagInternal);

@@ -1007,14 +1007,14 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     int bits, const Slot* __restrict__ table, int32_t* __restrict__ nbr,
     unsigned long long* __restrict__ key2, int32_t* __restrict__ val2, int window_shift,
     KmapStatus* st) {
-  // tbl[k][p] = (which of the 27 blocks around a voxel's block holds its neighbour at
-  // offset k, for a voxel at place p) << 8 | (that neighbour's place in its block); the
-  // lanes of a warp read one offset's row at their own places, without bank conflicts
+  // tbl[k][p] = (2 x which of the 27 blocks around a voxel's block holds its neighbour
+  // at offset k, for a voxel at place p, + which half of that block's mask) << 5 | (the
+  // neighbour's bit in that half); the lanes of a warp read one offset's row at their
+  // own places, without bank conflicts
   __shared__ uint16_t tbl[27 * 64];
-  // per warp: the 27 blocks of up to kRunsAtOnce runs {mask low, mask high, first
-  // position, first position of the upper half}, the runs' block keys, and the 32
-  // voxels' rows
-  __shared__ uint4 s_blk[kProbeWarps][kRunsAtOnce][27];
+  // per warp: the 27 blocks of up to kRunsAtOnce runs, each as two halves {32-bit mask,
+  // first position of the half}, the runs' block keys, and the 32 voxels' rows
+  __shared__ uint2 s_blk[kProbeWarps][kRunsAtOnce][54];
   __shared__ unsigned long long s_runkey[kProbeWarps][32];
   __shared__ uint32_t s_need[kProbeWarps][32];   // per run: the blocks its voxels reach
   // per warp: the lookups of the runs held at once, run << 5 | block (0..26), in order
@@ -1027,7 +1027,8 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
               lx = (p & 1) | ((p >> 2) & 2);
     const int nz = lz + k / 9 - 1, ny = ly + (k / 3) % 3 - 1, nx = lx + k % 3 - 1;
     const int kb = 9 * ((nz >> 2) + 1) + 3 * ((ny >> 2) + 1) + ((nx >> 2) + 1);
-    tbl[e] = static_cast<uint16_t>((kb << 8) | place_in_block(nz & 3, ny & 3, nx & 3));
+    const int np = place_in_block(nz & 3, ny & 3, nx & 3);
+    tbl[e] = static_cast<uint16_t>(((2 * kb + (np >> 5)) << 5) | (np & 31));
   }
   for (int p = threadIdx.x; p < 64; p += kProbeThreads) {
     uint32_t need = 0;
@@ -1051,7 +1052,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   uint32_t* need_sm = s_need[wid];
-  uint4 (*blk_sm)[27] = s_blk[wid];
+  uint2 (*blk_sm)[54] = s_blk[wid];
   unsigned long long* runkey = s_runkey[wid];
   int32_t* row_sm = s_row[wid];
   // Block keys are (batch | Morton code of the block's coordinates); a neighbour block's
@@ -1118,23 +1119,20 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
         int32_t bb = 0;
         if (inside) block_lookup(table, key, cmask, max_probe, bm, bb, full);
         const uint32_t lo = static_cast<uint32_t>(bm), hi = static_cast<uint32_t>(bm >> 32);
-        blk_sm[r][kb] = make_uint4(lo, hi, static_cast<uint32_t>(bb),
-                                   static_cast<uint32_t>(bb) + __popc(lo));
+        blk_sm[r][2 * kb] = make_uint2(lo, static_cast<uint32_t>(bb));
+        blk_sm[r][2 * kb + 1] = make_uint2(hi, static_cast<uint32_t>(bb) + __popc(lo));
       }
       __syncwarp();
       if (valid && run >= g0 && run < g0 + G) {   // this lane's voxel: its 27 neighbours
-        const uint4* nb = blk_sm[run - g0];
+        const uint2* nb = blk_sm[run - g0];
 #pragma unroll
         for (int k = 0; k < 27; ++k) {
           const uint32_t e = tbl[k * 64 + p];
-          const uint4 b4 = nb[e >> 8];
-          const uint32_t bit = e & 63u;
-          const bool upper = bit >= 32;
-          const uint32_t word = upper ? b4.y : b4.x;
-          const uint32_t b5 = bit & 31u;
+          const uint2 half = nb[e >> 5];   // {mask half, its first position}
+          const uint32_t b5 = e & 31u;
           int32_t val = -1;
-          if ((word >> b5) & 1u) {
-            const uint32_t pos = (upper ? b4.w : b4.z) + __popc(word & ((1u << b5) - 1u));
+          if ((half.x >> b5) & 1u) {
+            const uint32_t pos = half.y + __popc(half.x & ((1u << b5) - 1u));
             present_mask |= 1u << k;
             if (pos < n32) val = __ldg(ix + pos);
             else bad = true;

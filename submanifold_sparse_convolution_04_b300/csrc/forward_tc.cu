@@ -104,10 +104,19 @@ struct Params {
 __device__ __forceinline__ uint32_t tile_mask(const Params& p, int tile) {
   return p.tmask ? ((__ldg(p.tmask + tile) & 0x7FFFFFFu) | (1u << 13)) : 0x7FFFFFFu;
 }
-// The i-th set bit of m.
+// The i-th (from 0) set bit of m: a binary search over popcounts of halves, without a
+// loop over the bits below it.
 __device__ __forceinline__ int nth_offset(uint32_t m, int i) {
-  for (int q = 0; q < i; ++q) m &= m - 1u;
-  return __ffs(m) - 1;
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const int c = __popc((m >> pos) & ((1u << w) - 1u));
+    if (i >= c) {
+      i -= c;
+      pos += w;
+    }
+  }
+  return pos;
 }
 
 // Walks a CTA's stages in order: stage g is step g - g0 of local tile lt, a step being
@@ -134,6 +143,31 @@ struct StageCursor {
       }
     }
     return lt < ntl;
+  }
+};
+
+// Stage g of a cursor as (offset index in its tile, channel chunk). A group's stages
+// advance by G at a time: inside one tile that is a fixed step (dq offsets, dr chunks,
+// with carry), so only the first stage of a tile divides.
+struct StagePos {
+  int lt = -1, oi = 0, c = 0;
+  uint32_t g = 0;
+  __device__ __forceinline__ void locate(const StageCursor& cur, uint32_t gg, uint32_t G,
+                                         int nchunks, int dq, int dr) {
+    if (cur.lt == lt && gg == g + G) {
+      c += dr;
+      oi += dq;
+      if (c >= nchunks) {
+        c -= nchunks;
+        ++oi;
+      }
+    } else {
+      const uint32_t kc = gg - cur.g0;
+      oi = static_cast<int>(kc / static_cast<uint32_t>(nchunks));
+      c = static_cast<int>(kc - static_cast<uint32_t>(oi) * static_cast<uint32_t>(nchunks));
+    }
+    lt = cur.lt;
+    g = gg;
   }
 };
 
@@ -310,24 +344,26 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
     int32_t jn[8];
     // cur: this group's stage; nxt: the one after it (its rows load a stage ahead)
     StageCursor cur, nxt;
+    StagePos pc, pn;
+    const int dq = G / p.nchunks, dr = G % p.nchunks;
     cur.start(p, ntl);
     nxt.start(p, ntl);
     if (nxt.seek(p, ntl, grp)) {
-      const uint32_t kc = grp - nxt.g0;
-      load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM,
-                nth_offset(nxt.mask, static_cast<int>(kc / p.nchunks)), rsub, jn, bad);
+      pn.locate(nxt, grp, G, p.nchunks, dq, dr);
+      load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM, nth_offset(nxt.mask, pn.oi),
+                rsub, jn, bad);
     }
     for (uint32_t g = grp; cur.seek(p, ntl, g); g += G) {
-      const uint32_t kc = g - cur.g0;
-      const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
-      const int k = nth_offset(cur.mask, static_cast<int>(kc / static_cast<uint32_t>(p.nchunks)));
+      pc.locate(cur, g, G, p.nchunks, dq, dr);
+      const int c = pc.c;
+      const int k = nth_offset(cur.mask, pc.oi);
       int32_t j[8];
 #pragma unroll
       for (int m = 0; m < 8; ++m) j[m] = jn[m];
       if (nxt.seek(p, ntl, g + G)) {   // next stage's rows: in flight while this stage is issued
-        const uint32_t kc2 = g + G - nxt.g0;
-        load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM,
-                  nth_offset(nxt.mask, static_cast<int>(kc2 / p.nchunks)), rsub, jn, bad);
+        pn.locate(nxt, g + G, G, p.nchunks, dq, dr);
+        load_rows(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM, nth_offset(nxt.mask, pn.oi),
+                  rsub, jn, bad);
       }
       const uint32_t s = g % S;
       const uint32_t ph = (g / S) & 1u;
@@ -385,8 +421,8 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
       const uint32_t d_tmem = tmem_base + buf * C::kBufCols;
       const uint32_t spt = __popc(tile_mask(p, blockIdx.x + t * gridDim.x)) *
                            static_cast<uint32_t>(p.nchunks);
-      for (uint32_t kc = 0; kc < spt; ++kc) {
-        const int c = static_cast<int>(kc % static_cast<uint32_t>(p.nchunks));
+      int c = 0;   // the stage's channel chunk, counted along (no division per stage)
+      for (uint32_t kc = 0; kc < spt; ++kc, c = (c + 1 == p.nchunks) ? 0 : c + 1) {
         const uint32_t s = g % S;
         const uint32_t ph = (g / S) & 1u;
         if (!warp_wait(full0 + 8 * s, ph, abort_flag)) {

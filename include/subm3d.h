@@ -120,8 +120,8 @@ SUBM3D_API size_t subm3d_kmap_workspace_bytes_ex(int64_t N, int64_t hash_capacit
  * z/y/x bits (its Morton code); the low 6 bits of the code are its place inside its
  * aligned 4x4x4 block, the bits above name the block. Each voxel finds or claims its
  * block's slot in an open-addressing hash table (64-bit block key, 64-bit occupancy
- * mask, the block's first position, a voxel count; bounded linear probing), sets its
- * bit in the mask and counts itself (a count above the mask's popcount is a duplicate
+ * mask, the block's first position; bounded linear probing) and sets its bit in the
+ * mask (two voxels on one coordinate set one bit: fewer bits than voxels is a duplicate
  * coordinate). Only the occupied blocks' keys
  * are radix-sorted; a scan of their popcounts gives each block its first position, and
  * each voxel's position (first position + rank of its bit) puts the voxels in Morton

@@ -116,13 +116,25 @@ struct TmParams {
 __device__ __forceinline__ uint32_t tm_tile_mask(const TmParams& p, int tile) {
   return p.tmask ? ((__ldg(p.tmask + tile) & 0x7FFFFFFu) | (1u << 13)) : 0x7FFFFFFu;
 }
+// The i-th (from 0) set bit of m: a binary search over popcounts of halves.
+__device__ __forceinline__ int tm_nth_bit(uint32_t m, int i) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const int c = __popc((m >> pos) & ((1u << w) - 1u));
+    if (i >= c) {
+      i -= c;
+      pos += w;
+    }
+  }
+  return pos;
+}
 // The offsets of pair j of a tile with mask m: its (2j)-th and (2j + 1)-th set bits
 // (k1 = -1 when the pair has only one).
 __device__ __forceinline__ void tm_pair_offsets(uint32_t m, int j, int& k0, int& k1) {
-  for (int i = 0; i < 2 * j; ++i) m &= m - 1u;
-  k0 = __ffs(m) - 1;
-  m &= m - 1u;
-  k1 = m ? __ffs(m) - 1 : -1;
+  k0 = tm_nth_bit(m, 2 * j);
+  const uint32_t above = m & ~((2u << k0) - 1u);   // set bits after k0
+  k1 = above ? __ffs(above) - 1 : -1;
 }
 
 __device__ __forceinline__ uint64_t tm_sw128_desc(uint32_t saddr) {

@@ -13,14 +13,14 @@
 // blocks by key, each block's voxels by place.
 //   1. insert  : validate each coordinate; find or claim its block's slot in an
 //                open-addressing hash table (splitmix64 of the block key, bounded linear
-//                probing, atomicCAS), OR its bit into the slot's 64-bit occupancy mask
-//                and count itself in the slot
-//   2. compact : the occupied slots (block key, slot index); a count above the mask's
-//                popcount is a duplicate coordinate
+//                probing, atomicCAS) and OR its bit into the slot's 64-bit occupancy
+//                mask
+//   2. compact : the occupied slots (block key, slot index)
 //   3. sort    : LSD radix sort of the block keys only (single-pass passes with
 //                decoupled look-back; passes whose digit is constant are skipped)
 //   4. starts  : exclusive scan of the sorted blocks' popcounts: each block's first
-//                position, stored in its slot
+//                position, stored in its slot; fewer positions than voxels (all of them
+//                valid and inserted) is a duplicate coordinate
 //   5. scatter : a voxel's position = its block's first position + the rank of its
 //                bit; (sort key, input row) stored there: the Morton order
 //   6. probe   : warps take 32 consecutive positions; per run of one block they look
@@ -81,9 +81,7 @@ struct __align__(32) Slot {
   unsigned long long key;    // block key, kEmptyKey when free
   unsigned long long mask;   // bit (Morton order of the voxel inside the block) per active voxel
   unsigned long long start;  // first sorted position of the block's voxels
-  unsigned long long count;  // hashed front end: voxels that set a bit (more than the mask's
-                             // popcount means a duplicate coordinate); one 32-byte load
-                             // brings the whole slot
+  unsigned long long pad;    // (one 32-byte load brings the whole slot)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -577,7 +575,7 @@ __global__ void kmap_table_init(Slot* table, int64_t cap_fixed, int64_t cap_max,
     s.key = kEmptyKey;
     s.mask = 0;
     s.start = 0;
-    s.count = 0;
+    s.pad = 0;
     table[i] = s;
   }
 }
@@ -669,13 +667,13 @@ __global__ void __launch_bounds__(256) kmap_blocks_insert(
 // the occupied blocks by their keys, each block's voxels by their place in it (the low
 // 6 bits of the code). So instead of sorting the N voxels' codes, the blocks are found
 // first and only their keys are sorted (about a tenth as many on surfaces):
-//   insert : each voxel finds or claims its block's slot, ORs its bit into the slot's
-//            mask and adds one to the slot's count;
-//   compact: the occupied slots' keys and indices, with the smallest and largest key
-//            (a count above the mask's popcount is a duplicate coordinate);
+//   insert : each voxel finds or claims its block's slot and ORs its bit into the
+//            slot's mask;
+//   compact: the occupied slots' keys and indices, with the smallest and largest key;
 //   sort   : the LSD radix sort of (block key, slot) (count read on the device);
 //   starts : an exclusive scan of the sorted blocks' popcounts (per-tile sums, a scan
-//            of those, then each block's first position into its slot);
+//            of those, then each block's first position into its slot); fewer
+//            positions than voxels is a duplicate coordinate;
 //   scatter: each voxel's position is its block's first position plus the rank of its
 //            bit in the mask; its sort key and input row (and the order, if asked for)
 //            go there.
@@ -738,11 +736,11 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 // refill: the second launch, which runs only when the first table was too small.
 // can_grow: a block needing more than kGrowProbe probes marks the build for the
 // full-size table instead of failing. Each voxel looks its block up on its own (a read
-// first, atomicCAS only on an empty slot), then ORs its bit into the mask and counts
-// itself, both as reductions that return nothing (the compaction compares the count
-// with the mask's popcount to find duplicates). (Grouping a warp's lanes by block with
-// match/reduce intrinsics, reading back the old mask, or taking four voxels per thread
-// to overlap their lookups -- fewer warps then fit -- each measured slower.)
+// first, atomicCAS only on an empty slot), then ORs its bit into the mask as a reduction
+// that returns nothing (duplicates show up later as fewer mask bits than voxels).
+// (Grouping a warp's lanes by block with match/reduce intrinsics, reading back the old
+// mask, or taking four voxels per thread to overlap their lookups -- fewer warps then
+// fit -- each measured slower.)
 __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
                                                      int res, int bits, Slot* table,
                                                      uint32_t* __restrict__ slot_of, bool refill,
@@ -777,7 +775,6 @@ __global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ co
         atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
       } else {
         atomicOr(&table[h].mask, 1ull << (key & 63u));
-        atomicAdd(&table[h].count, 1ull);
         sidx = static_cast<uint32_t>(h);
       }
     }
@@ -799,9 +796,6 @@ __global__ void __launch_bounds__(256) kmap_h_compact(const Slot* __restrict__ t
     const unsigned long long i = b0 + threadIdx.x;
     const unsigned long long k = i < cap ? __ldcg(&table[i].key) : kEmptyKey;
     const uint32_t occ = k != kEmptyKey;
-    if (occ && static_cast<unsigned long long>(__popcll(__ldcg(&table[i].mask))) !=
-                   __ldcg(&table[i].count))
-      atomicOr(&st->flags, kFlagDup);   // two voxels set one bit
     uint32_t total;
     const uint32_t before = block_exclusive_scan256(occ, tmp, &total);
     if (threadIdx.x == 0)
@@ -874,7 +868,11 @@ __global__ void __launch_bounds__(256) kmap_h_tsum(const int32_t* __restrict__ b
 
 // One block: the per-tile sums to exclusive prefixes, in place; the total is the number
 // of positions.
-__global__ void __launch_bounds__(256) kmap_h_tscan(uint32_t* __restrict__ tsum, KmapStatus* st) {
+// Also the duplicate test: every voxel inserted (no coordinate out of range, no block
+// that failed to fit) and fewer distinct codes (mask bits) than voxels means that two
+// voxels share a coordinate.
+__global__ void __launch_bounds__(256) kmap_h_tscan(uint32_t* __restrict__ tsum, int64_t N,
+                                                    KmapStatus* st) {
   __shared__ uint32_t tmp[8];
   const unsigned long long nb = st->nblocks;
   const int64_t ntile = static_cast<int64_t>((nb + kStartTile - 1) / kStartTile);
@@ -887,7 +885,11 @@ __global__ void __launch_bounds__(256) kmap_h_tscan(uint32_t* __restrict__ tsum,
     if (t < ntile) tsum[t] = static_cast<uint32_t>(carry + before);
     carry += total;
   }
-  if (threadIdx.x == 0) st->npos = carry;
+  if (threadIdx.x == 0) {
+    st->npos = carry;
+    if (carry < static_cast<unsigned long long>(N) && !(st->flags & (kFlagCoord | kFlagFull)))
+      atomicOr(&st->flags, kFlagDup);
+  }
 }
 
 __global__ void __launch_bounds__(256) kmap_h_apply(const int32_t* __restrict__ b0,
@@ -1857,7 +1859,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     const int tiles = static_cast<int>((N + kStartTile - 1) / kStartTile);
     kmap_h_tsum<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
     SUBM3D_LAUNCHED("kmap_h_tsum");
-    kmap_h_tscan<<<1, 256, 0, stream>>>(tsum, st);
+    kmap_h_tscan<<<1, 256, 0, stream>>>(tsum, N, st);
     SUBM3D_LAUNCHED("kmap_h_tscan");
     kmap_h_apply<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
     SUBM3D_LAUNCHED("kmap_h_apply");

@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
   // per warp: the lookups of the runs held at once, run << 5 | block (0..26), in order
   __shared__ uint8_t s_list[kProbeWarps][kRunsAtOnce * 27];
   __shared__ uint32_t need_tbl[64];              // per place: the blocks a voxel there reaches
-  __shared__ int32_t s_row[kProbeWarps][32 * 27];
+  __shared__ __align__(16) int32_t s_row[kProbeWarps][32 * 27];
   for (int e = threadIdx.x; e < 27 * 64; e += kProbeThreads) {
     const int k = e >> 6, p = e & 63;
     const int lz = ((p >> 2) & 1) | ((p >> 4) & 2), ly = ((p >> 1) & 1) | ((p >> 3) & 2),
@@ -1146,13 +1146,17 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     }
     // the 32 rows, out of shared memory
     if (MODE == kProbeSorted) {   // contiguous: rows of consecutive sorted positions
-      int32_t* dst = nbr + w * 32 * 27;
+      int32_t* dst = nbr + w * 32 * 27;   // 3456 bytes per warp: 16-byte aligned
       // (streaming stores: the table is written once and must not push the block table
-      // and the sort arrays, which the probe keeps reading, out of L2)
-      for (int i = lane; i < nvalid * 27; i += 32) __stcs(dst + i, row_sm[i]);
+      // and the sort arrays, which the probe keeps reading, out of L2); 16 bytes a lane
+      const int nw = nvalid * 27, n4 = nw >> 2;
+      const int4* src4 = reinterpret_cast<const int4*>(row_sm);
+      int4* dst4 = reinterpret_cast<int4*>(dst);
+      for (int i = lane; i < n4; i += 32) __stcs(dst4 + i, src4[i]);
+      for (int i = 4 * n4 + lane; i < nw; i += 32) __stcs(dst + i, row_sm[i]);
       if (valid) {
         key2[s] = (static_cast<unsigned long long>(s >> window_shift) << 27) | present_mask;
-        val2[s] = static_cast<int32_t>(s);
+        if (val2) val2[s] = static_cast<int32_t>(s);   // (not needed by a window-1 plan)
       }
     } else {                      // row by row, each to its input row
       for (int j = 0; j < nvalid; ++j) {
@@ -1926,7 +1930,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
       // plan is the Morton order itself: the probe writes its rows straight into the
       // plan, and perm and the tile masks follow from the probe's outputs.
       kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
-          mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, k2a, v2a, 0, st);
+          mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, k2a, nullptr, 0, st);
       SUBM3D_LAUNCHED("kmap_probe_sorted");
       g_stage.mark("probe (Morton order) + masks", stream);
       kmap_morton_plan<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(

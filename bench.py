@@ -336,16 +336,16 @@ def kmap_algorithmic_bytes(N, grouped, window):
     a slot index 4 N out; scatter: coords and slot 20 N in, block-grouped keys and rows
     12 N out; probe: keys and rows 12 N in, the table 108 N out (the radix sort of the
     occupied blocks moves 12 bytes per block per pass, about a twelfth of N blocks, and
-    is left out). The tile plan's probe also writes grouping keys and values (12 N).
-    Window 1 (the Morton order): the probe's rows are the plan's, and the plan index
-    reads keys and rows (12 N) and writes perm (4 N). Larger windows: the grouping sort
-    (24 N per pass) and the plan index (keys, values, rows 16 N in; perm 4 N out; the
-    table's 108 N read and written again in plan order)."""
+    is left out). Window 1 (the Morton order): the probe's rows are the plan's, and the
+    probe also writes perm (4 N). Larger windows: the probe writes grouping keys and
+    values (12 N); then the grouping sort (24 N per pass) and the plan index (keys,
+    values, rows 16 N in; perm 4 N out; the table's 108 N read and written again in plan
+    order)."""
     base = 16 * N + 4 * N + 20 * N + 12 * N + 12 * N + 108 * N
     if not grouped:
         return base
     if window == 1:
-        return base + 12 * N + 12 * N + 4 * N
+        return base + 4 * N
     last_window = (N - 1) // window
     passes2 = (27 + last_window.bit_length() + 7) // 8
     return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N

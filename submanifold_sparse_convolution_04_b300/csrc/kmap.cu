@@ -963,7 +963,9 @@ __global__ void __launch_bounds__(256) kmap_h_scatter(
 //   kProbeNbr     each voxel's row of nbr at its input row;
 //   kProbeSorted  its row at its sorted position (a Morton-ordered copy of the table,
 //                 which the tile plan reorders) and its 27-bit presence mask as a
-//                 grouping key (window << 27 | mask) with its sorted position as the value.
+//                 grouping key (window << 27 | mask) with its sorted position as the
+//                 value -- or, for a plan of one-voxel windows (perm given), the plan's
+//                 perm entry and the OR of the masks into the tile's offset mask.
 enum ProbeMode { kProbeNbr = 0, kProbeSorted = 1 };
 constexpr int kProbeThreads = 128;
 constexpr int kProbeWarps = kProbeThreads / 32;
@@ -1008,7 +1010,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     const int32_t* __restrict__ ix0, const int32_t* __restrict__ ix1, int64_t N, int res,
     int bits, const Slot* __restrict__ table, int32_t* __restrict__ nbr,
     unsigned long long* __restrict__ key2, int32_t* __restrict__ val2, int window_shift,
-    KmapStatus* st) {
+    int32_t* __restrict__ perm, uint32_t* __restrict__ tmask, KmapStatus* st) {
   // tbl[k][p] = (2 x which of the 27 blocks around a voxel's block holds its neighbour
   // at offset k, for a voxel at place p, + which half of that block's mask) << 5 | (the
   // neighbour's bit in that half); the lanes of a warp read one offset's row at their
@@ -1077,7 +1079,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     const unsigned long long m = valid ? mk[s] : ~0ull;
     const unsigned long long blk = m >> 6;
     int32_t orow = -1;   // the row this lane's voxel is written to
-    if (MODE == kProbeNbr && valid) orow = __ldg(ix + s);
+    if ((MODE == kProbeNbr || perm) && valid) orow = __ldg(ix + s);
     const unsigned long long prev = __shfl_up_sync(kAll, blk, 1);
     const unsigned newb = __ballot_sync(kAll, valid && (lane == 0 || prev != blk));
     const int run = __popc(newb & ((2u << lane) - 1u)) - 1;   // this lane's run, from 0
@@ -1154,9 +1156,13 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
       int4* dst4 = reinterpret_cast<int4*>(dst);
       for (int i = lane; i < n4; i += 32) __stcs(dst4 + i, src4[i]);
       for (int i = 4 * n4 + lane; i < nw; i += 32) __stcs(dst + i, row_sm[i]);
-      if (valid) {
+      if (perm) {   // a window-1 plan: perm and the tile's offset mask directly
+        if (valid) perm[s] = orow;
+        const uint32_t m = __reduce_or_sync(kAll, present_mask);
+        if (lane == 0) atomicOr(tmask + (w >> 2), m | (1u << 13));   // 4 warps per tile
+      } else if (valid) {
         key2[s] = (static_cast<unsigned long long>(s >> window_shift) << 27) | present_mask;
-        if (val2) val2[s] = static_cast<int32_t>(s);   // (not needed by a window-1 plan)
+        val2[s] = static_cast<int32_t>(s);
       }
     } else {                      // row by row, each to its input row
       for (int j = 0; j < nvalid; ++j) {
@@ -1220,33 +1226,6 @@ __global__ void __launch_bounds__(128) kmap_plan_index(
     __syncthreads();
   }
   if (bad) atomicOr(&st->flags, kFlagInternal);
-}
-
-// The plan of one-voxel windows (the Morton order itself), a block of 128 threads per
-// tile: perm[r] = the input row at Morton position r, the tile's offset mask the OR of
-// its rows' masks (the grouping keys the probe wrote, window bits zero) with the centre.
-__global__ void __launch_bounds__(128) kmap_morton_plan(
-    const unsigned long long* __restrict__ k2, const int32_t* __restrict__ ix0,
-    const int32_t* __restrict__ ix1, int64_t N, int64_t ntiles, int32_t* __restrict__ perm,
-    uint32_t* __restrict__ tmask, const KmapStatus* st) {
-  const int32_t* ix = (st->plan[kMaxPasses] & 1) ? ix1 : ix0;
-  // positions past npos exist only when the build failed (a skipped voxel)
-  const int64_t npos = static_cast<int64_t>(st->npos) < N ? static_cast<int64_t>(st->npos) : N;
-  __shared__ uint32_t wm[4];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t r = t * 128 + threadIdx.x;
-    uint32_t m = 0;
-    if (r < N) {
-      perm[r] = r < npos ? ix[r] : -1;
-      if (r < npos) m = static_cast<uint32_t>(k2[r]) & 0x7FFFFFFu;
-    }
-    for (int o = 16; o > 0; o >>= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
-    if (lane == 0) wm[warp] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) tmask[t] = wm[0] | wm[1] | wm[2] | wm[3] | (1u << 13);
-    __syncthreads();
-  }
 }
 
 // Folds the build's status into the device error word (asynchronous builds).
@@ -1905,7 +1884,7 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
   const int probe_grid = grid_for((N + 31) / 32 * 32, kProbeThreads, fit);
   if (!grouped) {
     kmap_probe<kProbeNbr><<<probe_grid, kProbeThreads, 0, stream>>>(
-        mk0, mk1, ix0, ix1, N, res, bits, table, nbr, nullptr, nullptr, 0, st);
+        mk0, mk1, ix0, ix1, N, res, bits, table, nbr, nullptr, nullptr, 0, nullptr, nullptr, st);
     SUBM3D_LAUNCHED("kmap_probe");
     g_stage.mark("probe", stream);
   } else {
@@ -1928,18 +1907,17 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     if (window == 1) {
       // Windows of one voxel: the stable sort by (position, mask) is the identity, so the
       // plan is the Morton order itself: the probe writes its rows straight into the
-      // plan, and perm and the tile masks follow from the probe's outputs.
+      // plan, with perm, and ORs each warp's masks into its tile's (cleared first; the
+      // four warps of a probe block hold one 128-row tile).
+      SUBM3D_CUDA_TRY(cudaMemsetAsync(tmask, 0, sizeof(uint32_t) * PL.ntiles, stream));
       kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
-          mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, k2a, nullptr, 0, st);
+          mk0, mk1, ix0, ix1, N, res, bits, table, pnbr, nullptr, nullptr, 0, perm, tmask, st);
       SUBM3D_LAUNCHED("kmap_probe_sorted");
-      g_stage.mark("probe (Morton order) + masks", stream);
-      kmap_morton_plan<<<grid_for(PL.ntiles * 128, 128, 16), 128, 0, stream>>>(
-          k2a, ix0, ix1, N, PL.ntiles, perm, tmask, st);
-      SUBM3D_LAUNCHED("kmap_morton_plan");
-      g_stage.mark("plan index (Morton order)", stream);
+      g_stage.mark("probe (Morton order) + plan", stream);
     } else {
       kmap_probe<kProbeSorted><<<probe_grid, kProbeThreads, 0, stream>>>(
-          mk0, mk1, ix0, ix1, N, res, bits, table, nbr_sorted, k2a, v2a, wshift, st);
+          mk0, mk1, ix0, ix1, N, res, bits, table, nbr_sorted, k2a, v2a, wshift, nullptr, nullptr,
+          st);
       SUBM3D_LAUNCHED("kmap_probe_sorted");
       g_stage.mark("probe (Morton order) + masks", stream);
       kmap_plan2<<<1, 1, 0, stream>>>(npass2, st);

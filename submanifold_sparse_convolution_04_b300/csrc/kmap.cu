@@ -75,6 +75,8 @@ struct KmapStatus {
   unsigned long long cap;        // hash capacity in use (a power of two)
   unsigned long long kmin, kmax; // smallest and largest sort key
   unsigned long long npos;       // positions of the block-grouped order the probe walks
+  unsigned int scan_ctr;         // next tile of the block-start scan
+  unsigned int pad4;
 };
 
 struct __align__(32) Slot {
@@ -179,6 +181,8 @@ __global__ void kmap_init(KmapStatus* st, uint32_t* hist, uint32_t* hist2) {
     st->kmin = ~0ull;
     st->kmax = 0;
     st->npos = 0;
+    st->scan_ctr = 0;
+    st->pad4 = 0;
   }
   for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) {
     hist[i] = 0;
@@ -406,115 +410,121 @@ __global__ void __launch_bounds__(kSortThreads) kmap_onesweep(
   __shared__ uint32_t tmp[8];
   __shared__ uint32_t s_tile;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) s_tile = atomicAdd(&S.counter[pass], 1u);
-  for (int i = threadIdx.x; i < kWarpsPerSort * 257; i += kSortThreads) wcnt[i] = 0;
-  __syncthreads();
-  const int64_t tile = s_tile;
-  // more blocks than tiles: nothing to do (tiles are handed out in order, so no tile that
-  // holds keys waits for one past the end)
-  if (tile * kTile >= N) return;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t tile0 = tile * kTile;
-  const int64_t base = tile0 + warp * kPerWarp;
-  unsigned long long key[kRounds];
-  int32_t row[kRounds];
-  uint32_t rank[kRounds];
+  // A block takes tiles until none are left (the grid is what fits on the GPU at once;
+  // every tile is taken by a running block, so a look-back only ever waits for tiles
+  // that running blocks hold).
+  for (;;) {
+    if (threadIdx.x == 0) s_tile = atomicAdd(&S.counter[pass], 1u);
+    for (int i = threadIdx.x; i < kWarpsPerSort * 257; i += kSortThreads) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t tile = s_tile;
+    // past the last tile (tiles are handed out in order, so no tile that holds keys waits
+    // for one past the end)
+    if (tile * kTile >= N) return;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int64_t tile0 = tile * kTile;
+    const int64_t base = tile0 + warp * kPerWarp;
+    unsigned long long key[kRounds];
+    int32_t row[kRounds];
+    uint32_t rank[kRounds];
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int64_t e = base + r * 32 + lane;
-    const bool valid = e < N;
-    key[r] = valid ? src[e] : 0ull;
-    row[r] = valid ? isrc[e] : 0;
-  }
-#pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const bool valid = base + r * 32 + lane < N;
-    const uint32_t d = valid ? static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u) : 256u;
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    const uint32_t before = __popc(peers & lt_mask);
-    const uint32_t prior = wcnt[warp * 257 + d];
-    __syncwarp();
-    if (before == 0) wcnt[warp * 257 + d] = prior + __popc(peers);
-    __syncwarp();
-    rank[r] = prior + before;
-  }
-  __syncthreads();
-  const int d = threadIdx.x;   // this thread's digit from here on
-  uint32_t run = 0;            // keys of digit d in this tile
-  for (int w = 0; w < kWarpsPerSort; ++w) {
-    const uint32_t c = wcnt[w * 257 + d];
-    wcnt[w * 257 + d] = run;
-    run += c;
-  }
-  {
-    uint32_t total;
-    loff[d] = block_exclusive_scan256(run, tmp, &total);
-  }
-  // publish this tile's count, then look back for the count before it
-  const unsigned long long tag = static_cast<unsigned long long>(pass + 1) << 34;
-  unsigned long long* my = S.status + tile * 256 + d;
-  uint32_t before_tile = 0;
-  if (tile == 0) {
-    st_relaxed_u64(my, tag | kTileInclusive | run);
-  } else {
-    st_relaxed_u64(my, tag | kTileAggregate | run);
-    // eight earlier tiles' words are read at once; the walk goes on from the first one
-    // not yet published (waiting for it, bounded) until an inclusive count ends it
-    int64_t t = tile - 1;
-    const unsigned long long t0 = global_timer_ns();
-    bool late = false;
-    for (uint32_t it = 0; t >= 0; ++it) {
-      unsigned long long v[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        v[q] = t - q >= 0 ? ld_relaxed_u64(S.status + (t - q) * 256 + d)
-                          : (tag | kTileInclusive);   // before tile 0: nothing
-      int used = 0;
-      bool done = false;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (done || used < q) continue;   // stopped at an unpublished word
-        const unsigned long long flag = (v[q] >> 34) == static_cast<unsigned long long>(pass + 1)
-                                            ? (v[q] & (3ull << 32)) : 0ull;
-        if (flag == 0) continue;          // not published yet (or an earlier pass's word)
-        before_tile += static_cast<uint32_t>(v[q]);
-        ++used;
-        if (flag == kTileInclusive) done = true;
-      }
-      if (done) break;
-      t -= used;
-      if (used < 8 && (it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
-        late = true;
-        break;
-      }
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t e = base + r * 32 + lane;
+      const bool valid = e < N;
+      key[r] = valid ? src[e] : 0ull;
+      row[r] = valid ? isrc[e] : 0;
     }
-    if (late) atomicOr(&st->flags, kFlagInternal);
-    st_relaxed_u64(my, tag | kTileInclusive | (before_tile + run));
-  }
-  gbase[d] = S.gofs[pass * 256 + d] + before_tile;
-  __syncthreads();
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int64_t e = base + r * 32 + lane;
-    if (e < N) {
-      const uint32_t dd = static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u);
-      const uint32_t local = loff[dd] + wcnt[warp * 257 + dd] + rank[r];
-      skey[local] = key[r];
-      srow[local] = row[r];
+    for (int r = 0; r < kRounds; ++r) {
+      const bool valid = base + r * 32 + lane < N;
+      const uint32_t d = valid ? static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u) : 256u;
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      const uint32_t before = __popc(peers & lt_mask);
+      const uint32_t prior = wcnt[warp * 257 + d];
+      __syncwarp();
+      if (before == 0) wcnt[warp * 257 + d] = prior + __popc(peers);
+      __syncwarp();
+      rank[r] = prior + before;
     }
-  }
-  __syncthreads();
-  const int nvalid = static_cast<int>((N - tile0) < kTile ? (N - tile0) : kTile);
-  for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
-    const unsigned long long k = skey[i];
-    const uint32_t dd = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
-    const int64_t pos = int64_t(gbase[dd]) + (i - static_cast<int>(loff[dd]));
-    if (pos >= 0 && pos < N) {
-      dst[pos] = k;
-      idst[pos] = srow[i];
+    __syncthreads();
+    const int d = threadIdx.x;   // this thread's digit from here on
+    uint32_t run = 0;            // keys of digit d in this tile
+    for (int w = 0; w < kWarpsPerSort; ++w) {
+      const uint32_t c = wcnt[w * 257 + d];
+      wcnt[w * 257 + d] = run;
+      run += c;
+    }
+    {
+      uint32_t total;
+      loff[d] = block_exclusive_scan256(run, tmp, &total);
+    }
+    // publish this tile's count, then look back for the count before it
+    const unsigned long long tag = static_cast<unsigned long long>(pass + 1) << 34;
+    unsigned long long* my = S.status + tile * 256 + d;
+    uint32_t before_tile = 0;
+    if (tile == 0) {
+      st_relaxed_u64(my, tag | kTileInclusive | run);
     } else {
-      atomicOr(&st->flags, kFlagInternal);
+      st_relaxed_u64(my, tag | kTileAggregate | run);
+      // eight earlier tiles' words are read at once; the walk goes on from the first one
+      // not yet published (waiting for it, bounded) until an inclusive count ends it
+      int64_t t = tile - 1;
+      const unsigned long long t0 = global_timer_ns();
+      bool late = false;
+      for (uint32_t it = 0; t >= 0; ++it) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          v[q] = t - q >= 0 ? ld_relaxed_u64(S.status + (t - q) * 256 + d)
+                            : (tag | kTileInclusive);   // before tile 0: nothing
+        int used = 0;
+        bool done = false;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (done || used < q) continue;   // stopped at an unpublished word
+          const unsigned long long flag = (v[q] >> 34) == static_cast<unsigned long long>(pass + 1)
+                                              ? (v[q] & (3ull << 32)) : 0ull;
+          if (flag == 0) continue;          // not published yet (or an earlier pass's word)
+          before_tile += static_cast<uint32_t>(v[q]);
+          ++used;
+          if (flag == kTileInclusive) done = true;
+        }
+        if (done) break;
+        t -= used;
+        if (used < 8 && (it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+          late = true;
+          break;
+        }
+      }
+      if (late) atomicOr(&st->flags, kFlagInternal);
+      st_relaxed_u64(my, tag | kTileInclusive | (before_tile + run));
     }
+    gbase[d] = S.gofs[pass * 256 + d] + before_tile;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t e = base + r * 32 + lane;
+      if (e < N) {
+        const uint32_t dd = static_cast<uint32_t>((key[r] >> (8 * pass)) & 255u);
+        const uint32_t local = loff[dd] + wcnt[warp * 257 + dd] + rank[r];
+        skey[local] = key[r];
+        srow[local] = row[r];
+      }
+    }
+    __syncthreads();
+    const int nvalid = static_cast<int>((N - tile0) < kTile ? (N - tile0) : kTile);
+    for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
+      const unsigned long long k = skey[i];
+      const uint32_t dd = static_cast<uint32_t>((k >> (8 * pass)) & 255u);
+      const int64_t pos = int64_t(gbase[dd]) + (i - static_cast<int>(loff[dd]));
+      if (pos >= 0 && pos < N) {
+        dst[pos] = k;
+        idst[pos] = srow[i];
+      } else {
+        atomicOr(&st->flags, kFlagInternal);
+      }
+    }
+    __syncthreads();   // the tile's shared arrays are free for the next one
   }
 }
 
@@ -700,6 +710,8 @@ __global__ void kmap_h_init(Slot* table, unsigned long long cap, uint32_t* hist,
     st->kmin = ~0ull;
     st->kmax = 0;
     st->npos = 0;
+    st->scan_ctr = 0;
+    st->pad4 = 0;
   }
   for (int64_t i = tid; i < kHistParts * kMaxPasses * 256; i += stride) {
     hist[i] = 0;
@@ -739,46 +751,66 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 // first, atomicCAS only on an empty slot), then ORs its bit into the mask as a reduction
 // that returns nothing (duplicates show up later as fewer mask bits than voxels).
 // (Grouping a warp's lanes by block with match/reduce intrinsics, reading back the old
-// mask, or taking four voxels per thread to overlap their lookups -- fewer warps then
-// fit -- each measured slower.)
-__global__ void __launch_bounds__(256) kmap_h_insert(const int4* __restrict__ coords, int64_t N,
-                                                     int res, int bits, Slot* table,
-                                                     uint32_t* __restrict__ slot_of, bool refill,
-                                                     bool can_grow, KmapStatus* st) {
+// mask, or four voxels per thread -- fewer warps then fit -- each measured slower; two
+// voxels per thread at 32 registers keep every warp resident.)
+__global__ void __launch_bounds__(256, 8) kmap_h_insert(const int4* __restrict__ coords,
+                                                        int64_t N, int res, int bits, Slot* table,
+                                                        uint32_t* __restrict__ slot_of,
+                                                        bool refill, bool can_grow,
+                                                        KmapStatus* st) {
   if (refill && !(st->flags & kFlagGrow)) return;
   const unsigned long long cap = st->cap;
   const unsigned long long cmask = cap - 1;
   const int max_probe = cap < kMaxProbe ? static_cast<int>(cap) : kMaxProbe;
   const int limit = can_grow ? (kGrowProbe < max_probe ? kGrowProbe : max_probe) : max_probe;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < N; i += stride) {
-    const int4 c = coords[i];
-    uint32_t sidx = kSkip;
-    if (!coord_ok(c, res)) {
-      atomicOr(&st->flags, kFlagCoord);
-      atomicMin(&st->bad_row, static_cast<long long>(i));
-    } else {
-      const unsigned long long key = sort_key(c, bits);
-      const unsigned long long blk = key >> 6;
-      unsigned long long hh = mix64(blk) & cmask;
-      long long h = -1;
-      for (int probe = 0; probe < limit; ++probe) {
-        unsigned long long k = __ldcg(&table[hh].key);
-        if (k == kEmptyKey) k = atomicCAS(&table[hh].key, kEmptyKey, blk);
-        if (k == kEmptyKey || k == blk) {
-          h = static_cast<long long>(hh);
-          break;
-        }
-        hh = (hh + 1) & cmask;
+  // two voxels per round (i and i + stride): their coordinate loads and first slot reads
+  // are in flight together, at a register count that keeps every warp resident
+  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < N; i0 += 2 * stride) {
+    int4 c[2];
+    c[0] = coords[i0];
+    c[1] = i0 + stride < N ? coords[i0 + stride] : make_int4(-1, 0, 0, 0);
+    unsigned long long key[2], hh[2], k0[2];
+    bool ok[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t i = i0 + u * stride;
+      ok[u] = i < N && coord_ok(c[u], res);
+      if (i < N && !ok[u]) {
+        atomicOr(&st->flags, kFlagCoord);
+        atomicMin(&st->bad_row, static_cast<long long>(i));
       }
-      if (h < 0) {
-        atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
-      } else {
-        atomicOr(&table[h].mask, 1ull << (key & 63u));
-        sidx = static_cast<uint32_t>(h);
-      }
+      key[u] = sort_key(c[u], bits);
+      hh[u] = mix64(key[u] >> 6) & cmask;
+      k0[u] = ok[u] ? __ldcg(&table[hh[u]].key) : 0ull;
     }
-    slot_of[i] = sidx;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= N) break;
+      uint32_t sidx = kSkip;
+      if (ok[u]) {
+        const unsigned long long blk = key[u] >> 6;
+        unsigned long long h = hh[u], k = k0[u];
+        long long found = -1;
+        for (int probe = 0; probe < limit; ++probe) {
+          if (probe > 0) k = __ldcg(&table[h].key);
+          if (k == kEmptyKey) k = atomicCAS(&table[h].key, kEmptyKey, blk);
+          if (k == kEmptyKey || k == blk) {
+            found = static_cast<long long>(h);
+            break;
+          }
+          h = (h + 1) & cmask;
+        }
+        if (found < 0) {
+          atomicOr(&st->flags, can_grow ? kFlagGrow : kFlagFull);
+        } else {
+          atomicOr(&table[found].mask, 1ull << (key[u] & 63u));
+          sidx = static_cast<uint32_t>(found);
+        }
+      }
+      slot_of[i] = sidx;
+    }
   }
 }
 
@@ -841,82 +873,92 @@ __device__ __forceinline__ const int32_t* sorted_slots(const int32_t* b0, const 
   return (st->plan[kMaxPasses] & 1) ? b1 : b0;
 }
 
-__global__ void __launch_bounds__(256) kmap_h_tsum(const int32_t* __restrict__ b0,
-                                                   const int32_t* __restrict__ b1,
-                                                   const Slot* __restrict__ table,
-                                                   uint32_t* __restrict__ tsum,
-                                                   const KmapStatus* st) {
-  const unsigned long long nb = st->nblocks;
-  const unsigned long long t0 = blockIdx.x * static_cast<unsigned long long>(kStartTile);
-  if (t0 >= nb) return;
-  const int32_t* bs = sorted_slots(b0, b1, st);
-  uint32_t c = 0;
-  for (int q = 0; q < kStartTile / 256; ++q) {
-    const unsigned long long e = t0 + q * 256 + threadIdx.x;
-    if (e < nb) c += __popcll(table[bs[e]].mask);
-  }
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  __shared__ uint32_t w[8];
-  if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = c;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t t = 0;
-    for (int k = 0; k < 8; ++k) t += w[k];
-    tsum[blockIdx.x] = t;
-  }
-}
 
-// One block: the per-tile sums to exclusive prefixes, in place; the total is the number
-// of positions.
-// Also the duplicate test: every voxel inserted (no coordinate out of range, no block
-// that failed to fit) and fewer distinct codes (mask bits) than voxels means that two
-// voxels share a coordinate.
-__global__ void __launch_bounds__(256) kmap_h_tscan(uint32_t* __restrict__ tsum, int64_t N,
-                                                    KmapStatus* st) {
+
+
+// The block starts in one pass (a decoupled look-back scan, as the sort passes use it): a
+// block takes the next tile of 2048 sorted blocks (tile numbers from a counter, in order),
+// sums their popcounts, publishes the sum, walks back over the earlier tiles' published
+// values to the count before its own (every wait bounded), publishes its inclusive count
+// and writes each block's first position into its slot. The last tile also records the
+// number of positions and the duplicate test (every voxel valid and inserted, fewer
+// distinct codes than voxels).
+constexpr unsigned long long kScanTag = 15ull << 34;   // no sort pass uses this tag
+
+__global__ void __launch_bounds__(256) kmap_h_starts(const int32_t* __restrict__ b0,
+                                                     const int32_t* __restrict__ b1,
+                                                     Slot* table,
+                                                     unsigned long long* __restrict__ status,
+                                                     int64_t N, KmapStatus* st) {
   __shared__ uint32_t tmp[8];
+  __shared__ uint32_t s_tile;
+  __shared__ unsigned long long s_before;
   const unsigned long long nb = st->nblocks;
   const int64_t ntile = static_cast<int64_t>((nb + kStartTile - 1) / kStartTile);
-  unsigned long long carry = 0;
-  for (int64_t b = 0; b < ntile; b += 256) {
-    const int64_t t = b + threadIdx.x;
-    const uint32_t v = t < ntile ? tsum[t] : 0u;
-    uint32_t total;
-    const uint32_t before = block_exclusive_scan256(v, tmp, &total);
-    if (t < ntile) tsum[t] = static_cast<uint32_t>(carry + before);
-    carry += total;
-  }
-  if (threadIdx.x == 0) {
-    st->npos = carry;
-    if (carry < static_cast<unsigned long long>(N) && !(st->flags & (kFlagCoord | kFlagFull)))
-      atomicOr(&st->flags, kFlagDup);
-  }
-}
-
-__global__ void __launch_bounds__(256) kmap_h_apply(const int32_t* __restrict__ b0,
-                                                    const int32_t* __restrict__ b1, Slot* table,
-                                                    const uint32_t* __restrict__ tsum,
-                                                    const KmapStatus* st) {
-  __shared__ uint32_t tmp[8];
-  const unsigned long long nb = st->nblocks;
-  const unsigned long long t0 = blockIdx.x * static_cast<unsigned long long>(kStartTile);
-  if (t0 >= nb) return;
   const int32_t* bs = sorted_slots(b0, b1, st);
   constexpr int kPer = kStartTile / 256;
-  const unsigned long long e0 = t0 + threadIdx.x * kPer;
-  int32_t slot[kPer];
-  uint32_t cnt[kPer], mine = 0;
+  for (;;) {
+    if (threadIdx.x == 0) s_tile = atomicAdd(&st->scan_ctr, 1u);
+    __syncthreads();
+    const int64_t t = s_tile;
+    if (t >= ntile) {
+      if (nb == 0 && t == 0) {   // no block at all (every coordinate out of range)
+        st->npos = 0;
+        if (N > 0 && !(st->flags & (kFlagCoord | kFlagFull))) atomicOr(&st->flags, kFlagDup);
+      }
+      return;
+    }
+    const unsigned long long e0 = t * static_cast<unsigned long long>(kStartTile) +
+                                  threadIdx.x * kPer;
+    int32_t slot[kPer];
+    uint32_t cnt[kPer], mine = 0;
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    slot[q] = e0 + q < nb ? bs[e0 + q] : -1;
-    cnt[q] = slot[q] >= 0 ? static_cast<uint32_t>(__popcll(table[slot[q]].mask)) : 0u;
-    mine += cnt[q];
-  }
-  uint32_t total;
-  unsigned long long at = tsum[blockIdx.x] + block_exclusive_scan256(mine, tmp, &total);
+    for (int q = 0; q < kPer; ++q) {
+      slot[q] = e0 + q < nb ? bs[e0 + q] : -1;
+      cnt[q] = slot[q] >= 0 ? static_cast<uint32_t>(__popcll(table[slot[q]].mask)) : 0u;
+      mine += cnt[q];
+    }
+    uint32_t total;
+    const uint32_t pre = block_exclusive_scan256(mine, tmp, &total);
+    if (threadIdx.x == 0) {
+      unsigned long long* my = status + t * 256;
+      unsigned long long before = 0;
+      if (t == 0) {
+        st_relaxed_u64(my, kScanTag | kTileInclusive | total);
+      } else {
+        st_relaxed_u64(my, kScanTag | kTileAggregate | total);
+        const unsigned long long t0 = global_timer_ns();
+        for (int64_t u = t - 1; u >= 0;) {
+          const unsigned long long v = ld_relaxed_u64(status + u * 256);
+          if ((v & (63ull << 34)) != kScanTag || !(v & (3ull << 32))) {   // not yet published
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicOr(&st->flags, kFlagInternal);
+              break;
+            }
+            continue;
+          }
+          before += static_cast<uint32_t>(v);
+          if ((v & (3ull << 32)) == kTileInclusive) break;
+          --u;
+        }
+        st_relaxed_u64(my, kScanTag | kTileInclusive | (before + total));
+      }
+      s_before = before;
+      if (t == ntile - 1) {
+        const unsigned long long npos = before + total;
+        st->npos = npos;
+        if (npos < static_cast<unsigned long long>(N) && !(st->flags & (kFlagCoord | kFlagFull)))
+          atomicOr(&st->flags, kFlagDup);
+      }
+    }
+    __syncthreads();
+    unsigned long long at = s_before + pre;
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    if (slot[q] >= 0) table[slot[q]].start = at;
-    at += cnt[q];
+    for (int q = 0; q < kPer; ++q) {
+      if (slot[q] >= 0) table[slot[q]].start = at;
+      at += cnt[q];
+    }
+    __syncthreads();   // s_tile and s_before are free for the next tile
   }
 }
 
@@ -1300,7 +1342,26 @@ int launch_radix(unsigned long long* k0, unsigned long long* k1, int32_t* v0, in
   kmap_digit_starts<<<1, 256, 0, stream>>>(hist, npass, S);
   SUBM3D_LAUNCHED("kmap_digit_starts");
   g_stage.mark("digit histograms", stream);
-  const int grid = static_cast<int>(ntile);
+  // the blocks that fit on the GPU at once (each takes tiles until none are left)
+  static PerDevice<int> fit[2];
+  int per_sm = 0;
+  {
+    const int which = small_tiles ? 1 : 0;
+    const int rc = fit[which].get(&per_sm, [which](int* v) -> int {
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n,
+          which ? reinterpret_cast<const void*>(kmap_onesweep<kBlockSortItems>)
+                : reinterpret_cast<const void*>(kmap_onesweep<kSortItems>),
+          kSortThreads,
+          which ? scatter_smem(kSortThreads * kBlockSortItems) : scatter_smem(kSortTile));
+      *v = (e == cudaSuccess && n > 0) ? n : 1;
+      return static_cast<int>(SUBM3D_OK);
+    });
+    if (rc != SUBM3D_OK) return rc;
+  }
+  const int64_t resident = int64_t(num_sms()) * per_sm;
+  const int grid = static_cast<int>(ntile < resident ? ntile : resident);
   for (int p = 0; p < npass; ++p) {
     if (small_tiles)
       kmap_onesweep<kBlockSortItems>
@@ -1838,14 +1899,12 @@ int kmap_run(const char* fn, const int32_t* coords, int64_t N, int32_t res, int3
     const int rc = launch_radix(mk0, mk1, ix0, bv1, N, npass_b, hist, ws + L.cnt, L.nblk, plans,
                                 st, stream, "block sort pass", &st->nblocks, true);
     if (rc != SUBM3D_OK) return rc;
-    uint32_t* tsum = reinterpret_cast<uint32_t*>(sort_scratch(ws + L.cnt, L.nblk).status);
-    const int tiles = static_cast<int>((N + kStartTile - 1) / kStartTile);
-    kmap_h_tsum<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
-    SUBM3D_LAUNCHED("kmap_h_tsum");
-    kmap_h_tscan<<<1, 256, 0, stream>>>(tsum, N, st);
-    SUBM3D_LAUNCHED("kmap_h_tscan");
-    kmap_h_apply<<<tiles, 256, 0, stream>>>(ix0, bv1, table, tsum, st);
-    SUBM3D_LAUNCHED("kmap_h_apply");
+    // the scan's published counts reuse the sort's status words (cleared by its
+    // histogram kernel, then tagged by its passes, never with the scan's tag)
+    unsigned long long* scan_status = sort_scratch(ws + L.cnt, L.nblk).status;
+    kmap_h_starts<<<grid_for((N + kStartTile - 1) / kStartTile * 256, 256, 4), 256, 0, stream>>>(
+        ix0, bv1, table, scan_status, N, st);
+    SUBM3D_LAUNCHED("kmap_h_starts");
     g_stage.mark("block starts", stream);
     kmap_h_scatter<<<grid_for(N, 256, 8), 256, 0, stream>>>(c4, slot_of, N, bits, table, mk0, ix0,
                                                             order, st);

@@ -1542,26 +1542,31 @@ __global__ void __launch_bounds__(kSortThreads) ds_emit(
   const unsigned long long* mk = second ? mk1 : mk0;
   const int32_t* ix = second ? ix1 : ix0;
   const int64_t s0 = blockIdx.x * int64_t(kDsTile) + threadIdx.x * int64_t(kSortItems);
-  uint32_t h = 0;
-  for (int j = 0; j < kSortItems; ++j) {
-    const int64_t s = s0 + j;
-    if (s < N && parent_starts(mk, s)) ++h;
-  }
+  // this thread's keys, and the one before them, read once
+  unsigned long long kk[kSortItems + 1];
+  kk[0] = s0 > 0 && s0 - 1 < N ? mk[s0 - 1] : ~0ull;
+#pragma unroll
+  for (int j = 0; j < kSortItems; ++j) kk[j + 1] = s0 + j < N ? mk[s0 + j] : ~0ull;
+  uint32_t heads = 0;   // bit j: position s0 + j starts a parent
+#pragma unroll
+  for (int j = 0; j < kSortItems; ++j)
+    if (s0 + j < N && (s0 + j == 0 || (kk[j] >> 3) != (kk[j + 1] >> 3))) heads |= 1u << j;
   __shared__ uint32_t tmp[8];
   uint32_t total;
-  const uint32_t pre = block_exclusive_scan256(h, tmp, &total);
+  const uint32_t pre = block_exclusive_scan256(__popc(heads), tmp, &total);
   int64_t p = int64_t(tsum[blockIdx.x]) + pre - 1;   // parent of the position before s0
+#pragma unroll
   for (int j = 0; j < kSortItems; ++j) {
     const int64_t s = s0 + j;
     if (s >= N) break;
-    const bool head = parent_starts(mk, s);
+    const bool head = (heads >> j) & 1u;
     if (head) ++p;
     const int32_t row = ix[s];
     parent[row] = static_cast<int32_t>(p);
     if (head) {
       // the parent's coordinates and the children's bits from the sort keys (the lowest
       // Morton triple is (z&1)<<2 | (y&1)<<1 | (x&1), the child bit)
-      const unsigned long long k0 = mk[s];
+      const unsigned long long k0 = kk[j + 1];
       const unsigned long long morton = k0 & ((1ull << (3 * bits)) - 1ull);
       coarse[p] = make_int4(static_cast<int>(k0 >> (3 * bits)),
                             static_cast<int>(compact3(morton >> 2) >> 1),
@@ -1654,11 +1659,17 @@ __global__ void __launch_bounds__(256) ds_pool(const T* __restrict__ feats, int 
     float acc[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) acc[k] = mode == SUBM3D_POOL_MAX ? -INFINITY : 0.f;
-    for (int32_t s = a; s < b; ++s) {
-      float v[V];
-      Vec<T, V>::load(feats + int64_t(ix[s]) * C + c0, v);
+    for (int32_t s = a; s < b; s += 2) {   // two children in flight per round
+      const bool two = s + 1 < b;
+      const int32_t r0 = ix[s], r1 = two ? ix[s + 1] : 0;
+      float v[V], u[V];
+      Vec<T, V>::load(feats + int64_t(r0) * C + c0, v);
+      if (two) Vec<T, V>::load(feats + int64_t(r1) * C + c0, u);
 #pragma unroll
-      for (int k = 0; k < V; ++k) acc[k] = mode == SUBM3D_POOL_MAX ? fmaxf(acc[k], v[k]) : acc[k] + v[k];
+      for (int k = 0; k < V; ++k) {
+        acc[k] = mode == SUBM3D_POOL_MAX ? fmaxf(acc[k], v[k]) : acc[k] + v[k];
+        if (two) acc[k] = mode == SUBM3D_POOL_MAX ? fmaxf(acc[k], u[k]) : acc[k] + u[k];
+      }
     }
     if (mode == SUBM3D_POOL_MEAN) {
       const float n = static_cast<float>(b - a);

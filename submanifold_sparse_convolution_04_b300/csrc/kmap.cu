@@ -1115,6 +1115,10 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
   const int64_t nwarps = (int64_t(gridDim.x) * kProbeThreads) >> 5;
   for (int64_t w = (blockIdx.x * int64_t(kProbeThreads) + threadIdx.x) >> 5; w * 32 < N;
        w += nwarps) {
+    if (MODE == kProbeSorted) {   // the previous rows' bulk copy has read the staging rows
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
     const int64_t s = w * 32 + lane;
     const bool valid = s < N;
     const int nvalid = (N - w * 32) < 32 ? static_cast<int>(N - w * 32) : 32;
@@ -1191,12 +1195,16 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     // the 32 rows, out of shared memory
     if (MODE == kProbeSorted) {   // contiguous: rows of consecutive sorted positions
       int32_t* dst = nbr + w * 32 * 27;   // 3456 bytes per warp: 16-byte aligned
-      // (streaming stores: the table is written once and must not push the block table
-      // and the sort arrays, which the probe keeps reading, out of L2); 16 bytes a lane
+      // one bulk copy of the staged rows (whole 16-byte pieces; the copy engine writes
+      // them while the warp goes on, and the next round waits only for it to have read
+      // the staging rows), the ragged tail of a partial warp by plain stores
       const int nw = nvalid * 27, n4 = nw >> 2;
-      const int4* src4 = reinterpret_cast<const int4*>(row_sm);
-      int4* dst4 = reinterpret_cast<int4*>(dst);
-      for (int i = lane; i < n4; i += 32) __stcs(dst4 + i, src4[i]);
+      fence_proxy_async_smem();   // the lanes' row writes before the copy reads them
+      __syncwarp();
+      if (lane == 0 && n4 > 0) {
+        bulk_store(dst, smem_u32(row_sm), static_cast<uint32_t>(n4) * 16u);
+        bulk_commit();
+      }
       for (int i = 4 * n4 + lane; i < nw; i += 32) __stcs(dst + i, row_sm[i]);
       if (perm) {   // a window-1 plan: perm and the tile's offset mask directly
         if (valid) perm[s] = orow;
@@ -1214,6 +1222,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     }
     __syncwarp();
   }
+  if (MODE == kProbeSorted && lane == 0) bulk_wait_all();   // every row written
   if (__any_sync(kAll, full) && lane == 0) atomicOr(&st->flags, kFlagFull);
   if (__any_sync(kAll, bad) && lane == 0) atomicOr(&st->flags, kFlagInternal);
 }

@@ -78,6 +78,11 @@ struct TmRoles {
   static constexpr int kThreads = 32 * (kNbrWarp + 1);  // 704 staged, 960 otherwise
   static constexpr int kWarpStaging = STAGED ? 2 * kRowsStaging : 0;   // a buffer per offset
   static constexpr int kStagingBytes = kProducerWarps * kWarpStaging;
+  // per-thread form: the epilogue warps' output rows pass through shared memory (32 rows
+  // of up to 128 bytes per warp, a 16-byte pad per row) so that whole rows leave with
+  // coalesced stores; the staged form has no room left for it
+  static constexpr int kEpiPitch = 128 + 16;
+  static constexpr int kEpiStagingBytes = STAGED ? 0 : 4 * 32 * kEpiPitch;
   static_assert(kAColBase + kStages * kStageCols <= 512, "tensor memory layout");
   static_assert(kStages % kGroups == 0, "slots per group");
   static_assert(((kEpiWarp0 & 3) + 0) >= 0, "epilogue warps cover the four lane groups");
@@ -89,7 +94,8 @@ struct TmCfg {
   static constexpr int kTapBytes = NMMA * 128;               // one [NMMA x 64] weight tile
   static constexpr int kWBytes = R::kStages * 2 * kTapBytes;  // two taps per stage
   static constexpr int kUsed = 1024 /*alignment*/ + kWBytes + 2 * kNbrTileBytes +
-                               512 /*barriers*/ + 256 * 4 /*bias*/ + R::kStagingBytes;
+                               512 /*barriers*/ + 256 * 4 /*bias*/ + R::kStagingBytes +
+                               R::kEpiStagingBytes;
   // at least half the SM's shared memory, so that one CTA (which takes all of tensor
   // memory) runs per SM
   static constexpr int kSmemBytes = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
@@ -261,6 +267,8 @@ __global__ void __launch_bounds__(TmRoles<STAGED>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* bias_sm = reinterpret_cast<float*>(misc + 512);
   const uint32_t sStage = smem_u32(misc + 512 + 256 * 4);   // producers' row staging
+  // epilogue row staging (per-thread form; there the producers' staging is empty)
+  uint8_t* epi_stage = misc + 512 + 256 * 4 + R::kStagingBytes;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -540,6 +548,7 @@ __global__ void __launch_bounds__(TmRoles<STAGED>::kThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int lg = warp & 3;                  // tensor-memory lane group of this warp
+    uint8_t* stg = epi_stage + (warp - kEpiWarp0) * 32 * R::kEpiPitch;
     for (int t = 0; t < ntl; ++t) {
       const int tile = blockIdx.x + t * gridDim.x;
       const uint32_t buf = t & 1u;
@@ -561,7 +570,9 @@ __global__ void __launch_bounds__(TmRoles<STAGED>::kThreads, 1)
         prefetch_row_l2(rrow, p.O * 2);
         rnext = ld_row16(rrow);
       }
-      if (!mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag)) {
+      // (warp-uniform: the staged write-out below is a warp-wide step)
+      const bool acc_ok = mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, acc_ok)) {
         *abort_flag = 1;
         atomicOr(p.err, kDevErrTimeout);
         break;
@@ -580,12 +591,30 @@ __global__ void __launch_bounds__(TmRoles<STAGED>::kThreads, 1)
           tc_fence_before();
           mbar_arrive(acce0 + 8 * buf);
         }
-        const int col0 = cc * 8;
+          const int col0 = cc * 8;
         if (row < p.N) {
-          // streaming store: the output is not read again here, the gathered rows are
-          __stcs(reinterpret_cast<uint4*>(orow + col0),
-                 epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act));
+          const uint4 y = epilogue8_bf16(v, bias_sm + col0, rrow != nullptr, rcur, p.act);
+          if constexpr (STAGED) {
+            // streaming store: the output is not read again here, the gathered rows are
+            __stcs(reinterpret_cast<uint4*>(orow + col0), y);
+          } else {   // into this lane's staging row (the pad makes the 32 rows conflict-free)
+            *reinterpret_cast<uint4*>(stg + lane * R::kEpiPitch + cc * 16) = y;
+          }
         }
+      }
+      if constexpr (!STAGED) {
+        // the warp's 32 rows out of shared memory, whole rows per group of lanes (a row's
+        // 16-byte pieces on consecutive lanes), each to the output row its lane named
+        __syncwarp();
+        constexpr int kPieces = NMMA / 8;   // 16-byte pieces per row (O = NMMA here)
+        for (int e = lane; e < 32 * kPieces; e += 32) {
+          const int rr = e / kPieces, c = e - rr * kPieces;
+          const int64_t orr = __shfl_sync(0xffffffffu, row, rr);
+          if (orr < p.N && c * 8 < p.O)
+            __stcs(reinterpret_cast<uint4*>(p.out + orr * p.O) + c,
+                   *reinterpret_cast<const uint4*>(stg + rr * R::kEpiPitch + c * 16));
+        }
+        __syncwarp();   // the staging rows are free for the next tile
       }
     }
   }

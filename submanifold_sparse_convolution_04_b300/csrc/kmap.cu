@@ -1013,16 +1013,16 @@ constexpr int kProbeThreads = 128;
 constexpr int kProbeWarps = kProbeThreads / 32;
 constexpr int kRunsAtOnce = 6;   // runs of a warp's 32 voxels whose blocks are held at once
 
-// One hash lookup: the block's occupancy mask and first sorted position (0 and 0 when
-// the block is not in the table). A slot is one 32-byte load.
+// One hash lookup from slot h on, at most `probes` slots: the block's occupancy mask and
+// first sorted position (0 and 0 when the block is not in the table). A slot is one
+// 32-byte load.
 __device__ __forceinline__ void block_lookup(const Slot* __restrict__ table,
-                                             unsigned long long key, unsigned long long cmask,
-                                             int max_probe, unsigned long long& mask,
-                                             int32_t& start, bool& full) {
-  unsigned long long h = mix64(key) & cmask;
+                                             unsigned long long key, unsigned long long h,
+                                          unsigned long long cmask, int probes,
+                                          unsigned long long& mask, int32_t& start, bool& full) {
   mask = 0;
   start = 0;
-  for (int probe = 0; probe < max_probe; ++probe) {
+  for (int probe = 0; probe < probes; ++probe) {
     uint32_t w[8];
     asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
@@ -1054,12 +1054,13 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     unsigned long long* __restrict__ key2, int32_t* __restrict__ val2, int window_shift,
     int32_t* __restrict__ perm, uint32_t* __restrict__ tmask, KmapStatus* st) {
   // tbl[k][p] = (2 x which of the 27 blocks around a voxel's block holds its neighbour
-  // at offset k, for a voxel at place p, + which half of that block's mask) << 5 | (the
-  // neighbour's bit in that half); the lanes of a warp read one offset's row at their
-  // own places, without bank conflicts
+  // at offset k, for a voxel at place p, + which half of that block's mask) << 5 |
+  // (31 - the neighbour's bit in that half): shifted left by that amount, the half has
+  // the neighbour's bit as its sign and its popcount is the neighbour's rank + 1; the
+  // lanes of a warp read one offset's row at their own places, without bank conflicts
   __shared__ uint16_t tbl[27 * 64];
   // per warp: the 27 blocks of up to kRunsAtOnce runs, each as two halves {32-bit mask,
-  // first position of the half}, the runs' block keys, and the 32 voxels' rows
+  // first position of the half - 1}, the runs' block keys, and the 32 voxels' rows
   __shared__ uint2 s_blk[kProbeWarps][kRunsAtOnce][54];
   __shared__ unsigned long long s_runkey[kProbeWarps][32];
   __shared__ uint32_t s_need[kProbeWarps][32];   // per run: the blocks its voxels reach
@@ -1074,7 +1075,7 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     const int nz = lz + k / 9 - 1, ny = ly + (k / 3) % 3 - 1, nx = lx + k % 3 - 1;
     const int kb = 9 * ((nz >> 2) + 1) + 3 * ((ny >> 2) + 1) + ((nx >> 2) + 1);
     const int np = place_in_block(nz & 3, ny & 3, nx & 3);
-    tbl[e] = static_cast<uint16_t>(((2 * kb + (np >> 5)) << 5) | (np & 31));
+    tbl[e] = static_cast<uint16_t>(((2 * kb + (np >> 5)) << 5) | (31 - (np & 31)));
   }
   for (int p = threadIdx.x; p < 64; p += kProbeThreads) {
     uint32_t need = 0;
@@ -1113,8 +1114,16 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
   constexpr unsigned kAll = 0xffffffffu;
   bool full = false, bad = false;
   const int64_t nwarps = (int64_t(gridDim.x) * kProbeThreads) >> 5;
-  for (int64_t w = (blockIdx.x * int64_t(kProbeThreads) + threadIdx.x) >> 5; w * 32 < N;
-       w += nwarps) {
+  const bool want_row = MODE == kProbeNbr || perm != nullptr;
+  // a round's sort key and row, loaded one round ahead
+  int64_t w = (blockIdx.x * int64_t(kProbeThreads) + threadIdx.x) >> 5;
+  unsigned long long m_next = ~0ull;
+  int32_t orow_next = -1;
+  if (w * 32 + lane < N) {
+    m_next = mk[w * 32 + lane];
+    if (want_row) orow_next = __ldg(ix + w * 32 + lane);
+  }
+  for (; w * 32 < N; w += nwarps) {
     if (MODE == kProbeSorted) {   // the previous rows' bulk copy has read the staging rows
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
@@ -1122,10 +1131,18 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
     const int64_t s = w * 32 + lane;
     const bool valid = s < N;
     const int nvalid = (N - w * 32) < 32 ? static_cast<int>(N - w * 32) : 32;
-    const unsigned long long m = valid ? mk[s] : ~0ull;
+    const unsigned long long m = m_next;
     const unsigned long long blk = m >> 6;
-    int32_t orow = -1;   // the row this lane's voxel is written to
-    if ((MODE == kProbeNbr || perm) && valid) orow = __ldg(ix + s);
+    const int32_t orow = orow_next;   // the row this lane's voxel is written to
+    {
+      const int64_t sn = s + nwarps * 32;
+      m_next = ~0ull;
+      orow_next = -1;
+      if (sn < N) {
+        m_next = mk[sn];
+        if (want_row) orow_next = __ldg(ix + sn);
+      }
+    }
     const unsigned long long prev = __shfl_up_sync(kAll, blk, 1);
     const unsigned newb = __ballot_sync(kAll, valid && (lane == 0 || prev != blk));
     const int run = __popc(newb & ((2u << lane) - 1u)) - 1;   // this lane's run, from 0
@@ -1153,24 +1170,65 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
         total += __popc(nm);
       }
       __syncwarp();
-      for (int q = lane; q < total; q += 32) {
-        const int e = list[q];
-        const int r = e >> 5, kb = e & 31;
-        const int dz = kb / 9 - 1, dy = (kb / 3) % 3 - 1, dx = kb % 3 - 1;
-        unsigned long long key = runkey[g0 + r];
-        bool inside = true;
-        if (dx > 0) { inside &= (key & ax) < lx; key = (((key | ~ax) + 1) & ax) | (key & ~ax); }
-        if (dx < 0) { inside &= (key & ax) != 0; key = (((key & ax) - 1) & ax) | (key & ~ax); }
-        if (dy > 0) { inside &= (key & ay) < ly; key = (((key | ~ay) + 1) & ay) | (key & ~ay); }
-        if (dy < 0) { inside &= (key & ay) != 0; key = (((key & ay) - 1) & ay) | (key & ~ay); }
-        if (dz > 0) { inside &= (key & az) < lz; key = (((key | ~az) + 1) & az) | (key & ~az); }
-        if (dz < 0) { inside &= (key & az) != 0; key = (((key & az) - 1) & az) | (key & ~az); }
-        unsigned long long bm = 0;
-        int32_t bb = 0;
-        if (inside) block_lookup(table, key, cmask, max_probe, bm, bb, full);
-        const uint32_t lo = static_cast<uint32_t>(bm), hi = static_cast<uint32_t>(bm >> 32);
-        blk_sm[r][2 * kb] = make_uint2(lo, static_cast<uint32_t>(bb));
-        blk_sm[r][2 * kb + 1] = make_uint2(hi, static_cast<uint32_t>(bb) + __popc(lo));
+      // a lane's lookups go kLookups at a time, their first slots loaded together (a
+      // further probe, after a collision, is rare)
+      constexpr int kLookups = 2;
+      for (int q0 = 0; q0 < total; q0 += 32 * kLookups) {
+        unsigned long long key[kLookups];
+        bool use[kLookups];
+        int ent[kLookups];
+        uint4 first[kLookups];
+        uint32_t first_start[kLookups];
+#pragma unroll
+        for (int u = 0; u < kLookups; ++u) {
+          const int q = q0 + 32 * u + lane;
+          ent[u] = q < total ? list[q] : -1;
+          key[u] = 0;
+          use[u] = false;
+          if (ent[u] >= 0) {
+            const int kb = ent[u] & 31;
+            const int dz = kb / 9 - 1, dy = (kb / 3) % 3 - 1, dx = kb % 3 - 1;
+            unsigned long long k = runkey[g0 + (ent[u] >> 5)];
+            bool inside = true;
+            if (dx > 0) { inside &= (k & ax) < lx; k = (((k | ~ax) + 1) & ax) | (k & ~ax); }
+            if (dx < 0) { inside &= (k & ax) != 0; k = (((k & ax) - 1) & ax) | (k & ~ax); }
+            if (dy > 0) { inside &= (k & ay) < ly; k = (((k | ~ay) + 1) & ay) | (k & ~ay); }
+            if (dy < 0) { inside &= (k & ay) != 0; k = (((k & ay) - 1) & ay) | (k & ~ay); }
+            if (dz > 0) { inside &= (k & az) < lz; k = (((k | ~az) + 1) & az) | (k & ~az); }
+            if (dz < 0) { inside &= (k & az) != 0; k = (((k & az) - 1) & az) | (k & ~az); }
+            key[u] = k;
+            use[u] = inside;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kLookups; ++u) {
+          if (use[u]) {
+            const Slot* sl = table + (mix64(key[u]) & cmask);
+            first[u] = __ldg(reinterpret_cast<const uint4*>(sl));   // key, mask
+            first_start[u] = __ldg(reinterpret_cast<const uint32_t*>(&sl->start));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kLookups; ++u) {
+          if (ent[u] < 0) continue;
+          unsigned long long bm = 0;
+          int32_t bb = 0;
+          if (use[u]) {
+            const unsigned long long k =
+                (static_cast<unsigned long long>(first[u].y) << 32) | first[u].x;
+            if (k == key[u]) {
+              bm = (static_cast<unsigned long long>(first[u].w) << 32) | first[u].z;
+              bb = static_cast<int32_t>(first_start[u]);
+            } else if (k != kEmptyKey) {
+              block_lookup(table, key[u], (mix64(key[u]) + 1) & cmask, cmask, max_probe - 1,
+                           bm, bb, full);
+            }
+          }
+          const int r = ent[u] >> 5, kb = ent[u] & 31;
+          const uint32_t lo = static_cast<uint32_t>(bm), hi = static_cast<uint32_t>(bm >> 32);
+          blk_sm[r][2 * kb] = make_uint2(lo, static_cast<uint32_t>(bb) - 1u);
+          blk_sm[r][2 * kb + 1] = make_uint2(hi, static_cast<uint32_t>(bb) + __popc(lo) - 1u);
+        }
       }
       __syncwarp();
       if (valid && run >= g0 && run < g0 + G) {   // this lane's voxel: its 27 neighbours
@@ -1178,11 +1236,11 @@ __global__ void __launch_bounds__(kProbeThreads, 7) kmap_probe(
 #pragma unroll
         for (int k = 0; k < 27; ++k) {
           const uint32_t e = tbl[k * 64 + p];
-          const uint2 half = nb[e >> 5];   // {mask half, its first position}
-          const uint32_t b5 = e & 31u;
+          const uint2 half = nb[e >> 5];   // {mask half, its first position - 1}
+          const uint32_t t = __funnelshift_l(0u, half.x, e);   // half.x << (e & 31)
           int32_t val = -1;
-          if ((half.x >> b5) & 1u) {
-            const uint32_t pos = half.y + __popc(half.x & ((1u << b5) - 1u));
+          if (static_cast<int32_t>(t) < 0) {   // the neighbour's bit
+            const uint32_t pos = half.y + __popc(t);
             present_mask |= 1u << k;
             if (pos < n32) val = __ldg(ix + pos);
             else bad = true;

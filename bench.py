@@ -21,6 +21,7 @@ Python API with pinned-host inputs copied in and the output copied back every st
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -353,7 +354,8 @@ def kmap_algorithmic_bytes(N, grouped, window):
 
 def spread(xs):
     s = sorted(xs)
-    return {"min": s[0], "median": statistics.median(s), "max": s[-1], "mean": statistics.mean(s)}
+    return {"min": s[0], "median": statistics.median(s), "max": s[-1], "mean": statistics.mean(s),
+            "max_at_step": max(range(len(xs)), key=xs.__getitem__)}
 
 
 def run_ours(args, world, rank, local):
@@ -433,7 +435,7 @@ def run_ours(args, world, rank, local):
         build(c, kmap)
         forward(f, kmap, w, b, r, out)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(args.warmup - 3, 1)):   # + 3 more just before the timed region
         step()
     subm3d_forward_status()
     run_build = lambda: build(c, kmap)
@@ -464,10 +466,14 @@ def run_ours(args, world, rank, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
-    barrier(world)
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    for _ in range(3):   # warm again after the sampler's start: the GPU busy up to the region
+        run_build()
+        run_forward()
+    barrier(world)
+    torch.cuda.synchronize()
+    gc.disable()         # no collector pause of the launching thread inside the region
     launches0 = subm3d_kernel_launches()
     e0.record(stream)
     for s in range(K):
@@ -478,6 +484,7 @@ def run_ours(args, world, rank, local):
         ev[s][2].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     launches = subm3d_kernel_launches() - launches0
     if graph_launches is not None:      # replays launch the captured kernels, not the host
         launches = graph_launches * K
@@ -624,7 +631,8 @@ def run_ours(args, world, rank, local):
         "mvoxels_per_s": world * N / (ms_per_step / 1e3) / 1e6,
         "kmap_ms": kmap_ms, "forward_us": fwd_ms * 1e3,
         "kmap_ms_spread": spread(kmap_each),
-        "forward_us_spread": {k: v * 1e3 for k, v in spread(fwd_each).items()},
+        "forward_us_spread": {k: (v if k == "max_at_step" else v * 1e3)
+                              for k, v in spread(fwd_each).items()},
         "forward_tflops": flops / (fwd_ms / 1e3) / 1e12,
         "roofline": roof,
         "kmap_roofline": kmap_roof,
@@ -715,17 +723,20 @@ def run_resample(args, world, rank, local):
             nbytes = 2 * N * C * e + 20 * N
             kernel = "c2s_gather"
     stream = torch.cuda.current_stream()
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(args.warmup - 3, 1)):   # + 3 more just before the timed region
         step()
     subm3d_forward_status()
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
-    barrier(world)
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    for _ in range(3):   # warm again after the sampler's start: the GPU busy up to the region
+        step()
+    barrier(world)
+    torch.cuda.synchronize()
+    gc.disable()         # no collector pause of the launching thread inside the region
     launches0 = subm3d_kernel_launches()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -735,6 +746,7 @@ def run_resample(args, world, rank, local):
         ev[k][1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     launches = subm3d_kernel_launches() - launches0
     clk = clocks.stop()
     barrier(world)

@@ -9,9 +9,15 @@
 // One persistent CTA per SM loops over tiles of 128 output rows. For each tile the
 // reduction runs over 27 offsets x ceil(I / 64) channel chunks; every (offset,
 // chunk) step is one pipeline stage in shared memory:
-//   A = the 128 gathered neighbour rows, 64 channels each (16 KB), written with
-//       16-byte cp.async (an absent neighbour, nbr = -1, zero-fills and reads
-//       nothing) in the 128-byte-swizzled K-major layout the tensor core reads;
+//   A = the 128 gathered neighbour rows, 64 channels each (16 KB), in the
+//       128-byte-swizzled K-major layout the tensor core reads, written either
+//       - by tensor-copy gathers (cp.async.bulk.tensor tile::gather4: four rows of 64
+//         channels per copy, half of an 8-row swizzle group; an absent neighbour is
+//         the row coordinate -1, outside the feature tensor, which the copy fills
+//         with zeros) when I is a multiple of 64 and O <= 128: one producer warp per
+//         ring slot, a lane per four rows, the stage's bytes counted on its barrier;
+//       - or by 16-byte cp.async (an absent neighbour zero-fills and reads nothing),
+//         groups of four producer warps (below);
 //   B = W_k[:, chunk] = weight[:, kz, ky, kx, chunk], an [O x 64] K-major tile (I is
 //       contiguous in the checkpoint layout, so no transpose), fetched by TMA with
 //       the same 128-byte swizzle; out-of-range rows/columns are zero-filled.
@@ -46,6 +52,7 @@
 // Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the
 // device error word, stops the CTA's pipeline, drains what is in flight and
 // releases tensor memory before the CTA exits.
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,17 +67,21 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxGroups = 6;     // producer groups of four warps
 constexpr int kGroupThreads = 128;
 
-template <int NMMA>
+// TG: the rows gathered by TMA (tile::gather4, four rows per copy, one producer warp per
+// ring slot); otherwise by cp.async (groups of four producer warps).
+template <int NMMA, bool TG>
 struct Cfg {
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = NMMA * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kMisc = 1024 /*alignment slack*/ + 512 /*barriers*/ + 4 * 256 /*bias*/;
   static constexpr int kFit = (kSmemLimit - kMisc) / kStageBytes;
-  static constexpr int kGroups = kFit < kMaxGroups ? kFit : kMaxGroups;
+  static constexpr int kMaxG = TG ? 16 : kMaxGroups;
+  static constexpr int kGroups = kFit < kMaxG ? kFit : kMaxG;
   static constexpr int kSlots = kFit / kGroups;            // ring slots per group
   static constexpr int kStages = kGroups * kSlots;
-  static constexpr int kMmaWarp = 4 * kGroups;
+  static constexpr int kGroupWarps = TG ? 1 : 4;
+  static constexpr int kMmaWarp = kGroupWarps * kGroups;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
   static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
   // one tile's accumulator: NMMA columns, placed at a power-of-two column stride
@@ -275,10 +286,44 @@ __device__ __forceinline__ void load_rows(const Params& p, int64_t row0, int k, 
   }
 }
 
-template <int NMMA>
-__global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
-    fwd_tc(const __grid_constant__ CUtensorMap wmap, const Params p) {
-  using C = Cfg<NMMA>;
+// Rows 4 lane + m (m = 0..3) of a TMA-gathered stage of tile-row block row0 at offset k:
+// their input rows, -1 (a coordinate outside the feature tensor: the copy fills zeros)
+// for an absent neighbour or a row past N. An entry outside [-1, N) is reported through
+// `bad` and treated as absent.
+__device__ __forceinline__ void load_rows4(const Params& p, int64_t row0, int k, int lane,
+                                           int32_t (&j)[4], bool& bad) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int64_t row = row0 + 4 * lane + m;
+    int32_t v = -1;
+    if (row < p.N) {
+      v = __ldg(p.nbr + row * 27 + k);
+      if (v < -1 || v >= p.N) {
+        bad = true;
+        v = -1;
+      }
+    }
+    j[m] = v;
+  }
+}
+
+// Four rows (y0..y3) of 64 channels from column x of a 2D tensor map into shared memory
+// at dst (128-byte swizzle, rows 128 bytes apart), completing on `bar` by bytes.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, const int32_t (&y)[4]) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3]),
+      "r"(bar)
+      : "memory");
+}
+
+template <int NMMA, bool TG>
+__global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
+    fwd_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap fmap,
+           const Params p) {
+  using C = Cfg<NMMA, TG>;
   constexpr int S = C::kStages;
   constexpr int G = C::kGroups;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -308,7 +353,9 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, kGroupThreads + 1);   // a group's noinc arrivals + the TMA's
+      // cp.async: a group's noinc arrivals + the weight TMA's; TMA gathers: one arrival
+      // with the stage's bytes
+      mbar_init(full0 + 8 * s, TG ? 1 : kGroupThreads + 1);
       mbar_init(empty0 + 8 * s, 1);                  // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -319,6 +366,7 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&wmap);
+    if (TG) tma_prefetch_desc(&fmap);
   }
   if (warp >= C::kEpiWarp0) {
     for (int o = tid - C::kEpiWarp0 * 32; o < NMMA; o += 128)
@@ -333,7 +381,63 @@ __global__ void __launch_bounds__(Cfg<NMMA>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < C::kMmaWarp) {
+  if (TG && warp < C::kMmaWarp) {
+    // ----------------------------------------------- producers, rows gathered by TMA
+    // warp grp owns the stages g = grp (mod G); lane l copies rows 4 l .. 4 l + 3 of a
+    // stage with one gather4 into their 128-byte-swizzled places (rows 4 l .. 4 l + 3 of
+    // the K-major A tile: half of an 8-row swizzle group, 512 bytes), lane 0 first
+    // announcing the stage's bytes and fetching its weight tap
+    const int grp = warp;
+    bool bad = false, aborted = false;
+    uint32_t last = 0;
+    int32_t jn[4];
+    StageCursor cur, nxt;
+    StagePos pc, pn;
+    const int dq = G / p.nchunks, dr = G % p.nchunks;
+    cur.start(p, ntl);
+    nxt.start(p, ntl);
+    if (nxt.seek(p, ntl, grp)) {
+      pn.locate(nxt, grp, G, p.nchunks, dq, dr);
+      load_rows4(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM, nth_offset(nxt.mask, pn.oi),
+                 lane, jn, bad);
+    }
+    for (uint32_t g = grp; cur.seek(p, ntl, g); g += G) {
+      pc.locate(cur, g, G, p.nchunks, dq, dr);
+      const int c = pc.c;
+      const int k = nth_offset(cur.mask, pc.oi);
+      int32_t j[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) j[m] = jn[m];
+      if (nxt.seek(p, ntl, g + G)) {
+        pn.locate(nxt, g + G, G, p.nchunks, dq, dr);
+        load_rows4(p, int64_t(blockIdx.x + nxt.lt * gridDim.x) * kBM, nth_offset(nxt.mask, pn.oi),
+                   lane, jn, bad);
+      }
+      const uint32_t s = g % S;
+      const uint32_t ph = (g / S) & 1u;
+      if (!warp_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
+        aborted = true;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full0 + 8 * s, C::kABytes + C::kBBytes);
+        tma_load_3d(sB + s * C::kBBytes, &wmap, full0 + 8 * s, c * kKC, k, 0);
+      }
+      __syncwarp();
+      tma_gather4(sA + s * C::kABytes + lane * 512, &fmap, full0 + 8 * s, c * kKC, j);
+      last = g + G;
+    }
+    if (bad) atomicOr(p.err, kDevErrBadNbr);
+    if (aborted && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, kDevErrTimeout);
+      // no copy of this warp may still be landing in shared memory when the CTA exits
+      // (without an abort the MMA warp has waited for every stage)
+      for (uint32_t x = last >= static_cast<uint32_t>(S) ? last - S : 0u; x < last; ++x)
+        if (x % G == static_cast<uint32_t>(grp)) drain_wait(full0 + 8 * (x % S), (x / S) & 1u);
+    }
+    __syncwarp();
+  } else if (warp < C::kMmaWarp) {
     // ------------------------------------------------------------------ producers
     const int grp = warp >> 2;
     const int gt = tid & (kGroupThreads - 1);
@@ -528,11 +632,11 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-template <int NMMA>
+template <int NMMA, bool TG>
 int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) {
-  using C = Cfg<NMMA>;
+  using C = Cfg<NMMA, TG>;
   static PerDevice<bool> attr_set;
-  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(fwd_tc<NMMA>),
+  const int arc = set_smem_limit_once(attr_set, reinterpret_cast<const void*>(fwd_tc<NMMA, TG>),
                                       C::kSmemBytes, "fwd_tc");
   if (arc != SUBM3D_OK) return arc;
   EncodeTiledFn encode = get_encode();
@@ -555,9 +659,29 @@ int launch(const Params& prm, const __nv_bfloat16* weight, cudaStream_t stream) 
               static_cast<int>(r), (const void*)weight, prm.I, prm.O);
     return SUBM3D_ERR_CUDA;
   }
+  // the feature rows for the TMA gathers: [N rows x I channels], boxes of one row of 64
+  // channels, the same 128-byte swizzle as the A tile; a row coordinate outside [0, N)
+  // reads zeros
+  CUtensorMap fmap;
+  std::memset(&fmap, 0, sizeof(fmap));
+  if (TG) {
+    const cuuint64_t fdims[2] = {static_cast<cuuint64_t>(prm.I), static_cast<cuuint64_t>(prm.N)};
+    const cuuint64_t fstrides[1] = {static_cast<cuuint64_t>(prm.I) * 2};
+    const cuuint32_t fbox[2] = {kKC, 1};
+    const cuuint32_t festr[2] = {1, 1};
+    const CUresult fr = encode(&fmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                               const_cast<__nv_bfloat16*>(prm.feats), fdims, fstrides, fbox, festr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (fr != CUDA_SUCCESS) {
+      set_error("subm3d_forward: cuTensorMapEncodeTiled failed (%d) for feats=%p N=%lld I=%d",
+                static_cast<int>(fr), (const void*)prm.feats, (long long)prm.N, prm.I);
+      return SUBM3D_ERR_CUDA;
+    }
+  }
   const int grid = prm.ntiles < num_sms() ? prm.ntiles : num_sms();
-  fwd_tc<NMMA><<<grid, C::kThreads, C::kSmemBytes, stream>>>(map, prm);
-  SUBM3D_LAUNCHED("fwd_tc");
+  fwd_tc<NMMA, TG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(map, fmap, prm);
+  SUBM3D_LAUNCHED(TG ? "fwd_tc_tg" : "fwd_tc");
   return SUBM3D_OK;
 }
 
@@ -576,15 +700,25 @@ int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
   Params prm{feats, nbr, bias, out, static_cast<const __nv_bfloat16*>(epi.residual), epi.act,
              N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
   const int nmma = (O + 15) / 16 * 16;
+  // The rows by TMA gathers when every channel chunk is whole (the copies' column start a
+  // multiple of 64 channels, 128 bytes) and the weight tap is at most 128 rows: on a
+  // B300 the tensor-copy unit then keeps up (I = O = 128: 432 us against 564 us with
+  // cp.async on 753 k voxels), while with 256-row taps it also carries 32 KB of weight
+  // per stage and the cp.async gather is faster (521 against 625 us at I = O = 256).
+  const bool tg = I % kKC == 0 && N <= 0x7FFFFFFFll;
   switch (nmma) {
+#define SUBM3D_CASE_TG(n)                                                       \
+  case n:                                                                       \
+    return tg ? launch<n, true>(prm, weight, stream) : launch<n, false>(prm, weight, stream);
 #define SUBM3D_CASE(n) \
   case n:              \
-    return launch<n>(prm, weight, stream);
-    SUBM3D_CASE(16) SUBM3D_CASE(32) SUBM3D_CASE(48) SUBM3D_CASE(64)
-    SUBM3D_CASE(80) SUBM3D_CASE(96) SUBM3D_CASE(112) SUBM3D_CASE(128)
+    return launch<n, false>(prm, weight, stream);
+    SUBM3D_CASE_TG(16) SUBM3D_CASE_TG(32) SUBM3D_CASE_TG(48) SUBM3D_CASE_TG(64)
+    SUBM3D_CASE_TG(80) SUBM3D_CASE_TG(96) SUBM3D_CASE_TG(112) SUBM3D_CASE_TG(128)
     SUBM3D_CASE(144) SUBM3D_CASE(160) SUBM3D_CASE(176) SUBM3D_CASE(192)
     SUBM3D_CASE(208) SUBM3D_CASE(224) SUBM3D_CASE(240) SUBM3D_CASE(256)
 #undef SUBM3D_CASE
+#undef SUBM3D_CASE_TG
     default:
       set_error("subm3d_forward: O=%d outside the tensor-core kernel's range", O);
       return SUBM3D_ERR_UNSUPPORTED;

@@ -190,3 +190,61 @@ def test_kmap_front_ends_agree(dev, cfg_id):
     sorted_nbr, _ = subm3d_build_kmap_ex(c, case["res"], order=True)
     np.testing.assert_array_equal(hashed, sorted_nbr.cpu().numpy())
     np.testing.assert_array_equal(hashed, cpu.kernel_map(case["coords"], case["res"]))
+
+
+def one_voxel_per_block(rng, res, n):
+    """n voxels in n distinct 4x4x4 blocks of a res^3 grid, each at a random place."""
+    nb = res // 4
+    blocks = rng.choice(nb ** 3, size=n, replace=False)
+    bz, rem = np.divmod(blocks, nb * nb)
+    by, bx = np.divmod(rem, nb)
+    off = rng.integers(0, 4, size=(n, 3))
+    c = np.stack([np.zeros(n, np.int64), 4 * bz + off[:, 0], 4 * by + off[:, 1],
+                  4 * bx + off[:, 2]], axis=1)
+    return c.astype(np.int32)
+
+
+def test_kmap_growth_duplicates_and_full_table_one_voxel_per_block(dev):
+    # 6000 voxels, one per 4x4x4 block of a 128^3 grid, plus 600 +x neighbours: the
+    # blocks overfill the first (N/4) table, so it grows first. Then a duplicate and a
+    # fixed table that is too small, at this size.
+    rng = np.random.default_rng(21)
+    c = one_voxel_per_block(rng, 128, 6000)
+    c = np.concatenate([c, c[:600] + np.array([0, 0, 0, 1], np.int32)])
+    c = np.unique(c[(c[:, 3] < 128)], axis=0)
+    c = c[rng.permutation(len(c))]
+    want = ref.kernel_map(c, 128)
+    np.testing.assert_array_equal(gpu_nbr(c, 128, dev), want)
+    assert (want[:, 14] >= 0).sum() > 0
+    # a repeated row: ERR_DUPLICATE, and the next build is clean again
+    with pytest.raises(Subm3dError) as e:
+        gpu_nbr(np.concatenate([c, c[17:18]]), 128, dev)
+    assert e.value.code == B.ERR_DUPLICATE
+    np.testing.assert_array_equal(gpu_nbr(c, 128, dev), want)
+    # a fixed table smaller than the blocks: ERR_HASH_FULL; one that holds them works
+    nblk = len(np.unique(c[:, 1:] // 4, axis=0))
+    small = 1 << (nblk.bit_length() - 1)      # < nblk
+    ct = torch.from_numpy(c).to(dev)
+    with pytest.raises(Subm3dError) as e:
+        subm3d_build_kmap_ex(ct, 128, hash_capacity=small)
+    assert e.value.code == B.ERR_HASH_FULL
+    nbr, _ = subm3d_build_kmap_ex(ct, 128, hash_capacity=4 * small)
+    np.testing.assert_array_equal(nbr.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("batch,res,n", [(3, 64, 3000), (2, 128, 5000), (1, 1024, 3000)])
+def test_kmap_key_range_edges(dev, batch, res, n):
+    # blocks at both ends of the block-key range (the grid's first and last cell, in the
+    # first and last batch), one voxel per block elsewhere, in batches
+    rng = np.random.default_rng(batch * 7 + res)
+    rows = []
+    for b in range(batch):
+        c = one_voxel_per_block(rng, min(res, 128), n)
+        c[:, 0] = b
+        rows.append(c)
+    c = np.concatenate(rows)
+    corners = np.array([[0, 0, 0, 0], [batch - 1, res - 1, res - 1, res - 1],
+                        [batch - 1, res - 1, res - 1, res - 2]], np.int32)
+    c = np.unique(np.concatenate([c, corners]), axis=0)
+    c = c[rng.permutation(len(c))]
+    np.testing.assert_array_equal(gpu_nbr(c, res, dev), ref.kernel_map(c, res))

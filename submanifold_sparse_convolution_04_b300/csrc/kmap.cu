@@ -750,9 +750,10 @@ __device__ __forceinline__ unsigned long long sort_key(int4 c, int bits) {
 // full-size table instead of failing. Each voxel looks its block up on its own (a read
 // first, atomicCAS only on an empty slot), then ORs its bit into the mask as a reduction
 // that returns nothing (duplicates show up later as fewer mask bits than voxels).
-// (Grouping a warp's lanes by block with match/reduce intrinsics, reading back the old
-// mask, or four voxels per thread -- fewer warps then fit -- each measured slower; two
-// voxels per thread at 32 registers keep every warp resident.)
+// (Grouping a warp's lanes by block with match/reduce intrinsics, ORing the bits of
+// consecutive lanes in one block with shuffles before a single atomic per run, reading
+// back the old mask, or four voxels per thread -- fewer warps then fit -- each measured
+// slower; two voxels per thread at 32 registers keep every warp resident.)
 __global__ void __launch_bounds__(256, 8) kmap_h_insert(const int4* __restrict__ coords,
                                                         int64_t N, int res, int bits, Slot* table,
                                                         uint32_t* __restrict__ slot_of,

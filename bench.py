@@ -355,6 +355,20 @@ def kmap_algorithmic_bytes(N, grouped, window):
     return base + 12 * N + 24 * N * passes2 + 16 * N + 4 * N + 2 * 108 * N
 
 
+def warm_steps(step, seconds=0.3, at_least=3):
+    """Untimed steps for at least `seconds` of wall time (and `at_least` steps), with a
+    device sync every eight so that the host does not run far ahead of the GPU."""
+    import torch
+    t_end = time.perf_counter() + seconds
+    n = 0
+    while n < at_least or time.perf_counter() < t_end:
+        step()
+        n += 1
+        if n % 8 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+
 def spread(xs):
     s = sorted(xs)
     return {"min": s[0], "median": statistics.median(s), "max": s[-1], "mean": statistics.mean(s),
@@ -470,10 +484,9 @@ def run_ours(args, world, rank, local):
     cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
     clocks.start()
-    time.sleep(0.3)
-    for _ in range(3):   # warm again after the sampler's start: the GPU busy up to the region
-        run_build()
-        run_forward()
+    # the sampler needs ~0.3 s to start: the GPU runs warm-up steps meanwhile (an idle GPU
+    # drops to a low-power state, and light steps take tens of ms to bring it back)
+    warm_steps(lambda: (run_build(), run_forward()))
     barrier(world)
     torch.cuda.synchronize()
     gc.disable()         # no collector pause of the launching thread inside the region
@@ -734,9 +747,7 @@ def run_resample(args, world, rank, local):
     cvd = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(int(cvd[local]) if len(cvd) > local and cvd[local].isdigit() else local)
     clocks.start()
-    time.sleep(0.3)
-    for _ in range(3):   # warm again after the sampler's start: the GPU busy up to the region
-        step()
+    warm_steps(step)   # (as in the main bench: the GPU busy while the sampler starts)
     barrier(world)
     torch.cuda.synchronize()
     gc.disable()         # no collector pause of the launching thread inside the region

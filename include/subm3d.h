@@ -249,9 +249,9 @@ SUBM3D_API int subm3d_forward_grouped(const void* feats, const void* plan, const
  * array compiled into the library, so N is limited to SUBM3D_NOALLOC_MAX_VOXELS; a
  * larger N returns SUBM3D_ERR_ARG before any device work. Every GPU that loads the
  * library keeps that array until the process exits. The first call on a device looks
- * up the array's device address (make that first call before any stream capture
- * begins). Like subm3d_build_kmap, the call waits for `stream` at its end, so calls
- * from one host thread never overlap on the GPU. All calls share the one array: each
+ * up the array's device address. Like subm3d_build_kmap, the call waits for `stream`
+ * at its end (it reads the build's status back), so no call can be captured into a CUDA
+ * graph, and calls from one host thread never overlap on the GPU. All calls share the one array: each
  * call re-initialises what it reads, but calls made at the same time from several
  * host threads race on it.
  */

@@ -12,10 +12,10 @@
 // g_kmap_scratch is a file-scope __device__ array: every GPU that loads the library
 // holds its 16 MiB until the process exits. In host code its name is only a host-side
 // stand-in, so its device address is fetched with cudaGetSymbolAddress, once per
-// device, with that device current, by the first call made on that device (make that
-// first call before any stream capture begins). Like subm3d_build_kmap, each call
-// waits for its stream at its end, so two calls from one host thread never overlap on
-// the GPU. All calls share the array and the build re-initialises everything it reads,
+// device, with that device current, by the first call made on that device. Like
+// subm3d_build_kmap, each call waits for its stream at its end (it reads the build's
+// status back), so no call can be stream-captured, and two calls from one host thread
+// never overlap on the GPU. All calls share the array and the build re-initialises everything it reads,
 // so each call starts clean; calls made at the same time from several host threads race
 // on it.
 #include <mutex>

@@ -45,11 +45,11 @@ CSRC = os.path.join(ROOT, "submanifold_sparse_convolution_04_b300", "csrc")
 def forward_kernel(I, O):
     """(kernel name, source file) of the bf16 forward the library picks for I x O: the
     narrow kernel (gathered rows in tensor memory) for I, O in {16, 32, 48, 64}, else
-    the shared-memory-staged one, its rows gathered by TMA when I is a multiple of 64
-    and O <= 128, by cp.async otherwise."""
+    the shared-memory-staged one, its rows gathered by TMA when I is a multiple of 64,
+    by cp.async otherwise."""
     if I in (16, 32, 48, 64) and O in (16, 32, 48, 64):
         return "fwd_tm", os.path.join(CSRC, "forward_tm.cu")
-    if I % 64 == 0 and O <= 128:
+    if I % 64 == 0:
         return "fwd_tc_tg", os.path.join(CSRC, "forward_tc.cu")
     return "fwd_tc", os.path.join(CSRC, "forward_tc.cu")
 

@@ -276,8 +276,7 @@ SUBM3D_API int subm3d_build_kmap_noalloc(const int32_t* coords, int64_t N, int32
  *           {16, 32, 48, 64} run the narrow kernel (the gathered rows in tensor
  *           memory); other O <= 256 the kernel that stages them in shared memory
  *           (the rows copied there by tensor-copy gathers, four rows per copy, when
- *           I % 64 == 0 and O <= 128, else by cp.async); larger O the CUDA-core
- *           kernel. All three compute
+ *           I % 64 == 0, else by cp.async); larger O the CUDA-core kernel. All three compute
  *           the same sums (fp32 accumulation order may differ between them).
  *           SUBM3D_F32: fp32 inputs and accumulation on the CUDA cores.
  *   N, I, O N >= 0 (0 is a no-op), 1 <= I, O <= 4096.

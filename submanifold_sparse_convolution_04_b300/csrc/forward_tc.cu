@@ -68,31 +68,45 @@ constexpr int kMaxGroups = 6;     // producer groups of four warps
 constexpr int kGroupThreads = 128;
 
 // TG: the rows gathered by TMA (tile::gather4, four rows per copy, one producer warp per
-// ring slot); otherwise by cp.async (groups of four producer warps).
+// ring slot); otherwise by cp.async (groups of four producer warps). Each stage's weight
+// tap goes into the stage's own B slot, fetched with its rows -- except for taps wider
+// than 128 rows with TMA gathers (SPLIT): there a 32 KB tap per slot would leave room
+// for only four slots, so the taps get a ring of three slots of their own, filled in
+// stage order by a loader warp (a tap is needed only when its stage's MMAs issue, and
+// at that width a stage's MMAs take long enough to cover the tap's fetch), and the rows
+// get the rest of the shared memory (eight slots). At 128 rows and below the shorter
+// stages need the taps further ahead, and the joint slots are faster.
 template <int NMMA, bool TG>
 struct Cfg {
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = NMMA * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kMisc = 1024 /*alignment slack*/ + 512 /*barriers*/ + 4 * 256 /*bias*/;
-  static constexpr int kFit = (kSmemLimit - kMisc) / kStageBytes;
+  static constexpr bool kSplit = TG && NMMA > 128;
+  static constexpr int kSplitBSlots = 3;
+  static constexpr int kFit = kSplit ? (kSmemLimit - kMisc - kSplitBSlots * kBBytes) / kABytes
+                                     : (kSmemLimit - kMisc) / kStageBytes;
   static constexpr int kMaxG = TG ? 16 : kMaxGroups;
   static constexpr int kGroups = kFit < kMaxG ? kFit : kMaxG;
   static constexpr int kSlots = kFit / kGroups;            // ring slots per group
-  static constexpr int kStages = kGroups * kSlots;
+  static constexpr int kStages = kGroups * kSlots;          // A slots
+  static constexpr int kBSlots = kSplit ? kSplitBSlots : kStages;   // B slots
+  static constexpr int kNB = kSplit ? kBSlots : 0;          // barriers of the weight ring
   static constexpr int kGroupWarps = TG ? 1 : 4;
-  static constexpr int kMmaWarp = kGroupWarps * kGroups;
+  static constexpr int kLoadWarp = kGroupWarps * kGroups;   // SPLIT: the weight loader
+  static constexpr int kMmaWarp = kLoadWarp + (kSplit ? 1 : 0);
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
   static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
   // one tile's accumulator: NMMA columns, placed at a power-of-two column stride
   static constexpr int kBufCols = NMMA <= 16 ? 16 : NMMA <= 32 ? 32 : NMMA <= 64 ? 64
                                 : NMMA <= 128 ? 128 : 256;
   static constexpr int kTmemCols = 2 * kBufCols < 32 ? 32 : 2 * kBufCols;
-  static constexpr int kSmemBytes = kMisc + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kMisc + kStages * kABytes + kBSlots * kBBytes;
   static_assert(kGroups >= 3, "too few producer groups");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor memory");
   static_assert(kThreads <= 1024, "block too large");
-  static_assert(8 * (2 * kStages + 5) + 8 <= 512, "barrier area too small");
+  static_assert(8 * (2 * kStages + 2 * kNB + 5) + 8 <= 512, "barrier area too small");
 };
 
 struct Params {
@@ -330,17 +344,20 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
+  constexpr int SB = C::kBSlots;
   const uint32_t sA = base;                              // S x 16 KB
-  const uint32_t sB = base + S * C::kABytes;             // S x NMMA*128 B
-  uint8_t* misc = base_ptr + S * C::kStageBytes;
-  // barriers: full[S], empty[S], accf[2], acce[2], drain
+  const uint32_t sB = base + S * C::kABytes;             // SB x NMMA*128 B
+  uint8_t* misc = base_ptr + S * C::kABytes + SB * C::kBBytes;
+  // barriers: full[S], empty[S], (SPLIT) bfull[SB], bempty[SB], accf[2], acce[2], drain
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
-  const uint32_t accf0 = empty0 + 8 * S;
+  const uint32_t bfull0 = empty0 + 8 * S;
+  const uint32_t bempty0 = bfull0 + 8 * C::kNB;
+  const uint32_t accf0 = bempty0 + 8 * C::kNB;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 2 * C::kNB + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* bias_sm = reinterpret_cast<float*>(misc + 512);
 
@@ -354,9 +371,13 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // cp.async: a group's noinc arrivals + the weight TMA's; TMA gathers: one arrival
-      // with the stage's bytes
+      // with the stage's row bytes
       mbar_init(full0 + 8 * s, TG ? 1 : kGroupThreads + 1);
       mbar_init(empty0 + 8 * s, 1);                  // one tcgen05.commit
+    }
+    for (int b = 0; b < C::kNB; ++b) {
+      mbar_init(bfull0 + 8 * b, 1);                  // the loader's arrival with the tap's bytes
+      mbar_init(bempty0 + 8 * b, 1);                 // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -381,12 +402,12 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (TG && warp < C::kMmaWarp) {
+  if (TG && warp < C::kLoadWarp) {
     // ----------------------------------------------- producers, rows gathered by TMA
     // warp grp owns the stages g = grp (mod G); lane l copies rows 4 l .. 4 l + 3 of a
     // stage with one gather4 into their 128-byte-swizzled places (rows 4 l .. 4 l + 3 of
     // the K-major A tile: half of an 8-row swizzle group, 512 bytes), lane 0 first
-    // announcing the stage's bytes and fetching its weight tap
+    // announcing the stage's bytes (and, with joint slots, fetching its weight tap)
     const int grp = warp;
     bool bad = false, aborted = false;
     uint32_t last = 0;
@@ -420,8 +441,12 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * s, C::kABytes + C::kBBytes);
-        tma_load_3d(sB + s * C::kBBytes, &wmap, full0 + 8 * s, c * kKC, k, 0);
+        if (C::kSplit) {
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kABytes);
+        } else {
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kABytes + C::kBBytes);
+          tma_load_3d(sB + s * C::kBBytes, &wmap, full0 + 8 * s, c * kKC, k, 0);
+        }
       }
       __syncwarp();
       tma_gather4(sA + s * C::kABytes + lane * 512, &fmap, full0 + 8 * s, c * kKC, j);
@@ -435,6 +460,37 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
       // (without an abort the MMA warp has waited for every stage)
       for (uint32_t x = last >= static_cast<uint32_t>(S) ? last - S : 0u; x < last; ++x)
         if (x % G == static_cast<uint32_t>(grp)) drain_wait(full0 + 8 * (x % S), (x / S) & 1u);
+    }
+    __syncwarp();
+  } else if (C::kSplit && warp == C::kLoadWarp) {
+    // ----------------------------------------------- weight taps, in stage order (SPLIT)
+    bool aborted = false;
+    uint32_t last = 0;
+    StageCursor cur;
+    StagePos pc;
+    const int dq = 1 / p.nchunks, dr = 1 % p.nchunks;
+    cur.start(p, ntl);
+    for (uint32_t g = 0; cur.seek(p, ntl, g); ++g) {
+      pc.locate(cur, g, 1u, p.nchunks, dq, dr);
+      const uint32_t b = g % SB;
+      if (!warp_wait(bempty0 + 8 * b, ((g / SB) & 1u) ^ 1u, abort_flag)) {
+        aborted = true;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bfull0 + 8 * b, C::kBBytes);
+        tma_load_3d(sB + b * C::kBBytes, &wmap, bfull0 + 8 * b, pc.c * kKC,
+                    nth_offset(cur.mask, pc.oi), 0);
+      }
+      __syncwarp();
+      last = g + 1;
+    }
+    if (aborted && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, kDevErrTimeout);
+      // no tap may still be landing in shared memory when the CTA exits
+      for (uint32_t x = last >= static_cast<uint32_t>(SB) ? last - SB : 0u; x < last; ++x)
+        drain_wait(bfull0 + 8 * (x % SB), (x / SB) & 1u);
     }
     __syncwarp();
   } else if (warp < C::kMmaWarp) {
@@ -529,7 +585,9 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
       for (uint32_t kc = 0; kc < spt; ++kc, c = (c + 1 == p.nchunks) ? 0 : c + 1) {
         const uint32_t s = g % S;
         const uint32_t ph = (g / S) & 1u;
-        if (!warp_wait(full0 + 8 * s, ph, abort_flag)) {
+        const uint32_t b = C::kSplit ? g % SB : s;   // the stage's weight slot
+        if (!warp_wait(full0 + 8 * s, ph, abort_flag) ||
+            (C::kSplit && !warp_wait(bfull0 + 8 * b, (g / SB) & 1u, abort_flag))) {
           aborted = true;
           break;
         }
@@ -537,9 +595,10 @@ __global__ void __launch_bounds__(Cfg<NMMA, TG>::kThreads, 1)
         tc_fence_after();
         const int rem = p.I - c * kKC;
         const int ksteps = rem >= kKC ? 4 : (rem + 15) / 16;
-        mma_stage(d_tmem, sw128_desc(sA + s * C::kABytes), sw128_desc(sB + s * C::kBBytes), idesc,
+        mma_stage(d_tmem, sw128_desc(sA + s * C::kABytes), sw128_desc(sB + b * C::kBBytes), idesc,
                   ksteps, kc == 0 ? 0u : 1u);
         tc_commit_elect(empty0 + 8 * s);
+        if (C::kSplit) tc_commit_elect(bempty0 + 8 * b);
         ++g;
       }
       if (!aborted) tc_commit_elect(accf0 + 8 * buf);
@@ -701,24 +760,19 @@ int forward_launch_tc(const __nv_bfloat16* feats, const int32_t* nbr, const __nv
              N, I, O, (I + kKC - 1) / kKC, static_cast<int>(ntiles), err, plan.perm, plan.tmask};
   const int nmma = (O + 15) / 16 * 16;
   // The rows by TMA gathers when every channel chunk is whole (the copies' column start a
-  // multiple of 64 channels, 128 bytes) and the weight tap is at most 128 rows: on a
-  // B300 the tensor-copy unit then keeps up (I = O = 128: 432 us against 564 us with
-  // cp.async on 753 k voxels), while with 256-row taps it also carries 32 KB of weight
-  // per stage and the cp.async gather is faster (521 against 625 us at I = O = 256).
+  // multiple of 64 channels, 128 bytes): on a B300, 433 us against 564 us with cp.async
+  // at I = O = 128 (753 k voxels), and with the taps in a ring of their own 462 us
+  // against 512 us at I = O = 256 (278 k voxels).
   const bool tg = I % kKC == 0 && N <= 0x7FFFFFFFll;
   switch (nmma) {
-#define SUBM3D_CASE_TG(n)                                                       \
+#define SUBM3D_CASE(n)                                                          \
   case n:                                                                       \
     return tg ? launch<n, true>(prm, weight, stream) : launch<n, false>(prm, weight, stream);
-#define SUBM3D_CASE(n) \
-  case n:              \
-    return launch<n, false>(prm, weight, stream);
-    SUBM3D_CASE_TG(16) SUBM3D_CASE_TG(32) SUBM3D_CASE_TG(48) SUBM3D_CASE_TG(64)
-    SUBM3D_CASE_TG(80) SUBM3D_CASE_TG(96) SUBM3D_CASE_TG(112) SUBM3D_CASE_TG(128)
+    SUBM3D_CASE(16) SUBM3D_CASE(32) SUBM3D_CASE(48) SUBM3D_CASE(64)
+    SUBM3D_CASE(80) SUBM3D_CASE(96) SUBM3D_CASE(112) SUBM3D_CASE(128)
     SUBM3D_CASE(144) SUBM3D_CASE(160) SUBM3D_CASE(176) SUBM3D_CASE(192)
     SUBM3D_CASE(208) SUBM3D_CASE(224) SUBM3D_CASE(240) SUBM3D_CASE(256)
 #undef SUBM3D_CASE
-#undef SUBM3D_CASE_TG
     default:
       set_error("subm3d_forward: O=%d outside the tensor-core kernel's range", O);
       return SUBM3D_ERR_UNSUPPORTED;

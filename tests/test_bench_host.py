@@ -13,8 +13,9 @@ import bench  # noqa: E402
 
 @pytest.mark.parametrize("I,O,kernel", [(64, 64, "fwd_tm"), (16, 48, "fwd_tm"), (32, 32, "fwd_tm"),
                                         (128, 128, "fwd_tc_tg"), (64, 128, "fwd_tc_tg"),
-                                        (192, 80, "fwd_tc_tg"), (256, 256, "fwd_tc"),
-                                        (96, 96, "fwd_tc"), (72, 136, "fwd_tc"), (128, 256, "fwd_tc")])
+                                        (192, 80, "fwd_tc_tg"), (256, 256, "fwd_tc_tg"),
+                                        (128, 256, "fwd_tc_tg"), (96, 96, "fwd_tc"),
+                                        (72, 136, "fwd_tc"), (24, 40, "fwd_tc")])
 def test_forward_kernel_follows_the_dispatch(I, O, kernel):
     name, src = bench.forward_kernel(I, O)
     assert name == kernel

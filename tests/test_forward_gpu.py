@@ -112,8 +112,10 @@ def shell_case(seed, res, I, O, dtype, batch=1):
 @pytest.mark.parametrize("I,O", [(16, 16), (32, 64), (64, 32), (96, 96), (128, 256), (256, 128),
                                  (8, 8), (24, 40), (72, 136), (264, 48), (64, 256), (256, 256),
                                  (40, 264), (8, 520),
-                                 # rows by TMA gathers (I a multiple of 64, O <= 128)
-                                 (64, 128), (192, 80), (128, 16), (64, 72)])
+                                 # rows by TMA gathers (I a multiple of 64); above
+                                 # O = 128 with the weight taps in a ring of their own
+                                 (64, 128), (192, 80), (128, 16), (64, 72), (192, 144),
+                                 (64, 208)])
 def test_forward_bf16_shapes(dev, I, O):
     coords, v = shell_case(I * 7 + O, 40, I, O, "bf16", batch=2)
     N = coords.shape[0]

@@ -14,13 +14,15 @@
 //       - by tensor-copy gathers (cp.async.bulk.tensor tile::gather4: four rows of 64
 //         channels per copy, half of an 8-row swizzle group; an absent neighbour is
 //         the row coordinate -1, outside the feature tensor, which the copy fills
-//         with zeros) when I is a multiple of 64 and O <= 128: one producer warp per
-//         ring slot, a lane per four rows, the stage's bytes counted on its barrier;
+//         with zeros) when I is a multiple of 64: one producer warp per ring slot, a
+//         lane per four rows, the stage's bytes counted on its barrier;
 //       - or by 16-byte cp.async (an absent neighbour zero-fills and reads nothing),
 //         groups of four producer warps (below);
 //   B = W_k[:, chunk] = weight[:, kz, ky, kx, chunk], an [O x 64] K-major tile (I is
 //       contiguous in the checkpoint layout, so no transpose), fetched by TMA with
-//       the same 128-byte swizzle; out-of-range rows/columns are zero-filled.
+//       the same 128-byte swizzle; out-of-range rows/columns are zero-filled. It sits
+//       in the stage's own slot, fetched with the rows, except with TMA gathers and
+//       O > 128, where the taps have a three-slot ring of their own (see Cfg).
 // The row gathers are many small independent loads, and one warp can keep only a
 // few kilobytes of cp.async in flight, so the gather rate grows with the number of
 // warps issuing them, not with the depth of one warp's queue. The producers are
@@ -45,10 +47,11 @@
 // block epilogue] -> bf16 round-to-nearest-even -> one 16-byte store per 8 outputs)
 // while the tensor core works on tile t + 1.
 //
-// Warp roles: warps 0 .. 4G-1 producers (the first thread of each group also issues
-// its stages' weight TMA), warp 4G tensor-memory allocation + MMA issue (one lane),
-// warps 4G+1 .. 4G+4 epilogue (warp w reads tensor-memory lanes 32 (w % 4) ..
-// 32 (w % 4) + 31).
+// Warp roles: warps 0 .. 4G-1 (cp.async) or 0 .. G-1 (TMA gathers) producers (the
+// first thread of each group also issues its stages' weight TMA when the tap shares
+// the stage's slot), then, with the taps' own ring, one loader warp, then the warp that
+// allocates tensor memory and issues the MMAs (one lane), then four epilogue warps
+// (warp w reads tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31).
 // Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets the
 // device error word, stops the CTA's pipeline, drains what is in flight and
 // releases tensor memory before the CTA exits.

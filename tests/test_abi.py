@@ -212,3 +212,43 @@ def test_launchers_refuse_without_a_device_error_word(L):
                                     None) == B.ERR_CUDA
     assert L.subm3d_channel2spatial(p(16), p(32), p(48), 10, 4, 8, B.BF16, p(64), None) == B.ERR_CUDA
     assert L.subm3d_forward_status(None) == B.ERR_CUDA
+
+
+def test_tile_plan_host_checks(L):
+    p = ctypes.c_void_p
+    # a plan holds perm (4 B) and the nbr rows (108 B) per voxel and one offset mask per
+    # 128-row tile, each part 256-byte aligned
+    for N in (1, 1000, 3_000_000):
+        pb = L.subm3d_plan_bytes(N)
+        least = N * 112 + ((N + 127) // 128) * 4
+        assert least <= pb < least + 4096
+        assert L.subm3d_kmap_grouped_workspace_bytes(N) > L.subm3d_kmap_workspace_bytes(N)
+    assert L.subm3d_plan_bytes(-1) == 0
+    assert L.subm3d_build_kmap_grouped(None, 0, 16, 1, None, 0, None, 0, 0, None) == B.OK
+    good = dict(coords=p(16), N=10, res=16, window=1, plan=p(256), pb=L.subm3d_plan_bytes(10),
+                ws=p(512), wb=1 << 24, flags=0)
+
+    def call(**kw):
+        d = dict(good, **kw)
+        return L.subm3d_build_kmap_grouped(d["coords"], d["N"], d["res"], d["window"], d["plan"],
+                                           d["pb"], d["ws"], d["wb"], d["flags"], None)
+
+    for w in (3, -4, 1 << 31, 6):         # not a power of two in [1, 2^30] (0 is the default)
+        assert call(window=w) == B.ERR_ARG
+    assert call(pb=good["pb"] - 1) == B.ERR_ARG      # plan too small
+    assert call(plan=p(128)) == B.ERR_ARG            # plan not 256-byte aligned
+    assert call(plan=None) == B.ERR_ARG
+    assert call(coords=p(8)) == B.ERR_ARG            # coords not 16-byte aligned
+    assert call(wb=100) == B.ERR_WORKSPACE
+    assert call(ws=p(384)) == B.ERR_WORKSPACE        # workspace not 256-byte aligned
+    assert call(flags=4) == B.ERR_ARG                # unknown flag
+    assert call(res=0) == B.ERR_ARG and call(N=-1) == B.ERR_ARG
+    assert B.subm3d_last_error()
+    # the forward on a plan: no plan, a misaligned one, N out of range, bad shapes
+    f = L.subm3d_forward_grouped
+    assert f(p(256), None, p(768), None, None, 0, p(1024), 10, 32, 32, B.BF16, None) == B.ERR_ARG
+    assert f(p(256), p(128), p(768), None, None, 0, p(1024), 10, 32, 32, B.BF16, None) == B.ERR_ARG
+    assert f(p(256), p(256), p(768), None, None, 0, p(1024), -1, 32, 32, B.BF16, None) == B.ERR_ARG
+    assert f(p(256), p(256), p(768), None, None, 0, p(1024), 10, 12, 32, B.BF16, None) == \
+        B.ERR_UNSUPPORTED
+    assert f(None, None, None, None, None, 0, None, 0, 32, 32, B.BF16, None) == B.OK

@@ -149,6 +149,21 @@ def test_downsample_host_checks(L):
     assert b"workspace" in L.subm3d_last_error()
 
 
+def test_downsample_async_host_checks(L):
+    p = ctypes.c_void_p
+
+    def call(M=1024, N=10, res=16, order=None, w=256, nbytes=1 << 30, mode=0):
+        return L.subm3d_downsample_async(p(16), N, res, p(order) if order else None, None, 0,
+                                         B.BF16, mode, p(32), None, p(48), p(64),
+                                         p(M) if M else None, p(w), nbytes, None)
+    assert call(M=None) == B.ERR_ARG                  # the device word for M is required
+    assert call(M=1028) == B.ERR_ARG                  # and 8-byte aligned
+    assert call(N=-1) == B.ERR_ARG and call(res=0) == B.ERR_ARG and call(mode=7) == B.ERR_ARG
+    assert call(order=20) == B.ERR_ARG                # order not 16-byte aligned
+    assert call(nbytes=100) == B.ERR_WORKSPACE
+    assert b"subm3d_downsample" in L.subm3d_last_error()
+
+
 def test_upsample_and_pixel_shuffle_host_checks(L):
     p = ctypes.c_void_p
     assert L.subm3d_upsample(p(16), 4, 8, p(32), -1, B.BF16, p(64), None) == B.ERR_ARG
